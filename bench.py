@@ -1,0 +1,476 @@
+"""Benchmark of the streaming-reduction hot path on GB300.
+
+One step runs every kernel of the path once over its full synthetic workload,
+in this order (no kernel reads data the previous one could have left in the
+129 MB L2, since each input exceeds L2 and consecutive kernels read
+different arrays):
+
+  gemv      packed-int8 dequant GEMV, W 8192 x 16384, one vector
+  segments  ragged row sums of 65,536 segments of 63 x 32 f32
+  batched   packed-int8 dequant-dot, the same W against 16 vectors
+  wide      ragged row sums of a 16,384 x 16,384 f32 matrix
+
+The metric is HBM GB/s over algorithmic bytes (only the bytes the method
+must move: active rows, metadata, outputs).  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --profile {gemv,segments,batched,wide} [--launches N]
+      (no timing: runs one kernel's workload for an ncu capture)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "HBM GB/s and % of GB300 peak: ragged f32 row-sum, packed-int8 dequant-dot"
+WORKLOAD = ("gemv 8192x16384 int8 + 65536 ragged 63x32 f32 segments + batched dot 8192x16384x16 "
+            "int8 + 16384x16384 f32 ragged wide rows")
+ORDER = ("gemv", "segments", "batched", "wide")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------
+# workload
+# ----------------------------------------------------------------------------
+
+def make_inputs():
+    import synth
+    seg = synth.batched_segments()
+    wide = synth.wide_rows()
+    gemv = synth.dequant_gemv()
+    bat = synth.dequant_batched()
+    return {"segments": seg, "wide": wide, "gemv": gemv, "batched": bat}
+
+
+def algorithmic_bytes(inp) -> dict:
+    """Bytes each kernel must move once: active data, metadata and outputs."""
+    seg, wide = inp["segments"], inp["wide"]
+    out = {}
+    c = seg["counts"].astype(np.int64)
+    out["segments"] = int(128 * c.sum() + seg["num_segments"] * (4 + 4 + 16))
+    L = wide["counts"].astype(np.int64)
+    out["wide"] = int(4 * L.sum() + wide["num_segments"] * (4 + 16))
+    for name in ("gemv", "batched"):
+        d = inp[name]
+        n, k = d["w"].shape
+        b = d["x"].shape[0]
+        out[name] = int(n * k + 4 * n + b * k + 4 * b + 4 * n * b)
+    return out
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """Per-kernel DRAM bytes per launch from the committed ncu summary, valid
+    only while the kernel sources hash to the value recorded with it."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if d.get("source_hash") != source_hash():
+        return {}
+    return d.get("bytes_per_launch", {})
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int8_dequant_dot_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+class DeviceWorkload:
+    """Device copies of the inputs and outputs, and one launch per kernel."""
+
+    def __init__(self, inp, torch, loom, stream, depth=0):
+        self.torch, self.loom, self.stream = torch, loom, stream
+        self.inp = inp
+        dev = torch.device("cuda")
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        seg, wide, gemv, bat = inp["segments"], inp["wide"], inp["gemv"], inp["batched"]
+        self.d = {
+            "seg_values": t(seg["values"]), "seg_counts": t(seg["counts"]), "seg_init": t(seg["initial"]),
+            "wide_values": t(wide["values"]), "wide_counts": t(wide["counts"]),
+            "w": t(gemv["w"].view("<i4")), "sw": t(gemv["scale_w"]),
+            "x1": t(gemv["x"].view("<i4")), "sx1": t(gemv["scale_x"]),
+            "x16": t(bat["x"].view("<i4")), "sx16": t(bat["scale_x"]),
+        }
+        i32, f32 = torch.int32, torch.float32
+        S, R = seg["num_segments"], wide["num_segments"]
+        self.o = {
+            "seg": tuple(torch.empty(S, dtype=dt, device=dev) for dt in (i32, i32, f32, f32)),
+            "wide": tuple(torch.empty(R, dtype=dt, device=dev) for dt in (i32, i32, f32, f32)),
+            "y1": torch.empty((8192, 1), dtype=f32, device=dev),
+            "y16": torch.empty((8192, 16), dtype=f32, device=dev),
+        }
+        self.tuning = loom.make_tuning(depth=depth) if depth else None
+        self.launches_per_step = 4
+
+    def launch(self, name):
+        L, d, o, s = self.loom, self.d, self.o, self.stream
+        if name == "segments":
+            L.loom_row_sum_batched_ex(d["seg_values"], 65536, 2016, 63, 32, d["seg_counts"], d["seg_init"],
+                                      8, out=o["seg"], tuning=self.tuning, stream=s)
+        elif name == "wide":
+            L.loom_row_sum_batched_ex(d["wide_values"], 16384, 16384, 16384, 1, d["wide_counts"], None,
+                                      8, out=o["wide"], tuning=self.tuning, stream=s)
+        elif name == "gemv":
+            L.loom_i8_dequant_dot_ex(d["w"], d["sw"], 8192, 16384, d["x1"], d["sx1"], 1, y=o["y1"],
+                                     tuning=self.tuning, stream=s)
+        elif name == "batched":
+            L.loom_i8_dequant_dot_ex(d["w"], d["sw"], 8192, 16384, d["x16"], d["sx16"], 16, y=o["y16"],
+                                     tuning=self.tuning, stream=s)
+        else:
+            raise ValueError(name)
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_step(inp, threads):
+    import oracle
+    seg, wide, gemv, bat = inp["segments"], inp["wide"], inp["gemv"], inp["batched"]
+    oracle.i8_dequant_dot(gemv["w"], gemv["scale_w"], gemv["x"], gemv["scale_x"], threads=threads)
+    oracle.row_sum_batched(seg["values"], 2016, 63, 32, seg["counts"], seg["initial"], 8, threads=threads)
+    oracle.i8_dequant_dot(bat["w"], bat["scale_w"], bat["x"], bat["scale_x"], threads=threads)
+    oracle.row_sum_batched(wide["values"], 16384, 16384, 1, wide["counts"], None, 8, threads=threads)
+
+
+def cpu_baseline(inp, total_bytes, threads):
+    t0 = time.perf_counter()
+    oracle_step(inp, threads)
+    dt = time.perf_counter() - t0
+    return {"value": total_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "one full step (all four workloads), fp64/int64 C oracle, "
+                      f"{threads} threads over independent segments/rows; {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle timed as it stands on the host cores."""
+    if rank != 0:
+        return
+    inp = make_inputs()
+    alg = algorithmic_bytes(inp)
+    total = sum(alg.values())
+    threads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle_step(inp, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(inp, threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = total / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64+i64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "each step is one full pass of all four workloads"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import int8_dequant_dot_gb300 as loom
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    inp = make_inputs()
+    alg = algorithmic_bytes(inp)
+    total = sum(alg.values())
+    work = DeviceWorkload(inp, torch, loom, stream, depth=args.depth)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for name in ORDER:
+                work.launch(name)
+    stream.synchronize()
+
+    # timed region: per-kernel events on the launching stream
+    ev = {name: [] for name in ORDER}
+    step_start = torch.cuda.Event(enable_timing=True)
+    step_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)   # let the sampler attach before the timed work
+    with torch.cuda.stream(stream):
+        step_start.record(stream)
+        for _ in range(args.steps):
+            for name in ORDER:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                work.launch(name)
+                b.record(stream)
+                ev[name].append((a, b))
+        step_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = step_start.elapsed_time(step_end)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * total / (ms_per_step * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    traffic = recorded_traffic()
+    kernels = {}
+    for name in ORDER:
+        times = [a.elapsed_time(b) for a, b in ev[name]]
+        avg = sum(times) / len(times)
+        gbs = alg[name] / (avg * 1e-3) / 1e9
+        kernels[name] = {"alg_bytes": alg[name], "avg_ms": avg, "min_ms": min(times), "GB/s": gbs,
+                         "frac_of_" + peak_kind: gbs / peak,
+                         "frac_of_nominal_8TBs": gbs / 8000.0,
+                         "share": avg / ms_per_step}
+    dominant = max(ORDER, key=lambda n: kernels[n]["avg_ms"])
+    dk = kernels[dominant]
+    tr = traffic.get(dominant)
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GB/s"], "peak": peak,
+                "unit": "GB/s", "frac": dk["GB/s"] / peak, "peak_source": peak_kind,
+                "traffic": tr, "alg_bytes": dk["alg_bytes"]}
+
+    # end to end through the public API: pinned host inputs -> device -> kernels -> host results
+    e2e = run_e2e(args, inp, total, torch, loom, stream, work)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32+i32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "alg_bytes_per_step": total,
+                   "l2": "inputs larger than L2 (each >= 134 MB vs 129 MB); consecutive kernels read "
+                         "different arrays", "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
+                   "depth": args.depth or "default"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": work.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        threads = os.cpu_count() or 1
+        line["cpu_baseline"] = cpu_baseline(inp, total, threads)
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, inp, total, torch, loom, stream, work):
+    """Same metric through the binding with host buffers: every step copies its
+    inputs from pinned host memory, runs the four kernels and reads the results
+    back; the copies are inside the timed region."""
+    host = {}
+    for key, arr in (("seg_values", inp["segments"]["values"]), ("seg_counts", inp["segments"]["counts"]),
+                     ("seg_init", inp["segments"]["initial"]), ("wide_values", inp["wide"]["values"]),
+                     ("wide_counts", inp["wide"]["counts"]), ("w", inp["gemv"]["w"].view("<i4")),
+                     ("sw", inp["gemv"]["scale_w"]), ("x1", inp["gemv"]["x"].view("<i4")),
+                     ("sx1", inp["gemv"]["scale_x"]), ("x16", inp["batched"]["x"].view("<i4")),
+                     ("sx16", inp["batched"]["scale_x"])):
+        host[key] = torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
+    outs = [work.o["seg"], work.o["wide"], (work.o["y1"],), (work.o["y16"],)]
+    host_out = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in grp) for grp in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for grp in host_out for t in grp)
+    steps = max(1, min(args.steps, 5))
+
+    def one_step():
+        for key, t in host.items():
+            work.d[key].copy_(t, non_blocking=True)
+        for name in ORDER:
+            work.launch(name)
+        for grp_h, grp_d in zip(host_out, outs):
+            for h, d in zip(grp_h, grp_d):
+                h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one_step()
+    stream.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            one_step()
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def run_profile(args):
+    """One kernel's workload, `--launches` times, for an ncu capture (not timed)."""
+    import torch
+    import int8_dequant_dot_gb300 as loom
+    import synth
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    if args.profile in ("segments", "wide"):
+        inp = {"segments": synth.batched_segments() if args.profile == "segments" else None,
+               "wide": synth.wide_rows() if args.profile == "wide" else None}
+    else:
+        inp = {"gemv": synth.dequant_gemv() if args.profile == "gemv" else None,
+               "batched": synth.dequant_batched() if args.profile == "batched" else None}
+    work = _SingleWorkload(args.profile, inp, torch, loom, stream, args.depth)
+    with torch.cuda.stream(stream):
+        for _ in range(args.launches):
+            work.launch()
+    stream.synchronize()
+    print(json.dumps({"profile": args.profile, "launches": args.launches}))
+
+
+class _SingleWorkload:
+    def __init__(self, name, inp, torch, loom, stream, depth):
+        self.name, self.loom, self.stream = name, loom, stream
+        dev = torch.device("cuda")
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.tuning = loom.make_tuning(depth=depth) if depth else None
+        if name == "segments":
+            s = inp["segments"]
+            self.args = (t(s["values"]), 65536, 2016, 63, 32, t(s["counts"]), t(s["initial"]), 8)
+        elif name == "wide":
+            s = inp["wide"]
+            self.args = (t(s["values"]), 16384, 16384, 16384, 1, t(s["counts"]), None, 8)
+        else:
+            s = inp[name]
+            b = s["x"].shape[0]
+            self.args = (t(s["w"].view("<i4")), t(s["scale_w"]), 8192, 16384, t(s["x"].view("<i4")),
+                         t(s["scale_x"]), b)
+
+    def launch(self):
+        if self.name in ("segments", "wide"):
+            self.loom.loom_row_sum_batched_ex(*self.args, tuning=self.tuning, stream=self.stream)
+        else:
+            self.loom.loom_i8_dequant_dot_ex(*self.args, tuning=self.tuning, stream=self.stream)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--depth", type=int, default=0, help="read-ahead depth (0 = library default)")
+    ap.add_argument("--profile", choices=ORDER, default=None)
+    ap.add_argument("--launches", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.profile is None:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.profile:
+        run_profile(args)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist_mod
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    try:
+        run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

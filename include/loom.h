@@ -1,0 +1,174 @@
+/*
+ * loom.h -- C ABI of libloom, a GB300 (sm_103a) library for two streaming
+ * reductions described in the Loom documentation pages (ROCm hrx-system):
+ *
+ *   [P1] "Tune loop unrolling and pipelining"
+ *   [P3] "Kernels and launch configuration"
+ *
+ *  1. the ragged full-tile f32 row sum: a dynamic row count is split into
+ *     exact tiles, every full-tile row is reduced across its lanes and added
+ *     to a carried sum, and the partial final tile is summed separately
+ *     ([P1] "Derive full tiles from a ragged loop");
+ *  2. packed signed-byte dequantisation with dot accumulation
+ *     ([P1] "Apply the same controls to a packed dot product").
+ *
+ * Conventions for every entry point
+ *  - Pointers prefixed d_ are device pointers owned by the caller; the library
+ *    never allocates, frees or retains them and keeps no global mutable state,
+ *    so calls may be made from several host threads.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; the return value covers argument validation and
+ *    the launch only.  Faults found on the device are reported through the
+ *    optional error word (LOOM_DEVERR_* bits, atomically OR-ed; the caller
+ *    zeroes it) and, for results that could not be computed, NaN outputs.
+ *  - Empty work (no segments, no rows, empty batch) returns LOOM_OK and
+ *    launches nothing.
+ *  - Results do not depend on the read-ahead depth, the stream or earlier
+ *    calls: the same inputs give the same bits.
+ */
+#ifndef LOOM_H
+#define LOOM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LOOM_ABI_VERSION 1
+
+typedef enum loom_status {
+    LOOM_OK = 0,
+    LOOM_ERR_NULL = -1,    /* a required pointer is NULL */
+    LOOM_ERR_ALIGN = -2,   /* a pointer is not aligned to its element size */
+    LOOM_ERR_SHAPE = -3,   /* a size, stride or tile is outside the supported range */
+    LOOM_ERR_RANGE = -4,   /* a host-side count is outside [0, rows] */
+    LOOM_ERR_CUDA = -5,    /* the CUDA runtime refused the launch */
+    LOOM_ERR_TIMEOUT = -6, /* a device wait ran out (reported via the error word) */
+    LOOM_ERR_ARG = -7      /* any other invalid argument (unknown op, bad tuning) */
+} loom_status;
+
+/* Bits of the device error word. */
+#define LOOM_DEVERR_COUNT_RANGE 0x1 /* a device count was outside [0, rows]; clamped */
+#define LOOM_DEVERR_TIMEOUT 0x2     /* a staged copy did not land in time; NaN results */
+
+typedef enum loom_op {
+    LOOM_OP_I8_UNPACK = 0,       /* workload {n_words} */
+    LOOM_OP_FULL_TILE_SUM = 1,   /* workload {rows, lanes} */
+    LOOM_OP_ROW_SUM_BATCHED = 2, /* workload {num_segments, rows, lanes, staged (0/1), depth} */
+    LOOM_OP_I8_DEQUANT_DOT = 3   /* workload {n_rows, k, batch, staged (0/1), depth} */
+} loom_op;
+
+/* Launch geometry of one kernel launch.  `units_per_cta` logical work units
+ * (words, segments or output rows) map onto each CTA; the grid is the
+ * ceiling division of the workload by it, and units past the workload in the
+ * last CTA do no loads and no stores. */
+typedef struct loom_launch {
+    uint32_t grid[3];
+    uint32_t block[3];
+    uint32_t cluster[3];    /* always {1,1,1}: no kernel uses clusters */
+    uint32_t subgroup_size; /* 32 */
+    uint32_t smem_bytes;    /* dynamic shared memory per CTA */
+    uint32_t units_per_cta;
+    uint32_t kernel;        /* LOOM_KERNEL_* selected for this workload */
+} loom_launch;
+
+#define LOOM_KERNEL_UNPACK 1
+#define LOOM_KERNEL_ROWSUM_STAGED 2 /* bulk-copy read-ahead ring per warp */
+#define LOOM_KERNEL_ROWSUM_DIRECT 3 /* plain loads (unaligned inputs) */
+#define LOOM_KERNEL_DOT_STAGED_K 4  /* lanes across k, batch <= 4 */
+#define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 4 */
+#define LOOM_KERNEL_DOT_DIRECT 6    /* plain loads (unaligned or k % 16 != 0) */
+
+/* Maximum read-ahead depth (staged chunks in flight per warp). */
+#define LOOM_MAX_DEPTH 4
+
+/*
+ * Host launch-configuration routine: maps a workload to a launch without
+ * touching the device.  [P3] "A kernel owns two signatures" and "Workload is
+ * not workgroup count": the workload scalars alone determine the grid by
+ * ceiling division; for LOOM_OP_I8_UNPACK 1009 words give 4 CTAs of 256.
+ * `workload` holds `n_workload` scalars as listed for each loom_op; trailing
+ * optional entries (staged, depth) default to 1 and the library default.
+ * Errors: NULL out/workload -> LOOM_ERR_NULL; unknown op or too few entries
+ * -> LOOM_ERR_ARG; negative or unsupported sizes -> LOOM_ERR_SHAPE.
+ */
+loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_workload,
+                               loom_launch *out);
+
+/*
+ * One segment.  [P1] "Derive full tiles from a ragged loop": with
+ * F = tile_size * floor(count / tile_size) and t = count - F,
+ *   *d_final_row  = F,  *d_tail_count = t,
+ *   *d_full_sum   = initial + sum over rows r < F, lanes l of values[r][l],
+ *   *d_tail_sum   = sum over rows F <= r < count, lanes l of values[r][l].
+ * d_values: f32 [rows][lanes], row-major, contiguous, 4-byte aligned
+ * (16-byte alignment selects the bulk-copy path; it is never required).
+ * Sums are accumulated without rounding loss (error-free double-word f32)
+ * and rounded once, so they are within one f32 rounding of the exact sum.
+ * Errors: NULL -> LOOM_ERR_NULL; misaligned -> LOOM_ERR_ALIGN; rows < 0,
+ * lanes not 1 or 32, tile_size outside [1, 64], rows*lanes >= 2^31 ->
+ * LOOM_ERR_SHAPE; count outside [0, rows] -> LOOM_ERR_RANGE.
+ */
+loom_status loom_full_tile_sum(const float *d_values, int32_t rows, int32_t lanes, int32_t count,
+                               float initial, int32_t tile_size, int32_t *d_final_row,
+                               int32_t *d_tail_count, float *d_full_sum, float *d_tail_sum,
+                               void *stream);
+
+/*
+ * num_segments independent segments, each exactly loom_full_tile_sum above.
+ * Segment s holds f32 [rows][lanes] at d_values + s * seg_stride (elements);
+ * its count is d_counts[s] and its initial sum d_initial[s] (0 when
+ * d_initial is NULL).  Outputs are four arrays of num_segments entries
+ * (structure of arrays).  Wide ragged rows are the case lanes = 1: each row
+ * is a segment of `rows` one-lane records with its active length as count.
+ * A device count outside [0, rows] is clamped into range and sets
+ * LOOM_DEVERR_COUNT_RANGE in *d_error (d_error may be NULL).
+ * Errors: as loom_full_tile_sum, plus seg_stride < rows*lanes (when
+ * num_segments > 1) or num_segments < 0 -> LOOM_ERR_SHAPE.
+ */
+loom_status loom_row_sum_batched(const float *d_values, int64_t num_segments, int64_t seg_stride,
+                                 int32_t rows, int32_t lanes, const int32_t *d_counts,
+                                 const float *d_initial, int32_t tile_size, int32_t *d_final_row,
+                                 int32_t *d_tail_count, float *d_full_sum, float *d_tail_sum,
+                                 int32_t *d_error, void *stream);
+
+/*
+ * Dequantised dot products.  [P1] "Apply the same controls to a packed dot
+ * product": packed words are unpacked into signed bytes and accumulated as a
+ * dot product; here every weight row r has scale d_scale_w[r] and every
+ * activation vector b has scale d_scale_x[b]:
+ *   acc[r][b] = sum_k W[r][k] * X[b][k]                  (int32, exact)
+ *   y[r][b]   = (float)acc[r][b] * (d_scale_w[r] * d_scale_x[b])   (f32)
+ * d_w_packed: int32 [n_rows][k/4]; d_x_packed: int32 [batch][k/4].  Word j
+ * of a row holds elements 4j..4j+3, element 4j+i in bits [8i, 8i+7] as a
+ * signed byte (the little-endian int8 array viewed as int32 words).
+ * d_y: f32 [n_rows][batch]; d_acc: int32 [n_rows][batch] or NULL.
+ * Errors: NULL -> LOOM_ERR_NULL; misaligned -> LOOM_ERR_ALIGN; k % 4 != 0,
+ * k > 131068 (|acc| must stay below 2^31) or negative sizes -> LOOM_ERR_SHAPE.
+ */
+loom_status loom_i8_dequant_dot(const int32_t *d_w_packed, const float *d_scale_w, int32_t n_rows,
+                                int32_t k, const int32_t *d_x_packed, const float *d_scale_x,
+                                int32_t batch, float *d_y, int32_t *d_acc, void *stream);
+
+/*
+ * Unpack and convert: d_out[4j + i] = (float) signed byte i of d_packed[j].
+ * [P1] "Apply the same controls to a packed dot product" (bit-unpack into
+ * four 8-bit integers, then signed integer to float).  One thread per word,
+ * 256-thread CTAs, grid = ceil(n_words / 256) ([P3] "Over-dispatch safely").
+ * Errors: NULL -> LOOM_ERR_NULL; misaligned -> LOOM_ERR_ALIGN;
+ * n_words < 0 -> LOOM_ERR_SHAPE.
+ */
+loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *loom_status_string(int32_t status);
+
+/* LOOM_ABI_VERSION of the loaded library. */
+int32_t loom_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOOM_H */

@@ -1,0 +1,56 @@
+/*
+ * loom_tuning.h -- schedule controls and test hooks of libloom.
+ *
+ * The _ex entry points take the same arguments as their plain counterparts
+ * in loom.h, plus a device error word and an optional loom_tuning.  They
+ * exist for schedule experiments (read-ahead depth, serial control, plain
+ * loads) and for fault tests; none of these controls changes a result.
+ * [P1] = "Tune loop unrolling and pipelining" (Loom pages): the depth is the
+ * read-ahead depth of its pipeline(depth) ("Separate depth from unrolling"),
+ * depth 1 being the serial control.
+ */
+#ifndef LOOM_TUNING_H
+#define LOOM_TUNING_H
+
+#include "loom.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LOOM_PATH_AUTO 0   /* staged when inputs are 16-byte aligned, else direct */
+#define LOOM_PATH_STAGED 1 /* bulk-copy read-ahead ring; LOOM_ERR_ALIGN if not possible */
+#define LOOM_PATH_DIRECT 2 /* plain loads, no shared-memory staging */
+
+typedef struct loom_tuning {
+    int32_t depth;          /* staged chunks in flight per warp, 1..LOOM_MAX_DEPTH; 0 = default */
+    int32_t path;           /* LOOM_PATH_* */
+    int32_t units_per_warp; /* row sums: segments per warp, 1..32; 0 = default */
+    int32_t inject_stall;   /* fault test: issue no bulk copies, so every staged wait runs
+                               out after wait_ns; results become NaN, the error word gets
+                               LOOM_DEVERR_TIMEOUT, and the device stays usable */
+    int64_t wait_ns;        /* limit of each device wait in ns; 0 = default (1 s) */
+} loom_tuning;
+
+/* loom_row_sum_batched with tuning (NULL = defaults).  Extra errors:
+ * out-of-range tuning -> LOOM_ERR_ARG; LOOM_PATH_STAGED on unaligned input
+ * -> LOOM_ERR_ALIGN. */
+loom_status loom_row_sum_batched_ex(const float *d_values, int64_t num_segments,
+                                    int64_t seg_stride, int32_t rows, int32_t lanes,
+                                    const int32_t *d_counts, const float *d_initial,
+                                    int32_t tile_size, int32_t *d_final_row, int32_t *d_tail_count,
+                                    float *d_full_sum, float *d_tail_sum, int32_t *d_error,
+                                    const loom_tuning *tuning, void *stream);
+
+/* loom_i8_dequant_dot with a device error word (may be NULL) and tuning. */
+loom_status loom_i8_dequant_dot_ex(const int32_t *d_w_packed, const float *d_scale_w,
+                                   int32_t n_rows, int32_t k, const int32_t *d_x_packed,
+                                   const float *d_scale_x, int32_t batch, float *d_y,
+                                   int32_t *d_acc, int32_t *d_error, const loom_tuning *tuning,
+                                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOOM_TUNING_H */

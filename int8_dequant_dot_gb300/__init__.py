@@ -1,0 +1,257 @@
+"""Python binding of libloom (the C ABI in include/loom.h and loom_tuning.h).
+
+The functions keep the C names and only marshal arguments: tensors become
+device pointers, the stream defaults to torch's current stream, and a status
+other than LOOM_OK raises LoomError.  Every step of the computation runs in
+libloom's CUDA kernels; there is no fallback, and importing this module
+fails loudly when libloom.so has not been built (see build.py).
+
+Each function accepts either torch tensors or raw integer addresses.  Output
+tensors may be passed in; when omitted they are allocated with torch (on
+the inputs' device) and returned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libloom.so")
+
+LOOM_OK = 0
+LOOM_ERR_NULL = -1
+LOOM_ERR_ALIGN = -2
+LOOM_ERR_SHAPE = -3
+LOOM_ERR_RANGE = -4
+LOOM_ERR_CUDA = -5
+LOOM_ERR_TIMEOUT = -6
+LOOM_ERR_ARG = -7
+
+LOOM_DEVERR_COUNT_RANGE = 0x1
+LOOM_DEVERR_TIMEOUT = 0x2
+
+LOOM_OP_I8_UNPACK = 0
+LOOM_OP_FULL_TILE_SUM = 1
+LOOM_OP_ROW_SUM_BATCHED = 2
+LOOM_OP_I8_DEQUANT_DOT = 3
+
+LOOM_KERNEL_UNPACK = 1
+LOOM_KERNEL_ROWSUM_STAGED = 2
+LOOM_KERNEL_ROWSUM_DIRECT = 3
+LOOM_KERNEL_DOT_STAGED_K = 4
+LOOM_KERNEL_DOT_STAGED_B = 5
+LOOM_KERNEL_DOT_DIRECT = 6
+
+LOOM_MAX_DEPTH = 4
+LOOM_PATH_AUTO = 0
+LOOM_PATH_STAGED = 1
+LOOM_PATH_DIRECT = 2
+
+#: every extern "C" symbol the headers declare
+EXPORTS = (
+    "loom_launch_config", "loom_full_tile_sum", "loom_row_sum_batched", "loom_i8_dequant_dot",
+    "loom_i8_unpack", "loom_status_string", "loom_abi_version", "loom_row_sum_batched_ex",
+    "loom_i8_dequant_dot_ex",
+)
+
+
+class LoomError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {loom_status_string(status)} (status {status})")
+
+
+class loom_launch(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_uint32 * 3), ("block", ctypes.c_uint32 * 3),
+                ("cluster", ctypes.c_uint32 * 3), ("subgroup_size", ctypes.c_uint32),
+                ("smem_bytes", ctypes.c_uint32), ("units_per_cta", ctypes.c_uint32),
+                ("kernel", ctypes.c_uint32)]
+
+    def as_dict(self) -> dict:
+        return {"grid": tuple(self.grid), "block": tuple(self.block), "cluster": tuple(self.cluster),
+                "subgroup_size": self.subgroup_size, "smem_bytes": self.smem_bytes,
+                "units_per_cta": self.units_per_cta, "kernel": self.kernel}
+
+
+class loom_tuning(ctypes.Structure):
+    _fields_ = [("depth", ctypes.c_int32), ("path", ctypes.c_int32),
+                ("units_per_warp", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
+                ("wait_ns", ctypes.c_int64)]
+
+
+def _bind() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libloom.so is not built ({LIB_PATH}); run "
+                          "`python int8_dequant_dot_gb300/build.py` or __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    sig = {
+        "loom_launch_config": [i32, P, i32, ctypes.POINTER(loom_launch)],
+        "loom_full_tile_sum": [P, i32, i32, i32, f32, i32, P, P, P, P, P],
+        "loom_row_sum_batched": [P, i64, i64, i32, i32, P, P, i32, P, P, P, P, P, P],
+        "loom_row_sum_batched_ex": [P, i64, i64, i32, i32, P, P, i32, P, P, P, P, P,
+                                    ctypes.POINTER(loom_tuning), P],
+        "loom_i8_dequant_dot": [P, P, i32, i32, P, P, i32, P, P, P],
+        "loom_i8_dequant_dot_ex": [P, P, i32, i32, P, P, i32, P, P, P,
+                                   ctypes.POINTER(loom_tuning), P],
+        "loom_i8_unpack": [P, i64, P, P],
+        "loom_status_string": [i32],
+        "loom_abi_version": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = i32
+    lib.loom_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _bind()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def loom_abi_version() -> int:
+    return int(_lib.loom_abi_version())
+
+
+def loom_status_string(status: int) -> str:
+    return _lib.loom_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != LOOM_OK:
+        raise LoomError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream, like=None):
+    if stream is None:
+        import torch
+        dev = like.device if like is not None and hasattr(like, "device") else None
+        return torch.cuda.current_stream(dev).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def loom_launch_config(op: int, workload) -> dict:
+    arr = (ctypes.c_int64 * max(1, len(workload)))(*[int(v) for v in workload])
+    out = loom_launch()
+    _check(_lib.loom_launch_config(int(op), arr, len(workload), ctypes.byref(out)),
+           "loom_launch_config")
+    return out.as_dict()
+
+
+def _empty(like, shape, dtype):
+    import torch
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def loom_full_tile_sum(values, count: int, initial: float, tile_size: int = 8, *,
+                       rows: int | None = None, lanes: int | None = None, out=None, stream=None):
+    """One segment ``values[rows][lanes]``; returns ``(final_row, tail_count, full_sum,
+    tail_sum)`` as four one-element device tensors (or fills ``out``)."""
+    import torch
+    if rows is None or lanes is None:
+        rows, lanes = values.shape
+    if out is None:
+        out = (_empty(values, (1,), torch.int32), _empty(values, (1,), torch.int32),
+               _empty(values, (1,), torch.float32), _empty(values, (1,), torch.float32))
+    fr, tc, fs, ts = out
+    _check(_lib.loom_full_tile_sum(_ptr(values), int(rows), int(lanes), int(count), float(initial),
+                                   int(tile_size), _ptr(fr), _ptr(tc), _ptr(fs), _ptr(ts),
+                                   _stream(stream, values)), "loom_full_tile_sum")
+    return out
+
+
+def _row_sum_outputs(values, n):
+    import torch
+    return (_empty(values, (n,), torch.int32), _empty(values, (n,), torch.int32),
+            _empty(values, (n,), torch.float32), _empty(values, (n,), torch.float32))
+
+
+def loom_row_sum_batched(values, num_segments: int, seg_stride: int, rows: int, lanes: int,
+                         counts, initial=None, tile_size: int = 8, *, out=None, error=None,
+                         stream=None):
+    """Batched segments; returns ``(final_row, tail_count, full_sum, tail_sum)``."""
+    if out is None:
+        out = _row_sum_outputs(values, num_segments)
+    fr, tc, fs, ts = out
+    _check(_lib.loom_row_sum_batched(_ptr(values), int(num_segments), int(seg_stride), int(rows),
+                                     int(lanes), _ptr(counts), _ptr(initial), int(tile_size),
+                                     _ptr(fr), _ptr(tc), _ptr(fs), _ptr(ts), _ptr(error),
+                                     _stream(stream, values)), "loom_row_sum_batched")
+    return out
+
+
+def make_tuning(depth: int = 0, path: int = LOOM_PATH_AUTO, units_per_warp: int = 0,
+                inject_stall: bool = False, wait_ns: int = 0) -> loom_tuning:
+    return loom_tuning(int(depth), int(path), int(units_per_warp), int(bool(inject_stall)),
+                       int(wait_ns))
+
+
+def loom_row_sum_batched_ex(values, num_segments: int, seg_stride: int, rows: int, lanes: int,
+                            counts, initial=None, tile_size: int = 8, *, tuning=None, out=None,
+                            error=None, stream=None):
+    if out is None:
+        out = _row_sum_outputs(values, num_segments)
+    fr, tc, fs, ts = out
+    tp = ctypes.byref(tuning) if tuning is not None else None
+    _check(_lib.loom_row_sum_batched_ex(_ptr(values), int(num_segments), int(seg_stride), int(rows),
+                                        int(lanes), _ptr(counts), _ptr(initial), int(tile_size),
+                                        _ptr(fr), _ptr(tc), _ptr(fs), _ptr(ts), _ptr(error), tp,
+                                        _stream(stream, values)), "loom_row_sum_batched_ex")
+    return out
+
+
+def _dot_outputs(w, n_rows, batch, want_acc):
+    import torch
+    y = _empty(w, (n_rows, batch), torch.float32)
+    acc = _empty(w, (n_rows, batch), torch.int32) if want_acc else None
+    return y, acc
+
+
+def loom_i8_dequant_dot(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_x, batch: int, *,
+                        y=None, acc=None, want_acc: bool = False, stream=None):
+    """``y[n_rows][batch]`` (and ``acc`` when requested); returns ``(y, acc)``."""
+    if y is None:
+        y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
+        acc = acc if acc is not None else acc2
+    _check(_lib.loom_i8_dequant_dot(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
+                                    _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
+                                    _stream(stream, w_packed)), "loom_i8_dequant_dot")
+    return y, acc
+
+
+def loom_i8_dequant_dot_ex(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_x, batch: int,
+                           *, y=None, acc=None, want_acc: bool = False, error=None, tuning=None,
+                           stream=None):
+    if y is None:
+        y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
+        acc = acc if acc is not None else acc2
+    tp = ctypes.byref(tuning) if tuning is not None else None
+    _check(_lib.loom_i8_dequant_dot_ex(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
+                                       _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
+                                       _ptr(error), tp, _stream(stream, w_packed)),
+           "loom_i8_dequant_dot_ex")
+    return y, acc
+
+
+def loom_i8_unpack(packed, n_words: int, out=None, *, stream=None):
+    """``out[4j+i]`` = signed byte i of word j, as f32."""
+    import torch
+    if out is None:
+        out = _empty(packed, (4 * int(n_words),), torch.float32)
+    _check(_lib.loom_i8_unpack(_ptr(packed), int(n_words), _ptr(out), _stream(stream, packed)),
+           "loom_i8_unpack")
+    return out

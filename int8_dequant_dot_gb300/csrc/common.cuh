@@ -1,0 +1,154 @@
+// common.cuh -- device helpers shared by the streaming kernels (sm_103a).
+//
+//  * 1-D bulk copies global -> shared (cp.async.bulk) completing on an
+//    mbarrier with a transaction count; these stage the read-ahead queue.
+//  * Bounded mbarrier waits: a wait gives up after a time limit read from
+//    %globaltimer, so a copy that never lands ends the kernel with an error
+//    flag instead of a hang.
+//  * Error-free double-word accumulation (TwoSum) for f32 streams.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/loom.h"
+
+namespace loom {
+namespace dev {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// L2 policy for data that is read exactly once: evict first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is signalled on the
+// mbarrier at `bar` as a transaction count of `bytes`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of the barrier; false once `limit_ns` has passed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 15u) == 0 && global_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void flag_error(int32_t *word, int32_t bits)
+{
+    if (word)
+        atomicOr(word, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Double-word f32 accumulator.  `hi + lo` carries the running sum; every
+// addition to `hi` is split exactly into a rounded sum and its rounding error
+// (Knuth's TwoSum, six operations, valid for any operand order), and the
+// errors are summed in `lo` (the Sum2 scheme of Ogita, Rump and Oishi, 2005).
+// The explicit _rn intrinsics keep the compiler from contracting or
+// reassociating any of the steps.
+// ---------------------------------------------------------------------------
+struct DW {
+    float hi;
+    float lo;
+
+    __device__ __forceinline__ void add(float x)
+    {
+        const float s = __fadd_rn(hi, x);
+        const float bp = __fsub_rn(s, hi);
+        const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
+        hi = s;
+        lo = __fadd_rn(lo, e);
+    }
+
+    // Combine with the accumulator of lane (lane ^ m) for m = 16..1.  Both
+    // partners compute identical results (the rounded sum is commutative and
+    // TwoSum's error term is exact), so every lane ends with the same value.
+    __device__ __forceinline__ void warp_allreduce()
+    {
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            const float oh = __shfl_xor_sync(FULL_MASK, hi, m);
+            const float ol = __shfl_xor_sync(FULL_MASK, lo, m);
+            const float s = __fadd_rn(hi, oh);
+            const float bp = __fsub_rn(s, hi);
+            const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(oh, bp));
+            hi = s;
+            lo = __fadd_rn(__fadd_rn(lo, ol), e);
+        }
+    }
+
+    __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
+};
+
+__device__ __forceinline__ int32_t warp_sum_i32(int32_t v)
+{
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+        v += __shfl_xor_sync(FULL_MASK, v, m);
+    return v;
+}
+
+}  // namespace dev
+}  // namespace loom

@@ -1,0 +1,437 @@
+// dequant_dot.cu -- packed signed-byte dequantised dot products on sm_103a.
+//
+// Method (Loom pages, "Tune loop unrolling and pipelining", section "Apply
+// the same controls to a packed dot product"): each 32-bit field holds four
+// signed bytes; they are unpacked, scaled and accumulated as a dot product.
+// The workload here uses int8 weights W[n_rows][k] with a scale per row and
+// int8 activations X[batch][k] with a scale per vector:
+//   acc[r][b] = sum_k W[r][k] * X[b][k]   (int32: exact, order-free)
+//   y[r][b]   = (float)acc[r][b] * (scale_w[r] * scale_x[b])
+//
+// GB300 design
+//  * __dp4a does the unpack and four multiply-adds of one packed word in one
+//    instruction; accumulation is int32, so results are exact and do not
+//    depend on the order of the k terms (|acc| <= 2^14 * k < 2^31).
+//  * Weights stream once through HBM.  Each warp owns its rows and a private
+//    ring of `depth` shared-memory stages filled by bulk copies (the
+//    read-ahead queue); activations are small and stay in L1/L2.
+//  * batch <= 4 ("lanes across k"): one row per unit; every lane takes one
+//    16-byte group of the row per 512-byte slot, dp4a against the matching
+//    activation words, and the warp sums its lanes at the end of the row.
+//  * batch > 4 ("lanes across the batch"): eight rows per unit; lane b of
+//    each half-warp owns vector b and keeps a slice of its activations in
+//    registers, reused for all eight rows; weight words are read from the
+//    stage as broadcasts, and the two half-warps split the k range.
+//  * Unaligned inputs or k % 16 != 0 take a plain-load kernel.
+#include "common.cuh"
+#include "internal.h"
+
+namespace loom {
+namespace {
+
+using dev::FULL_MASK;
+
+__device__ __forceinline__ float dequant(int32_t acc, float sw, float sx)
+{
+    return __fmul_rn(__int2float_rn(acc), __fmul_rn(sw, sx));
+}
+
+__device__ __forceinline__ void dp4a4(int32_t &acc, const int4 &w, const int4 &x)
+{
+    acc = __dp4a(w.x, x.x, acc);
+    acc = __dp4a(w.y, x.y, acc);
+    acc = __dp4a(w.z, x.z, acc);
+    acc = __dp4a(w.w, x.w, acc);
+}
+
+__device__ __forceinline__ void store_result(const DotParams &p, int32_t r, int b, int32_t acc,
+                                             bool valid)
+{
+    const int64_t o = (int64_t)r * p.y_stride + b;
+    p.y[o] = valid ? dequant(acc, __ldg(p.scale_w + r), __ldg(p.scale_x + b))
+                   : __int_as_float(0x7fc00000);
+    if (p.acc)
+        p.acc[o] = valid ? acc : INT32_MIN;
+}
+
+// Per-warp ring of `depth` stages of `stage_bytes`, with one mbarrier each.
+struct Ring {
+    uint32_t data0, bar0;
+    int depth;
+    uint32_t stage_bytes;
+    int ps = 0, cs = 0;
+    uint32_t cphase = 0;
+    uint32_t issued = 0, consumed = 0;
+
+    __device__ void init(int lane)
+    {
+        if (lane == 0) {
+            for (int s = 0; s < depth; ++s)
+                dev::mbar_init(bar0 + 8 * s, 1);
+            dev::fence_barrier_init();
+        }
+        __syncwarp();
+    }
+    __device__ uint32_t pstage() const { return data0 + ps * stage_bytes; }
+    __device__ uint32_t pbar() const { return bar0 + 8 * ps; }
+    __device__ void pnext()
+    {
+        ++issued;
+        ps = (ps + 1 == depth) ? 0 : ps + 1;
+    }
+    __device__ bool wait(uint64_t limit_ns)
+    {
+        const bool landed = dev::mbar_wait_bounded(bar0 + 8 * cs, cphase, limit_ns);
+        return __all_sync(FULL_MASK, landed);
+    }
+    __device__ void cnext()
+    {
+        __syncwarp();
+        ++consumed;
+        cs = (cs + 1 == depth) ? 0 : cs + 1;
+        cphase ^= (cs == 0) ? 1u : 0u;
+    }
+    // After a failed wait: let copies already in flight land (bounded).
+    __device__ void drain(uint64_t limit_ns, bool any_issued)
+    {
+        if (!any_issued)
+            return;
+        int s = cs;
+        uint32_t ph = cphase;
+        for (uint32_t i = consumed; i < issued; ++i) {
+            dev::mbar_wait_bounded(bar0 + 8 * s, ph, limit_ns);
+            s = (s + 1 == depth) ? 0 : s + 1;
+            ph ^= (s == 0) ? 1u : 0u;
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// batch <= 4: lanes across k.  Unit = one row; rows_per_warp consecutive rows.
+// ---------------------------------------------------------------------------
+constexpr int K_ROWS_PER_WARP = 4;
+
+template <int NB>
+__global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_k_kernel(const DotParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int32_t r0 = (blockIdx.x * DOT_WARPS + warp) * K_ROWS_PER_WARP;
+    if (r0 >= p.n_rows)
+        return;
+    const int n = min(K_ROWS_PER_WARP, p.n_rows - r0);
+    const int32_t kw = p.k_words;
+    const int32_t nchunks = (kw + DOT_K_CHUNK_WORDS - 1) / DOT_K_CHUNK_WORDS;
+    const int D = p.depth;
+    const uint32_t stage_bytes = DOT_K_CHUNK_WORDS * 4;
+
+    Ring ring;
+    ring.depth = D;
+    ring.stage_bytes = stage_bytes;
+    ring.data0 = dev::smem_u32(smem) + warp * D * stage_bytes;
+    ring.bar0 = dev::smem_u32(smem) + DOT_WARPS * D * stage_bytes + warp * D * 8;
+    ring.init(lane);
+    const uint64_t policy = dev::l2_evict_first_policy();
+    const int32_t total = n * nchunks;
+
+    int pchunk = 0;  // flattened (row, chunk) index of the next copy
+    auto produce = [&]() {
+        if (pchunk >= total)
+            return;
+        const int row = pchunk / nchunks;
+        const int32_t off = (pchunk - row * nchunks) * DOT_K_CHUNK_WORDS;
+        if (lane == 0 && !p.inject_stall) {
+            const uint32_t bytes = (uint32_t)min(DOT_K_CHUNK_WORDS, kw - off) * 4u;
+            dev::mbar_arrive_expect_tx(ring.pbar(), bytes);
+            dev::bulk_g2s(ring.pstage(), p.w + (int64_t)(r0 + row) * kw + off, bytes, ring.pbar(),
+                          policy);
+        }
+        ++pchunk;
+        ring.pnext();
+    };
+    for (int s = 0; s < D; ++s)
+        produce();
+
+    // Vectors past the batch (NB rounds it up) re-read vector 0 and are not stored.
+    const int4 *x4[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+        x4[b] = reinterpret_cast<const int4 *>(p.x + (int64_t)(b < p.batch ? b : 0) * kw);
+    const unsigned char *ring_base = smem + (size_t)warp * D * stage_bytes;
+
+    int failed_at = n;
+    for (int row = 0; row < n && failed_at == n; ++row) {
+        int32_t acc[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+            acc[b] = 0;
+        for (int j = 0; j < nchunks; ++j) {
+            if (!ring.wait(p.wait_ns)) {
+                failed_at = row;
+                break;
+            }
+            const int32_t off = j * DOT_K_CHUNK_WORDS;
+            const int32_t m = min(DOT_K_CHUNK_WORDS, kw - off);
+            const int4 *s4 = reinterpret_cast<const int4 *>(ring_base + ring.cs * stage_bytes);
+#pragma unroll 4
+            for (int e = lane * 4; e < m; e += 128) {
+                const int4 wv = s4[e >> 2];
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    dp4a4(acc[b], wv, __ldg(x4[b] + ((off + e) >> 2)));
+            }
+            ring.cnext();
+            produce();
+        }
+        if (failed_at != n)
+            break;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int32_t s = dev::warp_sum_i32(acc[b]);
+            if (lane == b && b < p.batch)
+                store_result(p, r0 + row, b, s, true);
+        }
+    }
+    if (failed_at < n) {
+        dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+        ring.drain(p.wait_ns, !p.inject_stall);
+        for (int row = failed_at; row < n; ++row)
+            if (lane < p.batch)
+                store_result(p, r0 + row, lane, 0, false);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// batch in (4, 16]: lanes across the batch.  Unit = DOT_B_ROWS rows.
+// Chunk = DOT_B_CHUNK_WORDS words of each unit row (one bulk copy per row).
+// Lane (h, b): vector b = lane & 15, half h = lane >> 4.  Within a chunk the
+// 16-byte groups alternate between the halves (group g -> half g & 1).
+// ---------------------------------------------------------------------------
+template <int NB>
+__global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_b_kernel(const DotParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int b = lane & 15;
+    const int h = lane >> 4;
+    const int32_t r0 = (blockIdx.x * DOT_WARPS + warp) * DOT_B_ROWS;
+    if (r0 >= p.n_rows)
+        return;
+    const int n = min(DOT_B_ROWS, p.n_rows - r0);
+    const int32_t kw = p.k_words;
+    const int32_t nchunks = (kw + DOT_B_CHUNK_WORDS - 1) / DOT_B_CHUNK_WORDS;
+    const int D = p.depth;
+    constexpr uint32_t row_bytes = DOT_B_CHUNK_WORDS * 4;
+    constexpr uint32_t stage_bytes = DOT_B_ROWS * row_bytes;
+
+    Ring ring;
+    ring.depth = D;
+    ring.stage_bytes = stage_bytes;
+    ring.data0 = dev::smem_u32(smem) + warp * D * stage_bytes;
+    ring.bar0 = dev::smem_u32(smem) + DOT_WARPS * D * stage_bytes + warp * D * 8;
+    ring.init(lane);
+    const uint64_t policy = dev::l2_evict_first_policy();
+
+    int pj = 0;
+    auto produce = [&]() {
+        if (pj >= nchunks)
+            return;
+        const int32_t off = pj * DOT_B_CHUNK_WORDS;
+        const uint32_t bytes = (uint32_t)min(DOT_B_CHUNK_WORDS, kw - off) * 4u;
+        if (!p.inject_stall) {
+            if (lane == 0)
+                dev::mbar_arrive_expect_tx(ring.pbar(), bytes * n);
+            __syncwarp();
+            if (lane < n)
+                dev::bulk_g2s(ring.pstage() + lane * row_bytes, p.w + (int64_t)(r0 + lane) * kw + off,
+                              bytes, ring.pbar(), policy);
+        }
+        ++pj;
+        ring.pnext();
+    };
+    for (int s = 0; s < D; ++s)
+        produce();
+
+    const bool active = b < p.batch;
+    const int4 *xrow = reinterpret_cast<const int4 *>(p.x + (int64_t)(active ? b : 0) * kw);
+    int32_t acc[DOT_B_ROWS];
+#pragma unroll
+    for (int r = 0; r < DOT_B_ROWS; ++r)
+        acc[r] = 0;
+
+    bool failed = false;
+    for (int j = 0; j < nchunks; ++j) {
+        if (!ring.wait(p.wait_ns)) {
+            failed = true;
+            break;
+        }
+        const int32_t off = j * DOT_B_CHUNK_WORDS;
+        const int32_t groups = min(DOT_B_CHUNK_WORDS, kw - off) >> 2;  // 16-byte groups
+        const unsigned char *stage = smem + (size_t)warp * D * stage_bytes + ring.cs * stage_bytes;
+        // This half's groups: g = 2q + h.
+        constexpr int QMAX = DOT_B_CHUNK_WORDS / 8;
+        int4 xv[QMAX];
+#pragma unroll
+        for (int q = 0; q < QMAX; ++q) {
+            const int g = 2 * q + h;
+            xv[q] = (active && g < groups) ? __ldg(xrow + (off >> 2) + g) : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int r = 0; r < DOT_B_ROWS; ++r) {
+            if (r < n) {
+                const int4 *wrow = reinterpret_cast<const int4 *>(stage + r * row_bytes);
+#pragma unroll
+                for (int q = 0; q < QMAX; ++q) {
+                    const int g = 2 * q + h;
+                    if (g < groups)
+                        dp4a4(acc[r], wrow[g], xv[q]);
+                }
+            }
+        }
+        ring.cnext();
+        produce();
+    }
+    if (failed) {
+        dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+        ring.drain(p.wait_ns, !p.inject_stall);
+    }
+#pragma unroll
+    for (int r = 0; r < DOT_B_ROWS; ++r) {
+        const int32_t s = acc[r] + __shfl_xor_sync(FULL_MASK, acc[r], 16);
+        if (r < n && h == 0 && active)
+            store_result(p, r0 + r, b, s, !failed);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Plain loads: any 4-byte aligned input, any k % 4 == 0.  One warp per row.
+// ---------------------------------------------------------------------------
+template <int NB>
+__global__ void __launch_bounds__(DOT_WARPS * 32) dot_direct_kernel(const DotParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int32_t r = blockIdx.x * DOT_WARPS + (threadIdx.x >> 5);
+    if (r >= p.n_rows)
+        return;
+    const int32_t kw = p.k_words;
+    const int32_t *wr = p.w + (int64_t)r * kw;
+    int32_t acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+        acc[b] = 0;
+    for (int32_t w = lane; w < kw; w += 32) {
+        const int32_t wv = __ldg(wr + w);
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+            if (b < p.batch)
+                acc[b] = __dp4a(wv, __ldg(p.x + (int64_t)b * kw + w), acc[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const int32_t s = dev::warp_sum_i32(acc[b]);
+        if (lane == b && b < p.batch)
+            store_result(p, r, b, s, true);
+    }
+}
+
+template <int NB>
+cudaError_t launch_nb(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream)
+{
+    if (L.grid[0] == 0)
+        return cudaSuccess;
+    switch (kind) {
+    case DotKernel::StagedK:
+        return launch_with(dot_staged_k_kernel<NB>, L, stream, p);
+    case DotKernel::StagedB:
+        return launch_with(dot_staged_b_kernel<NB>, L, stream, p);
+    default:
+        return launch_with(dot_direct_kernel<NB>, L, stream, p);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Unpack: one thread per packed word, 256-thread CTAs.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(UNPACK_BLOCK) unpack_kernel(const int32_t *__restrict__ packed,
+                                                              int64_t n_words, float *__restrict__ out)
+{
+    const int64_t j = (int64_t)blockIdx.x * UNPACK_BLOCK + threadIdx.x;
+    if (j >= n_words)
+        return;  // over-dispatched invocation: no load, no store
+    const uint32_t w = (uint32_t)__ldg(packed + j);
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v[i] = (float)(int32_t)(int8_t)(uint8_t)(w >> (8 * i));
+    if ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+        reinterpret_cast<float4 *>(out)[j] = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            out[4 * j + i] = v[i];
+    }
+}
+
+}  // namespace
+
+DotKernel dot_select(bool aligned, int32_t k, int32_t batch_pass)
+{
+    if (!aligned || (k % 16) != 0)
+        return DotKernel::Direct;
+    return batch_pass <= 4 ? DotKernel::StagedK : DotKernel::StagedB;
+}
+
+int dot_rows_per_cta(DotKernel kind)
+{
+    switch (kind) {
+    case DotKernel::StagedK:
+        return DOT_WARPS * K_ROWS_PER_WARP;
+    case DotKernel::StagedB:
+        return DOT_WARPS * DOT_B_ROWS;
+    default:
+        return DOT_WARPS;
+    }
+}
+
+uint32_t dot_smem_bytes(DotKernel kind, int depth)
+{
+    switch (kind) {
+    case DotKernel::StagedK:
+        return (uint32_t)(DOT_WARPS * depth * (DOT_K_CHUNK_WORDS * 4 + 8));
+    case DotKernel::StagedB:
+        return (uint32_t)(DOT_WARPS * depth * (DOT_B_ROWS * DOT_B_CHUNK_WORDS * 4 + 8));
+    default:
+        return 0;
+    }
+}
+
+cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream)
+{
+    const int nb = p.batch;
+    if (kind == DotKernel::StagedK) {
+        if (nb == 1)
+            return launch_nb<1>(p, kind, L, stream);
+        if (nb == 2)
+            return launch_nb<2>(p, kind, L, stream);
+        return launch_nb<4>(p, kind, L, stream);  // 3 or 4
+    }
+    if (kind == DotKernel::StagedB)
+        return launch_nb<16>(p, kind, L, stream);
+    if (nb <= 1)
+        return launch_nb<1>(p, kind, L, stream);
+    if (nb <= 4)
+        return launch_nb<4>(p, kind, L, stream);
+    return launch_nb<16>(p, kind, L, stream);
+}
+
+cudaError_t launch_unpack(const int32_t *packed, int64_t n_words, float *out, const loom_launch &L,
+                          cudaStream_t stream)
+{
+    if (L.grid[0] == 0)
+        return cudaSuccess;
+    return launch_with(unpack_kernel, L, stream, packed, n_words, out);
+}
+
+}  // namespace loom

@@ -1,0 +1,96 @@
+// internal.h -- parameters and launchers shared between the host API layer
+// (loom_api.cu) and the kernel translation units.  Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <utility>
+#include <cuda_runtime.h>
+
+#include "../../include/loom.h"
+
+namespace loom {
+
+// ---- row sum -------------------------------------------------------------
+constexpr int RS_WARPS = 4;             // warps per CTA
+constexpr int RS_CHUNK_ELEMS = 1024;    // one staged chunk: 4 KiB of f32
+constexpr int RS_SLOT_ELEMS = 128;      // one warp-wide read: 32 lanes x float4
+constexpr int RS_DEFAULT_DEPTH = 4;
+
+struct RowSumParams {
+    const float *values;
+    int64_t num_units;    // segments
+    int64_t unit_stride;  // elements between segment starts
+    int32_t rows, lanes, tile;
+    const int32_t *counts;  // device counts, or NULL to use count_scalar
+    int32_t count_scalar;
+    const float *initial;   // device initial sums, or NULL to use initial_scalar
+    float initial_scalar;
+    int32_t *final_row, *tail_count;
+    float *full_sum, *tail_sum;
+    int32_t *error;         // device error word or NULL
+    int32_t depth;          // chunks in flight per warp (staged path)
+    int32_t units_per_warp;
+    uint64_t wait_ns;       // limit of each barrier wait
+    int32_t inject_stall;   // test hook: issue no copies (every wait runs out)
+};
+
+int row_sum_default_units_per_warp(int32_t rows, int32_t lanes);
+uint32_t row_sum_smem_bytes(bool staged, int depth);
+cudaError_t launch_row_sum(const RowSumParams &p, bool staged, const loom_launch &L,
+                           cudaStream_t stream);
+
+// ---- dequantised dot -----------------------------------------------------
+constexpr int DOT_WARPS = 4;
+constexpr int DOT_K_CHUNK_WORDS = 1024;   // lanes-across-k path: 4 KiB of one row
+constexpr int DOT_B_ROWS = 8;             // lanes-across-batch path: rows per warp
+constexpr int DOT_B_CHUNK_WORDS = 128;    // ... 512 B of each of those rows per chunk
+constexpr int DOT_MAX_BATCH_PER_PASS = 16;
+constexpr int DOT_DEFAULT_DEPTH = 4;
+
+struct DotParams {
+    const int32_t *w;      // [n_rows][k/4]
+    const float *scale_w;
+    const int32_t *x;      // [batch][k/4]
+    const float *scale_x;
+    int32_t n_rows, k_words, batch;  // batch of this pass (<= 16)
+    int32_t y_stride;      // elements between output rows (the full batch)
+    float *y;              // already offset to this pass's first vector
+    int32_t *acc;          // same layout as y, or NULL
+    int32_t *error;
+    int32_t depth;
+    uint64_t wait_ns;
+    int32_t inject_stall;
+};
+
+enum class DotKernel { StagedK, StagedB, Direct };
+
+DotKernel dot_select(bool aligned, int32_t k, int32_t batch_pass);
+uint32_t dot_smem_bytes(DotKernel kind, int depth);
+int dot_rows_per_cta(DotKernel kind);
+cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream);
+
+// ---- unpack ----------------------------------------------------------------
+constexpr int UNPACK_BLOCK = 256;
+cudaError_t launch_unpack(const int32_t *packed, int64_t n_words, float *out, const loom_launch &L,
+                          cudaStream_t stream);
+
+// Launch a kernel with the geometry of L (grid.x, block.x, dynamic smem).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_with(void (*kernel)(KArgs...), const loom_launch &L, cudaStream_t stream,
+                        Args &&...args)
+{
+    if (L.smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)L.smem_bytes);
+        if (e != cudaSuccess)
+            return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid[0], L.grid[1], L.grid[2]);
+    cfg.blockDim = dim3(L.block[0], L.block[1], L.block[2]);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace loom

@@ -1,0 +1,384 @@
+// loom_api.cu -- host side of libloom: argument validation, the launch
+// configuration routine and the extern "C" entry points of loom.h and
+// loom_tuning.h.
+//
+// The launch configuration follows the Loom pages ("Kernels and launch
+// configuration", sections "A kernel owns two signatures" and "Workload is
+// not workgroup count"): workload scalars alone decide the geometry, the
+// grid is the ceiling division of the workload by the units one CTA owns,
+// and every entry point launches with exactly the geometry this routine
+// returns, so the division lives in one place.
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+#include "../../include/loom_tuning.h"
+
+namespace loom {
+namespace {
+
+constexpr uint64_t DEFAULT_WAIT_NS = 1000000000ull;  // 1 s per barrier wait
+constexpr int64_t MAX_K = 131068;                   // 128*128*k < 2^31 and k % 4 == 0
+
+bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+
+int64_t ceil_div(int64_t n, int64_t d) { return (n + d - 1) / d; }
+
+void fill_launch(loom_launch *out, int64_t grid, uint32_t block, uint32_t smem, uint32_t units,
+                 uint32_t kernel)
+{
+    std::memset(out, 0, sizeof(*out));
+    out->grid[0] = (uint32_t)grid;
+    out->grid[1] = out->grid[2] = 1;
+    out->block[0] = block;
+    out->block[1] = out->block[2] = 1;
+    out->cluster[0] = out->cluster[1] = out->cluster[2] = 1;
+    out->subgroup_size = 32;
+    out->smem_bytes = smem;
+    out->units_per_cta = units;
+    out->kernel = kernel;
+}
+
+struct Tuning {
+    int depth;
+    int path;
+    int upw;
+    int stall;
+    uint64_t wait_ns;
+};
+
+loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
+{
+    out->depth = default_depth;
+    out->path = LOOM_PATH_AUTO;
+    out->upw = 0;
+    out->stall = 0;
+    out->wait_ns = DEFAULT_WAIT_NS;
+    if (!t)
+        return LOOM_OK;
+    if (t->depth < 0 || t->depth > LOOM_MAX_DEPTH || t->path < 0 || t->path > 2 ||
+        t->units_per_warp < 0 || t->units_per_warp > 32 || t->wait_ns < 0)
+        return LOOM_ERR_ARG;
+    if (t->depth)
+        out->depth = t->depth;
+    out->path = t->path;
+    out->upw = t->units_per_warp;
+    out->stall = t->inject_stall != 0;
+    if (t->wait_ns)
+        out->wait_ns = (uint64_t)t->wait_ns;
+    return LOOM_OK;
+}
+
+// ---- geometry of each op ----------------------------------------------------
+
+loom_status row_sum_geometry(int64_t num_segments, int64_t rows, int64_t lanes, bool staged,
+                             int depth, int upw, loom_launch *out)
+{
+    if (num_segments < 0 || rows < 0 || (lanes != 1 && lanes != 32) || rows * lanes >= (1ll << 31))
+        return LOOM_ERR_SHAPE;
+    if (depth < 1 || depth > LOOM_MAX_DEPTH || upw < 0 || upw > 32)
+        return LOOM_ERR_ARG;
+    if (upw == 0)
+        upw = row_sum_default_units_per_warp((int32_t)rows, (int32_t)lanes);
+    const int64_t per_cta = (int64_t)RS_WARPS * upw;
+    const int64_t grid = ceil_div(num_segments, per_cta);
+    if (grid > 0x7fffffff)
+        return LOOM_ERR_SHAPE;
+    fill_launch(out, grid, RS_WARPS * 32, row_sum_smem_bytes(staged, depth), (uint32_t)per_cta,
+                staged ? LOOM_KERNEL_ROWSUM_STAGED : LOOM_KERNEL_ROWSUM_DIRECT);
+    return LOOM_OK;
+}
+
+loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned, int depth,
+                         loom_launch *out)
+{
+    if (n_rows < 0 || n_rows > 0x7fffffff || k < 0 || k > MAX_K || (k % 4) != 0 || batch < 0 ||
+        batch > 0x7fffffff)
+        return LOOM_ERR_SHAPE;
+    if (depth < 1 || depth > LOOM_MAX_DEPTH)
+        return LOOM_ERR_ARG;
+    const int32_t pass = (int32_t)(batch < DOT_MAX_BATCH_PER_PASS ? batch : DOT_MAX_BATCH_PER_PASS);
+    const DotKernel kind = dot_select(aligned, (int32_t)k, pass);
+    const int rows_per_cta = dot_rows_per_cta(kind);
+    const int64_t grid = (batch == 0) ? 0 : ceil_div(n_rows, rows_per_cta);
+    const uint32_t id = kind == DotKernel::StagedK   ? LOOM_KERNEL_DOT_STAGED_K
+                        : kind == DotKernel::StagedB ? LOOM_KERNEL_DOT_STAGED_B
+                                                     : LOOM_KERNEL_DOT_DIRECT;
+    fill_launch(out, grid, DOT_WARPS * 32, dot_smem_bytes(kind, depth), (uint32_t)rows_per_cta, id);
+    return LOOM_OK;
+}
+
+// ---- row sums -------------------------------------------------------------
+
+loom_status row_sum_common(const float *values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                           int32_t lanes, const int32_t *counts, int32_t count_scalar,
+                           const float *initial, float initial_scalar, int32_t tile,
+                           int32_t *final_row, int32_t *tail_count, float *full_sum, float *tail_sum,
+                           int32_t *error, const loom_tuning *tuning, void *stream)
+{
+    if (num_segments < 0 || rows < 0 || (lanes != 1 && lanes != 32) ||
+        (int64_t)rows * lanes >= (1ll << 31) || tile < 1 || tile > 64 || seg_stride < 0)
+        return LOOM_ERR_SHAPE;
+    if (num_segments > 1 && seg_stride < (int64_t)rows * lanes)
+        return LOOM_ERR_SHAPE;
+    if (num_segments > 1 && seg_stride > 0 && num_segments - 1 > (INT64_MAX - rows * (int64_t)lanes) / seg_stride)
+        return LOOM_ERR_SHAPE;
+    Tuning t;
+    loom_status st = read_tuning(tuning, RS_DEFAULT_DEPTH, &t);
+    if (st != LOOM_OK)
+        return st;
+    if (num_segments == 0)
+        return LOOM_OK;
+    if (!values || !final_row || !tail_count || !full_sum || !tail_sum)
+        return LOOM_ERR_NULL;
+    if (misaligned(values, 4) || misaligned(counts, 4) || misaligned(initial, 4) ||
+        misaligned(final_row, 4) || misaligned(tail_count, 4) || misaligned(full_sum, 4) ||
+        misaligned(tail_sum, 4) || misaligned(error, 4))
+        return LOOM_ERR_ALIGN;
+
+    const bool can_stage = !misaligned(values, 16) && (seg_stride % 4 == 0 || num_segments == 1);
+    bool staged;
+    if (t.path == LOOM_PATH_STAGED) {
+        if (!can_stage)
+            return LOOM_ERR_ALIGN;
+        staged = true;
+    } else if (t.path == LOOM_PATH_DIRECT) {
+        staged = false;
+    } else {
+        staged = can_stage;
+    }
+    loom_launch L;
+    st = row_sum_geometry(num_segments, rows, lanes, staged, t.depth, t.upw, &L);
+    if (st != LOOM_OK)
+        return st;
+
+    RowSumParams p;
+    p.values = values;
+    p.num_units = num_segments;
+    p.unit_stride = seg_stride;
+    p.rows = rows;
+    p.lanes = lanes;
+    p.tile = tile;
+    p.counts = counts;
+    p.count_scalar = count_scalar;
+    p.initial = initial;
+    p.initial_scalar = initial_scalar;
+    p.final_row = final_row;
+    p.tail_count = tail_count;
+    p.full_sum = full_sum;
+    p.tail_sum = tail_sum;
+    p.error = error;
+    p.depth = t.depth;
+    p.units_per_warp = (int32_t)(L.units_per_cta / RS_WARPS);
+    p.wait_ns = t.wait_ns;
+    p.inject_stall = t.stall;
+    cudaError_t e = launch_row_sum(p, staged, L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LOOM_OK : LOOM_ERR_CUDA;
+}
+
+// ---- dequantised dot ------------------------------------------------------
+
+loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, int32_t k,
+                       const int32_t *x, const float *scale_x, int32_t batch, float *y, int32_t *acc,
+                       int32_t *error, const loom_tuning *tuning, void *stream)
+{
+    if (n_rows < 0 || batch < 0 || k < 0 || k > MAX_K || (k % 4) != 0)
+        return LOOM_ERR_SHAPE;
+    Tuning t;
+    loom_status st = read_tuning(tuning, DOT_DEFAULT_DEPTH, &t);
+    if (st != LOOM_OK)
+        return st;
+    if (n_rows == 0 || batch == 0)
+        return LOOM_OK;
+    if ((k > 0 && (!w || !x)) || !scale_w || !scale_x || !y)  // k == 0 reads no weights
+        return LOOM_ERR_NULL;
+    if (misaligned(w, 4) || misaligned(scale_w, 4) || misaligned(x, 4) || misaligned(scale_x, 4) ||
+        misaligned(y, 4) || misaligned(acc, 4) || misaligned(error, 4))
+        return LOOM_ERR_ALIGN;
+    const bool can_stage = !misaligned(w, 16) && !misaligned(x, 16) && (k % 16) == 0;
+    bool staged;
+    if (t.path == LOOM_PATH_STAGED) {
+        if (!can_stage)
+            return LOOM_ERR_ALIGN;
+        staged = true;
+    } else if (t.path == LOOM_PATH_DIRECT) {
+        staged = false;
+    } else {
+        staged = can_stage;
+    }
+    const int32_t kw = k / 4;
+    for (int32_t b0 = 0; b0 < batch; b0 += DOT_MAX_BATCH_PER_PASS) {
+        const int32_t nb = (batch - b0) < DOT_MAX_BATCH_PER_PASS ? (batch - b0) : DOT_MAX_BATCH_PER_PASS;
+        loom_launch L;
+        st = dot_geometry(n_rows, k, nb, staged, t.depth, &L);
+        if (st != LOOM_OK)
+            return st;
+        const DotKernel kind = dot_select(staged, k, nb);
+        DotParams p;
+        p.w = w;
+        p.scale_w = scale_w;
+        p.x = x + (int64_t)b0 * kw;
+        p.scale_x = scale_x + b0;
+        p.n_rows = n_rows;
+        p.k_words = kw;
+        p.batch = nb;
+        p.y_stride = batch;
+        p.y = y + b0;
+        p.acc = acc ? acc + b0 : nullptr;
+        p.error = error;
+        p.depth = t.depth;
+        p.wait_ns = t.wait_ns;
+        p.inject_stall = t.stall;
+        cudaError_t e = launch_dot(p, kind, L, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess)
+            return LOOM_ERR_CUDA;
+    }
+    return LOOM_OK;
+}
+
+}  // namespace
+}  // namespace loom
+
+using namespace loom;
+
+extern "C" {
+
+int32_t loom_abi_version(void) { return LOOM_ABI_VERSION; }
+
+const char *loom_status_string(int32_t status)
+{
+    switch (status) {
+    case LOOM_OK:
+        return "ok";
+    case LOOM_ERR_NULL:
+        return "a required pointer is NULL";
+    case LOOM_ERR_ALIGN:
+        return "a pointer is not aligned as required";
+    case LOOM_ERR_SHAPE:
+        return "a size, stride or tile is outside the supported range";
+    case LOOM_ERR_RANGE:
+        return "a count is outside [0, rows]";
+    case LOOM_ERR_CUDA:
+        return "the CUDA runtime refused the launch";
+    case LOOM_ERR_TIMEOUT:
+        return "a device wait ran out";
+    case LOOM_ERR_ARG:
+        return "invalid argument";
+    default:
+        return "unknown status";
+    }
+}
+
+loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_workload,
+                               loom_launch *out)
+{
+    if (!workload || !out)
+        return LOOM_ERR_NULL;
+    auto opt = [&](int i, int64_t dflt) { return n_workload > i ? workload[i] : dflt; };
+    switch (op) {
+    case LOOM_OP_I8_UNPACK: {
+        if (n_workload < 1)
+            return LOOM_ERR_ARG;
+        if (workload[0] < 0 || ceil_div(workload[0], UNPACK_BLOCK) > 0x7fffffff)
+            return LOOM_ERR_SHAPE;
+        fill_launch(out, ceil_div(workload[0], UNPACK_BLOCK), UNPACK_BLOCK, 0, UNPACK_BLOCK,
+                    LOOM_KERNEL_UNPACK);
+        return LOOM_OK;
+    }
+    case LOOM_OP_FULL_TILE_SUM:
+        if (n_workload < 2)
+            return LOOM_ERR_ARG;
+        return row_sum_geometry(1, workload[0], workload[1], opt(2, 1) != 0,
+                                (int)opt(3, RS_DEFAULT_DEPTH), 1, out);
+    case LOOM_OP_ROW_SUM_BATCHED:
+        if (n_workload < 3)
+            return LOOM_ERR_ARG;
+        return row_sum_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0,
+                                (int)opt(4, RS_DEFAULT_DEPTH), 0, out);
+    case LOOM_OP_I8_DEQUANT_DOT:
+        if (n_workload < 3)
+            return LOOM_ERR_ARG;
+        return dot_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0,
+                            (int)opt(4, DOT_DEFAULT_DEPTH), out);
+    default:
+        return LOOM_ERR_ARG;
+    }
+}
+
+loom_status loom_full_tile_sum(const float *d_values, int32_t rows, int32_t lanes, int32_t count,
+                               float initial, int32_t tile_size, int32_t *d_final_row,
+                               int32_t *d_tail_count, float *d_full_sum, float *d_tail_sum, void *stream)
+{
+    if (rows < 0 || (lanes != 1 && lanes != 32) || (int64_t)rows * lanes >= (1ll << 31) ||
+        tile_size < 1 || tile_size > 64)
+        return LOOM_ERR_SHAPE;
+    if (count < 0 || count > rows)
+        return LOOM_ERR_RANGE;
+    loom_tuning t = {};
+    t.units_per_warp = 1;
+    return row_sum_common(d_values, 1, (int64_t)rows * lanes, rows, lanes, nullptr, count, nullptr,
+                          initial, tile_size, d_final_row, d_tail_count, d_full_sum, d_tail_sum,
+                          nullptr, &t, stream);
+}
+
+loom_status loom_row_sum_batched(const float *d_values, int64_t num_segments, int64_t seg_stride,
+                                 int32_t rows, int32_t lanes, const int32_t *d_counts,
+                                 const float *d_initial, int32_t tile_size, int32_t *d_final_row,
+                                 int32_t *d_tail_count, float *d_full_sum, float *d_tail_sum,
+                                 int32_t *d_error, void *stream)
+{
+    return loom_row_sum_batched_ex(d_values, num_segments, seg_stride, rows, lanes, d_counts,
+                                   d_initial, tile_size, d_final_row, d_tail_count, d_full_sum,
+                                   d_tail_sum, d_error, nullptr, stream);
+}
+
+loom_status loom_row_sum_batched_ex(const float *d_values, int64_t num_segments, int64_t seg_stride,
+                                    int32_t rows, int32_t lanes, const int32_t *d_counts,
+                                    const float *d_initial, int32_t tile_size, int32_t *d_final_row,
+                                    int32_t *d_tail_count, float *d_full_sum, float *d_tail_sum,
+                                    int32_t *d_error, const loom_tuning *tuning, void *stream)
+{
+    if (num_segments > 0 && !d_counts)
+        return LOOM_ERR_NULL;
+    return row_sum_common(d_values, num_segments, seg_stride, rows, lanes, d_counts, 0, d_initial, 0.f,
+                          tile_size, d_final_row, d_tail_count, d_full_sum, d_tail_sum, d_error,
+                          tuning, stream);
+}
+
+loom_status loom_i8_dequant_dot(const int32_t *d_w_packed, const float *d_scale_w, int32_t n_rows,
+                                int32_t k, const int32_t *d_x_packed, const float *d_scale_x,
+                                int32_t batch, float *d_y, int32_t *d_acc, void *stream)
+{
+    return dot_common(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y, d_acc,
+                      nullptr, nullptr, stream);
+}
+
+loom_status loom_i8_dequant_dot_ex(const int32_t *d_w_packed, const float *d_scale_w, int32_t n_rows,
+                                   int32_t k, const int32_t *d_x_packed, const float *d_scale_x,
+                                   int32_t batch, float *d_y, int32_t *d_acc, int32_t *d_error,
+                                   const loom_tuning *tuning, void *stream)
+{
+    return dot_common(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y, d_acc,
+                      d_error, tuning, stream);
+}
+
+loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)
+{
+    if (n_words < 0)
+        return LOOM_ERR_SHAPE;
+    loom_launch L;
+    const int64_t wl[1] = {n_words};
+    loom_status st = loom_launch_config(LOOM_OP_I8_UNPACK, wl, 1, &L);
+    if (st != LOOM_OK)
+        return st;
+    if (n_words == 0)
+        return LOOM_OK;
+    if (!d_packed || !d_out)
+        return LOOM_ERR_NULL;
+    if (misaligned(d_packed, 4) || misaligned(d_out, 4))
+        return LOOM_ERR_ALIGN;
+    cudaError_t e = launch_unpack(d_packed, n_words, d_out, L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LOOM_OK : LOOM_ERR_CUDA;
+}
+
+}  // extern "C"

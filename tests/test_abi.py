@@ -1,0 +1,175 @@
+"""The C ABI on a machine without a GPU: symbols, launch arithmetic, validation.
+
+No call here reaches the device: every entry-point call is rejected by host
+validation (or is empty work) before anything is launched.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def loom():
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_dequant_dot_gb300 as m
+    return m
+
+
+def _declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^\s*(?:loom_status|const char \*|int32_t)\s*(loom_\w+)\(", text,
+                                    re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported(loom):
+    declared = _declared_functions()
+    assert declared == set(loom.EXPORTS)
+    nm = subprocess.run(["nm", "-D", "--defined-only", loom.LIB_PATH], capture_output=True, text=True)
+    exported = set(re.findall(r"\sT\s(loom_\w+)$", nm.stdout, re.M))
+    assert declared <= exported
+    for name in declared:
+        assert getattr(loom.library(), name)
+
+
+def test_version_and_strings(loom):
+    assert loom.loom_abi_version() == 1
+    for st in range(-7, 1):
+        assert loom.loom_status_string(st)
+    assert loom.loom_status_string(-99) == "unknown status"
+
+
+def test_unpack_launch_matches_page_example(loom):
+    # 1009 elements in 256-wide workgroups -> 4 workgroups
+    # (page "Kernels and launch configuration", "Workload is not workgroup count").
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_UNPACK, [1009])
+    assert L["grid"] == (4, 1, 1) and L["block"] == (256, 1, 1) and L["cluster"] == (1, 1, 1)
+    for n in (0, 1, 255, 256, 257, 1009, 10**9):
+        L = loom.loom_launch_config(loom.LOOM_OP_I8_UNPACK, [n])
+        assert L["grid"][0] == oracle.workgroups(n, 256)
+
+
+@pytest.mark.parametrize("rows,lanes", [(63, 32), (16384, 1), (1, 32), (1000, 1)])
+def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
+    for s in (0, 1, 15, 16, 17, 1000, 65536, 65537):
+        L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes])
+        assert L["grid"][0] == oracle.workgroups(s, L["units_per_cta"])
+        assert L["block"] == (128, 1, 1) and L["subgroup_size"] == 32
+        assert L["kernel"] == loom.LOOM_KERNEL_ROWSUM_STAGED
+        d = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes, 0])
+        assert d["kernel"] == loom.LOOM_KERNEL_ROWSUM_DIRECT and d["smem_bytes"] == 0
+    # one stage of 4 KiB plus one barrier per warp and depth
+    for depth in range(1, 5):
+        L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [10, rows, lanes, 1, depth])
+        assert L["smem_bytes"] == 4 * depth * (4096 + 8)
+
+
+def test_dot_launch(loom):
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 1])
+    assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_K
+    assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 16])
+    assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_B
+    assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16388, 16])
+    assert L["kernel"] == loom.LOOM_KERNEL_DOT_DIRECT
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [77, 64, 0])
+    assert L["grid"][0] == 0
+
+
+def test_launch_config_errors(loom):
+    with pytest.raises(loom.LoomError) as e:
+        loom.loom_launch_config(99, [1])
+    assert e.value.status == loom.LOOM_ERR_ARG
+    with pytest.raises(loom.LoomError) as e:
+        loom.loom_launch_config(loom.LOOM_OP_I8_UNPACK, [-1])
+    assert e.value.status == loom.LOOM_ERR_SHAPE
+    for bad in ([5, 63, 7], [5, -1, 32], [5, 1 << 27, 32]):
+        with pytest.raises(loom.LoomError) as e:
+            loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, bad)
+        assert e.value.status == loom.LOOM_ERR_SHAPE
+    with pytest.raises(loom.LoomError) as e:
+        loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [5, 63, 32, 1, 9])
+    assert e.value.status == loom.LOOM_ERR_ARG
+    for bad in ([5, 6, 1], [5, 131072, 1], [-1, 16, 1]):
+        with pytest.raises(loom.LoomError) as e:
+            loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, bad)
+        assert e.value.status == loom.LOOM_ERR_SHAPE
+
+
+A = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+def test_row_sum_validation(loom):
+    lib = loom.library()
+    call = lambda values, S, stride, rows, lanes, counts, tile, outs=(A, A, A, A): \
+        lib.loom_row_sum_batched(values, S, stride, rows, lanes, counts, None, tile, *outs, None, None)
+    assert call(None, 0, 0, 63, 32, None, 8) == loom.LOOM_OK           # empty work
+    assert call(None, 1, 2016, 63, 32, A, 8) == loom.LOOM_ERR_NULL
+    assert call(A, 1, 2016, 63, 32, None, 8) == loom.LOOM_ERR_NULL
+    assert call(A, 1, 2016, 63, 32, A, 8, (A, None, A, A)) == loom.LOOM_ERR_NULL
+    assert call(A + 2, 1, 2016, 63, 32, A, 8) == loom.LOOM_ERR_ALIGN
+    assert call(A, 1, 2016, 63, 32, A + 1, 8) == loom.LOOM_ERR_ALIGN
+    assert call(A, 1, 2016, 63, 16, A, 8) == loom.LOOM_ERR_SHAPE        # lanes
+    assert call(A, 1, 2016, 63, 32, A, 0) == loom.LOOM_ERR_SHAPE        # tile
+    assert call(A, 1, 2016, 63, 32, A, 65) == loom.LOOM_ERR_SHAPE
+    assert call(A, 2, 2000, 63, 32, A, 8) == loom.LOOM_ERR_SHAPE        # overlapping segments
+    assert call(A, -1, 2016, 63, 32, A, 8) == loom.LOOM_ERR_SHAPE
+    assert call(A, 1, 2016, -1, 32, A, 8) == loom.LOOM_ERR_SHAPE
+    assert call(A, 1, 1 << 26, 1 << 26, 32, A, 8) == loom.LOOM_ERR_SHAPE  # rows*lanes >= 2^31
+    t = loom.make_tuning(depth=9)
+    st = lib.loom_row_sum_batched_ex(A, 1, 2016, 63, 32, A, None, 8, A, A, A, A, None,
+                                     loom.ctypes.byref(t), None)
+    assert st == loom.LOOM_ERR_ARG
+    t = loom.make_tuning(path=loom.LOOM_PATH_STAGED)
+    st = lib.loom_row_sum_batched_ex(A + 4, 1, 2016, 63, 32, A, None, 8, A, A, A, A, None,
+                                     loom.ctypes.byref(t), None)
+    assert st == loom.LOOM_ERR_ALIGN
+
+
+def test_full_tile_sum_validation(loom):
+    lib = loom.library()
+    f = lambda values, rows, lanes, count, tile, fr=A: lib.loom_full_tile_sum(
+        values, rows, lanes, count, 0.5, tile, fr, A, A, A, None)
+    assert f(A, 63, 32, 64, 8) == loom.LOOM_ERR_RANGE
+    assert f(A, 63, 32, -1, 8) == loom.LOOM_ERR_RANGE
+    assert f(None, 63, 32, 61, 8) == loom.LOOM_ERR_NULL
+    assert f(A, 63, 32, 61, 8, None) == loom.LOOM_ERR_NULL
+    assert f(A, 63, 8, 61, 8) == loom.LOOM_ERR_SHAPE
+    assert f(A + 1, 63, 32, 61, 8) == loom.LOOM_ERR_ALIGN
+
+
+def test_dot_validation(loom):
+    lib = loom.library()
+    d = lambda w, n, k, x, b, y=A, acc=None: lib.loom_i8_dequant_dot(w, A, n, k, x, A, b, y, acc, None)
+    assert d(None, 0, 64, None, 4) == loom.LOOM_OK       # no rows
+    assert d(None, 4, 64, None, 0) == loom.LOOM_OK       # empty batch
+    assert d(None, 4, 64, A, 4) == loom.LOOM_ERR_NULL
+    assert d(A, 4, 64, A, 4, None) == loom.LOOM_ERR_NULL
+    assert d(A, 4, 62, A, 4) == loom.LOOM_ERR_SHAPE       # k % 4
+    assert d(A, 4, 131072, A, 4) == loom.LOOM_ERR_SHAPE   # |acc| could reach 2^31
+    assert d(A, -4, 64, A, 4) == loom.LOOM_ERR_SHAPE
+    assert d(A + 2, 4, 64, A, 4) == loom.LOOM_ERR_ALIGN
+    assert d(A, 4, 64, A, 4, A, A + 3) == loom.LOOM_ERR_ALIGN
+
+
+def test_unpack_validation(loom):
+    lib = loom.library()
+    assert lib.loom_i8_unpack(None, 0, None, None) == loom.LOOM_OK
+    assert lib.loom_i8_unpack(None, 5, A, None) == loom.LOOM_ERR_NULL
+    assert lib.loom_i8_unpack(A, -1, A, None) == loom.LOOM_ERR_SHAPE
+    assert lib.loom_i8_unpack(A + 2, 5, A, None) == loom.LOOM_ERR_ALIGN

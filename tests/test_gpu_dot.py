@@ -1,0 +1,179 @@
+"""GPU parity of the packed-int8 dequantised dot product and the unpack kernel.
+
+Integer accumulators must match the oracle bit for bit; y must be within a
+relative 1e-5 of the fp64 oracle (the kernel's three f32 roundings give at
+most about 2e-7).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import assert_rel, check_guard, guarded, loom_module, require_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+Y_REL = 1e-5
+Y_TIGHT = 4 * 2.0**-24   # three roundings: sw*sx, (float)acc, the product
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = require_gpu()
+    return torch, loom_module()
+
+
+def packed(a: np.ndarray) -> np.ndarray:
+    """int8 [r][k] -> int32 [r][k/4]: the same bytes read as little-endian words."""
+    a = np.ascontiguousarray(a, dtype=np.int8)
+    if a.shape[1] == 0:
+        return np.zeros((a.shape[0], 0), np.int32)
+    return np.ascontiguousarray(a.view("<i4"), dtype=np.int32)
+
+
+def run_dot(loom, torch, d, tuning=None, error=None, want_acc=True):
+    w = to_dev(packed(d["w"]), torch)
+    x = to_dev(packed(d["x"]), torch)
+    sw, sx = to_dev(d["scale_w"], torch), to_dev(d["scale_x"], torch)
+    n, k = d["w"].shape
+    b = d["x"].shape[0]
+    if tuning is None and error is None:
+        y, acc = loom.loom_i8_dequant_dot(w, sw, n, k, x, sx, b, want_acc=want_acc)
+    else:
+        y, acc = loom.loom_i8_dequant_dot_ex(w, sw, n, k, x, sx, b, want_acc=want_acc,
+                                             tuning=tuning, error=error)
+    torch.cuda.synchronize()
+    return y.cpu().numpy(), (acc.cpu().numpy() if acc is not None else None)
+
+
+def check(d, y, acc, what, rows=None):
+    want_acc, want_y = oracle.i8_dequant_dot(d["w"], d["scale_w"], d["x"], d["scale_x"], threads=8)
+    assert np.array_equal(acc.astype(np.int64), want_acc), what + ": acc"
+    assert_rel(y, want_y, Y_REL, what + ": y")
+    assert_rel(y, want_y, Y_TIGHT, what + ": y (three roundings)")
+
+
+def small(n, k, b, seed):
+    return synth.dequant_batched(n_rows=n, k=k, batch=b, seed=seed)
+
+
+@pytest.mark.parametrize("n,k,b", [(1, 16, 1), (37, 1040, 1), (37, 1040, 2), (37, 1040, 3),
+                                   (64, 4096, 4), (37, 1040, 5), (33, 4112, 16), (9, 512, 17),
+                                   (70, 2048, 33), (37, 0, 3), (5, 16, 16)])
+def test_dot_small(env, n, k, b):
+    torch, loom = env
+    d = small(n, k, b, seed=n * 1000 + k + b)
+    y, acc = run_dot(loom, torch, d)
+    check(d, y, acc, f"{n}x{k}x{b}")
+
+
+@pytest.mark.parametrize("k", [4, 12, 20, 1044])
+def test_dot_k_not_multiple_of_16_takes_direct(env, k):
+    torch, loom = env
+    for b in (1, 4, 16):
+        d = small(19, k, b, seed=k * 7 + b)
+        y, acc = run_dot(loom, torch, d)
+        check(d, y, acc, f"k={k} b={b}")
+
+
+def test_dot_extremes(env):
+    torch, loom = env
+    k = 16384
+    w = np.empty((4, k), np.int8)
+    w[0], w[1], w[2] = -128, 127, 0
+    w[3, 0::2], w[3, 1::2] = 100, -100
+    x = np.empty((2, k), np.int8)
+    x[0], x[1] = -128, 127
+    d = dict(w=w, x=x, scale_w=np.ones(4, np.float32), scale_x=np.array([1.0, 0.5], np.float32))
+    y, acc = run_dot(loom, torch, d)
+    assert acc[0, 0] == 2**28 and acc[1, 0] == -127 * 128 * k and acc[0, 1] == -128 * 127 * k
+    assert acc[2].tolist() == [0, 0] and acc[3].tolist() == [0, 0]
+    check(d, y, acc, "extremes")
+
+
+def test_dot_path_and_depth_invariance(env):
+    torch, loom = env
+    for b in (1, 16):
+        d = small(129, 8192, b, seed=31 + b)
+        ref_y, ref_acc = run_dot(loom, torch, d)
+        check(d, ref_y, ref_acc, f"b={b}")
+        for depth in (1, 2, 3, 4):
+            t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_STAGED)
+            y, acc = run_dot(loom, torch, d, tuning=t)
+            assert np.array_equal(acc, ref_acc) and np.array_equal(y.view(np.int32), ref_y.view(np.int32))
+        y, acc = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_DIRECT))
+        assert np.array_equal(acc, ref_acc) and np.array_equal(y.view(np.int32), ref_y.view(np.int32))
+
+
+def test_dot_guard_bands(env):
+    torch, loom = env
+    n, k, b = 35, 2048, 5
+    d = small(n, k, b, seed=77)
+    ybuf, y = guarded(torch, n * b, torch.float32)
+    abuf, acc = guarded(torch, n * b, torch.int32)
+    loom.loom_i8_dequant_dot(to_dev(packed(d["w"]), torch), to_dev(d["scale_w"], torch), n, k,
+                             to_dev(packed(d["x"]), torch), to_dev(d["scale_x"], torch), b,
+                             y=y, acc=acc)
+    torch.cuda.synchronize()
+    check_guard(ybuf, n * b)
+    check_guard(abuf, n * b)
+    check(d, y.cpu().numpy().reshape(n, b), acc.cpu().numpy().reshape(n, b), "guarded")
+
+
+def test_dot_without_acc_output(env):
+    torch, loom = env
+    d = small(40, 1024, 16, seed=3)
+    y, acc = run_dot(loom, torch, d, want_acc=False)
+    assert acc is None
+    _, want_y = oracle.i8_dequant_dot(d["w"], d["scale_w"], d["x"], d["scale_x"])
+    assert_rel(y, want_y, Y_REL, "y only")
+
+
+def test_dot_injected_stall(env):
+    torch, loom = env
+    for b in (1, 16):
+        d = small(64, 4096, b, seed=5 + b)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000, path=loom.LOOM_PATH_STAGED)
+        y, acc = run_dot(loom, torch, d, tuning=t, error=err)
+        assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
+        assert np.isnan(y).all()
+        y, acc = run_dot(loom, torch, d)
+        check(d, y, acc, "after timeout")
+
+
+@pytest.fixture(scope="module")
+def weights():
+    return synth.dequant_weights()
+
+
+def test_gemv_full_workload(env, weights):
+    torch, loom = env
+    d = synth.dequant_gemv()
+    y, acc = run_dot(loom, torch, d)
+    check(d, y, acc, "8192 x 16384 x 1")
+
+
+def test_batched_full_workload(env, weights):
+    torch, loom = env
+    d = synth.dequant_batched()
+    y, acc = run_dot(loom, torch, d)
+    check(d, y, acc, "8192 x 16384 x 16")
+
+
+def test_unpack_every_byte_and_over_dispatch(env):
+    torch, loom = env
+    n = 1009  # four CTAs of 256; the last runs 15 idle invocations
+    words = synth.splitmix64(2024, 0, n).astype(np.uint32)
+    words[:256] = np.arange(256, dtype=np.uint32) * 0x01010101  # every byte in every position
+    buf, out = guarded(torch, 4 * n, torch.float32)
+    loom.loom_i8_unpack(to_dev(words.view(np.int32), torch), n, out)
+    torch.cuda.synchronize()
+    check_guard(buf, 4 * n)
+    got = out.cpu().numpy()
+    want = np.array([oracle.unpack_word(int(w)) for w in words], dtype=np.float32).reshape(-1)
+    assert np.array_equal(got, want)
+    # unaligned output (4-byte only) uses scalar stores, same values
+    ubuf = torch.full((4 * n + 1,), float("nan"), device="cuda")
+    loom.loom_i8_unpack(to_dev(words.view(np.int32), torch), n, ubuf[1:])
+    torch.cuda.synchronize()
+    assert np.array_equal(ubuf[1:].cpu().numpy(), want) and np.isnan(ubuf[0].item())
