@@ -54,9 +54,12 @@ typedef enum loom_status {
 
 typedef enum loom_op {
     LOOM_OP_I8_UNPACK = 0,       /* workload {n_words} */
-    LOOM_OP_FULL_TILE_SUM = 1,   /* workload {rows, lanes} */
-    LOOM_OP_ROW_SUM_BATCHED = 2, /* workload {num_segments, rows, lanes, staged (0/1), depth} */
-    LOOM_OP_I8_DEQUANT_DOT = 3   /* workload {n_rows, k, batch, staged (0/1), depth} */
+    LOOM_OP_FULL_TILE_SUM = 1,   /* workload {rows, lanes, staged (0/1), depth, warps_per_cta,
+                                    chunk_bytes} */
+    LOOM_OP_ROW_SUM_BATCHED = 2, /* workload {num_segments, rows, lanes, staged (0/1), depth,
+                                    warps_per_cta, units_per_warp, chunk_bytes} */
+    LOOM_OP_I8_DEQUANT_DOT = 3   /* workload {n_rows, k, batch, staged (0/1), depth,
+                                    warps_per_cta, rows_per_warp} */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
@@ -76,8 +79,8 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_UNPACK 1
 #define LOOM_KERNEL_ROWSUM_STAGED 2 /* bulk-copy read-ahead ring per warp */
 #define LOOM_KERNEL_ROWSUM_DIRECT 3 /* plain loads (unaligned inputs) */
-#define LOOM_KERNEL_DOT_STAGED_K 4  /* lanes across k, batch <= 4 */
-#define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 4 */
+#define LOOM_KERNEL_DOT_STAGED_K 4  /* lanes across k, batch <= 2 */
+#define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 2 */
 #define LOOM_KERNEL_DOT_DIRECT 6    /* plain loads (unaligned or k % 16 != 0) */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp). */
@@ -89,7 +92,9 @@ typedef struct loom_launch {
  * not workgroup count": the workload scalars alone determine the grid by
  * ceiling division; for LOOM_OP_I8_UNPACK 1009 words give 4 CTAs of 256.
  * `workload` holds `n_workload` scalars as listed for each loom_op; trailing
- * optional entries (staged, depth) default to 1 and the library default.
+ * optional entries may be left out: staged defaults to 1, the schedule
+ * entries (depth, warps_per_cta, units/rows per warp, chunk_bytes) to the
+ * library's defaults (also selected by 0).
  * Errors: NULL out/workload -> LOOM_ERR_NULL; unknown op or too few entries
  * -> LOOM_ERR_ARG; negative or unsupported sizes -> LOOM_ERR_SHAPE.
  */

@@ -25,7 +25,11 @@ extern "C" {
 typedef struct loom_tuning {
     int32_t depth;          /* staged chunks in flight per warp, 1..LOOM_MAX_DEPTH; 0 = default */
     int32_t path;           /* LOOM_PATH_* */
-    int32_t units_per_warp; /* row sums: segments per warp, 1..32; 0 = default */
+    int32_t units_per_warp; /* row sums: segments per warp, 1..32; dot: rows per warp
+                               of the batch <= 2 kernel, 1, 2 or 4; 0 = default */
+    int32_t warps_per_cta;  /* 1, 2, 4 or 8; 0 = default */
+    int32_t chunk_bytes;    /* row sums: bytes per staged chunk, a multiple of 512 in
+                               [512, 32768]; 0 = default */
     int32_t inject_stall;   /* fault test: issue no bulk copies, so every staged wait runs
                                out after wait_ns; results become NaN, the error word gets
                                LOOM_DEVERR_TIMEOUT, and the device stays usable */

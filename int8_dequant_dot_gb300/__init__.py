@@ -75,7 +75,8 @@ class loom_launch(ctypes.Structure):
 
 class loom_tuning(ctypes.Structure):
     _fields_ = [("depth", ctypes.c_int32), ("path", ctypes.c_int32),
-                ("units_per_warp", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
+                ("units_per_warp", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
+                ("chunk_bytes", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
                 ("wait_ns", ctypes.c_int64)]
 
 
@@ -195,9 +196,10 @@ def loom_row_sum_batched(values, num_segments: int, seg_stride: int, rows: int, 
 
 
 def make_tuning(depth: int = 0, path: int = LOOM_PATH_AUTO, units_per_warp: int = 0,
-                inject_stall: bool = False, wait_ns: int = 0) -> loom_tuning:
-    return loom_tuning(int(depth), int(path), int(units_per_warp), int(bool(inject_stall)),
-                       int(wait_ns))
+                warps_per_cta: int = 0, chunk_bytes: int = 0, inject_stall: bool = False,
+                wait_ns: int = 0) -> loom_tuning:
+    return loom_tuning(int(depth), int(path), int(units_per_warp), int(warps_per_cta),
+                       int(chunk_bytes), int(bool(inject_stall)), int(wait_ns))
 
 
 def loom_row_sum_batched_ex(values, num_segments: int, seg_stride: int, rows: int, lanes: int,

@@ -139,8 +139,130 @@ struct DW {
         }
     }
 
+    // Add another double word (h, l): TwoSum on the high parts, low parts summed.
+    __device__ __forceinline__ void add_dw(float h, float l)
+    {
+        const float s = __fadd_rn(hi, h);
+        const float bp = __fsub_rn(s, hi);
+        const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(h, bp));
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, l), e);
+    }
+
     __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
 };
+
+// ---------------------------------------------------------------------------
+// Two independent double-word accumulators advanced together with packed
+// f32x2 instructions (sm_100 and later): the same TwoSum steps as DW, each
+// instruction working on two lanes of a 64-bit register pair.  Every packed
+// operation rounds each half exactly as the scalar instruction would, so a
+// DW2 gives the same bits as two DW accumulators fed the same values.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pack2(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t r, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+struct DW2 {
+    uint64_t hi;
+    uint64_t lo;
+
+    __device__ __forceinline__ void add(uint64_t x)
+    {
+        const uint64_t s = add2(hi, x);
+        const uint64_t bp = sub2(s, hi);
+        const uint64_t e = add2(sub2(hi, sub2(s, bp)), sub2(x, bp));
+        hi = s;
+        lo = add2(lo, e);
+    }
+
+    // Add another packed double word, half by half (TwoSum on the high parts,
+    // low parts summed), as DW::add_dw does for one half.
+    __device__ __forceinline__ void add_dw(uint64_t h, uint64_t l)
+    {
+        const uint64_t s = add2(hi, h);
+        const uint64_t bp = sub2(s, hi);
+        const uint64_t e = add2(sub2(hi, sub2(s, bp)), sub2(h, bp));
+        hi = s;
+        lo = add2(add2(lo, l), e);
+    }
+
+    // The packed double word of lane (lane ^ m).
+    __device__ __forceinline__ DW2 shfl_xor(int m) const
+    {
+        float h0, h1, l0, l1;
+        unpack2(hi, h0, h1);
+        unpack2(lo, l0, l1);
+        return DW2{pack2(__shfl_xor_sync(FULL_MASK, h0, m), __shfl_xor_sync(FULL_MASK, h1, m)),
+                   pack2(__shfl_xor_sync(FULL_MASK, l0, m), __shfl_xor_sync(FULL_MASK, l1, m))};
+    }
+
+    __device__ __forceinline__ void add_dw(const DW2 &o) { add_dw(o.hi, o.lo); }
+
+    // Butterfly over the warp (lane ^ 16 .. lane ^ 1) of both halves at once;
+    // as for DW, every lane ends with identical bits.
+    __device__ __forceinline__ void warp_allreduce()
+    {
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1)
+            add_dw(shfl_xor(m));
+    }
+};
+
+__device__ __forceinline__ DW2 select(bool c, const DW2 &a, const DW2 &b)
+{
+    return DW2{c ? a.hi : b.hi, c ? a.lo : b.lo};
+}
+
+// The butterfly of DW2::warp_allreduce applied to four values a, b, c, d at
+// once.  At the first level the lanes with bit 4 clear keep (a, b) and the
+// others keep (c, d), each sending its partner the pair it drops; at the
+// second level bit 3 picks one of the two; the last three levels are the
+// plain butterfly.  Every partial is formed from the same operands as in
+// warp_allreduce (TwoSum and the low-part sum are symmetric in their
+// operands), so lane l ends with exactly the bits warp_allreduce would give
+// for value (l >> 3) & 3 -- a for lanes 0-7, b for 8-15, c for 16-23, d for
+// 24-31 -- at about a third of the shuffles and additions.
+__device__ __forceinline__ DW2 warp_allreduce4(const DW2 &a, const DW2 &b, const DW2 &c, const DW2 &d,
+                                               int lane)
+{
+    const bool upper = (lane & 16) != 0;
+    DW2 k1 = select(upper, c, a);
+    DW2 k2 = select(upper, d, b);
+    const DW2 r1 = select(upper, a, c).shfl_xor(16);
+    const DW2 r2 = select(upper, b, d).shfl_xor(16);
+    k1.add_dw(r1);
+    k2.add_dw(r2);
+    const bool odd = (lane & 8) != 0;
+    DW2 k = select(odd, k2, k1);
+    k.add_dw(select(odd, k1, k2).shfl_xor(8));
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1)
+        k.add_dw(k.shfl_xor(m));
+    return k;
+}
 
 __device__ __forceinline__ int32_t warp_sum_i32(int32_t v)
 {

@@ -15,10 +15,10 @@
 //  * Weights stream once through HBM.  Each warp owns its rows and a private
 //    ring of `depth` shared-memory stages filled by bulk copies (the
 //    read-ahead queue); activations are small and stay in L1/L2.
-//  * batch <= 4 ("lanes across k"): one row per unit; every lane takes one
-//    16-byte group of the row per 512-byte slot, dp4a against the matching
-//    activation words, and the warp sums its lanes at the end of the row.
-//  * batch > 4 ("lanes across the batch"): eight rows per unit; lane b of
+//  * batch <= 2 ("lanes across k"): every lane takes one 16-byte group of a
+//    row per 512-byte slot, dp4a against the matching activation words held
+//    in registers for several rows, and the warp sums its lanes per row.
+//  * batch > 2 ("lanes across the batch"): eight rows per unit; lane b of
 //    each half-warp owns vector b and keeps a slice of its activations in
 //    registers, reused for all eight rows; weight words are read from the
 //    stage as broadcasts, and the two half-warps split the k range.
@@ -107,20 +107,26 @@ struct Ring {
 };
 
 // ---------------------------------------------------------------------------
-// batch <= 4: lanes across k.  Unit = one row; rows_per_warp consecutive rows.
+// batch <= 2: lanes across k.  A warp owns RPW consecutive rows and walks k in
+// chunks of DOT_K_CHUNK_WORDS words; for each chunk it holds the activation
+// words of its lanes in registers (the next chunk's are fetched while the
+// current one is used) and streams that chunk of every row through the ring,
+// so each activation word is loaded once per RPW rows.
+// Lane l takes words 4l..4l+3 of every 128-word slot; each row's partial dot
+// products are summed across the warp at the end.
 // ---------------------------------------------------------------------------
-constexpr int K_ROWS_PER_WARP = 4;
-
-template <int NB>
-__global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_k_kernel(const DotParams p)
+template <int NB, int RPW>
+__global__ void __launch_bounds__(256) dot_staged_k_kernel(const DotParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int S = DOT_K_CHUNK_WORDS / 128;  // slots per chunk
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int32_t r0 = (blockIdx.x * DOT_WARPS + warp) * K_ROWS_PER_WARP;
+    const int warps = blockDim.x >> 5;
+    const int32_t r0 = (int32_t)(((int64_t)blockIdx.x * warps + warp) * RPW);
     if (r0 >= p.n_rows)
         return;
-    const int n = min(K_ROWS_PER_WARP, p.n_rows - r0);
+    const int n = min(RPW, p.n_rows - r0);
     const int32_t kw = p.k_words;
     const int32_t nchunks = (kw + DOT_K_CHUNK_WORDS - 1) / DOT_K_CHUNK_WORDS;
     const int D = p.depth;
@@ -130,24 +136,24 @@ __global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_k_kernel(const DotP
     ring.depth = D;
     ring.stage_bytes = stage_bytes;
     ring.data0 = dev::smem_u32(smem) + warp * D * stage_bytes;
-    ring.bar0 = dev::smem_u32(smem) + DOT_WARPS * D * stage_bytes + warp * D * 8;
+    ring.bar0 = dev::smem_u32(smem) + warps * D * stage_bytes + warp * D * 8;
     ring.init(lane);
     const uint64_t policy = dev::l2_evict_first_policy();
-    const int32_t total = n * nchunks;
+    const int32_t total = n * nchunks;   // copy t: chunk t / n of row t % n
 
-    int pchunk = 0;  // flattened (row, chunk) index of the next copy
+    int pt = 0;
     auto produce = [&]() {
-        if (pchunk >= total)
+        if (pt >= total)
             return;
-        const int row = pchunk / nchunks;
-        const int32_t off = (pchunk - row * nchunks) * DOT_K_CHUNK_WORDS;
+        const int j = pt / n;
+        const int r = pt - j * n;
+        const int32_t off = j * DOT_K_CHUNK_WORDS;
         if (lane == 0 && !p.inject_stall) {
             const uint32_t bytes = (uint32_t)min(DOT_K_CHUNK_WORDS, kw - off) * 4u;
             dev::mbar_arrive_expect_tx(ring.pbar(), bytes);
-            dev::bulk_g2s(ring.pstage(), p.w + (int64_t)(r0 + row) * kw + off, bytes, ring.pbar(),
-                          policy);
+            dev::bulk_g2s(ring.pstage(), p.w + (int64_t)(r0 + r) * kw + off, bytes, ring.pbar(), policy);
         }
-        ++pchunk;
+        ++pt;
         ring.pnext();
     };
     for (int s = 0; s < D; ++s)
@@ -160,45 +166,76 @@ __global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_k_kernel(const DotP
         x4[b] = reinterpret_cast<const int4 *>(p.x + (int64_t)(b < p.batch ? b : 0) * kw);
     const unsigned char *ring_base = smem + (size_t)warp * D * stage_bytes;
 
-    int failed_at = n;
-    for (int row = 0; row < n && failed_at == n; ++row) {
-        int32_t acc[NB];
+    auto load_x = [&](int j, int4 (&xv)[NB][S]) {
+        const int32_t off = j * DOT_K_CHUNK_WORDS;
+        const int32_t m = min(DOT_K_CHUNK_WORDS, kw - off);
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int32_t e = lane * 4 + 128 * s;
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                xv[b][s] = e < m ? __ldg(x4[b] + ((off + e) >> 2)) : make_int4(0, 0, 0, 0);
+        }
+    };
+
+    int32_t acc[RPW][NB];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int b = 0; b < NB; ++b)
-            acc[b] = 0;
-        for (int j = 0; j < nchunks; ++j) {
-            if (!ring.wait(p.wait_ns)) {
-                failed_at = row;
-                break;
+            acc[r][b] = 0;
+
+    int4 xv[NB][S];
+    if (nchunks > 0)
+        load_x(0, xv);
+    bool failed = false;
+    for (int j = 0; j < nchunks && !failed; ++j) {
+        const int32_t m = min(DOT_K_CHUNK_WORDS, kw - j * DOT_K_CHUNK_WORDS);
+        int4 xn[NB][S];
+        if (j + 1 < nchunks)
+            load_x(j + 1, xn);   // next chunk's activations, in flight during this one
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            if (r < n && !failed) {
+                if (!ring.wait(p.wait_ns)) {
+                    failed = true;
+                } else {
+                    const int4 *s4 = reinterpret_cast<const int4 *>(ring_base + ring.cs * stage_bytes);
+#pragma unroll
+                    for (int s = 0; s < S; ++s) {
+                        const int32_t e = lane * 4 + 128 * s;
+                        if (e < m) {
+                            const int4 wv = s4[e >> 2];
+#pragma unroll
+                            for (int b = 0; b < NB; ++b)
+                                dp4a4(acc[r][b], wv, xv[b][s]);
+                        }
+                    }
+                    ring.cnext();
+                    produce();
+                }
             }
-            const int32_t off = j * DOT_K_CHUNK_WORDS;
-            const int32_t m = min(DOT_K_CHUNK_WORDS, kw - off);
-            const int4 *s4 = reinterpret_cast<const int4 *>(ring_base + ring.cs * stage_bytes);
-#pragma unroll 4
-            for (int e = lane * 4; e < m; e += 128) {
-                const int4 wv = s4[e >> 2];
+        }
+        if (j + 1 < nchunks) {
+#pragma unroll
+            for (int s = 0; s < S; ++s)
 #pragma unroll
                 for (int b = 0; b < NB; ++b)
-                    dp4a4(acc[b], wv, __ldg(x4[b] + ((off + e) >> 2)));
-            }
-            ring.cnext();
-            produce();
-        }
-        if (failed_at != n)
-            break;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int32_t s = dev::warp_sum_i32(acc[b]);
-            if (lane == b && b < p.batch)
-                store_result(p, r0 + row, b, s, true);
+                    xv[b][s] = xn[b][s];
         }
     }
-    if (failed_at < n) {
+    if (failed) {
         dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
         ring.drain(p.wait_ns, !p.inject_stall);
-        for (int row = failed_at; row < n; ++row)
-            if (lane < p.batch)
-                store_result(p, r0 + row, lane, 0, false);
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int32_t sum = dev::warp_sum_i32(acc[r][b]);
+            if (r < n && lane == b && b < p.batch)
+                store_result(p, r0 + r, b, sum, !failed);
+        }
     }
 }
 
@@ -209,14 +246,15 @@ __global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_k_kernel(const DotP
 // 16-byte groups alternate between the halves (group g -> half g & 1).
 // ---------------------------------------------------------------------------
 template <int NB>
-__global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_b_kernel(const DotParams p)
+__global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int warps = blockDim.x >> 5;
     const int b = lane & 15;
     const int h = lane >> 4;
-    const int32_t r0 = (blockIdx.x * DOT_WARPS + warp) * DOT_B_ROWS;
+    const int32_t r0 = (int32_t)(((int64_t)blockIdx.x * warps + warp) * DOT_B_ROWS);
     if (r0 >= p.n_rows)
         return;
     const int n = min(DOT_B_ROWS, p.n_rows - r0);
@@ -230,7 +268,7 @@ __global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_b_kernel(const DotP
     ring.depth = D;
     ring.stage_bytes = stage_bytes;
     ring.data0 = dev::smem_u32(smem) + warp * D * stage_bytes;
-    ring.bar0 = dev::smem_u32(smem) + DOT_WARPS * D * stage_bytes + warp * D * 8;
+    ring.bar0 = dev::smem_u32(smem) + warps * D * stage_bytes + warp * D * 8;
     ring.init(lane);
     const uint64_t policy = dev::l2_evict_first_policy();
 
@@ -309,10 +347,10 @@ __global__ void __launch_bounds__(DOT_WARPS * 32) dot_staged_b_kernel(const DotP
 // Plain loads: any 4-byte aligned input, any k % 4 == 0.  One warp per row.
 // ---------------------------------------------------------------------------
 template <int NB>
-__global__ void __launch_bounds__(DOT_WARPS * 32) dot_direct_kernel(const DotParams p)
+__global__ void __launch_bounds__(256, 1) dot_direct_kernel(const DotParams p)
 {
     const int lane = threadIdx.x & 31;
-    const int32_t r = blockIdx.x * DOT_WARPS + (threadIdx.x >> 5);
+    const int32_t r = (int32_t)((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
     if (r >= p.n_rows)
         return;
     const int32_t kw = p.k_words;
@@ -337,18 +375,13 @@ __global__ void __launch_bounds__(DOT_WARPS * 32) dot_direct_kernel(const DotPar
 }
 
 template <int NB>
-cudaError_t launch_nb(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream)
+cudaError_t launch_staged_k(const DotParams &p, const loom_launch &L, cudaStream_t stream)
 {
-    if (L.grid[0] == 0)
-        return cudaSuccess;
-    switch (kind) {
-    case DotKernel::StagedK:
-        return launch_with(dot_staged_k_kernel<NB>, L, stream, p);
-    case DotKernel::StagedB:
-        return launch_with(dot_staged_b_kernel<NB>, L, stream, p);
-    default:
-        return launch_with(dot_direct_kernel<NB>, L, stream, p);
-    }
+    if (p.rows_per_warp >= 4)
+        return launch_with(dot_staged_k_kernel<NB, 4>, L, stream, p);
+    if (p.rows_per_warp == 2 || p.rows_per_warp == 3)
+        return launch_with(dot_staged_k_kernel<NB, 2>, L, stream, p);
+    return launch_with(dot_staged_k_kernel<NB, 1>, L, stream, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -380,28 +413,28 @@ DotKernel dot_select(bool aligned, int32_t k, int32_t batch_pass)
 {
     if (!aligned || (k % 16) != 0)
         return DotKernel::Direct;
-    return batch_pass <= 4 ? DotKernel::StagedK : DotKernel::StagedB;
+    return batch_pass <= 2 ? DotKernel::StagedK : DotKernel::StagedB;
 }
 
-int dot_rows_per_cta(DotKernel kind)
+int dot_rows_per_warp(DotKernel kind, int tuned)
 {
     switch (kind) {
-    case DotKernel::StagedK:
-        return DOT_WARPS * K_ROWS_PER_WARP;
+    case DotKernel::StagedK:   // 1, 2 or 4 rows (other requests round down)
+        return tuned >= 4 ? 4 : tuned >= 2 ? 2 : tuned == 1 ? 1 : DOT_K_DEFAULT_ROWS;
     case DotKernel::StagedB:
-        return DOT_WARPS * DOT_B_ROWS;
+        return DOT_B_ROWS;
     default:
-        return DOT_WARPS;
+        return 1;
     }
 }
 
-uint32_t dot_smem_bytes(DotKernel kind, int depth)
+uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps)
 {
     switch (kind) {
     case DotKernel::StagedK:
-        return (uint32_t)(DOT_WARPS * depth * (DOT_K_CHUNK_WORDS * 4 + 8));
+        return (uint32_t)(warps * depth * (DOT_K_CHUNK_WORDS * 4 + 8));
     case DotKernel::StagedB:
-        return (uint32_t)(DOT_WARPS * depth * (DOT_B_ROWS * DOT_B_CHUNK_WORDS * 4 + 8));
+        return (uint32_t)(warps * depth * (DOT_B_ROWS * DOT_B_CHUNK_WORDS * 4 + 8));
     default:
         return 0;
     }
@@ -409,21 +442,21 @@ uint32_t dot_smem_bytes(DotKernel kind, int depth)
 
 cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream)
 {
+    if (L.grid[0] == 0)
+        return cudaSuccess;
     const int nb = p.batch;
-    if (kind == DotKernel::StagedK) {
-        if (nb == 1)
-            return launch_nb<1>(p, kind, L, stream);
-        if (nb == 2)
-            return launch_nb<2>(p, kind, L, stream);
-        return launch_nb<4>(p, kind, L, stream);  // 3 or 4
+    switch (kind) {
+    case DotKernel::StagedK:
+        return nb == 1 ? launch_staged_k<1>(p, L, stream) : launch_staged_k<2>(p, L, stream);
+    case DotKernel::StagedB:
+        return launch_with(dot_staged_b_kernel<16>, L, stream, p);
+    default:
+        if (nb <= 1)
+            return launch_with(dot_direct_kernel<1>, L, stream, p);
+        if (nb <= 4)
+            return launch_with(dot_direct_kernel<4>, L, stream, p);
+        return launch_with(dot_direct_kernel<16>, L, stream, p);
     }
-    if (kind == DotKernel::StagedB)
-        return launch_nb<16>(p, kind, L, stream);
-    if (nb <= 1)
-        return launch_nb<1>(p, kind, L, stream);
-    if (nb <= 4)
-        return launch_nb<4>(p, kind, L, stream);
-    return launch_nb<16>(p, kind, L, stream);
 }
 
 cudaError_t launch_unpack(const int32_t *packed, int64_t n_words, float *out, const loom_launch &L,

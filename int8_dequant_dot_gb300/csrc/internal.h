@@ -11,10 +11,12 @@
 namespace loom {
 
 // ---- row sum -------------------------------------------------------------
-constexpr int RS_WARPS = 4;             // warps per CTA
-constexpr int RS_CHUNK_ELEMS = 1024;    // one staged chunk: 4 KiB of f32
+constexpr int RS_DEFAULT_WARPS = 1;    // warps per CTA (a CTA's slot frees when its warp ends)
+constexpr int RS_DEFAULT_WARPS_WIDE = 2;  // lanes = 1 (wide rows)
+constexpr int RS_DEFAULT_CHUNK_ELEMS = 1024;       // one staged chunk: 4 KiB of f32 ...
+constexpr int RS_DEFAULT_CHUNK_ELEMS_LONG = 2048;  // ... 8 KiB for units above 4096 elements
 constexpr int RS_SLOT_ELEMS = 128;      // one warp-wide read: 32 lanes x float4
-constexpr int RS_DEFAULT_DEPTH = 4;
+constexpr int RS_DEFAULT_DEPTH = 2;    // measured best on GB300 (more warps per SM)
 
 struct RowSumParams {
     const float *values;
@@ -30,22 +32,24 @@ struct RowSumParams {
     int32_t *error;         // device error word or NULL
     int32_t depth;          // chunks in flight per warp (staged path)
     int32_t units_per_warp;
+    int32_t chunk_elems;    // elements per staged chunk (multiple of 128)
     uint64_t wait_ns;       // limit of each barrier wait
     int32_t inject_stall;   // test hook: issue no copies (every wait runs out)
 };
 
 int row_sum_default_units_per_warp(int32_t rows, int32_t lanes);
-uint32_t row_sum_smem_bytes(bool staged, int depth);
+uint32_t row_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems);
 cudaError_t launch_row_sum(const RowSumParams &p, bool staged, const loom_launch &L,
                            cudaStream_t stream);
 
 // ---- dequantised dot -----------------------------------------------------
-constexpr int DOT_WARPS = 4;
+constexpr int DOT_DEFAULT_WARPS = 2;     // warps per CTA of the staged kernels
+constexpr int DOT_K_DEFAULT_ROWS = 4;     // lanes-across-k path: rows per warp
 constexpr int DOT_K_CHUNK_WORDS = 1024;   // lanes-across-k path: 4 KiB of one row
 constexpr int DOT_B_ROWS = 8;             // lanes-across-batch path: rows per warp
 constexpr int DOT_B_CHUNK_WORDS = 128;    // ... 512 B of each of those rows per chunk
 constexpr int DOT_MAX_BATCH_PER_PASS = 16;
-constexpr int DOT_DEFAULT_DEPTH = 4;
+constexpr int DOT_DEFAULT_DEPTH = 2;
 
 struct DotParams {
     const int32_t *w;      // [n_rows][k/4]
@@ -58,6 +62,7 @@ struct DotParams {
     int32_t *acc;          // same layout as y, or NULL
     int32_t *error;
     int32_t depth;
+    int32_t rows_per_warp;  // lanes-across-k path
     uint64_t wait_ns;
     int32_t inject_stall;
 };
@@ -65,8 +70,8 @@ struct DotParams {
 enum class DotKernel { StagedK, StagedB, Direct };
 
 DotKernel dot_select(bool aligned, int32_t k, int32_t batch_pass);
-uint32_t dot_smem_bytes(DotKernel kind, int depth);
-int dot_rows_per_cta(DotKernel kind);
+uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps);
+int dot_rows_per_warp(DotKernel kind, int tuned_rows_per_warp);
 cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream);
 
 // ---- unpack ----------------------------------------------------------------

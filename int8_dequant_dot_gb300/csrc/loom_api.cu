@@ -43,26 +43,43 @@ struct Tuning {
     int depth;
     int path;
     int upw;
+    int warps;
+    int chunk_bytes;
     int stall;
     uint64_t wait_ns;
 };
+
+bool valid_warps(int64_t w) { return w == 1 || w == 2 || w == 4 || w == 8; }
+bool valid_chunk(int64_t b) { return b >= 512 && b <= 32768 && b % 512 == 0; }
+
+// Measured on GB300: 4 KiB chunks for small segments, 8 KiB for long rows.
+int64_t default_chunk_bytes(int64_t rows, int64_t lanes)
+{
+    return 4 * (rows * lanes > 4096 ? RS_DEFAULT_CHUNK_ELEMS_LONG : RS_DEFAULT_CHUNK_ELEMS);
+}
 
 loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
 {
     out->depth = default_depth;
     out->path = LOOM_PATH_AUTO;
     out->upw = 0;
+    out->warps = 0;
+    out->chunk_bytes = 0;
     out->stall = 0;
     out->wait_ns = DEFAULT_WAIT_NS;
     if (!t)
         return LOOM_OK;
     if (t->depth < 0 || t->depth > LOOM_MAX_DEPTH || t->path < 0 || t->path > 2 ||
-        t->units_per_warp < 0 || t->units_per_warp > 32 || t->wait_ns < 0)
+        t->units_per_warp < 0 || t->units_per_warp > 32 || t->wait_ns < 0 ||
+        (t->warps_per_cta != 0 && !valid_warps(t->warps_per_cta)) ||
+        (t->chunk_bytes != 0 && !valid_chunk(t->chunk_bytes)))
         return LOOM_ERR_ARG;
     if (t->depth)
         out->depth = t->depth;
     out->path = t->path;
     out->upw = t->units_per_warp;
+    out->warps = t->warps_per_cta;
+    out->chunk_bytes = t->chunk_bytes;
     out->stall = t->inject_stall != 0;
     if (t->wait_ns)
         out->wait_ns = (uint64_t)t->wait_ns;
@@ -72,39 +89,52 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
 // ---- geometry of each op ----------------------------------------------------
 
 loom_status row_sum_geometry(int64_t num_segments, int64_t rows, int64_t lanes, bool staged,
-                             int depth, int upw, loom_launch *out)
+                             int64_t depth, int64_t upw, int64_t warps, int64_t chunk_bytes,
+                             loom_launch *out)
 {
     if (num_segments < 0 || rows < 0 || (lanes != 1 && lanes != 32) || rows * lanes >= (1ll << 31))
         return LOOM_ERR_SHAPE;
-    if (depth < 1 || depth > LOOM_MAX_DEPTH || upw < 0 || upw > 32)
+    if (warps == 0)
+        warps = lanes == 1 ? RS_DEFAULT_WARPS_WIDE : RS_DEFAULT_WARPS;
+    if (chunk_bytes == 0)
+        chunk_bytes = default_chunk_bytes(rows, lanes);
+    if (depth < 1 || depth > LOOM_MAX_DEPTH || upw < 0 || upw > 32 || !valid_warps(warps) ||
+        !valid_chunk(chunk_bytes))
         return LOOM_ERR_ARG;
     if (upw == 0)
         upw = row_sum_default_units_per_warp((int32_t)rows, (int32_t)lanes);
-    const int64_t per_cta = (int64_t)RS_WARPS * upw;
+    const int64_t per_cta = warps * upw;
     const int64_t grid = ceil_div(num_segments, per_cta);
     if (grid > 0x7fffffff)
         return LOOM_ERR_SHAPE;
-    fill_launch(out, grid, RS_WARPS * 32, row_sum_smem_bytes(staged, depth), (uint32_t)per_cta,
+    const uint32_t smem = row_sum_smem_bytes(staged, (int)depth, (int)warps, (int)(chunk_bytes / 4));
+    if (smem > 227 * 1024)
+        return LOOM_ERR_ARG;
+    fill_launch(out, grid, (uint32_t)warps * 32, smem, (uint32_t)per_cta,
                 staged ? LOOM_KERNEL_ROWSUM_STAGED : LOOM_KERNEL_ROWSUM_DIRECT);
     return LOOM_OK;
 }
 
-loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned, int depth,
-                         loom_launch *out)
+loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned, int64_t depth,
+                         int64_t warps, int64_t rows_per_warp, loom_launch *out)
 {
     if (n_rows < 0 || n_rows > 0x7fffffff || k < 0 || k > MAX_K || (k % 4) != 0 || batch < 0 ||
         batch > 0x7fffffff)
         return LOOM_ERR_SHAPE;
-    if (depth < 1 || depth > LOOM_MAX_DEPTH)
+    if (warps == 0)
+        warps = DOT_DEFAULT_WARPS;
+    if (depth < 1 || depth > LOOM_MAX_DEPTH || !valid_warps(warps) || rows_per_warp < 0 ||
+        rows_per_warp > 32)
         return LOOM_ERR_ARG;
     const int32_t pass = (int32_t)(batch < DOT_MAX_BATCH_PER_PASS ? batch : DOT_MAX_BATCH_PER_PASS);
     const DotKernel kind = dot_select(aligned, (int32_t)k, pass);
-    const int rows_per_cta = dot_rows_per_cta(kind);
+    const int64_t rows_per_cta = warps * dot_rows_per_warp(kind, (int)rows_per_warp);
     const int64_t grid = (batch == 0) ? 0 : ceil_div(n_rows, rows_per_cta);
     const uint32_t id = kind == DotKernel::StagedK   ? LOOM_KERNEL_DOT_STAGED_K
                         : kind == DotKernel::StagedB ? LOOM_KERNEL_DOT_STAGED_B
                                                      : LOOM_KERNEL_DOT_DIRECT;
-    fill_launch(out, grid, DOT_WARPS * 32, dot_smem_bytes(kind, depth), (uint32_t)rows_per_cta, id);
+    fill_launch(out, grid, (uint32_t)warps * 32, dot_smem_bytes(kind, (int)depth, (int)warps),
+                (uint32_t)rows_per_cta, id);
     return LOOM_OK;
 }
 
@@ -148,7 +178,7 @@ loom_status row_sum_common(const float *values, int64_t num_segments, int64_t se
         staged = can_stage;
     }
     loom_launch L;
-    st = row_sum_geometry(num_segments, rows, lanes, staged, t.depth, t.upw, &L);
+    st = row_sum_geometry(num_segments, rows, lanes, staged, t.depth, t.upw, t.warps, t.chunk_bytes, &L);
     if (st != LOOM_OK)
         return st;
 
@@ -169,7 +199,8 @@ loom_status row_sum_common(const float *values, int64_t num_segments, int64_t se
     p.tail_sum = tail_sum;
     p.error = error;
     p.depth = t.depth;
-    p.units_per_warp = (int32_t)(L.units_per_cta / RS_WARPS);
+    p.units_per_warp = (int32_t)(L.units_per_cta / (L.block[0] / 32));
+    p.chunk_elems = (int32_t)((t.chunk_bytes ? t.chunk_bytes : default_chunk_bytes(rows, lanes)) / 4);
     p.wait_ns = t.wait_ns;
     p.inject_stall = t.stall;
     cudaError_t e = launch_row_sum(p, staged, L, static_cast<cudaStream_t>(stream));
@@ -210,7 +241,7 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     for (int32_t b0 = 0; b0 < batch; b0 += DOT_MAX_BATCH_PER_PASS) {
         const int32_t nb = (batch - b0) < DOT_MAX_BATCH_PER_PASS ? (batch - b0) : DOT_MAX_BATCH_PER_PASS;
         loom_launch L;
-        st = dot_geometry(n_rows, k, nb, staged, t.depth, &L);
+        st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, &L);
         if (st != LOOM_OK)
             return st;
         const DotKernel kind = dot_select(staged, k, nb);
@@ -227,6 +258,7 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         p.acc = acc ? acc + b0 : nullptr;
         p.error = error;
         p.depth = t.depth;
+        p.rows_per_warp = (int32_t)(L.units_per_cta / (L.block[0] / 32));
         p.wait_ns = t.wait_ns;
         p.inject_stall = t.stall;
         cudaError_t e = launch_dot(p, kind, L, static_cast<cudaStream_t>(stream));
@@ -289,17 +321,17 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         if (n_workload < 2)
             return LOOM_ERR_ARG;
         return row_sum_geometry(1, workload[0], workload[1], opt(2, 1) != 0,
-                                (int)opt(3, RS_DEFAULT_DEPTH), 1, out);
+                                opt(3, RS_DEFAULT_DEPTH), 1, opt(4, 0), opt(5, 0), out);
     case LOOM_OP_ROW_SUM_BATCHED:
         if (n_workload < 3)
             return LOOM_ERR_ARG;
         return row_sum_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0,
-                                (int)opt(4, RS_DEFAULT_DEPTH), 0, out);
+                                opt(4, RS_DEFAULT_DEPTH), opt(6, 0), opt(5, 0), opt(7, 0), out);
     case LOOM_OP_I8_DEQUANT_DOT:
         if (n_workload < 3)
             return LOOM_ERR_ARG;
         return dot_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0,
-                            (int)opt(4, DOT_DEFAULT_DEPTH), out);
+                            opt(4, DOT_DEFAULT_DEPTH), opt(5, 0), opt(6, 0), out);
     default:
         return LOOM_ERR_ARG;
     }

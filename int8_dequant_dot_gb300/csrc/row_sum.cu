@@ -17,16 +17,18 @@
 //    `depth` chunks are in flight while the warp sums the oldest one.  This
 //    is the read-ahead queue of the pages' pipeline(depth): depth 1 is the
 //    serial control, and the depth never changes a result.
-//  * Summation is error-free: every lane keeps a double-word (hi, lo)
-//    accumulator per output fed by TwoSum, and the lanes are combined by a
+//  * Summation is error-free: every lane keeps double-word (hi, lo)
+//    accumulators fed by TwoSum -- two packed f32x2 pairs per output, so one
+//    instruction advances two accumulators -- and the lanes are combined by a
 //    __shfl_xor_sync butterfly (the subgroup reduce).  The pages add row sums
 //    to the carried f32 sum in source order so that the result does not
 //    depend on the schedule; here each addition is exact, so the carried
 //    value is the exact sum (up to the rounding of the tiny lo parts) in any
 //    association, and the association used is fixed by the shape alone.
 //    Each f32 output is rounded once from hi + lo.
-//  * Element e of a segment (row-major offset) goes to lane (e mod 128)/4;
-//    every lane adds its elements in increasing e.  The direct path (plain
+//  * Element e of a segment (row-major offset) goes to lane (e mod 128)/4 and
+//    accumulator e mod 4; every accumulator adds its elements in increasing e
+//    and the four are folded in a fixed order (LaneSums::finish).  The direct path (plain
 //    loads, for inputs that are not 16-byte aligned) uses the same mapping
 //    and order, so both paths return identical bits.
 //  * Over-dispatch: units past num_units in the last CTA do no loads and no
@@ -38,48 +40,155 @@ namespace loom {
 namespace {
 
 using dev::DW;
+using dev::DW2;
 using dev::FULL_MASK;
+using dev::pack2;
 
-__device__ __forceinline__ void add_split(DW &full, DW &tail, float x, int32_t g, int32_t split)
-{
-    if (g < split)
-        full.add(x);
-    else
-        tail.add(x);
-}
+// Per-lane partial sums of one segment: elements 4q+0/4q+1 of each float4 go
+// to the first packed pair, 4q+2/4q+3 to the second, for the full-tile part
+// and for the tail separately.
+struct LaneSums {
+    DW2 full01, full23, tail01, tail23;
 
-// Four consecutive elements starting at unit offset g.
-__device__ __forceinline__ void accumulate4(DW &full, DW &tail, const float4 &v, int32_t g,
-                                            int32_t split)
+    __device__ __forceinline__ void reset(float initial)
+    {
+        full01.hi = pack2(initial, 0.f);
+        full01.lo = full23.hi = full23.lo = 0;
+        tail01.hi = tail01.lo = tail23.hi = tail23.lo = 0;
+    }
+    __device__ __forceinline__ void full4(const float4 &v)
+    {
+        full01.add(pack2(v.x, v.y));
+        full23.add(pack2(v.z, v.w));
+    }
+    __device__ __forceinline__ void tail4(const float4 &v)
+    {
+        tail01.add(pack2(v.x, v.y));
+        tail23.add(pack2(v.z, v.w));
+    }
+    // A float4 whose first `nf` (1..3) elements are full-tile elements: each
+    // element goes to one side and the other side receives an exact zero.
+    __device__ __forceinline__ void straddle4(const float4 &v, int nf)
+    {
+        const bool f1 = nf > 1, f2 = nf > 2;
+        full01.add(pack2(v.x, f1 ? v.y : 0.f));
+        full23.add(pack2(f2 ? v.z : 0.f, 0.f));
+        tail01.add(pack2(0.f, f1 ? 0.f : v.y));
+        tail23.add(pack2(f2 ? 0.f : v.z, v.w));
+    }
+    // One trailing element at unit offset g (at most three per segment).
+    __device__ __forceinline__ void add1(float x, int32_t g, int32_t split)
+    {
+        if (g < split)
+            full01.add(pack2(x, 0.f));
+        else
+            tail01.add(pack2(x, 0.f));
+    }
+
+    // The lane's (full, tail) as one packed double word.  Fixed order: pairs
+    // (0,1) + (2,3) element-wise, then the two halves of each side.
+    __device__ __forceinline__ DW2 fold() const
+    {
+        DW2 f = full01;
+        f.add_dw(full23);   // (f_even, f_odd)
+        DW2 t = tail01;
+        t.add_dw(tail23);   // (t_even, t_odd)
+        float fh0, fh1, fl0, fl1, th0, th1, tl0, tl1;
+        dev::unpack2(f.hi, fh0, fh1);
+        dev::unpack2(f.lo, fl0, fl1);
+        dev::unpack2(t.hi, th0, th1);
+        dev::unpack2(t.lo, tl0, tl1);
+        DW2 ft{pack2(fh0, th0), pack2(fl0, tl0)};
+        ft.add_dw(pack2(fh1, th1), pack2(fl1, tl1));
+        return ft;   // (full, tail)
+    }
+
+    // Elements [0, m) of a chunk starting at unit offset `off`, read through
+    // `load(e)` (e = element offset in the chunk, a multiple of 4); elements
+    // below `split` (unit offset) are full-tile elements.  Lane l takes the
+    // float4s at e = 4l + 128i in increasing i.
+    template <typename Load>
+    __device__ __forceinline__ void chunk(Load load, int lane, int32_t off, int32_t m, int32_t split)
+    {
+        const int32_t mf = min(max(split - off, 0), m);   // chunk elements below the split
+        int32_t e = lane * 4;
+#pragma unroll 4
+        for (; e + 4 <= mf; e += RS_SLOT_ELEMS)
+            full4(load(e));
+        if (e < m) {   // this lane's first float4 not wholly below the split
+            if (e < mf)
+                straddle4(load(e), mf - e);
+            else
+                tail4(load(e));
+            e += RS_SLOT_ELEMS;
+        }
+#pragma unroll 4
+        for (; e < m; e += RS_SLOT_ELEMS)
+            tail4(load(e));
+    }
+};
+
+// Issues the warp's chunks in order (lane 0 issues, every lane tracks the cursor).
+struct Producer {
+    int pk, pj, ps;
+    uint32_t issued;
+
+    __device__ __forceinline__ void issue(const RowSumParams &p, int lane, int n, int64_t u0,
+                                          int32_t nchunks, int32_t nbulk, int D, uint32_t ring0,
+                                          uint32_t bar0, uint64_t policy)
+    {
+        while (pk < n) {
+            if (pj < __shfl_sync(FULL_MASK, nchunks, pk))
+                break;
+            ++pk;
+            pj = 0;
+        }
+        if (pk >= n)
+            return;
+        const int32_t nb = __shfl_sync(FULL_MASK, nbulk, pk);
+        if (lane == 0 && !p.inject_stall) {
+            const int32_t off = pj * p.chunk_elems;
+            const uint32_t bytes = (uint32_t)min(p.chunk_elems, nb - off) * 4u;
+            const float *src = p.values + (u0 + pk) * p.unit_stride + off;
+            dev::mbar_arrive_expect_tx(bar0 + 8 * ps, bytes);
+            dev::bulk_g2s(ring0 + ps * (p.chunk_elems * 4), src, bytes, bar0 + 8 * ps, policy);
+        }
+        ++pj;
+        ++issued;
+        ps = (ps + 1 == D) ? 0 : ps + 1;
+    }
+};
+
+// Reduces the (full, tail) partials of up to four consecutive units across
+// the warp and stores their sums; units past `g` are padding.
+__device__ __forceinline__ void finish_group(const RowSumParams &p, int lane, int64_t ubase, int g,
+                                             const DW2 &a, const DW2 &b, const DW2 &c, const DW2 &d)
 {
-    if (g + 4 <= split) {
-        full.add(v.x);
-        full.add(v.y);
-        full.add(v.z);
-        full.add(v.w);
-    } else if (g >= split) {
-        tail.add(v.x);
-        tail.add(v.y);
-        tail.add(v.z);
-        tail.add(v.w);
-    } else {
-        add_split(full, tail, v.x, g, split);
-        add_split(full, tail, v.y, g + 1, split);
-        add_split(full, tail, v.z, g + 2, split);
-        add_split(full, tail, v.w, g + 3, split);
+    const DW2 k = dev::warp_allreduce4(a, b, c, d, lane);
+    const int j = (lane >> 3) & 3;
+    if ((lane & 7) == 0 && j < g) {
+        float h0, h1, l0, l1;
+        dev::unpack2(k.hi, h0, h1);
+        dev::unpack2(k.lo, l0, l1);
+        p.full_sum[ubase + j] = __fadd_rn(h0, l0);
+        p.tail_sum[ubase + j] = __fadd_rn(h1, l1);
     }
 }
 
-template <bool STAGED>
-__global__ void __launch_bounds__(RS_WARPS * 32) row_sum_kernel(const RowSumParams p)
+// MINB: register budget hint (CTAs of 256 threads per SM).  3 caps registers
+// for many short-lived warps (small segments); 2 suits long rows.
+template <bool STAGED, int MINB>
+__global__ void __launch_bounds__(256, MINB) row_sum_kernel(const RowSumParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int64_t u0 = ((int64_t)blockIdx.x * RS_WARPS + warp) * p.units_per_warp;
+    const int warps = blockDim.x >> 5;
+    const int64_t u0 = ((int64_t)blockIdx.x * warps + warp) * p.units_per_warp;
     if (u0 >= p.num_units)
         return;  // over-dispatched warp: no loads, no stores
     const int n = (int)min((int64_t)p.units_per_warp, p.num_units - u0);
+    const int32_t CH = p.chunk_elems;
 
     // Lane k describes unit u0 + k (units_per_warp <= 32).
     int32_t c = 0;
@@ -95,13 +204,12 @@ __global__ void __launch_bounds__(RS_WARPS * 32) row_sum_kernel(const RowSumPara
     const int32_t n_active = c * p.lanes;     // active elements
     const int32_t split = F * p.lanes;        // first tail element
     const int32_t nbulk = n_active & ~3;      // elements moved as 16-byte blocks
-    const int32_t nchunks = (nbulk + RS_CHUNK_ELEMS - 1) / RS_CHUNK_ELEMS;
+    const int32_t nchunks = (nbulk + CH - 1) / CH;
 
     const int D = p.depth;
-    float *ring = reinterpret_cast<float *>(smem) + (size_t)warp * D * RS_CHUNK_ELEMS;
+    float *ring = reinterpret_cast<float *>(smem) + (size_t)warp * D * CH;
     const uint32_t ring0 = dev::smem_u32(ring);
-    const uint32_t bar0 =
-        dev::smem_u32(smem + (size_t)RS_WARPS * D * RS_CHUNK_ELEMS * sizeof(float)) + warp * D * 8;
+    const uint32_t bar0 = dev::smem_u32(smem + (size_t)warps * D * CH * sizeof(float)) + warp * D * 8;
 
     uint64_t policy = 0;
     if (STAGED) {
@@ -114,40 +222,16 @@ __global__ void __launch_bounds__(RS_WARPS * 32) row_sum_kernel(const RowSumPara
         policy = dev::l2_evict_first_policy();
     }
 
-    // Producer cursor: next chunk to issue is chunk pj of unit pk, into stage ps.
-    int pk = 0, pj = 0, ps = 0;
-    uint32_t issued = 0;
-    auto produce = [&]() {
-        while (pk < n) {
-            if (pj < __shfl_sync(FULL_MASK, nchunks, pk))
-                break;
-            ++pk;
-            pj = 0;
-        }
-        if (pk >= n)
-            return;
-        const int32_t nb = __shfl_sync(FULL_MASK, nbulk, pk);
-        if (lane == 0 && !p.inject_stall) {
-            const int32_t off = pj * RS_CHUNK_ELEMS;
-            const uint32_t bytes = (uint32_t)min(RS_CHUNK_ELEMS, nb - off) * 4u;
-            const float *src = p.values + (u0 + pk) * p.unit_stride + off;
-            dev::mbar_arrive_expect_tx(bar0 + 8 * ps, bytes);
-            dev::bulk_g2s(ring0 + ps * (RS_CHUNK_ELEMS * 4), src, bytes, bar0 + 8 * ps, policy);
-        }
-        ++pj;
-        ++issued;
-        ps = (ps + 1 == D) ? 0 : ps + 1;
-    };
-
+    Producer prod{0, 0, 0, 0u};
     if (STAGED)
         for (int s = 0; s < D; ++s)
-            produce();
+            prod.issue(p, lane, n, u0, nchunks, nbulk, D, ring0, bar0, policy);
 
     int cs = 0;            // consumer stage
     uint32_t cphase = 0;   // parity of the phase the consumer waits for
     uint32_t consumed = 0;
     int failed_at = n;     // first unit whose data never arrived
-    float out_full = 0.f, out_tail = 0.f;
+    DW2 pend0{0, 0}, pend1{0, 0}, pend2{0, 0}, pend3{0, 0};   // folded partials of a group of 4
 
     for (int k = 0; k < n; ++k) {
         const int32_t kc = __shfl_sync(FULL_MASK, nchunks, k);
@@ -157,38 +241,33 @@ __global__ void __launch_bounds__(RS_WARPS * 32) row_sum_kernel(const RowSumPara
         const float kinit = __shfl_sync(FULL_MASK, init, k);
         const float *ubase = p.values + (u0 + k) * p.unit_stride;
 
-        DW full{lane == 0 ? kinit : 0.f, 0.f};
-        DW tail{0.f, 0.f};
+        LaneSums acc;
+        acc.reset(lane == 0 ? kinit : 0.f);
         bool ok = true;
         for (int j = 0; j < kc; ++j) {
-            const int32_t off = j * RS_CHUNK_ELEMS;
-            const int32_t m = min(RS_CHUNK_ELEMS, kb - off);
+            const int32_t off = j * CH;
+            const int32_t m = min(CH, kb - off);
             if (STAGED) {
                 const bool landed = dev::mbar_wait_bounded(bar0 + 8 * cs, cphase, p.wait_ns);
                 if (!__all_sync(FULL_MASK, landed)) {
                     ok = false;
                     break;
                 }
-                const float4 *s4 = reinterpret_cast<const float4 *>(ring + cs * RS_CHUNK_ELEMS);
-#pragma unroll 4
-                for (int e = lane * 4; e < m; e += RS_SLOT_ELEMS)
-                    accumulate4(full, tail, s4[e >> 2], off + e, ks);
+                const float4 *s4 = reinterpret_cast<const float4 *>(ring + (size_t)cs * CH);
+                acc.chunk([&](int32_t e) { return s4[e >> 2]; }, lane, off, m, ks);
                 __syncwarp();
                 ++consumed;
                 cs = (cs + 1 == D) ? 0 : cs + 1;
                 cphase ^= (cs == 0) ? 1u : 0u;
-                produce();  // refill the stage just released
+                prod.issue(p, lane, n, u0, nchunks, nbulk, D, ring0, bar0, policy);  // refill
             } else {
                 const float *src = ubase + off;
-#pragma unroll 4
-                for (int e = lane * 4; e < m; e += RS_SLOT_ELEMS) {
-                    float4 v;
-                    v.x = __ldg(src + e);
-                    v.y = __ldg(src + e + 1);
-                    v.z = __ldg(src + e + 2);
-                    v.w = __ldg(src + e + 3);
-                    accumulate4(full, tail, v, off + e, ks);
-                }
+                acc.chunk(
+                    [&](int32_t e) {
+                        return make_float4(__ldg(src + e), __ldg(src + e + 1), __ldg(src + e + 2),
+                                           __ldg(src + e + 3));
+                    },
+                    lane, off, m, ks);
             }
         }
         if (!ok) {
@@ -198,31 +277,47 @@ __global__ void __launch_bounds__(RS_WARPS * 32) row_sum_kernel(const RowSumPara
         // At most three trailing elements that do not fill a 16-byte block.
         if (lane < ka - kb) {
             const int32_t g = kb + lane;
-            add_split(full, tail, __ldg(ubase + g), g, ks);
+            acc.add1(__ldg(ubase + g), g, ks);
         }
-        full.warp_allreduce();
-        tail.warp_allreduce();
-        if (lane == k) {
-            out_full = full.value();
-            out_tail = tail.value();
+        const DW2 ft = acc.fold();
+        const int q = k & 3;
+        if (q == 0)
+            pend0 = ft;
+        else if (q == 1)
+            pend1 = ft;
+        else if (q == 2)
+            pend2 = ft;
+        else
+            pend3 = ft;
+        if (q == 3 || k == n - 1) {
+            const DW2 z{0, 0};
+            finish_group(p, lane, u0 + (k & ~3), q + 1, pend0, q >= 1 ? pend1 : z, q >= 2 ? pend2 : z,
+                         q >= 3 ? pend3 : z);
         }
     }
 
     if (failed_at < n) {
         dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+        // Units of the unfinished group before the failure still get their sums.
+        const int q = failed_at & 3;
+        if (q > 0) {
+            const DW2 z{0, 0};
+            finish_group(p, lane, u0 + (failed_at & ~3), q, pend0, q >= 2 ? pend1 : z,
+                         q >= 3 ? pend2 : z, z);
+        }
         // Let copies already in flight land before the warp leaves (bounded).
         if (STAGED && !p.inject_stall) {
             int s = cs;
             uint32_t ph = cphase;
-            for (uint32_t i = consumed; i < issued; ++i) {
+            for (uint32_t i = consumed; i < prod.issued; ++i) {
                 dev::mbar_wait_bounded(bar0 + 8 * s, ph, p.wait_ns);
                 s = (s + 1 == D) ? 0 : s + 1;
                 ph ^= (s == 0) ? 1u : 0u;
             }
         }
-        if (lane >= failed_at) {
-            out_full = __int_as_float(0x7fc00000);
-            out_tail = __int_as_float(0x7fc00000);
+        if (lane >= failed_at && lane < n) {
+            p.full_sum[u0 + lane] = __int_as_float(0x7fc00000);
+            p.tail_sum[u0 + lane] = __int_as_float(0x7fc00000);
         }
     }
 
@@ -230,8 +325,6 @@ __global__ void __launch_bounds__(RS_WARPS * 32) row_sum_kernel(const RowSumPara
         const int64_t u = u0 + lane;
         p.final_row[u] = F;
         p.tail_count[u] = c - F;
-        p.full_sum[u] = out_full;
-        p.tail_sum[u] = out_tail;
     }
 }
 
@@ -240,7 +333,8 @@ __global__ void __launch_bounds__(RS_WARPS * 32) row_sum_kernel(const RowSumPara
 int row_sum_default_units_per_warp(int32_t rows, int32_t lanes)
 {
     // About 32 KiB of (maximum) data per warp: long enough for the read-ahead
-    // ring to reach steady state, short enough for many CTAs per SM.
+    // ring to reach steady state, short enough for many CTAs per SM (63 x 32
+    // segments: 4 per warp; rows of 8 KiB or more: 1 per warp).
     const int64_t unit_bytes = (int64_t)rows * lanes * 4;
     if (unit_bytes <= 0)
         return 32;
@@ -252,11 +346,11 @@ int row_sum_default_units_per_warp(int32_t rows, int32_t lanes)
     return (int)upw;
 }
 
-uint32_t row_sum_smem_bytes(bool staged, int depth)
+uint32_t row_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems)
 {
     if (!staged)
         return 0;
-    return (uint32_t)(RS_WARPS * depth * (RS_CHUNK_ELEMS * 4 + 8));
+    return (uint32_t)(warps * depth * (chunk_elems * 4 + 8));
 }
 
 cudaError_t launch_row_sum(const RowSumParams &p, bool staged, const loom_launch &L,
@@ -264,8 +358,12 @@ cudaError_t launch_row_sum(const RowSumParams &p, bool staged, const loom_launch
 {
     if (L.grid[0] == 0)
         return cudaSuccess;
-    return staged ? launch_with(row_sum_kernel<true>, L, stream, p)
-                  : launch_with(row_sum_kernel<false>, L, stream, p);
+    const bool small_units = (int64_t)p.rows * p.lanes <= 4096;
+    if (staged)
+        return small_units ? launch_with(row_sum_kernel<true, 3>, L, stream, p)
+                           : launch_with(row_sum_kernel<true, 2>, L, stream, p);
+    return small_units ? launch_with(row_sum_kernel<false, 3>, L, stream, p)
+                       : launch_with(row_sum_kernel<false, 2>, L, stream, p);
 }
 
 }  // namespace loom

@@ -64,14 +64,23 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
     for s in (0, 1, 15, 16, 17, 1000, 65536, 65537):
         L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes])
         assert L["grid"][0] == oracle.workgroups(s, L["units_per_cta"])
-        assert L["block"] == (128, 1, 1) and L["subgroup_size"] == 32
+        assert L["block"][0] % 32 == 0 and L["subgroup_size"] == 32
         assert L["kernel"] == loom.LOOM_KERNEL_ROWSUM_STAGED
         d = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes, 0])
         assert d["kernel"] == loom.LOOM_KERNEL_ROWSUM_DIRECT and d["smem_bytes"] == 0
     # one stage of 4 KiB plus one barrier per warp and depth
     for depth in range(1, 5):
-        L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [10, rows, lanes, 1, depth])
-        assert L["smem_bytes"] == 4 * depth * (4096 + 8)
+        for warps in (1, 2, 4, 8):
+            for chunk in (512, 4096, 8192):
+                wl = [10, rows, lanes, 1, depth, warps, 0, chunk]
+                if warps * depth * (chunk + 8) > 227 * 1024:   # more than a CTA may hold
+                    with pytest.raises(loom.LoomError):
+                        loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, wl)
+                    continue
+                L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, wl)
+                assert L["smem_bytes"] == warps * depth * (chunk + 8) and L["block"][0] == 32 * warps
+    L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [10, rows, lanes, 1, 1, 1])
+    assert L["smem_bytes"] == (4096 if rows * lanes <= 4096 else 8192) + 8
 
 
 def test_dot_launch(loom):
@@ -98,9 +107,11 @@ def test_launch_config_errors(loom):
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, bad)
         assert e.value.status == loom.LOOM_ERR_SHAPE
-    with pytest.raises(loom.LoomError) as e:
-        loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [5, 63, 32, 1, 9])
-    assert e.value.status == loom.LOOM_ERR_ARG
+    for bad in ([5, 63, 32, 1, 9], [5, 63, 32, 1, 2, 3], [5, 63, 32, 1, 2, 1, 0, 1000],
+                [5, 63, 32, 1, 4, 8, 0, 32768]):   # depth, warps, chunk, shared memory
+        with pytest.raises(loom.LoomError) as e:
+            loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, bad)
+        assert e.value.status == loom.LOOM_ERR_ARG
     for bad in ([5, 6, 1], [5, 131072, 1], [-1, 16, 1]):
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, bad)

@@ -149,12 +149,13 @@ def test_batched_depth_and_path_invariance(env, config2):
     d, dev, want = config2
     ref = run_batched(loom, torch, dev["values"], 65536, 2016, 63, 32, dev["counts"], dev["initial"], 8)
     for depth in (1, 2, 3, 4):
-        for upw in (1, 4, 32):
-            t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_STAGED, units_per_warp=upw)
+        for upw, warps, chunk in ((1, 1, 4096), (4, 2, 8192), (32, 4, 512), (7, 1, 2048)):
+            t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_STAGED, units_per_warp=upw,
+                                 warps_per_cta=warps, chunk_bytes=chunk)
             got = run_batched(loom, torch, dev["values"], 65536, 2016, 63, 32, dev["counts"],
                               dev["initial"], 8, tuning=t)
             for a, b in zip(got, ref):
-                assert np.array_equal(a.view(np.int32), b.view(np.int32)), (depth, upw)
+                assert np.array_equal(a.view(np.int32), b.view(np.int32)), (depth, upw, warps, chunk)
     t = loom.make_tuning(path=loom.LOOM_PATH_DIRECT)
     got = run_batched(loom, torch, dev["values"], 65536, 2016, 63, 32, dev["counts"], dev["initial"], 8,
                       tuning=t)
