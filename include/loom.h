@@ -59,17 +59,19 @@ typedef enum loom_op {
     LOOM_OP_ROW_SUM_BATCHED = 2, /* workload {num_segments, rows, lanes, staged (0/1), depth,
                                     warps_per_cta, units_per_warp, chunk_bytes} */
     LOOM_OP_I8_DEQUANT_DOT = 3   /* workload {n_rows, k, batch, staged (0/1), depth,
-                                    warps_per_cta, rows_per_warp} */
+                                    warps_per_cta, rows_per_warp, engine (0 auto, 1 dp4a,
+                                    2 tensor)} */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
- * (words, segments or output rows) map onto each CTA; the grid is the
+ * (words, segments or output rows) map onto each CTA -- onto each cluster of
+ * cluster[0] CTAs when that is above 1; the grid is cluster[0] times the
  * ceiling division of the workload by it, and units past the workload in the
  * last CTA do no loads and no stores. */
 typedef struct loom_launch {
     uint32_t grid[3];
     uint32_t block[3];
-    uint32_t cluster[3];    /* always {1,1,1}: no kernel uses clusters */
+    uint32_t cluster[3];    /* {1,1,1}, or {2,1,1} for LOOM_KERNEL_DOT_TENSOR */
     uint32_t subgroup_size; /* 32 */
     uint32_t smem_bytes;    /* dynamic shared memory per CTA */
     uint32_t units_per_cta;
@@ -82,6 +84,8 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_STAGED_K 4  /* lanes across k, batch <= 2 */
 #define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 2 */
 #define LOOM_KERNEL_DOT_DIRECT 6    /* plain loads (unaligned or k % 16 != 0) */
+#define LOOM_KERNEL_DOT_TENSOR 7    /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass;
+                                       clusters of 2 CTAs split k */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp). */
 #define LOOM_MAX_DEPTH 4

@@ -18,9 +18,13 @@
 extern "C" {
 #endif
 
-#define LOOM_PATH_AUTO 0   /* staged when inputs are 16-byte aligned, else direct */
-#define LOOM_PATH_STAGED 1 /* bulk-copy read-ahead ring; LOOM_ERR_ALIGN if not possible */
+#define LOOM_PATH_AUTO 0   /* staged when inputs are 16-byte aligned, else direct; dot:
+                              tensor cores for 3..16 vectors when k allows */
+#define LOOM_PATH_STAGED 1 /* bulk-copy read-ahead ring (dot: dp4a kernels only);
+                              LOOM_ERR_ALIGN if not possible */
 #define LOOM_PATH_DIRECT 2 /* plain loads, no shared-memory staging */
+#define LOOM_PATH_TENSOR 3 /* dot only: the tensor-core kernel for every batch pass;
+                              LOOM_ERR_ALIGN / LOOM_ERR_SHAPE when not possible */
 
 typedef struct loom_tuning {
     int32_t depth;          /* staged chunks in flight per warp, 1..LOOM_MAX_DEPTH; 0 = default */

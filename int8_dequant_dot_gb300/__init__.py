@@ -41,11 +41,13 @@ LOOM_KERNEL_ROWSUM_DIRECT = 3
 LOOM_KERNEL_DOT_STAGED_K = 4
 LOOM_KERNEL_DOT_STAGED_B = 5
 LOOM_KERNEL_DOT_DIRECT = 6
+LOOM_KERNEL_DOT_TENSOR = 7
 
 LOOM_MAX_DEPTH = 4
 LOOM_PATH_AUTO = 0
 LOOM_PATH_STAGED = 1
 LOOM_PATH_DIRECT = 2
+LOOM_PATH_TENSOR = 3
 
 #: every extern "C" symbol the headers declare
 EXPORTS = (

@@ -240,8 +240,9 @@ __global__ void __launch_bounds__(256) dot_staged_k_kernel(const DotParams p)
 }
 
 // ---------------------------------------------------------------------------
-// batch in (4, 16]: lanes across the batch.  Unit = DOT_B_ROWS rows.
-// Chunk = DOT_B_CHUNK_WORDS words of each unit row (one bulk copy per row).
+// batch in (2, 16]: lanes across the batch.  Unit = DOT_B_ROWS rows.
+// A stage holds DOT_B_CHUNK_WORDS words of each unit row and of each
+// activation vector (one bulk copy per row and per vector).
 // Lane (h, b): vector b = lane & 15, half h = lane >> 4.  Within a chunk the
 // 16-byte groups alternate between the halves (group g -> half g & 1).
 // ---------------------------------------------------------------------------
@@ -258,11 +259,12 @@ __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
     if (r0 >= p.n_rows)
         return;
     const int n = min(DOT_B_ROWS, p.n_rows - r0);
+    const int nb = p.batch;
     const int32_t kw = p.k_words;
     const int32_t nchunks = (kw + DOT_B_CHUNK_WORDS - 1) / DOT_B_CHUNK_WORDS;
     const int D = p.depth;
     constexpr uint32_t row_bytes = DOT_B_CHUNK_WORDS * 4;
-    constexpr uint32_t stage_bytes = DOT_B_ROWS * row_bytes;
+    constexpr uint32_t stage_bytes = (DOT_B_ROWS + NB) * row_bytes;   // weights, then activations
 
     Ring ring;
     ring.depth = D;
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
     ring.bar0 = dev::smem_u32(smem) + warps * D * stage_bytes + warp * D * 8;
     ring.init(lane);
     const uint64_t policy = dev::l2_evict_first_policy();
+    const uint64_t keep = dev::l2_evict_last_policy();   // activations: re-read by every warp
 
     int pj = 0;
     auto produce = [&]() {
@@ -280,11 +283,14 @@ __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
         const uint32_t bytes = (uint32_t)min(DOT_B_CHUNK_WORDS, kw - off) * 4u;
         if (!p.inject_stall) {
             if (lane == 0)
-                dev::mbar_arrive_expect_tx(ring.pbar(), bytes * n);
+                dev::mbar_arrive_expect_tx(ring.pbar(), bytes * (n + nb));
             __syncwarp();
             if (lane < n)
                 dev::bulk_g2s(ring.pstage() + lane * row_bytes, p.w + (int64_t)(r0 + lane) * kw + off,
                               bytes, ring.pbar(), policy);
+            else if (lane >= DOT_B_ROWS && lane < DOT_B_ROWS + nb)
+                dev::bulk_g2s(ring.pstage() + lane * row_bytes,
+                              p.x + (int64_t)(lane - DOT_B_ROWS) * kw + off, bytes, ring.pbar(), keep);
         }
         ++pj;
         ring.pnext();
@@ -292,8 +298,7 @@ __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
     for (int s = 0; s < D; ++s)
         produce();
 
-    const bool active = b < p.batch;
-    const int4 *xrow = reinterpret_cast<const int4 *>(p.x + (int64_t)(active ? b : 0) * kw);
+    const bool active = b < nb;
     int32_t acc[DOT_B_ROWS];
 #pragma unroll
     for (int r = 0; r < DOT_B_ROWS; ++r)
@@ -308,13 +313,14 @@ __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
         const int32_t off = j * DOT_B_CHUNK_WORDS;
         const int32_t groups = min(DOT_B_CHUNK_WORDS, kw - off) >> 2;  // 16-byte groups
         const unsigned char *stage = smem + (size_t)warp * D * stage_bytes + ring.cs * stage_bytes;
-        // This half's groups: g = 2q + h.
+        // This half's groups: g = 2q + h, activations of vector b from the stage.
         constexpr int QMAX = DOT_B_CHUNK_WORDS / 8;
+        const int4 *xrow = reinterpret_cast<const int4 *>(stage + (DOT_B_ROWS + (active ? b : 0)) * row_bytes);
         int4 xv[QMAX];
 #pragma unroll
         for (int q = 0; q < QMAX; ++q) {
             const int g = 2 * q + h;
-            xv[q] = (active && g < groups) ? __ldg(xrow + (off >> 2) + g) : make_int4(0, 0, 0, 0);
+            xv[q] = (active && g < groups) ? xrow[g] : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int r = 0; r < DOT_B_ROWS; ++r) {
@@ -337,9 +343,9 @@ __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
     }
 #pragma unroll
     for (int r = 0; r < DOT_B_ROWS; ++r) {
-        const int32_t s = acc[r] + __shfl_xor_sync(FULL_MASK, acc[r], 16);
+        const int32_t sum = acc[r] + __shfl_xor_sync(FULL_MASK, acc[r], 16);
         if (r < n && h == 0 && active)
-            store_result(p, r0 + r, b, s, !failed);
+            store_result(p, r0 + r, b, sum, !failed);
     }
 }
 
@@ -434,7 +440,7 @@ uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps)
     case DotKernel::StagedK:
         return (uint32_t)(warps * depth * (DOT_K_CHUNK_WORDS * 4 + 8));
     case DotKernel::StagedB:
-        return (uint32_t)(warps * depth * (DOT_B_ROWS * DOT_B_CHUNK_WORDS * 4 + 8));
+        return (uint32_t)(warps * depth * ((DOT_B_ROWS + DOT_MAX_BATCH_PER_PASS) * DOT_B_CHUNK_WORDS * 4 + 8));
     default:
         return 0;
     }
@@ -446,6 +452,8 @@ cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L,
         return cudaSuccess;
     const int nb = p.batch;
     switch (kind) {
+    case DotKernel::Tensor:
+        return launch_dot_tc(p, L, stream);
     case DotKernel::StagedK:
         return nb == 1 ? launch_staged_k<1>(p, L, stream) : launch_staged_k<2>(p, L, stream);
     case DotKernel::StagedB:

@@ -67,12 +67,21 @@ struct DotParams {
     int32_t inject_stall;
 };
 
-enum class DotKernel { StagedK, StagedB, Direct };
+enum class DotKernel { StagedK, StagedB, Direct, Tensor };
 
 DotKernel dot_select(bool aligned, int32_t k, int32_t batch_pass);
 uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps);
 int dot_rows_per_warp(DotKernel kind, int tuned_rows_per_warp);
 cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream);
+
+// tensor-core path (dot_tc.cu): 128-row tiles, k split over a cluster of two CTAs
+bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass);
+uint32_t dot_tc_smem_bytes(int depth, int32_t k);
+int dot_tc_rows_per_cluster();
+constexpr int DOT_TC_THREADS = 192;
+constexpr int DOT_TC_DEFAULT_DEPTH = 4;
+constexpr int DOT_TC_CLUSTER = 2;
+cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t stream);
 
 // ---- unpack ----------------------------------------------------------------
 constexpr int UNPACK_BLOCK = 256;

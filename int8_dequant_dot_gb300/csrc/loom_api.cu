@@ -69,7 +69,7 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
     out->wait_ns = DEFAULT_WAIT_NS;
     if (!t)
         return LOOM_OK;
-    if (t->depth < 0 || t->depth > LOOM_MAX_DEPTH || t->path < 0 || t->path > 2 ||
+    if (t->depth < 0 || t->depth > LOOM_MAX_DEPTH || t->path < 0 || t->path > 3 ||
         t->units_per_warp < 0 || t->units_per_warp > 32 || t->wait_ns < 0 ||
         (t->warps_per_cta != 0 && !valid_warps(t->warps_per_cta)) ||
         (t->chunk_bytes != 0 && !valid_chunk(t->chunk_bytes)))
@@ -115,18 +115,33 @@ loom_status row_sum_geometry(int64_t num_segments, int64_t rows, int64_t lanes, 
     return LOOM_OK;
 }
 
+// engine: 0 = automatic, 1 = dp4a kernels only, 2 = tensor cores
 loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned, int64_t depth,
-                         int64_t warps, int64_t rows_per_warp, loom_launch *out)
+                         int64_t warps, int64_t rows_per_warp, int64_t engine, loom_launch *out)
 {
     if (n_rows < 0 || n_rows > 0x7fffffff || k < 0 || k > MAX_K || (k % 4) != 0 || batch < 0 ||
         batch > 0x7fffffff)
         return LOOM_ERR_SHAPE;
     if (warps == 0)
         warps = DOT_DEFAULT_WARPS;
-    if (depth < 1 || depth > LOOM_MAX_DEPTH || !valid_warps(warps) || rows_per_warp < 0 ||
-        rows_per_warp > 32)
+    if (depth < 0 || depth > LOOM_MAX_DEPTH || !valid_warps(warps) || rows_per_warp < 0 ||
+        rows_per_warp > 32 || engine < 0 || engine > 2)
         return LOOM_ERR_ARG;
     const int32_t pass = (int32_t)(batch < DOT_MAX_BATCH_PER_PASS ? batch : DOT_MAX_BATCH_PER_PASS);
+    const bool tc_ok = dot_tc_eligible(aligned, (int32_t)k, pass);
+    const bool use_tc = (engine == 2 || (engine == 0 && pass >= 3)) && tc_ok;
+    if (depth == 0)
+        depth = use_tc ? DOT_TC_DEFAULT_DEPTH : DOT_DEFAULT_DEPTH;
+    if (engine == 2 && !tc_ok)
+        return aligned ? LOOM_ERR_SHAPE : LOOM_ERR_ALIGN;
+    if (use_tc) {
+        const int64_t rows = dot_tc_rows_per_cluster();
+        const int64_t grid = (batch == 0) ? 0 : DOT_TC_CLUSTER * ceil_div(n_rows, rows);
+        fill_launch(out, grid, DOT_TC_THREADS, dot_tc_smem_bytes((int)depth, (int32_t)k), (uint32_t)rows,
+                    LOOM_KERNEL_DOT_TENSOR);
+        out->cluster[0] = DOT_TC_CLUSTER;
+        return LOOM_OK;
+    }
     const DotKernel kind = dot_select(aligned, (int32_t)k, pass);
     const int64_t rows_per_cta = warps * dot_rows_per_warp(kind, (int)rows_per_warp);
     const int64_t grid = (batch == 0) ? 0 : ceil_div(n_rows, rows_per_cta);
@@ -216,7 +231,7 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     if (n_rows < 0 || batch < 0 || k < 0 || k > MAX_K || (k % 4) != 0)
         return LOOM_ERR_SHAPE;
     Tuning t;
-    loom_status st = read_tuning(tuning, DOT_DEFAULT_DEPTH, &t);
+    loom_status st = read_tuning(tuning, 0, &t);   // depth 0: each kernel's own default
     if (st != LOOM_OK)
         return st;
     if (n_rows == 0 || batch == 0)
@@ -228,12 +243,15 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         return LOOM_ERR_ALIGN;
     const bool can_stage = !misaligned(w, 16) && !misaligned(x, 16) && (k % 16) == 0;
     bool staged;
-    if (t.path == LOOM_PATH_STAGED) {
+    int engine = 0;
+    if (t.path == LOOM_PATH_STAGED || t.path == LOOM_PATH_TENSOR) {
         if (!can_stage)
             return LOOM_ERR_ALIGN;
         staged = true;
+        engine = t.path == LOOM_PATH_TENSOR ? 2 : 1;
     } else if (t.path == LOOM_PATH_DIRECT) {
         staged = false;
+        engine = 1;
     } else {
         staged = can_stage;
     }
@@ -241,10 +259,14 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     for (int32_t b0 = 0; b0 < batch; b0 += DOT_MAX_BATCH_PER_PASS) {
         const int32_t nb = (batch - b0) < DOT_MAX_BATCH_PER_PASS ? (batch - b0) : DOT_MAX_BATCH_PER_PASS;
         loom_launch L;
-        st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, &L);
+        st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, engine, &L);
         if (st != LOOM_OK)
             return st;
-        const DotKernel kind = dot_select(staged, k, nb);
+        const int depth_used = (int)((L.kernel == LOOM_KERNEL_DOT_TENSOR)
+                                         ? (t.depth ? t.depth : DOT_TC_DEFAULT_DEPTH)
+                                         : (t.depth ? t.depth : DOT_DEFAULT_DEPTH));
+        const DotKernel kind =
+            L.kernel == LOOM_KERNEL_DOT_TENSOR ? DotKernel::Tensor : dot_select(staged, k, nb);
         DotParams p;
         p.w = w;
         p.scale_w = scale_w;
@@ -257,8 +279,8 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         p.y = y + b0;
         p.acc = acc ? acc + b0 : nullptr;
         p.error = error;
-        p.depth = t.depth;
-        p.rows_per_warp = (int32_t)(L.units_per_cta / (L.block[0] / 32));
+        p.depth = depth_used;
+        p.rows_per_warp = kind == DotKernel::Tensor ? 0 : (int32_t)(L.units_per_cta / (L.block[0] / 32));
         p.wait_ns = t.wait_ns;
         p.inject_stall = t.stall;
         cudaError_t e = launch_dot(p, kind, L, static_cast<cudaStream_t>(stream));
@@ -330,8 +352,8 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
     case LOOM_OP_I8_DEQUANT_DOT:
         if (n_workload < 3)
             return LOOM_ERR_ARG;
-        return dot_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0,
-                            opt(4, DOT_DEFAULT_DEPTH), opt(5, 0), opt(6, 0), out);
+        return dot_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0, opt(4, 0),
+                            opt(5, 0), opt(6, 0), opt(7, 0), out);
     default:
         return LOOM_ERR_ARG;
     }

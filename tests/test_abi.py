@@ -88,8 +88,16 @@ def test_dot_launch(loom):
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_K
     assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 16])
+    assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR and L["cluster"] == (2, 1, 1)
+    assert L["grid"][0] == 2 * oracle.workgroups(8192, L["units_per_cta"]) == 128
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8191, 16384, 16, 1, 2, 0, 0, 1])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_B
-    assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
+    assert L["grid"][0] == oracle.workgroups(8191, L["units_per_cta"])
+    for n in (1, 127, 128, 129, 8192):
+        L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [n, 1024, 5])
+        assert L["grid"][0] == L["cluster"][0] * oracle.workgroups(n, L["units_per_cta"])
+    with pytest.raises(loom.LoomError):   # tensor cores forced where k allows no tile
+        loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [64, 8, 16, 1, 2, 0, 0, 2])
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16388, 16])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_DIRECT
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [77, 64, 0])

@@ -104,6 +104,57 @@ def test_dot_path_and_depth_invariance(env):
         assert np.array_equal(acc, ref_acc) and np.array_equal(y.view(np.int32), ref_y.view(np.int32))
 
 
+@pytest.mark.parametrize("n,k,b", [(128, 1024, 16), (129, 1040, 3), (300, 2064, 7), (5, 16, 16),
+                                   (257, 16384, 16), (64, 49152, 16), (130, 128, 4)])
+def test_tensor_core_matches_dp4a_bitwise(env, n, k, b):
+    # Row tails (n % 128), k tails (k % 128), one-stage k, the longest k the
+    # tensor-memory budget allows, and partial batches: the tensor-core kernel
+    # must give the dp4a kernels' bits and the oracle's integers.
+    torch, loom = env
+    d = small(n, k, b, seed=n + 7 * k + 31 * b)
+    y_tc, acc_tc = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR))
+    y_dp, acc_dp = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_STAGED))
+    assert np.array_equal(acc_tc, acc_dp)
+    assert np.array_equal(y_tc.view(np.int32), y_dp.view(np.int32))
+    check(d, y_tc, acc_tc, f"tensor {n}x{k}x{b}")
+
+
+def test_tensor_core_exact_at_group_bound(env):
+    # 1024 products of -128 * -128 per accumulator group reach 2**24 exactly.
+    torch, loom = env
+    k = 4096
+    w = np.full((256, k), -128, np.int8)
+    w[1::2] = 127
+    x = np.full((16, k), -128, np.int8)
+    x[3] = 127
+    d = dict(w=w, x=x, scale_w=np.ones(256, np.float32), scale_x=np.ones(16, np.float32))
+    y, acc = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR))
+    assert acc[0, 0] == 128 * 128 * k and acc[1, 0] == -127 * 128 * k and acc[1, 3] == 127 * 127 * k
+    check(d, y, acc, "group bound")
+
+
+def test_tensor_core_depth_invariance(env):
+    torch, loom = env
+    d = small(384, 8192, 16, seed=99)
+    ref_y, ref_acc = run_dot(loom, torch, d)
+    check(d, ref_y, ref_acc, "tensor default")
+    for depth in (1, 2, 3, 4):
+        y, acc = run_dot(loom, torch, d, tuning=loom.make_tuning(depth=depth, path=loom.LOOM_PATH_TENSOR))
+        assert np.array_equal(acc, ref_acc) and np.array_equal(y.view(np.int32), ref_y.view(np.int32)), depth
+
+
+def test_tensor_core_injected_stall(env):
+    torch, loom = env
+    d = small(256, 4096, 16, seed=41)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000, path=loom.LOOM_PATH_TENSOR)
+    y, acc = run_dot(loom, torch, d, tuning=t, error=err)
+    assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
+    assert np.isnan(y).all()
+    y, acc = run_dot(loom, torch, d)
+    check(d, y, acc, "after tensor-core timeout")
+
+
 def test_dot_guard_bands(env):
     torch, loom = env
     n, k, b = 35, 2048, 5
