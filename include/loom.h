@@ -87,8 +87,8 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_TENSOR 7    /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass;
                                        clusters of 2 CTAs split k */
 
-/* Maximum read-ahead depth (staged chunks in flight per warp). */
-#define LOOM_MAX_DEPTH 4
+/* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
+#define LOOM_MAX_DEPTH 8
 
 /*
  * Host launch-configuration routine: maps a workload to a launch without

@@ -27,7 +27,8 @@ extern "C" {
                               LOOM_ERR_ALIGN / LOOM_ERR_SHAPE when not possible */
 
 typedef struct loom_tuning {
-    int32_t depth;          /* staged chunks in flight per warp, 1..LOOM_MAX_DEPTH; 0 = default */
+    int32_t depth;          /* staged chunks in flight per warp (per CTA for the tensor-core
+                               dot), 1..LOOM_MAX_DEPTH; 0 = default */
     int32_t path;           /* LOOM_PATH_* */
     int32_t units_per_warp; /* row sums: segments per warp, 1..32; dot: rows per warp
                                of the batch <= 2 kernel, 1, 2 or 4; 0 = default */

@@ -43,7 +43,7 @@ LOOM_KERNEL_DOT_STAGED_B = 5
 LOOM_KERNEL_DOT_DIRECT = 6
 LOOM_KERNEL_DOT_TENSOR = 7
 
-LOOM_MAX_DEPTH = 4
+LOOM_MAX_DEPTH = 8
 LOOM_PATH_AUTO = 0
 LOOM_PATH_STAGED = 1
 LOOM_PATH_DIRECT = 2

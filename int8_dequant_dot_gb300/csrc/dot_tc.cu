@@ -13,17 +13,20 @@
 //    int8 has no fast tensor path on sm_103a, but every int8 value is exact
 //    in f16, every product of two is exact in the f32 accumulator, and a sum
 //    of at most 1024 products stays within |2^24|, where f32 holds every
-//    integer.  Each group of 1024 k therefore accumulates in its own f32 TMEM
-//    columns; the groups are converted to int32 and added in the epilogue, so
-//    the int32 result is exact.
+//    integer.  The eight K = 16 slices of a stage go to eight separate f32
+//    accumulators (so consecutive MMAs are independent), and a block of 64
+//    stages shares one set of eight: each accumulator then sums 64 x 16 =
+//    1024 products.  The accumulators are converted to int32 and added in the
+//    epilogue, so the int32 result is exact.
 //  * Conversion int8 -> f16 is exact and cheap: a byte b becomes the f16 bit
 //    pattern 0x6400 | (b + 128) (the value 1024 + b + 128) by a byte permute,
 //    and one packed f16 subtraction of 1152 leaves b.
 //  * The weights stream once: a 2-D TMA copy brings a 128-row x 128-byte
-//    tile (128-byte swizzle) into a ring of `depth` shared-memory stages.  Four
-//    converter warps read their rows (thread t owns row t; the swizzle keeps
-//    the reads conflict-free), convert, and write the f16 operand straight
-//    into tensor memory with tcgen05.st: the A operand never goes back
+//    tile (128-byte swizzle) into a ring of `depth` shared-memory stages.
+//    Eight converter warps -- two per tensor-memory sub-partition, each half
+//    of every row -- read their bytes (the swizzle keeps the reads
+//    conflict-free), convert, and write the f16 operand straight into tensor
+//    memory with tcgen05.st: the A operand never goes back
 //    through shared memory, so shared-memory traffic stays at two bytes per
 //    weight byte.  The activation tile is converted into a 128-byte-swizzled
 //    K-major f16 tile in shared memory (the B operand).
@@ -48,9 +51,13 @@ namespace {
 constexpr int TC_M = 128;                  // rows per tile (MMA M)
 constexpr int TC_N = 16;                   // vectors per pass (MMA N)
 constexpr int TC_KS = 128;                 // k (bytes) per stage
-constexpr int TC_STAGES_PER_GROUP = 8;     // 1024 k per exact f32 accumulator group
+constexpr int TC_KSLICES = TC_KS / 16;     // MMAs per stage (K = 16 each)
+constexpr int TC_STAGES_PER_BLOCK = 64;    // stages whose products share accumulators
 constexpr int TC_CLUSTER = 2;              // CTAs splitting k for one tile
-constexpr int TC_THREADS = 192;            // 4 converter warps, producer warp, MMA warp
+constexpr int TC_CONV_WARPS = 8;           // two per TMEM sub-partition, each half a row
+constexpr int TC_PRODUCER_WARP = TC_CONV_WARPS;
+constexpr int TC_MMA_WARP = TC_CONV_WARPS + 1;
+constexpr int TC_THREADS = 32 * (TC_CONV_WARPS + 2);
 constexpr uint32_t TC_W_BYTES = TC_M * TC_KS;          // 16 KiB
 constexpr uint32_t TC_X_BYTES = TC_N * TC_KS;          // 2 KiB
 constexpr uint32_t TC_STAGE_BYTES = TC_W_BYTES + TC_X_BYTES;   // 18 KiB (1024-aligned)
@@ -69,6 +76,7 @@ struct TcParams {
     int32_t n_rows, batch, y_stride;
     int32_t stages_total;   // ceil(k / 128)
     int32_t depth;          // shared-memory stages
+    int32_t a_bufs;         // f16 A buffers in tensor memory (2 or 4)
     uint32_t tmem_cols;
     uint64_t wait_ns;
     int32_t inject_stall;
@@ -79,21 +87,21 @@ struct Layout {
     int S;
     __device__ uint32_t stage(int s) const { return base + s * TC_STAGE_BYTES; }
     __device__ uint32_t btile(int a) const { return base + S * TC_STAGE_BYTES + a * TC_B_BYTES; }
-    __device__ uint32_t red() const { return base + S * TC_STAGE_BYTES + 2 * TC_B_BYTES; }
+    __device__ uint32_t red() const { return base + S * TC_STAGE_BYTES + 4 * TC_B_BYTES; }
     __device__ uint32_t red_ok() const { return red() + TC_RED_BYTES; }
     __device__ uint32_t bars() const { return red_ok() + TC_M * 4; }
     __device__ uint32_t full(int s) const { return bars() + 8 * s; }
     __device__ uint32_t empty(int s) const { return bars() + 8 * (S + s); }
     __device__ uint32_t aready(int a) const { return bars() + 8 * (2 * S + a); }
-    __device__ uint32_t afree(int a) const { return bars() + 8 * (2 * S + 2 + a); }
-    __device__ uint32_t done() const { return bars() + 8 * (2 * S + 4); }
-    __device__ uint32_t tmem_slot() const { return bars() + 8 * (2 * S + 5); }
+    __device__ uint32_t afree(int a) const { return bars() + 8 * (2 * S + 4 + a); }
+    __device__ uint32_t done() const { return bars() + 8 * (2 * S + 8); }
+    __device__ uint32_t tmem_slot() const { return bars() + 8 * (2 * S + 9); }
     __device__ uint32_t abort_flag() const { return tmem_slot() + 4; }
 };
 
 uint32_t tc_smem_bytes(int S)
 {
-    return 1024 + S * TC_STAGE_BYTES + 2 * TC_B_BYTES + TC_RED_BYTES + TC_M * 4 + 8 * (2 * S + 5) + 16;
+    return 1024 + S * TC_STAGE_BYTES + 4 * TC_B_BYTES + TC_RED_BYTES + TC_M * 4 + 8 * (2 * S + 9) + 16;
 }
 
 // ---- PTX wrappers ----------------------------------------------------------
@@ -239,23 +247,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int32_t per_rank = (q.stages_total + TC_CLUSTER - 1) / TC_CLUSTER;
     const int32_t s_begin = (int32_t)rank * per_rank;
     const int32_t ns = max(0, min(q.stages_total, s_begin + per_rank) - s_begin);
-    const int ng = (ns + TC_STAGES_PER_GROUP - 1) / TC_STAGES_PER_GROUP;
+    const int ng = TC_KSLICES * ((ns + TC_STAGES_PER_BLOCK - 1) / TC_STAGES_PER_BLOCK);   // accumulators
 
     // ---- set-up: barriers, abort flag, tensor memory --------------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(L.full(s), 1);
-            dev::mbar_init(L.empty(s), 4);
+            dev::mbar_init(L.empty(s), TC_CONV_WARPS);
         }
-        for (int a = 0; a < 2; ++a) {
-            dev::mbar_init(L.aready(a), 4);
+        for (int a = 0; a < 4; ++a) {
+            dev::mbar_init(L.aready(a), TC_CONV_WARPS);
             dev::mbar_init(L.afree(a), 1);
         }
         dev::mbar_init(L.done(), 1);
         asm volatile("st.shared.u32 [%0], 0;" ::"r"(L.abort_flag()) : "memory");
         dev::fence_barrier_init();
     }
-    if (warp == 4) {
+    if (warp == TC_PRODUCER_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(L.tmem_slot()),
                      "r"(q.tmem_cols)
                      : "memory");
@@ -267,7 +275,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     cluster_sync();   // both CTAs of the pair are running before any remote access
     uint32_t tmem;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(L.tmem_slot()));
-    const uint32_t acc_col = 2 * TC_A_COLS;
+    const int NA = q.a_bufs;
+    const uint32_t acc_col = NA * TC_A_COLS;
 
     bool ok = true;   // this thread's role finished its part
     int32_t isum[TC_N];
@@ -275,7 +284,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int b = 0; b < TC_N; ++b)
         isum[b] = 0;
 
-    if (warp == 4) {
+    if (warp == TC_PRODUCER_WARP) {
         // ---- producer: 2-D TMA of the weight and activation tiles ------------
         int issued = 0;
         if (lane == 0) {
@@ -302,22 +311,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 dev::mbar_wait_bounded(L.full(i % S), (i / S) & 1, q.wait_ns);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == TC_MMA_WARP) {
         // ---- MMA issuer ----------------------------------------------------------
         if (lane == 0) {
             for (int i = 0; i < ns; ++i) {
-                const int a = i & 1;
-                if (!dev::mbar_wait_bounded(L.aready(a), (i >> 1) & 1, q.wait_ns) || aborted(L)) {
+                const int a = i % NA;
+                if (!dev::mbar_wait_bounded(L.aready(a), (i / NA) & 1, q.wait_ns) || aborted(L)) {
                     set_abort(L, q);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + acc_col + TC_N * (i / TC_STAGES_PER_GROUP);
-                const bool first = (i % TC_STAGES_PER_GROUP) == 0;
+                const uint32_t d0 = tmem + acc_col + TC_N * TC_KSLICES * (i / TC_STAGES_PER_BLOCK);
+                const uint32_t accumulate = (i % TC_STAGES_PER_BLOCK) == 0 ? 0u : 1u;
 #pragma unroll
-                for (int kk = 0; kk < TC_KS / 16; ++kk) {
+                for (int kk = 0; kk < TC_KSLICES; ++kk) {
                     const uint64_t bdesc = smem_desc_sw128(L.btile(a) + (kk >> 2) * 2048 + (kk & 3) * 32);
-                    tc_mma(d, tmem + a * TC_A_COLS + kk * 8, bdesc, (first && kk == 0) ? 0u : 1u);
+                    tc_mma(d0 + TC_N * kk, tmem + a * TC_A_COLS + kk * 8, bdesc, accumulate);
                 }
                 tc_commit(L.afree(a));   // A/B buffer a is free once these MMAs complete
             }
@@ -325,31 +334,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ---- converters (warps 0-3): thread t owns tile row t ---------------------
-        const int t = threadIdx.x;
-        const uint32_t tlane = (uint32_t)(warp * 32) << 16;
+        // ---- converters: warp w owns tile rows 32 (w % 4) .. +31 (its TMEM lanes)
+        // and half h = w / 4 of each row's 128 bytes; warps with h = 0 also
+        // convert the activation tile.
+        const int sub = warp & 3;
+        const int h = warp >> 2;
+        const int t = 32 * sub + lane;   // tile row
+        const uint32_t tlane = (uint32_t)(32 * sub) << 16;
         for (int i = 0; i < ns; ++i) {
             const int s = i % S;
-            const int a = i & 1;
+            const int a = i % NA;
             bool w_ok = dev::mbar_wait_bounded(L.full(s), (i / S) & 1, q.wait_ns);
-            if (w_ok && i >= 2)
-                w_ok = dev::mbar_wait_bounded(L.afree(a), ((i >> 1) - 1) & 1, q.wait_ns);
+            if (w_ok && i >= NA)
+                w_ok = dev::mbar_wait_bounded(L.afree(a), ((i / NA) - 1) & 1, q.wait_ns);
             if (!__all_sync(dev::FULL_MASK, w_ok) || aborted(L)) {
                 ok = false;
                 break;
             }
-            // weight row t (128 bytes, 128-byte swizzle) and a 16-byte piece of the activations
-            int4 wv[8];
+            // half a weight row (64 bytes, 128-byte swizzle) and, for h = 0, a 16-byte
+            // piece of the activations
+            int4 wv[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                wv[c] = lds128(L.stage(s) + t * 128 + ((c ^ (t & 7)) << 4));
-            const int4 xv = lds128(L.stage(s) + TC_W_BYTES + t * 16);
+            for (int c = 0; c < 4; ++c)
+                wv[c] = lds128(L.stage(s) + t * 128 + (((4 * h + c) ^ (t & 7)) << 4));
+            int4 xv = make_int4(0, 0, 0, 0);
+            if (h == 0)
+                xv = lds128(L.stage(s) + TC_W_BYTES + t * 16);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(L.empty(s));   // this warp is done with stage s
-            // A operand: 128 f16 of row t -> 64 TMEM columns of buffer a
+            // A operand: 64 f16 of row t -> 32 TMEM columns of buffer a
 #pragma unroll
-            for (int part = 0; part < 4; ++part) {
+            for (int part = 0; part < 2; ++part) {
                 uint32_t r[16];
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
@@ -359,21 +375,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     i8x4_to_f16x4((uint32_t)w.z, r[c2 * 8 + 4], r[c2 * 8 + 5]);
                     i8x4_to_f16x4((uint32_t)w.w, r[c2 * 8 + 6], r[c2 * 8 + 7]);
                 }
-                tc_st16(tmem + tlane + a * TC_A_COLS + part * 16, r);
+                tc_st16(tmem + tlane + a * TC_A_COLS + 32 * h + part * 16, r);
             }
             // B operand: activations of vector n = t / 8, k = 16 (t % 8) .. +15, into
             // the K-major 128-byte-swizzled f16 tile (two 64-k atoms of 16 rows).
-            {
+            if (h == 0) {
                 const int n = t >> 3, c8 = t & 7;
-                uint32_t h[8];
-                i8x4_to_f16x4((uint32_t)xv.x, h[0], h[1]);
-                i8x4_to_f16x4((uint32_t)xv.y, h[2], h[3]);
-                i8x4_to_f16x4((uint32_t)xv.z, h[4], h[5]);
-                i8x4_to_f16x4((uint32_t)xv.w, h[6], h[7]);
+                uint32_t hx[8];
+                i8x4_to_f16x4((uint32_t)xv.x, hx[0], hx[1]);
+                i8x4_to_f16x4((uint32_t)xv.y, hx[2], hx[3]);
+                i8x4_to_f16x4((uint32_t)xv.z, hx[4], hx[5]);
+                i8x4_to_f16x4((uint32_t)xv.w, hx[6], hx[7]);
                 const uint32_t atom = L.btile(a) + (c8 >> 2) * 2048 + (n >> 3) * 1024 + (n & 7) * 128;
                 const int c0 = 2 * (c8 & 3);
-                sts128(atom + (((c0) ^ (n & 7)) << 4), h[0], h[1], h[2], h[3]);
-                sts128(atom + (((c0 + 1) ^ (n & 7)) << 4), h[4], h[5], h[6], h[7]);
+                sts128(atom + (((c0) ^ (n & 7)) << 4), hx[0], hx[1], hx[2], hx[3]);
+                sts128(atom + (((c0 + 1) ^ (n & 7)) << 4), hx[4], hx[5], hx[6], hx[7]);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             fence_async_smem();
@@ -382,8 +398,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (lane == 0)
                 mbar_arrive(L.aready(a));
         }
-        // ---- epilogue part 1: read the f32 groups, convert to int32 ---------------
-        bool done_ok = ok && dev::mbar_wait_bounded(L.done(), 0, q.wait_ns);
+        // ---- epilogue part 1 (warps with h = 0): the f32 groups to int32 --------
+        bool done_ok = ok && h == 0 && dev::mbar_wait_bounded(L.done(), 0, q.wait_ns);
         done_ok = __all_sync(dev::FULL_MASK, done_ok);
         if (done_ok && !aborted(L)) {
             tc_fence_after();
@@ -394,13 +410,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int b = 0; b < TC_N; ++b)
                     isum[b] += __float2int_rn(__uint_as_float(v[b]));
             }
-        } else {
+        } else if (h == 0) {
             ok = false;
         }
         if (!ok)
             set_abort(L, q);
         // the second CTA of the pair hands its partial sums to the first
-        if (rank == 1) {
+        if (rank == 1 && h == 0) {
             const uint32_t dst = map_to_rank(L.red() + t * TC_N * 4, 0);
 #pragma unroll
             for (int b = 0; b < TC_N; b += 4)
@@ -439,7 +455,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     }
     // tensor memory is freed only after every MMA of this CTA has completed
-    if (warp == 4) {
+    if (warp == TC_PRODUCER_WARP) {
         if (lane == 0)
             dev::mbar_wait_bounded(L.done(), 0, q.wait_ns);
         __syncwarp();
@@ -485,24 +501,22 @@ bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t o
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass)
+// f32 accumulators of one CTA (16 columns each)
+int32_t tc_groups(int32_t k)
 {
-    if (!aligned || k < 16 || (k % 16) != 0 || batch_pass < 1 || batch_pass > TC_N)
-        return false;
     const int32_t stages = (k + TC_KS - 1) / TC_KS;
     const int32_t per_rank = (stages + TC_CLUSTER - 1) / TC_CLUSTER;
-    const int32_t groups = (per_rank + TC_STAGES_PER_GROUP - 1) / TC_STAGES_PER_GROUP;
-    return 2 * TC_A_COLS + TC_N * groups <= 512;
+    return TC_KSLICES * ((per_rank + TC_STAGES_PER_BLOCK - 1) / TC_STAGES_PER_BLOCK);
 }
+
+// Two A buffers: conversion of stage i + 1 overlaps the MMAs of stage i
+// (four measured slower on GB300: the 512-column allocation it needs costs
+// more than the extra overlap buys).
+int tc_a_bufs(int32_t) { return 2; }
 
 uint32_t tc_tmem_cols(int32_t k)
 {
-    const int32_t stages = (k + TC_KS - 1) / TC_KS;
-    const int32_t per_rank = (stages + TC_CLUSTER - 1) / TC_CLUSTER;
-    const int32_t groups = (per_rank + TC_STAGES_PER_GROUP - 1) / TC_STAGES_PER_GROUP;
-    return 2 * TC_A_COLS + TC_N * groups <= 256 ? 256u : 512u;
+    return tc_a_bufs(k) * TC_A_COLS + TC_N * tc_groups(k) <= 256 ? 256u : 512u;
 }
 
 // Shared memory per CTA, sized so that every CTA resident on an SM finds its
@@ -513,6 +527,15 @@ uint32_t tc_tmem_cols(int32_t k)
 // 512 columns, for more than half (one CTA per SM).
 constexpr uint32_t TC_MIN_SMEM_256 = 80u * 1024u;
 constexpr uint32_t TC_MIN_SMEM_512 = 120u * 1024u;
+
+}  // namespace
+
+bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass)
+{
+    if (!aligned || k < 16 || (k % 16) != 0 || batch_pass < 1 || batch_pass > TC_N)
+        return false;
+    return 2 * TC_A_COLS + TC_N * tc_groups(k) <= 512;
+}
 
 uint32_t dot_tc_smem_bytes(int depth, int32_t k)
 {
@@ -543,6 +566,7 @@ cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t
     q.y_stride = p.y_stride;
     q.stages_total = (int32_t)((k + TC_KS - 1) / TC_KS);
     q.depth = p.depth;
+    q.a_bufs = tc_a_bufs((int32_t)k);
     q.tmem_cols = tc_tmem_cols((int32_t)k);
     if (L.smem_bytes < (q.tmem_cols == 512u ? TC_MIN_SMEM_512 : TC_MIN_SMEM_256))
         return cudaErrorInvalidValue;   // too many CTAs per SM for the tensor memory

@@ -78,7 +78,7 @@ cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L,
 bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass);
 uint32_t dot_tc_smem_bytes(int depth, int32_t k);
 int dot_tc_rows_per_cluster();
-constexpr int DOT_TC_THREADS = 192;
+constexpr int DOT_TC_THREADS = 320;
 constexpr int DOT_TC_DEFAULT_DEPTH = 4;
 constexpr int DOT_TC_CLUSTER = 2;
 cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t stream);
