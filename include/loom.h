@@ -71,7 +71,7 @@ typedef enum loom_op {
 typedef struct loom_launch {
     uint32_t grid[3];
     uint32_t block[3];
-    uint32_t cluster[3];    /* {1,1,1}, or {2,1,1} for LOOM_KERNEL_DOT_TENSOR */
+    uint32_t cluster[3];    /* {1,1,1}, or {2 or 4,1,1} for LOOM_KERNEL_DOT_TENSOR */
     uint32_t subgroup_size; /* 32 */
     uint32_t smem_bytes;    /* dynamic shared memory per CTA */
     uint32_t units_per_cta;
@@ -85,7 +85,7 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 2 */
 #define LOOM_KERNEL_DOT_DIRECT 6    /* plain loads (unaligned or k % 16 != 0) */
 #define LOOM_KERNEL_DOT_TENSOR 7    /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass;
-                                       clusters of 2 CTAs split k */
+                                       clusters of 2 or 4 CTAs split k */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8

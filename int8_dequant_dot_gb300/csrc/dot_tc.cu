@@ -32,9 +32,10 @@
 //    K-major f16 tile in shared memory (the B operand).
 //  * One thread issues the MMAs; tcgen05.commit releases the A/B buffers and
 //    finally signals the epilogue.
-//  * Each 128-row tile is split along k over a cluster of two CTAs (128 CTAs
-//    for 8192 rows); the second CTA hands its int32 partial sums to the first
-//    through distributed shared memory, which adds them and applies the
+//  * Each 128-row tile is split along k over a cluster of four CTAs (two for
+//    short k; 256 CTAs for 8192 rows, two per SM, whose pipelines overlap);
+//    the other CTAs hand their int32 partial sums to the first through
+//    distributed shared memory, which adds them in rank order and applies the
 //    scales.  No global scratch, no atomics, deterministic.
 //  * Every wait is bounded; a wait that runs out sets LOOM_DEVERR_TIMEOUT,
 //    the kernel skips the remaining work, still meets every cluster barrier,
@@ -53,7 +54,6 @@ constexpr int TC_N = 16;                   // vectors per pass (MMA N)
 constexpr int TC_KS = 128;                 // k (bytes) per stage
 constexpr int TC_KSLICES = TC_KS / 16;     // MMAs per stage (K = 16 each)
 constexpr int TC_STAGES_PER_BLOCK = 64;    // stages whose products share accumulators
-constexpr int TC_CLUSTER = 2;              // CTAs splitting k for one tile
 constexpr int TC_CONV_WARPS = 8;           // two per TMEM sub-partition, each half a row
 constexpr int TC_PRODUCER_WARP = TC_CONV_WARPS;
 constexpr int TC_MMA_WARP = TC_CONV_WARPS + 1;
@@ -62,7 +62,7 @@ constexpr uint32_t TC_W_BYTES = TC_M * TC_KS;          // 16 KiB
 constexpr uint32_t TC_X_BYTES = TC_N * TC_KS;          // 2 KiB
 constexpr uint32_t TC_STAGE_BYTES = TC_W_BYTES + TC_X_BYTES;   // 18 KiB (1024-aligned)
 constexpr uint32_t TC_B_BYTES = TC_N * TC_KS * 2;      // f16 activation tile, 4 KiB
-constexpr uint32_t TC_RED_BYTES = TC_M * TC_N * 4;     // int32 partials handed between CTAs
+constexpr uint32_t TC_RED_BYTES = TC_M * TC_N * 4;     // int32 partials of one peer CTA
 constexpr uint32_t TC_A_COLS = 64;                     // TMEM columns of one f16 A buffer
 // instruction descriptor: D f32, A/B f16, both K-major, N = 16, M = 128
 constexpr uint32_t TC_IDESC = (1u << 4) | ((TC_N >> 3) << 17) | ((TC_M >> 4) << 24);
@@ -82,14 +82,24 @@ struct TcParams {
     int32_t inject_stall;
 };
 
+// Bytes of the stage ring; it also holds the hand-over buffers at the end.
+__host__ __device__ constexpr uint32_t tc_ring_bytes(int S, int peers)
+{
+    return ((uint32_t)S * TC_STAGE_BYTES > (uint32_t)peers * (TC_RED_BYTES + TC_M * 4))
+               ? (uint32_t)S * TC_STAGE_BYTES
+               : (((uint32_t)peers * (TC_RED_BYTES + TC_M * 4) + 1023u) & ~1023u);
+}
+
 struct Layout {
     uint32_t base;  // 1024-aligned shared address
     int S;
+    int peers;      // cluster size - 1
     __device__ uint32_t stage(int s) const { return base + s * TC_STAGE_BYTES; }
-    __device__ uint32_t btile(int a) const { return base + S * TC_STAGE_BYTES + a * TC_B_BYTES; }
-    __device__ uint32_t red() const { return base + S * TC_STAGE_BYTES + 4 * TC_B_BYTES; }
-    __device__ uint32_t red_ok() const { return red() + TC_RED_BYTES; }
-    __device__ uint32_t bars() const { return red_ok() + TC_M * 4; }
+    __device__ uint32_t btile(int a) const { return base + tc_ring_bytes(S, peers) + a * TC_B_BYTES; }
+    // The hand-over buffers reuse the stage ring once every stage is consumed.
+    __device__ uint32_t red() const { return base; }
+    __device__ uint32_t red_ok() const { return red() + peers * TC_RED_BYTES; }
+    __device__ uint32_t bars() const { return base + tc_ring_bytes(S, peers) + 2 * TC_B_BYTES; }
     __device__ uint32_t full(int s) const { return bars() + 8 * s; }
     __device__ uint32_t empty(int s) const { return bars() + 8 * (S + s); }
     __device__ uint32_t aready(int a) const { return bars() + 8 * (2 * S + a); }
@@ -99,9 +109,9 @@ struct Layout {
     __device__ uint32_t abort_flag() const { return tmem_slot() + 4; }
 };
 
-uint32_t tc_smem_bytes(int S)
+uint32_t tc_smem_bytes(int S, int cs)
 {
-    return 1024 + S * TC_STAGE_BYTES + 4 * TC_B_BYTES + TC_RED_BYTES + TC_M * 4 + 8 * (2 * S + 9) + 16;
+    return 1024 + tc_ring_bytes(S, cs - 1) + 2 * TC_B_BYTES + 8 * (2 * S + 9) + 16;
 }
 
 // ---- PTX wrappers ----------------------------------------------------------
@@ -230,6 +240,7 @@ __device__ __forceinline__ void set_abort(const Layout &L, const TcParams &q)
     dev::flag_error(q.error, LOOM_DEVERR_TIMEOUT);
 }
 
+template <int CS>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     dot_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                   const TcParams q)
@@ -239,12 +250,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     Layout L;
     L.base = (raw + 1023u) & ~1023u;
     L.S = q.depth;
+    L.peers = CS - 1;
     const int S = q.depth;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
-    const int32_t row0 = (int32_t)(blockIdx.x / TC_CLUSTER) * TC_M;
-    const int32_t per_rank = (q.stages_total + TC_CLUSTER - 1) / TC_CLUSTER;
+    const int32_t row0 = (int32_t)(blockIdx.x / CS) * TC_M;
+    const int32_t per_rank = (q.stages_total + CS - 1) / CS;
     const int32_t s_begin = (int32_t)rank * per_rank;
     const int32_t ns = max(0, min(q.stages_total, s_begin + per_rank) - s_begin);
     const int ng = TC_KSLICES * ((ns + TC_STAGES_PER_BLOCK - 1) / TC_STAGES_PER_BLOCK);   // accumulators
@@ -415,13 +427,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (!ok)
             set_abort(L, q);
-        // the second CTA of the pair hands its partial sums to the first
-        if (rank == 1 && h == 0) {
-            const uint32_t dst = map_to_rank(L.red() + t * TC_N * 4, 0);
+    }
+
+    // Every CTA of the cluster is past its stage ring (and its copies have
+    // landed) before the ring memory of the first CTA receives the partials.
+    tc_fence_before();
+    cluster_sync();
+    if (warp < TC_CONV_WARPS) {
+        const int h = warp >> 2;
+        const int t = 32 * (warp & 3) + lane;
+        // the other CTAs of the cluster hand their partial sums to the first
+        if (rank >= 1 && h == 0) {
+            const uint32_t dst = map_to_rank(L.red() + (rank - 1) * TC_RED_BYTES + t * TC_N * 4, 0);
 #pragma unroll
             for (int b = 0; b < TC_N; b += 4)
                 st_cluster_v4(dst + b * 4, isum[b], isum[b + 1], isum[b + 2], isum[b + 3]);
-            const uint32_t okdst = map_to_rank(L.red_ok() + t * 4, 0);
+            const uint32_t okdst = map_to_rank(L.red_ok() + (rank - 1) * TC_M * 4 + t * 4, 0);
             asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(okdst), "r"(ok && !aborted(L) ? 1u : 0u)
                          : "memory");
         }
@@ -433,18 +454,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     if (rank == 0 && threadIdx.x < TC_M) {
         const int t = threadIdx.x;
-        uint32_t peer_ok;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(peer_ok) : "r"(L.red_ok() + t * 4));
-        const bool valid = ok && !aborted(L) && peer_ok != 0;
+        bool valid = ok && !aborted(L);
+#pragma unroll
+        for (int r = 0; r < CS - 1; ++r) {
+            uint32_t peer_ok;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(peer_ok) : "r"(L.red_ok() + r * TC_M * 4 + t * 4));
+            valid = valid && peer_ok != 0;
+        }
         const int32_t row = row0 + t;
         if (row < q.n_rows) {
             const float sw = __ldg(q.scale_w + row);
 #pragma unroll
             for (int b = 0; b < TC_N; ++b) {
                 if (b < q.batch) {
-                    uint32_t other;
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(other) : "r"(L.red() + (t * TC_N + b) * 4));
-                    const int32_t total = isum[b] + (int32_t)other;
+                    int32_t total = isum[b];   // peers added in rank order
+#pragma unroll
+                    for (int r = 0; r < CS - 1; ++r) {
+                        uint32_t other;
+                        asm volatile("ld.shared.u32 %0, [%1];"
+                                     : "=r"(other)
+                                     : "r"(L.red() + r * TC_RED_BYTES + (t * TC_N + b) * 4));
+                        total += (int32_t)other;
+                    }
                     const int64_t o = (int64_t)row * q.y_stride + b;
                     q.y[o] = valid ? __fmul_rn(__int2float_rn(total), __fmul_rn(sw, __ldg(q.scale_x + b)))
                                    : __int_as_float(0x7fc00000);
@@ -501,11 +532,16 @@ bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t o
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Cluster size: four CTAs share a tile's k when each still gets a long
+// stream (two CTAs per SM then overlap their pipelines), else two.
+int tc_cluster(int32_t k) { return (k + TC_KS - 1) / TC_KS >= 64 ? 4 : 2; }
+
 // f32 accumulators of one CTA (16 columns each)
 int32_t tc_groups(int32_t k)
 {
     const int32_t stages = (k + TC_KS - 1) / TC_KS;
-    const int32_t per_rank = (stages + TC_CLUSTER - 1) / TC_CLUSTER;
+    const int cs = tc_cluster(k);
+    const int32_t per_rank = (stages + cs - 1) / cs;
     return TC_KSLICES * ((per_rank + TC_STAGES_PER_BLOCK - 1) / TC_STAGES_PER_BLOCK);
 }
 
@@ -539,12 +575,14 @@ bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass)
 
 uint32_t dot_tc_smem_bytes(int depth, int32_t k)
 {
-    const uint32_t b = tc_smem_bytes(depth);
+    const uint32_t b = tc_smem_bytes(depth, tc_cluster(k));
     const uint32_t floor = tc_tmem_cols(k) == 512u ? TC_MIN_SMEM_512 : TC_MIN_SMEM_256;
     return b > floor ? b : floor;
 }
 
 int dot_tc_rows_per_cluster() { return TC_M; }
+
+int dot_tc_cluster(int32_t k) { return tc_cluster(k); }
 
 cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t stream)
 {
@@ -573,8 +611,9 @@ cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t
     q.wait_ns = p.wait_ns;
     q.inject_stall = p.inject_stall;
 
-    cudaError_t e = cudaFuncSetAttribute(dot_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L.smem_bytes);
+    const int cs = tc_cluster((int32_t)k);
+    auto kernel = cs == 4 ? dot_tc_kernel<4> : dot_tc_kernel<2>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_bytes);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -584,12 +623,14 @@ cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = TC_CLUSTER;
+    attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dot_tc_kernel, tmw, tmx, q);
+    if ((int)L.cluster[0] != cs)
+        return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, kernel, tmw, tmx, q);
 }
 
 }  // namespace loom

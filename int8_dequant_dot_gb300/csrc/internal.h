@@ -74,13 +74,13 @@ uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps);
 int dot_rows_per_warp(DotKernel kind, int tuned_rows_per_warp);
 cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream);
 
-// tensor-core path (dot_tc.cu): 128-row tiles, k split over a cluster of two CTAs
+// tensor-core path (dot_tc.cu): 128-row tiles, k split over a cluster of 2 or 4 CTAs
 bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass);
 uint32_t dot_tc_smem_bytes(int depth, int32_t k);
 int dot_tc_rows_per_cluster();
 constexpr int DOT_TC_THREADS = 320;
-constexpr int DOT_TC_DEFAULT_DEPTH = 4;
-constexpr int DOT_TC_CLUSTER = 2;
+constexpr int DOT_TC_DEFAULT_DEPTH = 5;
+int dot_tc_cluster(int32_t k);
 cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t stream);
 
 // ---- unpack ----------------------------------------------------------------

@@ -136,10 +136,11 @@ loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned,
         return aligned ? LOOM_ERR_SHAPE : LOOM_ERR_ALIGN;
     if (use_tc) {
         const int64_t rows = dot_tc_rows_per_cluster();
-        const int64_t grid = (batch == 0) ? 0 : DOT_TC_CLUSTER * ceil_div(n_rows, rows);
+        const int cs = dot_tc_cluster((int32_t)k);
+        const int64_t grid = (batch == 0) ? 0 : cs * ceil_div(n_rows, rows);
         fill_launch(out, grid, DOT_TC_THREADS, dot_tc_smem_bytes((int)depth, (int32_t)k), (uint32_t)rows,
                     LOOM_KERNEL_DOT_TENSOR);
-        out->cluster[0] = DOT_TC_CLUSTER;
+        out->cluster[0] = (uint32_t)cs;
         return LOOM_OK;
     }
     const DotKernel kind = dot_select(aligned, (int32_t)k, pass);
