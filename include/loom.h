@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define LOOM_ABI_VERSION 1
+#define LOOM_ABI_VERSION 2
 
 typedef enum loom_status {
     LOOM_OK = 0,
@@ -60,18 +60,22 @@ typedef enum loom_op {
                                     warps_per_cta, units_per_warp, chunk_bytes} */
     LOOM_OP_I8_DEQUANT_DOT = 3   /* workload {n_rows, k, batch, staged (0/1), depth,
                                     warps_per_cta, rows_per_warp, engine (0 auto, 1 dp4a,
-                                    2 tensor)} */
+                                    2 tensor), workspace (0/1, default 1), sm_count (0 =
+                                    the current device), tc_units_per_stage,
+                                    tc_a_buffers, tc_ctas_per_sm} */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
- * (words, segments or output rows) map onto each CTA -- onto each cluster of
- * cluster[0] CTAs when that is above 1; the grid is cluster[0] times the
+ * (words, segments or output rows) map onto each CTA; the grid is the
  * ceiling division of the workload by it, and units past the workload in the
- * last CTA do no loads and no stores. */
+ * last CTA do no loads and no stores.  The tensor-core dot is persistent
+ * instead: its grid is min(work units, CTAs per SM x SMs) and each CTA takes
+ * an equal contiguous share -- at most units_per_cta -- of the list of
+ * 128-row x 128-k weight units (whole 128-row bands when no workspace). */
 typedef struct loom_launch {
     uint32_t grid[3];
     uint32_t block[3];
-    uint32_t cluster[3];    /* {1,1,1}, or {2 or 4,1,1} for LOOM_KERNEL_DOT_TENSOR */
+    uint32_t cluster[3];    /* {1,1,1}: no kernel uses thread-block clusters */
     uint32_t subgroup_size; /* 32 */
     uint32_t smem_bytes;    /* dynamic shared memory per CTA */
     uint32_t units_per_cta;
@@ -85,14 +89,15 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 2 */
 #define LOOM_KERNEL_DOT_DIRECT 6    /* plain loads (unaligned or k % 16 != 0) */
 #define LOOM_KERNEL_DOT_TENSOR 7    /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass;
-                                       clusters of 2 or 4 CTAs split k */
+                                       persistent grid, stream-K split of the weights */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8
 
 /*
  * Host launch-configuration routine: maps a workload to a launch without
- * touching the device.  [P3] "A kernel owns two signatures" and "Workload is
+ * touching the device (the tensor-core dot reads the SM count of the current
+ * device unless the workload gives one).  [P3] "A kernel owns two signatures" and "Workload is
  * not workgroup count": the workload scalars alone determine the grid by
  * ceiling division; for LOOM_OP_I8_UNPACK 1009 words give 4 CTAs of 256.
  * `workload` holds `n_workload` scalars as listed for each loom_op; trailing
@@ -153,12 +158,36 @@ loom_status loom_row_sum_batched(const float *d_values, int64_t num_segments, in
  * of a row holds elements 4j..4j+3, element 4j+i in bits [8i, 8i+7] as a
  * signed byte (the little-endian int8 array viewed as int32 words).
  * d_y: f32 [n_rows][batch]; d_acc: int32 [n_rows][batch] or NULL.
- * Errors: NULL -> LOOM_ERR_NULL; misaligned -> LOOM_ERR_ALIGN; k % 4 != 0,
- * k > 131068 (|acc| must stay below 2^31) or negative sizes -> LOOM_ERR_SHAPE.
+ * d_workspace / workspace_bytes: see loom_i8_dequant_dot_workspace_bytes
+ * (NULL / 0 is always valid).
+ * Errors: NULL -> LOOM_ERR_NULL; misaligned (the workspace: to 256 bytes) ->
+ * LOOM_ERR_ALIGN; k % 4 != 0, k > 131068 (|acc| must stay below 2^31) or
+ * negative sizes -> LOOM_ERR_SHAPE; a workspace shorter than its query ->
+ * LOOM_ERR_ARG.
  */
 loom_status loom_i8_dequant_dot(const int32_t *d_w_packed, const float *d_scale_w, int32_t n_rows,
                                 int32_t k, const int32_t *d_x_packed, const float *d_scale_x,
-                                int32_t batch, float *d_y, int32_t *d_acc, void *stream);
+                                int32_t batch, float *d_y, int32_t *d_acc, void *d_workspace,
+                                int64_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of the workspace that lets loom_i8_dequant_dot split 128-row bands
+ * of W between CTAs on the current device (0 when the tensor-core kernel is
+ * not taken: batch < 3, k < 16 or k % 16 != 0).  Splitting spreads the
+ * weights evenly over the SMs whatever n_rows is; without a workspace each
+ * CTA takes whole bands, which is slower when there are few bands per SM.
+ * The workspace (d_workspace, caller-owned device memory, 256-byte aligned)
+ * must be zero-filled once before its first use; every call that has
+ * completed on the device -- including one that timed out -- leaves it ready
+ * for the next (its arrival counters back at zero).  Calls that may run at
+ * the same time (other streams, other host threads) must not share one
+ * workspace.  workspace_bytes smaller than this
+ * size -> LOOM_ERR_ARG; d_workspace NULL -> no split.
+ * Errors: NULL bytes -> LOOM_ERR_NULL; sizes as for loom_i8_dequant_dot ->
+ * LOOM_ERR_SHAPE; no usable device -> LOOM_ERR_CUDA.
+ */
+loom_status loom_i8_dequant_dot_workspace_bytes(int32_t n_rows, int32_t k, int32_t batch,
+                                                int64_t *bytes);
 
 /*
  * Unpack and convert: d_out[4j + i] = (float) signed byte i of d_packed[j].

@@ -39,6 +39,12 @@ typedef struct loom_tuning {
                                out after wait_ns; results become NaN, the error word gets
                                LOOM_DEVERR_TIMEOUT, and the device stays usable */
     int64_t wait_ns;        /* limit of each device wait in ns; 0 = default (1 s) */
+    /* tensor-core dot schedule (depth above = its shared-memory stages) */
+    int32_t tc_units_per_stage; /* 128-k weight units per stage, 1 or 2; 0 = default (2) */
+    int32_t tc_a_buffers;       /* f16 A buffers in tensor memory, at least 2; 0 = default (3, or 4 at one
+                                   CTA per SM); the remaining columns hold accumulators */
+    int32_t tc_ctas_per_sm;     /* 1 (512 tensor-memory columns each) or 2 (256); 0 = 2 */
+    int32_t reserved;           /* must be 0 */
 } loom_tuning;
 
 /* loom_row_sum_batched with tuning (NULL = defaults).  Extra errors:
@@ -51,12 +57,14 @@ loom_status loom_row_sum_batched_ex(const float *d_values, int64_t num_segments,
                                     float *d_full_sum, float *d_tail_sum, int32_t *d_error,
                                     const loom_tuning *tuning, void *stream);
 
-/* loom_i8_dequant_dot with a device error word (may be NULL) and tuning. */
+/* loom_i8_dequant_dot with a device error word (may be NULL) and tuning.
+ * Extra errors: a tensor-core schedule that does not fit (shared or tensor
+ * memory) -> LOOM_ERR_ARG. */
 loom_status loom_i8_dequant_dot_ex(const int32_t *d_w_packed, const float *d_scale_w,
                                    int32_t n_rows, int32_t k, const int32_t *d_x_packed,
                                    const float *d_scale_x, int32_t batch, float *d_y,
-                                   int32_t *d_acc, int32_t *d_error, const loom_tuning *tuning,
-                                   void *stream);
+                                   int32_t *d_acc, void *d_workspace, int64_t workspace_bytes,
+                                   int32_t *d_error, const loom_tuning *tuning, void *stream);
 
 #ifdef __cplusplus
 }

@@ -53,7 +53,7 @@ LOOM_PATH_TENSOR = 3
 EXPORTS = (
     "loom_launch_config", "loom_full_tile_sum", "loom_row_sum_batched", "loom_i8_dequant_dot",
     "loom_i8_unpack", "loom_status_string", "loom_abi_version", "loom_row_sum_batched_ex",
-    "loom_i8_dequant_dot_ex",
+    "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes",
 )
 
 
@@ -79,7 +79,9 @@ class loom_tuning(ctypes.Structure):
     _fields_ = [("depth", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("units_per_warp", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
                 ("chunk_bytes", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
-                ("wait_ns", ctypes.c_int64)]
+                ("wait_ns", ctypes.c_int64), ("tc_units_per_stage", ctypes.c_int32),
+                ("tc_a_buffers", ctypes.c_int32), ("tc_ctas_per_sm", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 def _bind() -> ctypes.CDLL:
@@ -94,9 +96,10 @@ def _bind() -> ctypes.CDLL:
         "loom_row_sum_batched": [P, i64, i64, i32, i32, P, P, i32, P, P, P, P, P, P],
         "loom_row_sum_batched_ex": [P, i64, i64, i32, i32, P, P, i32, P, P, P, P, P,
                                     ctypes.POINTER(loom_tuning), P],
-        "loom_i8_dequant_dot": [P, P, i32, i32, P, P, i32, P, P, P],
-        "loom_i8_dequant_dot_ex": [P, P, i32, i32, P, P, i32, P, P, P,
+        "loom_i8_dequant_dot": [P, P, i32, i32, P, P, i32, P, P, P, i64, P],
+        "loom_i8_dequant_dot_ex": [P, P, i32, i32, P, P, i32, P, P, P, i64, P,
                                    ctypes.POINTER(loom_tuning), P],
+        "loom_i8_dequant_dot_workspace_bytes": [i32, i32, i32, ctypes.POINTER(i64)],
         "loom_i8_unpack": [P, i64, P, P],
         "loom_status_string": [i32],
         "loom_abi_version": [],
@@ -199,9 +202,11 @@ def loom_row_sum_batched(values, num_segments: int, seg_stride: int, rows: int, 
 
 def make_tuning(depth: int = 0, path: int = LOOM_PATH_AUTO, units_per_warp: int = 0,
                 warps_per_cta: int = 0, chunk_bytes: int = 0, inject_stall: bool = False,
-                wait_ns: int = 0) -> loom_tuning:
+                wait_ns: int = 0, tc_units_per_stage: int = 0, tc_a_buffers: int = 0,
+                tc_ctas_per_sm: int = 0) -> loom_tuning:
     return loom_tuning(int(depth), int(path), int(units_per_warp), int(warps_per_cta),
-                       int(chunk_bytes), int(bool(inject_stall)), int(wait_ns))
+                       int(chunk_bytes), int(bool(inject_stall)), int(wait_ns),
+                       int(tc_units_per_stage), int(tc_a_buffers), int(tc_ctas_per_sm), 0)
 
 
 def loom_row_sum_batched_ex(values, num_segments: int, seg_stride: int, rows: int, lanes: int,
@@ -225,28 +230,83 @@ def _dot_outputs(w, n_rows, batch, want_acc):
     return y, acc
 
 
+def loom_i8_dequant_dot_workspace_bytes(n_rows: int, k: int, batch: int) -> int:
+    """Bytes of the split-band workspace on the current device (0: none is used)."""
+    out = ctypes.c_int64(0)
+    _check(_lib.loom_i8_dequant_dot_workspace_bytes(int(n_rows), int(k), int(batch),
+                                                    ctypes.byref(out)),
+           "loom_i8_dequant_dot_workspace_bytes")
+    return int(out.value)
+
+
+def dot_workspace(n_rows: int, k: int, batch: int, device=None):
+    """A zero-filled workspace for ``loom_i8_dequant_dot`` on ``device`` (None when the
+    call would not use one).  The caller owns it; calls that may overlap need one each."""
+    import torch
+    nbytes = loom_i8_dequant_dot_workspace_bytes(n_rows, k, batch)
+    if nbytes == 0:
+        return None
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+#: workspace="auto": one zero-filled workspace per (device, stream), kept for reuse
+AUTO = "auto"
+_workspaces: dict = {}
+
+
+def _workspace(workspace, like, n_rows, k, batch, stream_handle):
+    """(address, bytes) of the workspace argument."""
+    if workspace is None:
+        return None, 0
+    if not (isinstance(workspace, str) and workspace == AUTO):
+        if isinstance(workspace, tuple):
+            return workspace
+        return _ptr(workspace), workspace.numel() * workspace.element_size()
+    import torch
+    nbytes = loom_i8_dequant_dot_workspace_bytes(n_rows, k, batch)
+    if nbytes == 0:
+        return None, 0
+    dev = like.device if hasattr(like, "device") else torch.device("cuda", torch.cuda.current_device())
+    key = (dev.index, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        # the zero fill runs on torch's current stream, the call on stream_handle:
+        # wait for both sides (also before an outgrown workspace is released)
+        torch.cuda.synchronize(dev)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)
+        _workspaces[key] = ws
+    return ws.data_ptr(), ws.numel()
+
+
 def loom_i8_dequant_dot(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_x, batch: int, *,
-                        y=None, acc=None, want_acc: bool = False, stream=None):
-    """``y[n_rows][batch]`` (and ``acc`` when requested); returns ``(y, acc)``."""
+                        y=None, acc=None, want_acc: bool = False, workspace=AUTO, stream=None):
+    """``y[n_rows][batch]`` (and ``acc`` when requested); returns ``(y, acc)``.
+    ``workspace``: a zero-filled tensor (see ``dot_workspace``), an ``(address, bytes)``
+    pair, None (no split), or "auto" (kept per device and stream)."""
     if y is None:
         y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
         acc = acc if acc is not None else acc2
+    st = _stream(stream, w_packed)
+    wp, wb = _workspace(workspace, w_packed, n_rows, k, batch, st)
     _check(_lib.loom_i8_dequant_dot(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
                                     _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
-                                    _stream(stream, w_packed)), "loom_i8_dequant_dot")
+                                    wp, int(wb), st), "loom_i8_dequant_dot")
     return y, acc
 
 
 def loom_i8_dequant_dot_ex(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_x, batch: int,
-                           *, y=None, acc=None, want_acc: bool = False, error=None, tuning=None,
-                           stream=None):
+                           *, y=None, acc=None, want_acc: bool = False, workspace=AUTO, error=None,
+                           tuning=None, stream=None):
     if y is None:
         y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
         acc = acc if acc is not None else acc2
     tp = ctypes.byref(tuning) if tuning is not None else None
+    st = _stream(stream, w_packed)
+    wp, wb = _workspace(workspace, w_packed, n_rows, k, batch, st)
     _check(_lib.loom_i8_dequant_dot_ex(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
                                        _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
-                                       _ptr(error), tp, _stream(stream, w_packed)),
+                                       wp, int(wb), _ptr(error), tp, st),
            "loom_i8_dequant_dot_ex")
     return y, acc
 

@@ -453,7 +453,7 @@ cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L,
     const int nb = p.batch;
     switch (kind) {
     case DotKernel::Tensor:
-        return launch_dot_tc(p, L, stream);
+        return cudaErrorInvalidValue;   // launched by launch_dot_tc with its schedule
     case DotKernel::StagedK:
         return nb == 1 ? launch_staged_k<1>(p, L, stream) : launch_staged_k<2>(p, L, stream);
     case DotKernel::StagedB:

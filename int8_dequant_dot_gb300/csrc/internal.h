@@ -65,6 +65,8 @@ struct DotParams {
     int32_t rows_per_warp;  // lanes-across-k path
     uint64_t wait_ns;
     int32_t inject_stall;
+    void *workspace;        // tensor-core path: split-band workspace, or NULL
+    int64_t workspace_bytes;
 };
 
 enum class DotKernel { StagedK, StagedB, Direct, Tensor };
@@ -74,14 +76,30 @@ uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps);
 int dot_rows_per_warp(DotKernel kind, int tuned_rows_per_warp);
 cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream);
 
-// tensor-core path (dot_tc.cu): 128-row tiles, k split over a cluster of 2 or 4 CTAs
+// tensor-core path (dot_tc.cu): a persistent grid splits the list of
+// 128-row x 128-k weight units into equal contiguous ranges
+struct DotTcConfig {
+    int32_t depth;            // shared-memory stages; 0 = default
+    int32_t units_per_stage;  // 1 or 2; 0 = default
+    int32_t a_bufs;           // f16 A buffers in tensor memory; 0 = default
+    int32_t ctas_per_sm;      // 1 or 2; 0 = default
+};
+struct DotTcPlan {
+    int64_t grid;
+    int64_t total_units;
+    int32_t units_per_band, quantum;
+    int32_t depth, ups, na, ng;
+    uint32_t tmem_cols, smem_bytes;
+    bool split;               // bands may be split between CTAs (needs the workspace)
+    int64_t sm_count;         // SMs the grid was sized for
+};
 bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass);
-uint32_t dot_tc_smem_bytes(int depth, int32_t k);
-int dot_tc_rows_per_cluster();
-constexpr int DOT_TC_THREADS = 320;
-constexpr int DOT_TC_DEFAULT_DEPTH = 5;
-int dot_tc_cluster(int32_t k);
-cudaError_t launch_dot_tc(const DotParams &p, const loom_launch &L, cudaStream_t stream);
+int dot_tc_threads();
+int dot_tc_rows_per_band();
+bool dot_tc_plan(int64_t n_rows, int32_t k, int64_t sm_count, const DotTcConfig &cfg, bool split,
+                 DotTcPlan *out);
+int64_t dot_tc_workspace_bytes(const DotTcPlan &plan);
+cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream);
 
 // ---- unpack ----------------------------------------------------------------
 constexpr int UNPACK_BLOCK = 256;

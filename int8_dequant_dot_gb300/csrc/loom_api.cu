@@ -47,6 +47,7 @@ struct Tuning {
     int chunk_bytes;
     int stall;
     uint64_t wait_ns;
+    DotTcConfig tc;
 };
 
 bool valid_warps(int64_t w) { return w == 1 || w == 2 || w == 4 || w == 8; }
@@ -67,12 +68,15 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
     out->chunk_bytes = 0;
     out->stall = 0;
     out->wait_ns = DEFAULT_WAIT_NS;
+    out->tc = DotTcConfig{0, 0, 0, 0};
     if (!t)
         return LOOM_OK;
     if (t->depth < 0 || t->depth > LOOM_MAX_DEPTH || t->path < 0 || t->path > 3 ||
         t->units_per_warp < 0 || t->units_per_warp > 32 || t->wait_ns < 0 ||
         (t->warps_per_cta != 0 && !valid_warps(t->warps_per_cta)) ||
-        (t->chunk_bytes != 0 && !valid_chunk(t->chunk_bytes)))
+        (t->chunk_bytes != 0 && !valid_chunk(t->chunk_bytes)) || t->tc_units_per_stage < 0 ||
+        t->tc_units_per_stage > 2 || t->tc_a_buffers < 0 || t->tc_a_buffers > 8 ||
+        t->tc_ctas_per_sm < 0 || t->tc_ctas_per_sm > 2 || t->reserved != 0)
         return LOOM_ERR_ARG;
     if (t->depth)
         out->depth = t->depth;
@@ -83,6 +87,20 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
     out->stall = t->inject_stall != 0;
     if (t->wait_ns)
         out->wait_ns = (uint64_t)t->wait_ns;
+    out->tc = DotTcConfig{t->depth, t->tc_units_per_stage, t->tc_a_buffers, t->tc_ctas_per_sm};
+    return LOOM_OK;
+}
+
+// SMs of the current device (the persistent tensor-core grid is sized by it).
+loom_status current_sm_count(int64_t *sms)
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    *sms = n;
     return LOOM_OK;
 }
 
@@ -115,9 +133,13 @@ loom_status row_sum_geometry(int64_t num_segments, int64_t rows, int64_t lanes, 
     return LOOM_OK;
 }
 
-// engine: 0 = automatic, 1 = dp4a kernels only, 2 = tensor cores
+// engine: 0 = automatic, 1 = dp4a kernels only, 2 = tensor cores.  For the
+// tensor-core kernel `tc` holds its schedule (tc.depth = stages), `split`
+// whether a workspace lets bands be split between CTAs, and `sms` the SM
+// count the persistent grid is sized for; *plan receives the schedule.
 loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned, int64_t depth,
-                         int64_t warps, int64_t rows_per_warp, int64_t engine, loom_launch *out)
+                         int64_t warps, int64_t rows_per_warp, int64_t engine, const DotTcConfig &tc,
+                         bool split, int64_t sms, loom_launch *out, DotTcPlan *plan)
 {
     if (n_rows < 0 || n_rows > 0x7fffffff || k < 0 || k > MAX_K || (k % 4) != 0 || batch < 0 ||
         batch > 0x7fffffff)
@@ -130,19 +152,24 @@ loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned,
     const int32_t pass = (int32_t)(batch < DOT_MAX_BATCH_PER_PASS ? batch : DOT_MAX_BATCH_PER_PASS);
     const bool tc_ok = dot_tc_eligible(aligned, (int32_t)k, pass);
     const bool use_tc = (engine == 2 || (engine == 0 && pass >= 3)) && tc_ok;
-    if (depth == 0)
-        depth = use_tc ? DOT_TC_DEFAULT_DEPTH : DOT_DEFAULT_DEPTH;
     if (engine == 2 && !tc_ok)
         return aligned ? LOOM_ERR_SHAPE : LOOM_ERR_ALIGN;
     if (use_tc) {
-        const int64_t rows = dot_tc_rows_per_cluster();
-        const int cs = dot_tc_cluster((int32_t)k);
-        const int64_t grid = (batch == 0) ? 0 : cs * ceil_div(n_rows, rows);
-        fill_launch(out, grid, DOT_TC_THREADS, dot_tc_smem_bytes((int)depth, (int32_t)k), (uint32_t)rows,
+        DotTcPlan pl;
+        DotTcConfig c = tc;
+        c.depth = (int32_t)depth;
+        if (!dot_tc_plan(n_rows, (int32_t)k, sms, c, split, &pl))
+            return LOOM_ERR_ARG;
+        const int64_t grid = batch == 0 ? 0 : pl.grid;
+        const int64_t per_cta = pl.grid ? pl.quantum * ceil_div(pl.total_units / pl.quantum, pl.grid) : 0;
+        fill_launch(out, grid, (uint32_t)dot_tc_threads(), pl.smem_bytes, (uint32_t)per_cta,
                     LOOM_KERNEL_DOT_TENSOR);
-        out->cluster[0] = (uint32_t)cs;
+        if (plan)
+            *plan = pl;
         return LOOM_OK;
     }
+    if (depth == 0)
+        depth = DOT_DEFAULT_DEPTH;
     const DotKernel kind = dot_select(aligned, (int32_t)k, pass);
     const int64_t rows_per_cta = warps * dot_rows_per_warp(kind, (int)rows_per_warp);
     const int64_t grid = (batch == 0) ? 0 : ceil_div(n_rows, rows_per_cta);
@@ -225,9 +252,21 @@ loom_status row_sum_common(const float *values, int64_t num_segments, int64_t se
 
 // ---- dequantised dot ------------------------------------------------------
 
+// Workspace of the tensor-core path for n_rows x k on `sms` SMs: enough for
+// the largest persistent grid (two CTAs per SM) whatever the schedule.
+int64_t dot_workspace_bytes(int64_t n_rows, int64_t k, int64_t sms)
+{
+    DotTcPlan pl;
+    DotTcConfig c{0, 1, 0, 2};
+    if (n_rows <= 0 || k < 16 || !dot_tc_plan(n_rows, (int32_t)k, sms, c, true, &pl))
+        return 0;
+    return dot_tc_workspace_bytes(pl);
+}
+
 loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, int32_t k,
                        const int32_t *x, const float *scale_x, int32_t batch, float *y, int32_t *acc,
-                       int32_t *error, const loom_tuning *tuning, void *stream)
+                       void *workspace, int64_t workspace_bytes, int32_t *error,
+                       const loom_tuning *tuning, void *stream)
 {
     if (n_rows < 0 || batch < 0 || k < 0 || k > MAX_K || (k % 4) != 0)
         return LOOM_ERR_SHAPE;
@@ -240,8 +279,10 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     if ((k > 0 && (!w || !x)) || !scale_w || !scale_x || !y)  // k == 0 reads no weights
         return LOOM_ERR_NULL;
     if (misaligned(w, 4) || misaligned(scale_w, 4) || misaligned(x, 4) || misaligned(scale_x, 4) ||
-        misaligned(y, 4) || misaligned(acc, 4) || misaligned(error, 4))
+        misaligned(y, 4) || misaligned(acc, 4) || misaligned(error, 4) || misaligned(workspace, 256))
         return LOOM_ERR_ALIGN;
+    if (workspace_bytes < 0 || (workspace && workspace_bytes == 0))
+        return LOOM_ERR_ARG;
     const bool can_stage = !misaligned(w, 16) && !misaligned(x, 16) && (k % 16) == 0;
     bool staged;
     int engine = 0;
@@ -257,15 +298,26 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         staged = can_stage;
     }
     const int32_t kw = k / 4;
+    int64_t sms = 0;
+    if (staged && k >= 16 && (k % 16) == 0 && engine != 1) {
+        st = current_sm_count(&sms);   // the tensor-core grid is sized by the device
+        if (st != LOOM_OK)
+            return st;
+    }
+    const bool split = workspace != nullptr;
     for (int32_t b0 = 0; b0 < batch; b0 += DOT_MAX_BATCH_PER_PASS) {
         const int32_t nb = (batch - b0) < DOT_MAX_BATCH_PER_PASS ? (batch - b0) : DOT_MAX_BATCH_PER_PASS;
         loom_launch L;
-        st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, engine, &L);
+        DotTcPlan plan;
+        st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, engine, t.tc, split,
+                          sms ? sms : 1, &L, &plan);
         if (st != LOOM_OK)
             return st;
-        const int depth_used = (int)((L.kernel == LOOM_KERNEL_DOT_TENSOR)
-                                         ? (t.depth ? t.depth : DOT_TC_DEFAULT_DEPTH)
-                                         : (t.depth ? t.depth : DOT_DEFAULT_DEPTH));
+        // the first pass is the widest, so a short workspace stops the call before any launch
+        if (L.kernel == LOOM_KERNEL_DOT_TENSOR && split &&
+            workspace_bytes < dot_tc_workspace_bytes(plan))
+            return LOOM_ERR_ARG;
+        const int depth_used = (int)(t.depth ? t.depth : DOT_DEFAULT_DEPTH);
         const DotKernel kind =
             L.kernel == LOOM_KERNEL_DOT_TENSOR ? DotKernel::Tensor : dot_select(staged, k, nb);
         DotParams p;
@@ -284,7 +336,11 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         p.rows_per_warp = kind == DotKernel::Tensor ? 0 : (int32_t)(L.units_per_cta / (L.block[0] / 32));
         p.wait_ns = t.wait_ns;
         p.inject_stall = t.stall;
-        cudaError_t e = launch_dot(p, kind, L, static_cast<cudaStream_t>(stream));
+        p.workspace = workspace;
+        p.workspace_bytes = workspace_bytes;
+        cudaError_t e = kind == DotKernel::Tensor
+                            ? launch_dot_tc(p, plan, static_cast<cudaStream_t>(stream))
+                            : launch_dot(p, kind, L, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess)
             return LOOM_ERR_CUDA;
     }
@@ -350,11 +406,24 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
             return LOOM_ERR_ARG;
         return row_sum_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0,
                                 opt(4, RS_DEFAULT_DEPTH), opt(6, 0), opt(5, 0), opt(7, 0), out);
-    case LOOM_OP_I8_DEQUANT_DOT:
+    case LOOM_OP_I8_DEQUANT_DOT: {
         if (n_workload < 3)
             return LOOM_ERR_ARG;
-        return dot_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0, opt(4, 0),
-                            opt(5, 0), opt(6, 0), opt(7, 0), out);
+        int64_t sms = opt(9, 0);
+        if (sms < 0 || sms > 4096)
+            return LOOM_ERR_ARG;
+        const bool aligned = opt(3, 1) != 0;
+        const int64_t pass = workload[2] < DOT_MAX_BATCH_PER_PASS ? workload[2] : DOT_MAX_BATCH_PER_PASS;
+        if (sms == 0 && aligned && workload[1] % 16 == 0 && workload[1] >= 16 &&
+            (opt(7, 0) == 2 || (opt(7, 0) == 0 && pass >= 3))) {
+            const loom_status st = current_sm_count(&sms);
+            if (st != LOOM_OK)
+                return st;
+        }
+        const DotTcConfig tc{0, (int32_t)opt(10, 0), (int32_t)opt(11, 0), (int32_t)opt(12, 0)};
+        return dot_geometry(workload[0], workload[1], workload[2], aligned, opt(4, 0), opt(5, 0),
+                            opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms ? sms : 1, out, nullptr);
+    }
     default:
         return LOOM_ERR_ARG;
     }
@@ -400,21 +469,41 @@ loom_status loom_row_sum_batched_ex(const float *d_values, int64_t num_segments,
                           tuning, stream);
 }
 
+loom_status loom_i8_dequant_dot_workspace_bytes(int32_t n_rows, int32_t k, int32_t batch,
+                                                int64_t *bytes)
+{
+    if (!bytes)
+        return LOOM_ERR_NULL;
+    if (n_rows < 0 || batch < 0 || k < 0 || k > MAX_K || (k % 4) != 0)
+        return LOOM_ERR_SHAPE;
+    *bytes = 0;
+    if (n_rows == 0 || batch < 3 || k < 16 || (k % 16) != 0)
+        return LOOM_OK;   // the tensor-core path is not taken
+    int64_t sms = 0;
+    const loom_status st = current_sm_count(&sms);
+    if (st != LOOM_OK)
+        return st;
+    *bytes = dot_workspace_bytes(n_rows, k, sms);
+    return LOOM_OK;
+}
+
 loom_status loom_i8_dequant_dot(const int32_t *d_w_packed, const float *d_scale_w, int32_t n_rows,
                                 int32_t k, const int32_t *d_x_packed, const float *d_scale_x,
-                                int32_t batch, float *d_y, int32_t *d_acc, void *stream)
+                                int32_t batch, float *d_y, int32_t *d_acc, void *d_workspace,
+                                int64_t workspace_bytes, void *stream)
 {
     return dot_common(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y, d_acc,
-                      nullptr, nullptr, stream);
+                      d_workspace, workspace_bytes, nullptr, nullptr, stream);
 }
 
 loom_status loom_i8_dequant_dot_ex(const int32_t *d_w_packed, const float *d_scale_w, int32_t n_rows,
                                    int32_t k, const int32_t *d_x_packed, const float *d_scale_x,
-                                   int32_t batch, float *d_y, int32_t *d_acc, int32_t *d_error,
+                                   int32_t batch, float *d_y, int32_t *d_acc, void *d_workspace,
+                                   int64_t workspace_bytes, int32_t *d_error,
                                    const loom_tuning *tuning, void *stream)
 {
     return dot_common(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y, d_acc,
-                      d_error, tuning, stream);
+                      d_workspace, workspace_bytes, d_error, tuning, stream);
 }
 
 loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)

@@ -3,6 +3,7 @@
 No call here reaches the device: every entry-point call is rejected by host
 validation (or is empty work) before anything is launched.
 """
+import ctypes
 import os
 import re
 import subprocess
@@ -43,7 +44,7 @@ def test_every_declared_symbol_is_exported(loom):
 
 
 def test_version_and_strings(loom):
-    assert loom.loom_abi_version() == 1
+    assert loom.loom_abi_version() == 2
     for st in range(-7, 1):
         assert loom.loom_status_string(st)
     assert loom.loom_status_string(-99) == "unknown status"
@@ -83,24 +84,53 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
     assert L["smem_bytes"] == (4096 if rows * lanes <= 4096 else 8192) + 8
 
 
+SMS = 152   # SM count given to the launch configuration (no device is needed then)
+
+
+def tc_grid(n_rows, k, ctas_per_sm=2, split=True):
+    """Persistent tensor-core grid: one CTA per share of the 128-row x 128-k weight units
+    (whole 128-row bands without a workspace), at most ctas_per_sm per SM."""
+    bands = oracle.workgroups(n_rows, 128)
+    units = bands * oracle.workgroups(k, 128) if split else bands
+    return min(units, ctas_per_sm * SMS), units
+
+
 def test_dot_launch(loom):
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 1])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_K
     assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
-    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 16])
-    assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR and L["cluster"] in ((2, 1, 1), (4, 1, 1))
-    assert L["grid"][0] == L["cluster"][0] * oracle.workgroups(8192, L["units_per_cta"])
+    wl = [8192, 16384, 16, 1, 0, 0, 0, 0, 1, SMS]
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl)
+    assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR and L["cluster"] == (1, 1, 1)
+    assert L["grid"] == (304, 1, 1) and L["block"] == (448, 1, 1)
+    assert L["units_per_cta"] == oracle.workgroups(64 * 128, 304)
+    assert 80 * 1024 <= L["smem_bytes"] <= 113 * 1024          # two CTAs per SM, no third
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl[:8] + [0, SMS])
+    assert L["grid"] == (64, 1, 1) and L["units_per_cta"] == 128   # whole bands
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl + [0, 0, 1])
+    assert L["grid"] == (152, 1, 1) and L["smem_bytes"] >= 120 * 1024   # one CTA per SM
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8191, 16384, 16, 1, 2, 0, 0, 1])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_B
     assert L["grid"][0] == oracle.workgroups(8191, L["units_per_cta"])
     for n in (1, 127, 128, 129, 8192):
-        L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [n, 1024, 5])
-        assert L["grid"][0] == L["cluster"][0] * oracle.workgroups(n, L["units_per_cta"])
+        for k in (16, 1024, 1040, 16384):
+            for split in (0, 1):
+                L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT,
+                                            [n, k, 5, 1, 0, 0, 0, 0, split, SMS])
+                grid, units = tc_grid(n, k, split=bool(split))
+                assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR
+                assert L["grid"][0] == grid and L["units_per_cta"] == oracle.workgroups(units, grid) * (
+                    1 if split else oracle.workgroups(k, 128))
     with pytest.raises(loom.LoomError):   # tensor cores forced where k allows no tile
         loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [64, 8, 16, 1, 2, 0, 0, 2])
+    for bad in ([0, 0, 4], [0, 0, 1], [0, 3, 0], [0, 0, 0, 3], [3, 2, 0, 0]):   # stages, units per stage, A buffers, CTAs per SM
+        with pytest.raises(loom.LoomError) as e:
+            loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT,
+                                    [8192, 16384, 16, 1, bad[0], 0, 0, 2, 1, SMS] + bad[1:])
+        assert e.value.status == loom.LOOM_ERR_ARG
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16388, 16])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_DIRECT
-    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [77, 64, 0])
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [77, 64, 0, 1, 0, 0, 0, 0, 1, SMS])
     assert L["grid"][0] == 0
 
 
@@ -174,7 +204,8 @@ def test_full_tile_sum_validation(loom):
 
 def test_dot_validation(loom):
     lib = loom.library()
-    d = lambda w, n, k, x, b, y=A, acc=None: lib.loom_i8_dequant_dot(w, A, n, k, x, A, b, y, acc, None)
+    d = lambda w, n, k, x, b, y=A, acc=None, ws=None, wsb=0: lib.loom_i8_dequant_dot(
+        w, A, n, k, x, A, b, y, acc, ws, wsb, None)
     assert d(None, 0, 64, None, 4) == loom.LOOM_OK       # no rows
     assert d(None, 4, 64, None, 0) == loom.LOOM_OK       # empty batch
     assert d(None, 4, 64, A, 4) == loom.LOOM_ERR_NULL
@@ -184,6 +215,20 @@ def test_dot_validation(loom):
     assert d(A, -4, 64, A, 4) == loom.LOOM_ERR_SHAPE
     assert d(A + 2, 4, 64, A, 4) == loom.LOOM_ERR_ALIGN
     assert d(A, 4, 64, A, 4, A, A + 3) == loom.LOOM_ERR_ALIGN
+    assert d(A, 4, 64, A, 4, ws=A + 16, wsb=1 << 20) == loom.LOOM_ERR_ALIGN   # workspace: 256 B
+    assert d(A, 4, 64, A, 4, ws=A, wsb=0) == loom.LOOM_ERR_ARG
+    assert d(A, 4, 64, A, 4, ws=A, wsb=-1) == loom.LOOM_ERR_ARG
+
+
+def test_dot_workspace_query(loom):
+    lib = loom.library()
+    out = ctypes.c_int64(-1)
+    q = lambda n, k, b: lib.loom_i8_dequant_dot_workspace_bytes(n, k, b, ctypes.byref(out))
+    for n, k, b in ((8192, 16384, 2), (8192, 16384, 0), (0, 1024, 16), (64, 8, 16), (64, 1040 + 4, 16)):
+        out.value = -1
+        assert q(n, k, b) == loom.LOOM_OK and out.value == 0    # no tensor-core pass
+    assert lib.loom_i8_dequant_dot_workspace_bytes(64, 64, 4, None) == loom.LOOM_ERR_NULL
+    assert q(-1, 64, 4) == loom.LOOM_ERR_SHAPE and q(64, 66, 4) == loom.LOOM_ERR_SHAPE
 
 
 def test_unpack_validation(loom):

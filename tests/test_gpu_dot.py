@@ -30,19 +30,26 @@ def packed(a: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(a.view("<i4"), dtype=np.int32)
 
 
-def run_dot(loom, torch, d, tuning=None, error=None, want_acc=True):
+def run_dot(loom, torch, d, tuning=None, error=None, want_acc=True, workspace="auto"):
     w = to_dev(packed(d["w"]), torch)
     x = to_dev(packed(d["x"]), torch)
     sw, sx = to_dev(d["scale_w"], torch), to_dev(d["scale_x"], torch)
     n, k = d["w"].shape
     b = d["x"].shape[0]
+    # NaN / sentinel outputs: a row the kernel failed to write cannot pass
+    y = torch.full((n, b), float("nan"), dtype=torch.float32, device="cuda")
+    acc = torch.full((n, b), -7777, dtype=torch.int32, device="cuda") if want_acc else None
     if tuning is None and error is None:
-        y, acc = loom.loom_i8_dequant_dot(w, sw, n, k, x, sx, b, want_acc=want_acc)
+        loom.loom_i8_dequant_dot(w, sw, n, k, x, sx, b, y=y, acc=acc, workspace=workspace)
     else:
-        y, acc = loom.loom_i8_dequant_dot_ex(w, sw, n, k, x, sx, b, want_acc=want_acc,
-                                             tuning=tuning, error=error)
+        loom.loom_i8_dequant_dot_ex(w, sw, n, k, x, sx, b, y=y, acc=acc, workspace=workspace,
+                                    tuning=tuning, error=error)
     torch.cuda.synchronize()
     return y.cpu().numpy(), (acc.cpu().numpy() if acc is not None else None)
+
+
+def same_bits(a, b):
+    return np.array_equal(np.asarray(a).view(np.int32), np.asarray(b).view(np.int32))
 
 
 def check(d, y, acc, what, rows=None):
@@ -105,22 +112,23 @@ def test_dot_path_and_depth_invariance(env):
 
 
 @pytest.mark.parametrize("n,k,b", [(128, 1024, 16), (129, 1040, 3), (300, 2064, 7), (5, 16, 16),
-                                   (257, 16384, 16), (64, 49152, 16), (130, 128, 4)])
+                                   (257, 16384, 16), (64, 131056, 16), (130, 128, 4), (2049, 4112, 16)])
 def test_tensor_core_matches_dp4a_bitwise(env, n, k, b):
-    # Row tails (n % 128), k tails (k % 128), one-stage k, the longest k the
-    # tensor-memory budget allows, and partial batches: the tensor-core kernel
-    # must give the dp4a kernels' bits and the oracle's integers.
+    # Row tails (n % 128), k tails (k % 128), one-unit k, the longest k the
+    # library accepts, partial batches and a unit list split unevenly over the
+    # whole grid: the tensor-core kernel must give the dp4a kernels' bits and
+    # the oracle's integers.
     torch, loom = env
     d = small(n, k, b, seed=n + 7 * k + 31 * b)
     y_tc, acc_tc = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR))
     y_dp, acc_dp = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_STAGED))
     assert np.array_equal(acc_tc, acc_dp)
-    assert np.array_equal(y_tc.view(np.int32), y_dp.view(np.int32))
+    assert same_bits(y_tc, y_dp)
     check(d, y_tc, acc_tc, f"tensor {n}x{k}x{b}")
 
 
 def test_tensor_core_exact_at_group_bound(env):
-    # 1024 products of -128 * -128 per accumulator group reach 2**24 exactly.
+    # 1024 products of -128 * -128 per accumulator reach 2**24 exactly.
     torch, loom = env
     k = 4096
     w = np.full((256, k), -128, np.int8)
@@ -133,26 +141,84 @@ def test_tensor_core_exact_at_group_bound(env):
     check(d, y, acc, "group bound")
 
 
-def test_tensor_core_depth_invariance(env):
+# (stages, units per stage, A buffers, CTAs per SM); 0 = default
+TC_SCHEDULES = [(0, 0, 0, 0), (1, 2, 0, 0), (1, 1, 0, 0), (2, 1, 0, 0), (5, 1, 0, 0), (2, 2, 2, 0),
+                (0, 0, 0, 1), (3, 2, 4, 1), (5, 2, 6, 1), (8, 1, 2, 1)]
+
+
+@pytest.mark.parametrize("n,k,b", [(384, 8192, 16), (2049, 4112, 16), (128, 1024, 5), (3, 256, 9)])
+def test_tensor_core_schedule_invariance(env, n, k, b):
+    # Every schedule -- split or whole bands, stage depth and width, A
+    # buffers, one or two CTAs per SM -- gives the same bits.
     torch, loom = env
-    d = small(384, 8192, 16, seed=99)
+    d = small(n, k, b, seed=99 + n + k)
     ref_y, ref_acc = run_dot(loom, torch, d)
     check(d, ref_y, ref_acc, "tensor default")
-    for depth in (1, 2, 3, 4):
-        y, acc = run_dot(loom, torch, d, tuning=loom.make_tuning(depth=depth, path=loom.LOOM_PATH_TENSOR))
-        assert np.array_equal(acc, ref_acc) and np.array_equal(y.view(np.int32), ref_y.view(np.int32)), depth
+    for ws in ("auto", None):
+        for depth, ups, na, cps in TC_SCHEDULES:
+            t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_TENSOR, tc_units_per_stage=ups,
+                                 tc_a_buffers=na, tc_ctas_per_sm=cps)
+            y, acc = run_dot(loom, torch, d, tuning=t, workspace=ws)
+            what = f"ws={ws} schedule={(depth, ups, na, cps)}"
+            assert np.array_equal(acc, ref_acc), what
+            assert same_bits(y, ref_y), what
+
+
+def test_tensor_core_schedules_that_do_not_fit(env):
+    torch, loom = env
+    d = small(128, 1024, 16, seed=5)
+    for depth, ups, na, cps in [(3, 2, 0, 0), (0, 0, 4, 0), (0, 0, 8, 1), (2, 2, 1, 0)]:
+        t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_TENSOR, tc_units_per_stage=ups,
+                             tc_a_buffers=na, tc_ctas_per_sm=cps)
+        with pytest.raises(loom.LoomError) as e:
+            run_dot(loom, torch, d, tuning=t)
+        assert e.value.status == loom.LOOM_ERR_ARG
+
+
+def test_tensor_core_workspace_reuse_and_size(env):
+    # One explicit workspace through many calls of different shapes (its
+    # counters must come back to zero after each), then one too short.
+    torch, loom = env
+    shapes = [(2049, 4112, 16), (300, 2064, 7), (8192 // 8, 16384, 16), (129, 1040, 3)]
+    need = max(loom.loom_i8_dequant_dot_workspace_bytes(n, k, b) for n, k, b in shapes)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for i, (n, k, b) in enumerate(shapes):
+            d = small(n, k, b, seed=11 * i + rep)
+            y, acc = run_dot(loom, torch, d, workspace=ws)
+            check(d, y, acc, f"reuse {rep} {n}x{k}x{b}")
+    n, k, b = shapes[0]
+    short = loom.loom_i8_dequant_dot_workspace_bytes(n, k, b) - 256
+    with pytest.raises(loom.LoomError) as e:
+        run_dot(loom, torch, small(n, k, b, seed=1), workspace=(ws.data_ptr(), short))
+    assert e.value.status == loom.LOOM_ERR_ARG
+    assert loom.loom_i8_dequant_dot_workspace_bytes(n, k, 2) == 0   # dp4a path: none
 
 
 def test_tensor_core_injected_stall(env):
+    # The stalled call reports a timeout and NaN outputs; the workspace it used
+    # is still clean, so the next call through it is exact.
     torch, loom = env
-    d = small(256, 4096, 16, seed=41)
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000, path=loom.LOOM_PATH_TENSOR)
-    y, acc = run_dot(loom, torch, d, tuning=t, error=err)
-    assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
-    assert np.isnan(y).all()
-    y, acc = run_dot(loom, torch, d)
-    check(d, y, acc, "after tensor-core timeout")
+    for n, k in ((256, 4096), (2049, 4112)):
+        d = small(n, k, 16, seed=41 + n)
+        ws = loom.dot_workspace(n, k, 16)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000, path=loom.LOOM_PATH_TENSOR)
+        y, acc = run_dot(loom, torch, d, tuning=t, error=err, workspace=ws)
+        assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
+        assert np.isnan(y).all() and (acc == np.iinfo(np.int32).min).all()
+        y, acc = run_dot(loom, torch, d, workspace=ws)
+        check(d, y, acc, "after tensor-core timeout")
+
+
+def test_tensor_core_batches_over_16(env):
+    # Passes of 16 vectors reuse the workspace one after another.
+    torch, loom = env
+    for b in (19, 32, 35):
+        d = small(700, 2048, b, seed=b)
+        y, acc = run_dot(loom, torch, d)
+        check(d, y, acc, f"b={b}")
 
 
 def test_dot_guard_bands(env):
