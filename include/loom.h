@@ -190,6 +190,23 @@ loom_status loom_i8_dequant_dot_workspace_bytes(int32_t n_rows, int32_t k, int32
                                                 int64_t *bytes);
 
 /*
+ * loom_i8_dequant_dot without a caller workspace and without any device
+ * allocation.  The Loom pages have no counterpart of this entry point: it is
+ * a deployment variant of the call above.  The bands of W are split between
+ * CTAs through scratch that the library holds in a fixed device array (8 MiB
+ * on each device, zero from module load, its address looked up once per
+ * device); results are the same bits as loom_i8_dequant_dot.  The scratch is
+ * shared by every call on a device, so calls that may run at the same time
+ * (other streams, other host threads) must be serialised by the caller.
+ * Errors: as loom_i8_dequant_dot; a problem whose split workspace would not
+ * fit the fixed scratch -> LOOM_ERR_ARG; no usable device -> LOOM_ERR_CUDA.
+ */
+loom_status loom_i8_dequant_dot_noalloc(const int32_t *d_w_packed, const float *d_scale_w,
+                                        int32_t n_rows, int32_t k, const int32_t *d_x_packed,
+                                        const float *d_scale_x, int32_t batch, float *d_y,
+                                        int32_t *d_acc, void *stream);
+
+/*
  * Unpack and convert: d_out[4j + i] = (float) signed byte i of d_packed[j].
  * [P1] "Apply the same controls to a packed dot product" (bit-unpack into
  * four 8-bit integers, then signed integer to float).  One thread per word,

@@ -53,7 +53,7 @@ LOOM_PATH_TENSOR = 3
 EXPORTS = (
     "loom_launch_config", "loom_full_tile_sum", "loom_row_sum_batched", "loom_i8_dequant_dot",
     "loom_i8_unpack", "loom_status_string", "loom_abi_version", "loom_row_sum_batched_ex",
-    "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes",
+    "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes", "loom_i8_dequant_dot_noalloc",
 )
 
 
@@ -100,6 +100,7 @@ def _bind() -> ctypes.CDLL:
         "loom_i8_dequant_dot_ex": [P, P, i32, i32, P, P, i32, P, P, P, i64, P,
                                    ctypes.POINTER(loom_tuning), P],
         "loom_i8_dequant_dot_workspace_bytes": [i32, i32, i32, ctypes.POINTER(i64)],
+        "loom_i8_dequant_dot_noalloc": [P, P, i32, i32, P, P, i32, P, P, P],
         "loom_i8_unpack": [P, i64, P, P],
         "loom_status_string": [i32],
         "loom_abi_version": [],
@@ -308,6 +309,20 @@ def loom_i8_dequant_dot_ex(w_packed, scale_w, n_rows: int, k: int, x_packed, sca
                                        _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
                                        wp, int(wb), _ptr(error), tp, st),
            "loom_i8_dequant_dot_ex")
+    return y, acc
+
+
+def loom_i8_dequant_dot_noalloc(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_x,
+                                batch: int, *, y=None, acc=None, want_acc: bool = False, stream=None):
+    """``loom_i8_dequant_dot`` with the library's fixed device scratch (no workspace, no
+    allocation in the library); calls that may overlap must be serialised."""
+    if y is None:
+        y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
+        acc = acc if acc is not None else acc2
+    _check(_lib.loom_i8_dequant_dot_noalloc(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
+                                            _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y),
+                                            _ptr(acc), _stream(stream, w_packed)),
+           "loom_i8_dequant_dot_noalloc")
     return y, acc
 
 

@@ -8,6 +8,7 @@
 // grid is the ceiling division of the workload by the units one CTA owns,
 // and every entry point launches with exactly the geometry this routine
 // returns, so the division lives in one place.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -263,6 +264,26 @@ int64_t dot_workspace_bytes(int64_t n_rows, int64_t k, int64_t sms)
     return dot_tc_workspace_bytes(pl);
 }
 
+// Argument checks of every dot entry point; *empty is set when there is no work.
+loom_status dot_check(const int32_t *w, const float *scale_w, int32_t n_rows, int32_t k, const int32_t *x,
+                      const float *scale_x, int32_t batch, const float *y, const int32_t *acc,
+                      const int32_t *error, bool *empty)
+{
+    *empty = false;
+    if (n_rows < 0 || batch < 0 || k < 0 || k > MAX_K || (k % 4) != 0)
+        return LOOM_ERR_SHAPE;
+    if (n_rows == 0 || batch == 0) {
+        *empty = true;
+        return LOOM_OK;
+    }
+    if ((k > 0 && (!w || !x)) || !scale_w || !scale_x || !y)  // k == 0 reads no weights
+        return LOOM_ERR_NULL;
+    if (misaligned(w, 4) || misaligned(scale_w, 4) || misaligned(x, 4) || misaligned(scale_x, 4) ||
+        misaligned(y, 4) || misaligned(acc, 4) || misaligned(error, 4))
+        return LOOM_ERR_ALIGN;
+    return LOOM_OK;
+}
+
 loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, int32_t k,
                        const int32_t *x, const float *scale_x, int32_t batch, float *y, int32_t *acc,
                        void *workspace, int64_t workspace_bytes, int32_t *error,
@@ -274,12 +295,11 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     loom_status st = read_tuning(tuning, 0, &t);   // depth 0: each kernel's own default
     if (st != LOOM_OK)
         return st;
-    if (n_rows == 0 || batch == 0)
-        return LOOM_OK;
-    if ((k > 0 && (!w || !x)) || !scale_w || !scale_x || !y)  // k == 0 reads no weights
-        return LOOM_ERR_NULL;
-    if (misaligned(w, 4) || misaligned(scale_w, 4) || misaligned(x, 4) || misaligned(scale_x, 4) ||
-        misaligned(y, 4) || misaligned(acc, 4) || misaligned(error, 4) || misaligned(workspace, 256))
+    bool empty = false;
+    st = dot_check(w, scale_w, n_rows, k, x, scale_x, batch, y, acc, error, &empty);
+    if (st != LOOM_OK || empty)
+        return st;
+    if (misaligned(workspace, 256))
         return LOOM_ERR_ALIGN;
     if (workspace_bytes < 0 || (workspace && workspace_bytes == 0))
         return LOOM_ERR_ARG;
@@ -344,6 +364,38 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         if (e != cudaSuccess)
             return LOOM_ERR_CUDA;
     }
+    return LOOM_OK;
+}
+
+// ---- fixed device scratch of loom_i8_dequant_dot_noalloc ---------------------
+// One array per device, zero at module load like every static device
+// variable; the split-band protocol leaves its counters at zero after each
+// call, so it needs no clearing.  8 MiB covers the workspace of a grid of two
+// CTAs on each of up to 255 SMs.
+constexpr int64_t NOALLOC_SCRATCH_BYTES = 8ll << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::atomic<void *> g_noalloc_addr[NOALLOC_MAX_DEVICES];
+
+// Device address of the scratch array on the current device, looked up once
+// per device with cudaGetSymbolAddress.
+loom_status noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    void *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return LOOM_ERR_CUDA;
+        }
+        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
     return LOOM_OK;
 }
 
@@ -504,6 +556,32 @@ loom_status loom_i8_dequant_dot_ex(const int32_t *d_w_packed, const float *d_sca
 {
     return dot_common(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y, d_acc,
                       d_workspace, workspace_bytes, d_error, tuning, stream);
+}
+
+loom_status loom_i8_dequant_dot_noalloc(const int32_t *d_w_packed, const float *d_scale_w,
+                                        int32_t n_rows, int32_t k, const int32_t *d_x_packed,
+                                        const float *d_scale_x, int32_t batch, float *d_y,
+                                        int32_t *d_acc, void *stream)
+{
+    bool empty = false;
+    loom_status st = dot_check(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y,
+                               d_acc, nullptr, &empty);
+    if (st != LOOM_OK || empty)
+        return st;
+    int64_t need = 0;
+    st = loom_i8_dequant_dot_workspace_bytes(n_rows, k, batch, &need);
+    if (st != LOOM_OK)
+        return st;
+    if (need > NOALLOC_SCRATCH_BYTES)
+        return LOOM_ERR_ARG;   // the grid would outgrow the fixed scratch
+    void *scratch = nullptr;
+    if (need > 0) {
+        st = noalloc_scratch(&scratch);
+        if (st != LOOM_OK)
+            return st;
+    }
+    return dot_common(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y, d_acc,
+                      scratch, scratch ? NOALLOC_SCRATCH_BYTES : 0, nullptr, nullptr, stream);
 }
 
 loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)
