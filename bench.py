@@ -128,7 +128,10 @@ class DeviceWorkload:
             "y16": torch.empty((8192, 16), dtype=f32, device=dev),
         }
         self.tuning = loom.make_tuning(depth=depth) if depth else None
-        self.launches_per_step = 4
+        # one kernel each for segments, wide and gemv; the batched dot is one tensor-core
+        # launch, or two when its schedule splits bands between CTAs (streaming + finishing)
+        L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 16, 1, 0, 0, 0, 0, 1])
+        self.launches_per_step = 3 + (2 if L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR_SPLIT else 1)
 
     def launch(self, name):
         L, d, o, s = self.loom, self.d, self.o, self.stream

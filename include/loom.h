@@ -62,20 +62,22 @@ typedef enum loom_op {
                                     warps_per_cta, rows_per_warp, engine (0 auto, 1 dp4a,
                                     2 tensor), workspace (0/1, default 1), sm_count (0 =
                                     the current device), tc_units_per_stage,
-                                    tc_a_buffers, tc_ctas_per_sm} */
+                                    tc_a_buffers, tc_pipelines, tc_schedule} */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
  * (words, segments or output rows) map onto each CTA; the grid is the
  * ceiling division of the workload by it, and units past the workload in the
- * last CTA do no loads and no stores.  The tensor-core dot is persistent
- * instead: its grid is min(work units, CTAs per SM x SMs) and each CTA takes
- * an equal contiguous share -- at most units_per_cta -- of the list of
- * 128-row x 128-k weight units (whole 128-row bands when no workspace). */
+ * last CTA do no loads and no stores.  The tensor-core dot runs one CTA per
+ * SM instead: with few 128-row bands, a cluster of cluster[0] CTAs per band
+ * (each an equal share of the band's 128-k units); otherwise min(work units,
+ * SMs) CTAs, each an equal contiguous share -- at most units_per_cta -- of the
+ * list of 128-row x 128-k weight units (of whole bands without a workspace). */
 typedef struct loom_launch {
     uint32_t grid[3];
     uint32_t block[3];
-    uint32_t cluster[3];    /* {1,1,1}: no kernel uses thread-block clusters */
+    uint32_t cluster[3];    /* {1,1,1}, or {C,1,1} when the tensor-core dot gives each band a
+                               cluster of C CTAs */
     uint32_t subgroup_size; /* 32 */
     uint32_t smem_bytes;    /* dynamic shared memory per CTA */
     uint32_t units_per_cta;
@@ -89,7 +91,10 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 2 */
 #define LOOM_KERNEL_DOT_DIRECT 6    /* plain loads (unaligned or k % 16 != 0) */
 #define LOOM_KERNEL_DOT_TENSOR 7    /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass;
-                                       persistent grid, stream-K split of the weights */
+                                       one CTA per SM, a cluster per band or whole bands */
+#define LOOM_KERNEL_DOT_TENSOR_SPLIT 8 /* the same kernel over equal shares of all units, then
+                                          a finishing kernel for the bands split between CTAs
+                                          (two launches per pass) */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8
@@ -172,17 +177,19 @@ loom_status loom_i8_dequant_dot(const int32_t *d_w_packed, const float *d_scale_
 
 /*
  * Bytes of the workspace that lets loom_i8_dequant_dot split 128-row bands
- * of W between CTAs on the current device (0 when the tensor-core kernel is
- * not taken: batch < 3, k < 16 or k % 16 != 0).  Splitting spreads the
- * weights evenly over the SMs whatever n_rows is; without a workspace each
- * CTA takes whole bands, which is slower when there are few bands per SM.
- * The workspace (d_workspace, caller-owned device memory, 256-byte aligned)
- * must be zero-filled once before its first use; every call that has
- * completed on the device -- including one that timed out -- leaves it ready
- * for the next (its arrival counters back at zero).  Calls that may run at
- * the same time (other streams, other host threads) must not share one
- * workspace.  workspace_bytes smaller than this
- * size -> LOOM_ERR_ARG; d_workspace NULL -> no split.
+ * of W between CTAs that are not in one cluster, on the current device (0
+ * when the tensor-core kernel is not taken: batch < 3, k < 16 or k % 16 !=
+ * 0).  It is the most any schedule uses; with few bands the call gives each
+ * band a cluster of CTAs and uses none of it.  With many bands, splitting
+ * spreads the weights evenly over the SMs; without a workspace each CTA then
+ * takes whole bands.
+ * The workspace (d_workspace, caller-owned device memory, 256-byte aligned,
+ * any contents) holds the partial sums of the split bands between the
+ * streaming kernel and a second, finishing kernel that the call launches
+ * after it on the same stream.  Calls that may run at the same time (other
+ * streams, other host threads) must not share one workspace.
+ * workspace_bytes smaller than this size -> LOOM_ERR_ARG; d_workspace NULL ->
+ * no split (one launch).
  * Errors: NULL bytes -> LOOM_ERR_NULL; sizes as for loom_i8_dequant_dot ->
  * LOOM_ERR_SHAPE; no usable device -> LOOM_ERR_CUDA.
  */
@@ -194,8 +201,8 @@ loom_status loom_i8_dequant_dot_workspace_bytes(int32_t n_rows, int32_t k, int32
  * allocation.  The Loom pages have no counterpart of this entry point: it is
  * a deployment variant of the call above.  The bands of W are split between
  * CTAs through scratch that the library holds in a fixed device array (8 MiB
- * on each device, zero from module load, its address looked up once per
- * device); results are the same bits as loom_i8_dequant_dot.  The scratch is
+ * on each device, its address looked up once per device); results are the
+ * same bits as loom_i8_dequant_dot.  The scratch is
  * shared by every call on a device, so calls that may run at the same time
  * (other streams, other host threads) must be serialised by the caller.
  * Errors: as loom_i8_dequant_dot; a problem whose split workspace would not

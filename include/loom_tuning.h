@@ -40,11 +40,19 @@ typedef struct loom_tuning {
                                LOOM_DEVERR_TIMEOUT, and the device stays usable */
     int64_t wait_ns;        /* limit of each device wait in ns; 0 = default (1 s) */
     /* tensor-core dot schedule (depth above = its shared-memory stages) */
-    int32_t tc_units_per_stage; /* 128-k weight units per stage, 1 or 2; 0 = default (2) */
-    int32_t tc_a_buffers;       /* f16 A buffers in tensor memory, at least 2; 0 = default (3, or 4 at one
-                                   CTA per SM); the remaining columns hold accumulators */
-    int32_t tc_ctas_per_sm;     /* 1 (512 tensor-memory columns each) or 2 (256); 0 = 2 */
-    int32_t reserved;           /* must be 0 */
+    int32_t tc_units_per_stage; /* 128-k weight units per stage, 1 .. converter groups of a
+                                   pipeline; 0 = default (one per group) */
+    int32_t tc_a_buffers;       /* f16 A buffers per pipeline in tensor memory, at least twice
+                                   the converter groups less one; 0 = default (that minimum);
+                                   the rest of the pipeline's columns hold accumulators */
+    int32_t tc_pipelines;       /* pipelines per CTA (one CTA per SM): 1 (four converter groups,
+                                   all 512 tensor-memory columns) or 2 (two groups and 256
+                                   columns each, the halves of the CTA's units); 0 = 2 */
+    int32_t tc_schedule;        /* how 128-row bands of W map onto CTAs: 0 choose; 1 whole
+                                   bands per CTA; 2 equal shares of all units, split bands
+                                   finished by a second kernel (needs the workspace, else
+                                   LOOM_ERR_ARG); 3 a cluster of CTAs per band (when the SMs
+                                   allow at least two per band, else as 1) */
 } loom_tuning;
 
 /* loom_row_sum_batched with tuning (NULL = defaults).  Extra errors:

@@ -42,6 +42,7 @@ LOOM_KERNEL_DOT_STAGED_K = 4
 LOOM_KERNEL_DOT_STAGED_B = 5
 LOOM_KERNEL_DOT_DIRECT = 6
 LOOM_KERNEL_DOT_TENSOR = 7
+LOOM_KERNEL_DOT_TENSOR_SPLIT = 8
 
 LOOM_MAX_DEPTH = 8
 LOOM_PATH_AUTO = 0
@@ -80,8 +81,8 @@ class loom_tuning(ctypes.Structure):
                 ("units_per_warp", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
                 ("chunk_bytes", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
                 ("wait_ns", ctypes.c_int64), ("tc_units_per_stage", ctypes.c_int32),
-                ("tc_a_buffers", ctypes.c_int32), ("tc_ctas_per_sm", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("tc_a_buffers", ctypes.c_int32), ("tc_pipelines", ctypes.c_int32),
+                ("tc_schedule", ctypes.c_int32)]
 
 
 def _bind() -> ctypes.CDLL:
@@ -204,10 +205,10 @@ def loom_row_sum_batched(values, num_segments: int, seg_stride: int, rows: int, 
 def make_tuning(depth: int = 0, path: int = LOOM_PATH_AUTO, units_per_warp: int = 0,
                 warps_per_cta: int = 0, chunk_bytes: int = 0, inject_stall: bool = False,
                 wait_ns: int = 0, tc_units_per_stage: int = 0, tc_a_buffers: int = 0,
-                tc_ctas_per_sm: int = 0) -> loom_tuning:
+                tc_pipelines: int = 0, tc_schedule: int = 0) -> loom_tuning:
     return loom_tuning(int(depth), int(path), int(units_per_warp), int(warps_per_cta),
                        int(chunk_bytes), int(bool(inject_stall)), int(wait_ns),
-                       int(tc_units_per_stage), int(tc_a_buffers), int(tc_ctas_per_sm), 0)
+                       int(tc_units_per_stage), int(tc_a_buffers), int(tc_pipelines), int(tc_schedule))
 
 
 def loom_row_sum_batched_ex(values, num_segments: int, seg_stride: int, rows: int, lanes: int,
@@ -241,16 +242,16 @@ def loom_i8_dequant_dot_workspace_bytes(n_rows: int, k: int, batch: int) -> int:
 
 
 def dot_workspace(n_rows: int, k: int, batch: int, device=None):
-    """A zero-filled workspace for ``loom_i8_dequant_dot`` on ``device`` (None when the
-    call would not use one).  The caller owns it; calls that may overlap need one each."""
+    """A workspace for ``loom_i8_dequant_dot`` on ``device`` (None when the call would not
+    use one).  The caller owns it; calls that may overlap need one each."""
     import torch
     nbytes = loom_i8_dequant_dot_workspace_bytes(n_rows, k, batch)
     if nbytes == 0:
         return None
-    return torch.zeros(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
 
 
-#: workspace="auto": one zero-filled workspace per (device, stream), kept for reuse
+#: workspace="auto": one workspace per (device, stream), kept for reuse
 AUTO = "auto"
 _workspaces: dict = {}
 
@@ -271,11 +272,10 @@ def _workspace(workspace, like, n_rows, k, batch, stream_handle):
     key = (dev.index, stream_handle)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        # the zero fill runs on torch's current stream, the call on stream_handle:
-        # wait for both sides (also before an outgrown workspace is released)
+        # calls on stream_handle may still use an outgrown workspace: let them
+        # finish before torch may hand its memory to anyone else
         torch.cuda.synchronize(dev)
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
-        torch.cuda.synchronize(dev)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         _workspaces[key] = ws
     return ws.data_ptr(), ws.numel()
 
@@ -283,8 +283,8 @@ def _workspace(workspace, like, n_rows, k, batch, stream_handle):
 def loom_i8_dequant_dot(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_x, batch: int, *,
                         y=None, acc=None, want_acc: bool = False, workspace=AUTO, stream=None):
     """``y[n_rows][batch]`` (and ``acc`` when requested); returns ``(y, acc)``.
-    ``workspace``: a zero-filled tensor (see ``dot_workspace``), an ``(address, bytes)``
-    pair, None (no split), or "auto" (kept per device and stream)."""
+    ``workspace``: a tensor (see ``dot_workspace``), an ``(address, bytes)`` pair, None
+    (no split), or "auto" (kept per device and stream)."""
     if y is None:
         y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
         acc = acc if acc is not None else acc2

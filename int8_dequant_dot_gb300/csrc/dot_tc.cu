@@ -23,29 +23,36 @@
 //    and one packed f16 subtraction of 1152 leaves b.
 //  * The weights stream once.  The work is a list of units -- 128 rows x 128
 //    k of W -- ordered band by band (a band is 128 rows), k fastest.  A
-//    persistent grid of two CTAs per SM splits that list into equal
-//    contiguous ranges (stream-K), so every SM moves the same number of
-//    bytes whatever the number of bands.  A 2-D TMA copy brings one or two
-//    units per stage (128 rows x 128 bytes each, 128-byte swizzle) plus the
-//    matching activation columns into a ring of `depth` shared-memory
-//    stages.  Eight converter warps -- two per tensor-memory sub-partition,
-//    each half of every row -- read their bytes (the swizzle keeps the reads
-//    conflict-free), convert, and write the f16 A operand straight into
-//    tensor memory with tcgen05.st; the activations become a 128-byte-
-//    swizzled K-major f16 B tile in shared memory.
-//  * One thread issues the MMAs; tcgen05.commit releases A/B buffers and
-//    hands finished accumulators to the epilogue warps.
-//  * A band split between CTAs is finished through a caller-owned workspace:
-//    each contributing CTA stores its int32 partial sums, then bumps a
-//    counter; the last to arrive adds all partials in CTA order, applies the
-//    scales, writes the outputs and resets the counter to zero.  Integer
-//    partial sums make the result independent of the arrival order.  With no
-//    workspace every CTA takes whole bands instead.
+//    persistent grid of one CTA per SM splits that list into equal contiguous
+//    ranges (stream-K), so every SM moves the same number of bytes whatever
+//    the number of bands.  Each CTA runs two independent pipelines on the two
+//    halves of its range; each has its own ring of shared-memory stages (2-D
+//    TMA copies of one or two units of 128 rows x 128 bytes, 128-byte
+//    swizzle, plus the matching activation columns), eight converter warps,
+//    an MMA thread, four epilogue warps and half of the tensor memory.  The
+//    converters of a pipeline take one unit of a stage per group of four warps
+//    -- each thread a whole row, whose bytes the swizzle keeps conflict-free --
+//    convert, and write the f16 A operand straight into tensor memory with
+//    tcgen05.st; the activations become a 128-byte-swizzled K-major f16 B tile
+//    in shared memory.
+//  * One thread per pipeline issues the MMAs; tcgen05.commit releases A/B
+//    buffers and hands finished accumulators to the epilogue warps.
+//  * A band shared by the two pipelines is merged in shared memory by the
+//    second to finish it.  A band split between CTAs leaves one record of
+//    int32 partial sums per CTA in a caller-owned workspace; a small second
+//    kernel, launched as a programmatic dependent of the first, adds the
+//    records of each split band in CTA order, applies the scales and writes
+//    the outputs, so the streaming kernel ends without any cross-CTA
+//    handshake.  With no workspace every CTA takes whole bands instead.
 //  * Every wait is bounded; a wait that runs out sets LOOM_DEVERR_TIMEOUT,
 //    every role stops at its next wait, issued copies and MMAs are allowed to
-//    finish, split bands still reach their counters (so the workspace is left
-//    clean), tensor memory is freed and the affected outputs are NaN.
+//    finish, records are still written (marked invalid), tensor memory is
+//    freed and the affected outputs are NaN.
 #include <cuda.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -58,20 +65,26 @@ constexpr int TC_N = 16;                     // vectors per pass (MMA N)
 constexpr int TC_KU = 128;                   // k (bytes) per unit
 constexpr int TC_KSLICES = TC_KU / 16;       // MMAs per unit (K = 16 each)
 constexpr int TC_UNITS_PER_GROUP = 8;        // units per f32 accumulator: 8 x 128 products
-constexpr int TC_CONV_WARPS = 8;             // two per TMEM sub-partition, each half a row
-constexpr int TC_EPI_WARP0 = TC_CONV_WARPS;  // four epilogue warps, one per sub-partition
+// Warps of a pipeline with g converter groups (four warps each, one per
+// tensor-memory sub-partition): 4 g converters, four epilogue warps (one per
+// sub-partition), the producer and the MMA issuer.
 constexpr int TC_EPI_WARPS = 4;
-constexpr int TC_PRODUCER_WARP = TC_EPI_WARP0 + TC_EPI_WARPS;
-constexpr int TC_MMA_WARP = TC_PRODUCER_WARP + 1;
-constexpr int TC_THREADS = 32 * (TC_MMA_WARP + 1);
+__host__ __device__ constexpr int tc_pipe_warps(int groups) { return 4 * groups + TC_EPI_WARPS + 2; }
+constexpr int TC_MAX_PIPES = 2;
+constexpr int TC_MAX_GROUPS = 4;
+constexpr int TC_MAX_CLUSTER = 4;                        // CTAs sharing one band
+constexpr int TC_THREADS = 32 * 2 * tc_pipe_warps(2);   // the largest CTA: two pipelines of two groups
+constexpr uint32_t TC_TMEM_COLS = 512;                   // the whole SM: one CTA per SM
 constexpr uint32_t TC_W_BOX = TC_M * TC_KU;          // 16 KiB of weights per unit
 constexpr uint32_t TC_X_UNIT = TC_N * TC_KU;         // 2 KiB of activations per unit
 constexpr uint32_t TC_B_BYTES = TC_N * TC_KU * 2;    // f16 activation tile of one unit, 4 KiB
 constexpr uint32_t TC_A_COLS = 64;                   // TMEM columns of one f16 A buffer
 constexpr uint32_t TC_ACC_COLS = TC_N;               // TMEM columns of one f32 accumulator
-constexpr int TC_MAX_UPS = 2;                        // units per stage
 constexpr int TC_MAX_ACC = 16;
-constexpr uint32_t TC_EPI_BAR = 1;                   // named barrier of the epilogue warps
+constexpr int TC_WHOLE = 0;     // every CTA takes whole bands (no workspace)
+constexpr int TC_SPLIT = 1;     // equal shares of the unit list; split bands finished by a second kernel
+constexpr int TC_CLUSTER = 2;   // a cluster of CTAs per band, merged through distributed shared memory
+constexpr uint32_t TC_EPI_BAR = 1;                   // named barriers 1, 2: epilogue warps of pipeline 0, 1
 constexpr uint32_t TC_REC_HDR = 16;                   // record header: validity word + padding
 constexpr uint32_t TC_REC_BYTES = TC_REC_HDR + 128 * 16 * 4;   // one split segment's partial sums
 // instruction descriptor: D f32, A/B f16, both K-major, N = 16, M = 128
@@ -83,27 +96,35 @@ struct TcParams {
     float *y;
     int32_t *acc;
     int32_t *error;
-    uint32_t *counters;   // [2 x SMs] split-band arrival counters, or NULL (no split)
-    char *records;        // [grid][2] records: validity header, then int32 [128][16] partial sums
+    char *records;        // [grid][2] records: validity header, then int32 [128][16] partial sums,
+                          // or NULL (no split)
     int32_t n_rows, batch, y_stride;
     int32_t units_per_band;   // ceil(k / 128)
     int64_t total_units;      // bands * units_per_band
     int32_t quantum;          // units per partition step: 1, or units_per_band (whole bands)
-    int32_t depth;            // shared-memory stages
+    int32_t depth;            // shared-memory stages per pipeline
     int32_t ups;              // units per stage (1 or 2)
-    int32_t na;               // f16 A buffers in tensor memory
-    int32_t ng;               // f32 accumulators in tensor memory
-    uint32_t tmem_cols;
+    int32_t na;               // f16 A buffers per pipeline in tensor memory
+    int32_t ng;               // f32 accumulators per pipeline in tensor memory
+    int32_t pipes;            // pipelines per CTA (1 or 2)
+    int32_t groups;           // converter groups per pipeline (= units per stage)
+    int32_t mode;             // TC_WHOLE, TC_SPLIT or TC_CLUSTER (how bands map onto CTAs)
+    int32_t cluster;          // CTAs per band in TC_CLUSTER mode
+    uint32_t cta_area;        // shared memory in front of the pipelines
+    uint32_t pipe_cols;       // tensor-memory columns of one pipeline
+    uint32_t pipe_bytes;      // shared memory of one pipeline
     uint64_t wait_ns;
     int32_t inject_stall;
 };
 
+// Shared memory of one pipeline (1024-aligned): its stage ring, B tiles and barriers.
 struct Layout {
-    uint32_t base;   // 1024-aligned shared address
-    int S, ups, na, ng;
+    uint32_t base;
+    int S, ups, na, ng, groups;
     __device__ uint32_t stage_bytes() const { return (uint32_t)ups * (TC_W_BOX + TC_X_UNIT); }
     __device__ uint32_t stage(int s) const { return base + (uint32_t)s * stage_bytes(); }
-    __device__ uint32_t xtile(int s) const { return stage(s) + (uint32_t)ups * TC_W_BOX; }
+    // activations of unit bx of stage s: [16 vectors][128 bytes]
+    __device__ uint32_t xtile(int s, int bx) const { return stage(s) + (uint32_t)ups * TC_W_BOX + (uint32_t)bx * TC_X_UNIT; }
     __device__ uint32_t btile(int a) const { return base + (uint32_t)S * stage_bytes() + (uint32_t)a * TC_B_BYTES; }
     __device__ uint32_t bars() const { return btile(na); }
     __device__ uint32_t full(int s) const { return bars() + 8 * s; }
@@ -113,16 +134,53 @@ struct Layout {
     __device__ uint32_t gfull(int g) const { return bars() + 8 * (2 * S + 2 * na + g); }
     __device__ uint32_t gfree(int g) const { return bars() + 8 * (2 * S + 2 * na + ng + g); }
     __device__ uint32_t done() const { return bars() + 8 * (2 * S + 2 * na + 2 * ng); }
-    __device__ uint32_t tmem_slot() const { return done() + 8; }
-    __device__ uint32_t abort_flag() const { return done() + 12; }
-    __device__ uint32_t last_flag() const { return done() + 16; }
-    __device__ uint32_t sx() const { return done() + 24; }   // the pass's vector scales, 16 f32
+    __device__ int n_bars() const { return 2 * S + 2 * na + 2 * ng + 1; }
+    // i-th barrier of the list above and its arrival count
+    __device__ void bar_init(int i) const
+    {
+        uint32_t count;
+        if (i < S) count = 1;
+        else if (i < 2 * S) count = 4 * groups;                 // every converter warp
+        else if (i < 2 * S + na) count = 4;                    // the four warps of one unit
+        else if (i < 2 * S + 2 * na) count = 1;
+        else if (i < 2 * S + 2 * na + ng) count = 1;
+        else if (i < 2 * S + 2 * na + 2 * ng) count = TC_EPI_WARPS;
+        else count = 1;
+        dev::mbar_init(bars() + 8 * i, count);
+    }
 };
 
-uint32_t tc_smem_bytes(int S, int ups, int na, int ng)
+// Shared memory of the whole CTA, in front of the pipelines.
+// Flags, the vector scales, the two pipelines' merge slots and, in a
+// cluster's first CTA, one slot per other CTA of the cluster.
+uint32_t tc_cta_area(int cluster)
 {
-    return 1024u + (uint32_t)S * ups * (TC_W_BOX + TC_X_UNIT) + (uint32_t)na * TC_B_BYTES +
-           8u * (2 * S + 2 * na + 2 * ng + 1) + 16u + 64u;
+    const uint32_t slots = 2u + (uint32_t)(cluster > 1 ? cluster - 1 : 0);
+    return 1024u + ((slots * TC_REC_BYTES + 1023u) & ~1023u);
+}
+
+struct CtaArea {
+    uint32_t base;
+    __device__ uint32_t tmem_slot() const { return base; }
+    __device__ uint32_t abort_flag() const { return base + 4; }
+    __device__ uint32_t merge_ctr() const { return base + 8; }
+    __device__ uint32_t second(int p) const { return base + 16 + 4 * p; }   // merge order, per pipeline
+    __device__ uint32_t sx(int p) const { return base + 64 + 64 * p; }       // the pass's vector scales
+    __device__ uint32_t cluster_in() const { return base + 192; }            // the other ranks' partials arrived
+    __device__ uint32_t merge(int p) const { return base + 1024 + (uint32_t)p * TC_REC_BYTES; }
+    __device__ uint32_t cslot(int r) const { return base + 1024 + (uint32_t)(2 + r) * TC_REC_BYTES; }
+};
+
+uint32_t tc_pipe_bytes(int S, int ups, int na, int ng)
+{
+    const uint32_t b = (uint32_t)S * ups * (TC_W_BOX + TC_X_UNIT) + (uint32_t)na * TC_B_BYTES +
+                       8u * (2 * S + 2 * na + 2 * ng + 1);
+    return (b + 1023u) & ~1023u;
+}
+
+uint32_t tc_smem_bytes(int pipes, int cluster, int S, int ups, int na, int ng)
+{
+    return 1024u + tc_cta_area(cluster) + (uint32_t)pipes * tc_pipe_bytes(S, ups, na, ng);
 }
 
 // ---- PTX wrappers ----------------------------------------------------------
@@ -141,31 +199,71 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Arrive on a barrier of another CTA of the cluster, releasing this thread's
+// (and, through the preceding CTA barrier, its warps') shared-memory stores.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void epi_barrier()
+__device__ __forceinline__ void epi_barrier(int p)
 {
-    asm volatile("bar.sync %0, %1;" ::"n"(TC_EPI_BAR), "n"(32 * TC_EPI_WARPS) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"r"(TC_EPI_BAR + p), "n"(32 * TC_EPI_WARPS) : "memory");
 }
 
 // bar.sync of the epilogue warps that also returns the AND of `v` over them.
-__device__ __forceinline__ bool epi_barrier_and(bool v)
+__device__ __forceinline__ bool epi_barrier_and(int p, bool v)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
         "bar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"(v ? 1u : 0u), "n"(TC_EPI_BAR), "n"(32 * TC_EPI_WARPS)
+        : "r"(v ? 1u : 0u), "r"(TC_EPI_BAR + p), "n"(32 * TC_EPI_WARPS)
         : "memory");
     return r != 0;
-}
-
-// 16-byte copy global (L2) -> shared memory by this thread, completed by cp.async.wait_group.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
@@ -196,6 +294,14 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc, u
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
         "r"(a), "l"(bdesc), "r"(TC_IDESC), "r"(accumulate)
         : "memory");
+}
+
+// The same, accumulating (the enable-input predicate as an immediate).
+__device__ __forceinline__ void tc_mma_acc(uint32_t d, uint32_t a, uint64_t bdesc)
+{
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d), "r"(a), "l"(bdesc),
+                 "r"(TC_IDESC)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar)
@@ -236,22 +342,22 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-__device__ __forceinline__ bool aborted(const Layout &L)
+__device__ __forceinline__ bool aborted(const CtaArea &C)
 {
     uint32_t v;
-    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(L.abort_flag()));
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(C.abort_flag()));
     return v != 0;
 }
 
-__device__ __forceinline__ void set_abort(const Layout &L, const TcParams &q)
+__device__ __forceinline__ void set_abort(const CtaArea &C, const TcParams &q)
 {
-    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(L.abort_flag()), "r"(1u) : "memory");
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(C.abort_flag()), "r"(1u) : "memory");
     dev::flag_error(q.error, LOOM_DEVERR_TIMEOUT);
 }
 
 // Wait for a phase of `bar`; false once the CTA has aborted or the limit
 // has passed (which aborts the CTA).
-__device__ __forceinline__ bool role_wait(const Layout &L, const TcParams &q, uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool role_wait(const CtaArea &L, const TcParams &q, uint32_t bar, uint32_t parity)
 {
     if (dev::mbar_try_wait(bar, parity))
         return true;
@@ -271,7 +377,7 @@ __device__ __forceinline__ bool role_wait(const Layout &L, const TcParams &q, ui
 }
 
 // The same, agreed by every lane of the warp.
-__device__ __forceinline__ bool warp_wait(const Layout &L, const TcParams &q, uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool warp_wait(const CtaArea &L, const TcParams &q, uint32_t bar, uint32_t parity)
 {
     return __all_sync(dev::FULL_MASK, role_wait(L, q, bar, parity));
 }
@@ -317,7 +423,7 @@ struct StageWalk {
 
 // Scale and store the sums of one row (all vectors of this pass); sw is the
 // row's scale, the vector scales are read from shared memory.
-__device__ __forceinline__ void store_row(const TcParams &q, const Layout &L, int64_t row, float sw,
+__device__ __forceinline__ void store_row(const TcParams &q, uint32_t sx_at, int64_t row, float sw,
                                           const int32_t (&sum)[TC_N], bool valid)
 {
     if (row >= q.n_rows)
@@ -326,7 +432,7 @@ __device__ __forceinline__ void store_row(const TcParams &q, const Layout &L, in
     for (int b = 0; b < TC_N; ++b) {
         if (b < q.batch) {
             float sx;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sx) : "r"(L.sx() + 4 * b));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sx) : "r"(sx_at + 4 * b));
             const int64_t o = row * q.y_stride + b;
             q.y[o] = valid ? __fmul_rn(__int2float_rn(sum[b]), __fmul_rn(sw, sx)) : __int_as_float(0x7fc00000);
             if (q.acc)
@@ -335,90 +441,133 @@ __device__ __forceinline__ void store_row(const TcParams &q, const Layout &L, in
     }
 }
 
-// Counter increment with release (this CTA's partial sums, ordered before it
-// by the epilogue barrier, become visible with it) and acquire (the last to
-// arrive sees every other partial).
-__device__ __forceinline__ uint32_t arrive_counter(uint32_t *ctr)
+// Intra-CTA arrival for the band the two pipelines share (release: this
+// pipeline's partial sums in shared memory; acquire: the other's).
+__device__ __forceinline__ uint32_t arrive_merge(uint32_t ctr)
 {
     uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(ctr) : "memory");
     return old;
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 2)
+__global__ void __launch_bounds__(TC_THREADS, 1)
     dot_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                   const TcParams q)
 {
     extern __shared__ unsigned char smem_raw[];
-    const uint32_t raw = dev::smem_u32(smem_raw);
+    const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
+    const CtaArea C{base};
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int PW = tc_pipe_warps(q.groups);
+    const int CONV = 4 * q.groups;             // converter warps of a pipeline
+    const int EPI0 = CONV;                     // its first epilogue warp
+    const int PRODUCER = EPI0 + TC_EPI_WARPS;
+    const int MMA = PRODUCER + 1;
+    const int p = warp / PW;                   // pipeline
+    const int w = warp % PW;                   // role within the pipeline
     Layout L;
-    L.base = (raw + 1023u) & ~1023u;
+    L.base = base + q.cta_area + (uint32_t)p * q.pipe_bytes;
     L.S = q.depth;
     L.ups = q.ups;
     L.na = q.na;
     L.ng = q.ng;
+    L.groups = q.groups;
     const int S = q.depth, NA = q.na, NG = q.ng;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
     const int64_t G = gridDim.x;
     const int64_t cta = blockIdx.x;
-    const int64_t u0 = part_begin(q, cta, G);
-    const int64_t u1 = part_begin(q, cta + 1, G);
     const int32_t UB = q.units_per_band;
+    // this CTA's units, and the halves of its pipelines
+    int64_t U0, U1;
+    uint32_t crank = 0;
+    if (q.mode == TC_CLUSTER) {
+        crank = cluster_rank();   // cluster b = blockIdx.x / C takes band b
+        const int64_t b0 = (int64_t)(blockIdx.x / q.cluster) * UB;
+        U0 = b0 + (int64_t)UB * crank / q.cluster;
+        U1 = b0 + (int64_t)UB * (crank + 1) / q.cluster;
+    } else {
+        U0 = part_begin(q, cta, G);
+        U1 = part_begin(q, cta + 1, G);
+    }
+    const int64_t M = q.pipes == 2 ? U0 + (U1 - U0) / 2 : U0;
+    const int64_t u0 = (q.pipes == 2 && p == 0) ? U0 : M;
+    const int64_t u1 = (q.pipes == 2 && p == 0) ? M : U1;
+    const int64_t ou0 = p == 0 ? M : U0;       // the other pipeline's units (empty with one pipeline)
+    const int64_t ou1 = q.pipes == 2 ? (p == 0 ? U1 : M) : ou0;
 
     // ---- set-up: barriers, flags, tensor memory ------------------------------
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            dev::mbar_init(L.full(s), 1);
-            dev::mbar_init(L.empty(s), TC_CONV_WARPS);
-        }
-        for (int a = 0; a < NA; ++a) {
-            dev::mbar_init(L.aready(a), TC_CONV_WARPS / 2);   // the four warps of one unit
-            dev::mbar_init(L.afree(a), 1);
-        }
-        for (int g = 0; g < NG; ++g) {
-            dev::mbar_init(L.gfull(g), 1);
-            dev::mbar_init(L.gfree(g), TC_EPI_WARPS);
-        }
-        dev::mbar_init(L.done(), 1);
-        asm volatile("st.shared.u32 [%0], 0;" ::"r"(L.abort_flag()) : "memory");
+    // Each producer initialises its pipeline's barriers and at once issues the
+    // copies of its first stages (they need nothing else), so the weights are
+    // on their way while the rest of the CTA sets up.
+    const uint64_t wpol = dev::l2_evict_first_policy();
+    const uint64_t xpol = dev::l2_evict_last_policy();
+    int issued = 0;        // producer: stages issued
+    if (w == PRODUCER && p < q.pipes) {
+        for (int i = lane; i < L.n_bars(); i += 32)
+            L.bar_init(i);
         dev::fence_barrier_init();
+        __syncwarp();
+        if (lane == 0 && !q.inject_stall) {
+            int i = 0;
+            for (StageWalk sw(u0, u1, UB, q.ups); sw.more() && i < S; ++i) {
+                const int cnt = sw.count();
+                dev::mbar_arrive_expect_tx(L.full(i), cnt * (TC_W_BOX + TC_X_UNIT));
+                for (int bx = 0; bx < cnt; ++bx) {
+                    tma_load_2d(L.stage(i) + bx * TC_W_BOX, &tmw, (sw.kb + bx) * TC_KU,
+                                (int32_t)(sw.band * TC_M), L.full(i), wpol);
+                    tma_load_2d(L.xtile(i, bx), &tmx, (sw.kb + bx) * TC_KU, 0, L.full(i), xpol);
+                }
+                sw.next(cnt);
+            }
+            issued = i;
+        }
     }
-    if (warp == TC_MMA_WARP && lane < TC_N) {
-        const float v = lane < q.batch ? __ldg(q.scale_x + lane) : 0.f;
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(L.sx() + 4 * lane), "f"(v) : "memory");
+    if (threadIdx.x == 0) {
+        asm volatile("st.shared.u32 [%0], 0;" ::"r"(C.abort_flag()) : "memory");
+        asm volatile("st.shared.u32 [%0], 0;" ::"r"(C.merge_ctr()) : "memory");
+        if (q.mode == TC_CLUSTER && crank == 0) {
+            dev::mbar_init(C.cluster_in(), (uint32_t)(q.cluster - 1));   // one arrival per other rank
+            dev::fence_barrier_init();
+        }
     }
-    if (warp == TC_PRODUCER_WARP) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(L.tmem_slot()),
-                     "r"(q.tmem_cols)
+    if (p == 0 && w == PRODUCER) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(C.tmem_slot()),
+                     "r"(TC_TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (q.mode == TC_CLUSTER)
+        cluster_sync();   // rank 0's barrier is initialised before any rank arrives on it
     uint32_t tmem;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(L.tmem_slot()));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(C.tmem_slot()));
+    tmem += (uint32_t)p * q.pipe_cols;   // this pipeline's columns
     const uint32_t acc_col = (uint32_t)NA * TC_A_COLS;
 
-    if (warp == TC_PRODUCER_WARP) {
+    if (p >= q.pipes) {
+        // no second pipeline: its warps only meet the final barrier
+    } else if (w == PRODUCER) {
         // ---- producer: 2-D TMA of weight units and activation columns --------
         if (lane == 0) {
-            const uint64_t wpol = dev::l2_evict_first_policy();
-            const uint64_t xpol = dev::l2_evict_last_policy();
-            int issued = 0;
             int i = 0;
             for (StageWalk sw(u0, u1, UB, q.ups); sw.more(); ++i) {
                 const int cnt = sw.count();
                 const int s = i % S;
-                if (i >= S && !role_wait(L, q, L.empty(s), ((i / S) - 1) & 1))
+                if (i < S) {   // issued during set-up (none when stalled on purpose)
+                    sw.next(cnt);
+                    continue;
+                }
+                if (!role_wait(C, q, L.empty(s), ((i / S) - 1) & 1))
                     break;
                 if (!q.inject_stall) {
-                    dev::mbar_arrive_expect_tx(L.full(s), cnt * TC_W_BOX + q.ups * TC_X_UNIT);
-                    for (int bx = 0; bx < cnt; ++bx)
+                    dev::mbar_arrive_expect_tx(L.full(s), cnt * (TC_W_BOX + TC_X_UNIT));
+                    for (int bx = 0; bx < cnt; ++bx) {
                         tma_load_2d(L.stage(s) + bx * TC_W_BOX, &tmw, (sw.kb + bx) * TC_KU,
                                     (int32_t)(sw.band * TC_M), L.full(s), wpol);
-                    tma_load_2d(L.xtile(s), &tmx, sw.kb * TC_KU, 0, L.full(s), xpol);
+                        tma_load_2d(L.xtile(s, bx), &tmx, (sw.kb + bx) * TC_KU, 0, L.full(s), xpol);
+                    }
                     ++issued;
                 }
                 sw.next(cnt);
@@ -428,61 +577,75 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
                 dev::mbar_wait_bounded(L.full(j % S), (j / S) & 1, q.wait_ns);
         }
         __syncwarp();
-    } else if (warp == TC_MMA_WARP) {
+    } else if (w == MMA) {
         // ---- MMA issuer: accumulator g takes up to 8 units of one band ------------
+        // This thread shares its scheduler with converter warps, so the loop
+        // keeps its own work small: descriptors and barrier addresses are
+        // formed once, buffer indices and phases advance by increments.
         if (lane == 0) {
-            int j = 0, g = 0;
+            const uint64_t bdesc0 = smem_desc_sw128(L.btile(0));   // + (byte offset >> 4) per tile and slice
+            const uint32_t aready0 = L.aready(0), afree0 = L.afree(0);
+            const uint32_t gfull0 = L.gfull(0), gfree0 = L.gfree(0);
+            int a = 0, gs = 0;                 // A buffer and accumulator of the next unit / group
+            uint32_t aph = 0, gph = 0;         // their barrier phase parities
+            int g = 0;
             bool ok = true;
             for (int64_t u = u0; u < u1 && ok;) {
                 const int64_t e = min(u1, (u / UB + 1) * UB);   // end of this band's segment
                 for (int64_t gu = u; gu < e && ok; gu += TC_UNITS_PER_GROUP) {
-                    const int gs = g % NG;
-                    if (g >= NG && !role_wait(L, q, L.gfree(gs), ((g / NG) - 1) & 1)) {
+                    if (g >= NG && !role_wait(C, q, gfree0 + 8 * gs, gph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     const int n_in = (int)min((int64_t)TC_UNITS_PER_GROUP, e - gu);
                     const uint32_t d = tmem + acc_col + gs * TC_ACC_COLS;
-                    for (int m = 0; m < n_in; ++m, ++j) {
-                        const int a = j % NA;
-                        if (!role_wait(L, q, L.aready(a), (j / NA) & 1)) {
+                    for (int m = 0; m < n_in; ++m) {
+                        if (!role_wait(C, q, aready0 + 8 * a, aph)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                        const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)a * (TC_B_BYTES >> 4));
+                        const uint32_t ta = tmem + (uint32_t)a * TC_A_COLS;
+                        tc_mma(d, ta, bd, m != 0 ? 1u : 0u);
 #pragma unroll
-                        for (int kk = 0; kk < TC_KSLICES; ++kk) {
-                            const uint64_t bdesc = smem_desc_sw128(L.btile(a) + (kk >> 2) * 2048 + (kk & 3) * 32);
-                            tc_mma(d, tmem + a * TC_A_COLS + kk * 8, bdesc, (m | kk) != 0 ? 1u : 0u);
+                        for (int kk = 1; kk < TC_KSLICES; ++kk)
+                            tc_mma_acc(d, ta + kk * 8, bd + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4));
+                        tc_commit(afree0 + 8 * a);   // A/B buffer a is free once these MMAs complete
+                        if (++a == NA) {
+                            a = 0;
+                            aph ^= 1u;
                         }
-                        tc_commit(L.afree(a));   // A/B buffer a is free once these MMAs complete
                     }
                     if (!ok)
                         break;
-                    tc_commit(L.gfull(gs));   // accumulator gs is final once these complete
+                    tc_commit(gfull0 + 8 * gs);   // accumulator gs is final once these complete
                     ++g;
+                    if (++gs == NG) {
+                        gs = 0;
+                        gph ^= 1u;
+                    }
                 }
                 u = e;
             }
             tc_commit(L.done());   // every MMA issued by this thread has completed
         }
         __syncwarp();
-    } else if (warp < TC_CONV_WARPS) {
+    } else if (w < CONV) {
         // ---- converters: warp w owns tile rows 32 (w % 4) .. +31 (its TMEM lanes)
         // of unit h = w / 4 of each stage (whole 128-byte rows).  Both units of
         // a stage are read at once, so the stage goes back to the producer
         // after one round of loads.
-        const int sub = warp & 3;
-        const int h = warp >> 2;
+        const int sub = w & 3;
+        const int h = w >> 2;
         const int t = 32 * sub + lane;   // tile row
         const uint32_t tlane = (uint32_t)(32 * sub) << 16;
-        const uint32_t xrow = (uint32_t)q.ups * TC_KU;   // bytes per activation row in a stage
         bool ok = true;
         int i = 0, j0 = 0;
         for (StageWalk sw(u0, u1, UB, q.ups); sw.more() && ok; ++i) {
             const int cnt = sw.count();
             const int s = i % S;
-            if (!warp_wait(L, q, L.full(s), (i / S) & 1)) {
+            if (!warp_wait(C, q, L.full(s), (i / S) & 1)) {
                 ok = false;
                 break;
             }
@@ -496,7 +659,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     wv[c] = lds128(wrow + ((c ^ (t & 7)) << 4));
-                xv = lds128(L.xtile(s) + (t >> 3) * xrow + h * TC_KU + (t & 7) * 16);
+                xv = lds128(L.xtile(s, h) + (t >> 3) * TC_KU + (t & 7) * 16);
             }
             __syncwarp();
             if (lane == 0)
@@ -504,7 +667,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
             if (mine) {
                 const int j = j0 + h;
                 const int a = j % NA;
-                if (j >= NA && !warp_wait(L, q, L.afree(a), ((j / NA) - 1) & 1)) {
+                if (j >= NA && !warp_wait(C, q, L.afree(a), ((j / NA) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -515,11 +678,11 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
                     uint32_t r[16];
 #pragma unroll
                     for (int c2 = 0; c2 < 2; ++c2) {
-                        const int4 &w = wv[part * 2 + c2];
-                        i8x4_to_f16x4((uint32_t)w.x, r[c2 * 8 + 0], r[c2 * 8 + 1]);
-                        i8x4_to_f16x4((uint32_t)w.y, r[c2 * 8 + 2], r[c2 * 8 + 3]);
-                        i8x4_to_f16x4((uint32_t)w.z, r[c2 * 8 + 4], r[c2 * 8 + 5]);
-                        i8x4_to_f16x4((uint32_t)w.w, r[c2 * 8 + 6], r[c2 * 8 + 7]);
+                        const int4 &v = wv[part * 2 + c2];
+                        i8x4_to_f16x4((uint32_t)v.x, r[c2 * 8 + 0], r[c2 * 8 + 1]);
+                        i8x4_to_f16x4((uint32_t)v.y, r[c2 * 8 + 2], r[c2 * 8 + 3]);
+                        i8x4_to_f16x4((uint32_t)v.z, r[c2 * 8 + 4], r[c2 * 8 + 5]);
+                        i8x4_to_f16x4((uint32_t)v.w, r[c2 * 8 + 6], r[c2 * 8 + 7]);
                     }
                     tc_st16(tmem + tlane + a * TC_A_COLS + part * 16, r);
                 }
@@ -549,15 +712,24 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
         }
     } else {
         // ---- epilogue warps: accumulators -> int32 row sums -> outputs ------------
-        const int sub = warp & 3;
+        const int sub = w & 3;
         const int t = 32 * sub + lane;   // tile row
         const uint32_t tlane = (uint32_t)(32 * sub) << 16;
-        const int64_t T = q.total_units;
+        const bool leader = w == EPI0 && lane == 0;
+        // the pass's vector scales, one copy per pipeline
+        if (w == EPI0 && lane < TC_N) {
+            const float v = lane < q.batch ? __ldg(q.scale_x + lane) : 0.f;
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(C.sx(p) + 4 * lane), "f"(v) : "memory");
+        }
+        epi_barrier(p);
         bool ok = true;
         int g = 0;
         for (int64_t u = u0; u < u1;) {
             const int64_t band = u / UB;
-            const int64_t e = min(u1, (band + 1) * UB);
+            const int64_t blo = band * UB, bhi = blo + UB;
+            const int64_t e = min(u1, bhi);
+            const int64_t row = band * TC_M + t;
+            const float sw = row < q.n_rows ? __ldg(q.scale_w + row) : 0.f;   // in flight during the drain
             int32_t isum[TC_N];
 #pragma unroll
             for (int b = 0; b < TC_N; ++b)
@@ -566,7 +738,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
                 if (!ok)
                     continue;
                 const int gs = g % NG;
-                if (!warp_wait(L, q, L.gfull(gs), (g / NG) & 1)) {
+                if (!warp_wait(C, q, L.gfull(gs), (g / NG) & 1)) {
                     ok = false;
                     continue;
                 }
@@ -581,112 +753,195 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
                 if (lane == 0)
                     mbar_arrive(L.gfree(gs));
             }
-            const int64_t row = band * TC_M + t;
-            const float sw = row < q.n_rows ? __ldg(q.scale_w + row) : 0.f;
-            const bool whole = u == band * UB && e == (band + 1) * UB;
-            if (whole) {
-                store_row(q, L, row, sw, isum, ok && !aborted(L));
-                u = e;
+            bool valid = ok && !aborted(C);
+            u = e;
+            if (blo >= u0 && bhi <= u1) {
+                store_row(q, C.sx(p), row, sw, isum, valid);   // this pipeline holds the whole band
                 continue;
             }
-            // ---- a split band: store the partial sums, then count this CTA in
-            const int64_t rec = 2 * cta + (u == u0 ? 0 : 1);
+            // ---- the band the two pipelines share: the second to finish adds both
+            if ((blo > ou0 ? blo : ou0) < (bhi < ou1 ? bhi : ou1)) {
+                const uint32_t mine = C.merge(p);
+#pragma unroll
+                for (int b = 0; b < TC_N; b += 4)
+                    sts128(mine + TC_REC_HDR + (t * TC_N + b) * 4, (uint32_t)isum[b], (uint32_t)isum[b + 1],
+                           (uint32_t)isum[b + 2], (uint32_t)isum[b + 3]);
+                valid = epi_barrier_and(p, valid);
+                if (leader) {
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(mine), "r"(valid ? 1u : 0u) : "memory");
+                    const uint32_t second = arrive_merge(C.merge_ctr());
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(C.second(p)), "r"(second) : "memory");
+                }
+                epi_barrier(p);
+                uint32_t second;
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(second) : "r"(C.second(p)));
+                if (!second)
+                    continue;   // the other pipeline finishes this band
+                const uint32_t other = C.merge(p ^ 1);
+                uint32_t hdr;
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hdr) : "r"(other));
+                valid = valid && hdr != 0;
+#pragma unroll
+                for (int b = 0; b < TC_N; b += 4) {
+                    const int4 v4 = lds128(other + TC_REC_HDR + (t * TC_N + b) * 4);
+                    isum[b] += v4.x;
+                    isum[b + 1] += v4.y;
+                    isum[b + 2] += v4.z;
+                    isum[b + 3] += v4.w;
+                }
+            }
+            if (blo >= U0 && bhi <= U1) {
+                store_row(q, C.sx(p), row, sw, isum, valid);   // this CTA holds the whole band
+                continue;
+            }
+            if (q.mode == TC_CLUSTER) {
+                // ---- the CTAs of a cluster share one band: rank 0 adds them in rank order
+                if (crank != 0) {
+                    const uint32_t slot = map_to_rank(C.cslot((int)crank - 1), 0);
+#pragma unroll
+                    for (int b = 0; b < TC_N; b += 4)
+                        st_cluster_v4(slot + TC_REC_HDR + (t * TC_N + b) * 4, (uint32_t)isum[b],
+                                      (uint32_t)isum[b + 1], (uint32_t)isum[b + 2], (uint32_t)isum[b + 3]);
+                    valid = epi_barrier_and(p, valid);   // every row is stored before the release below
+                    if (leader) {
+                        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(slot), "r"(valid ? 1u : 0u) : "memory");
+                        mbar_arrive_remote(map_to_rank(C.cluster_in(), 0));
+                    }
+                    continue;
+                }
+                bool got = mbar_try_wait_cluster(C.cluster_in(), 0);
+                if (!got) {
+                    const uint64_t t0 = dev::global_ns();
+                    for (uint32_t i = 1; !got; ++i) {
+                        got = mbar_try_wait_cluster(C.cluster_in(), 0);
+                        if (!got && (i & 15u) == 0 && dev::global_ns() - t0 > q.wait_ns)
+                            break;
+                    }
+                }
+                if (!got) {
+                    set_abort(C, q);
+                    valid = false;
+                }
+                for (int r = 0; r + 1 < q.cluster; ++r) {
+                    const uint32_t at = C.cslot(r);
+                    uint32_t hdr;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hdr) : "r"(at));
+                    valid = valid && hdr != 0;
+#pragma unroll
+                    for (int b = 0; b < TC_N; b += 4) {
+                        const int4 v4 = lds128(at + TC_REC_HDR + (t * TC_N + b) * 4);
+                        isum[b] += v4.x;
+                        isum[b + 1] += v4.y;
+                        isum[b + 2] += v4.z;
+                        isum[b + 3] += v4.w;
+                    }
+                }
+                store_row(q, C.sx(p), row, sw, isum, valid);
+                continue;
+            }
+            // ---- a band split between CTAs: this CTA's record of it (the
+            // finishing kernel adds the records of every CTA sharing the band)
+            const int64_t rec = 2 * cta + (band == U0 / UB ? 0 : 1);
             char *rp = q.records + rec * TC_REC_BYTES;
             int4 *dst = reinterpret_cast<int4 *>(rp + TC_REC_HDR + t * TC_N * 4);
 #pragma unroll
             for (int b = 0; b < TC_N; b += 4)
                 __stcg(dst + b / 4, make_int4(isum[b], isum[b + 1], isum[b + 2], isum[b + 3]));
-            const bool all_ok = epi_barrier_and(ok && !aborted(L));
-            const int64_t cf = owner_of(band * UB, T, G);
-            const int64_t cl = owner_of((band + 1) * UB - 1, T, G);
-            if (warp == TC_EPI_WARP0 && lane == 0) {
+            const bool all_ok = epi_barrier_and(p, valid);
+            if (leader)
                 __stcg(reinterpret_cast<int4 *>(rp), make_int4(all_ok ? 1 : 0, 0, 0, 0));
-                // the barrier above ordered every row's stores before this release
-                const uint32_t before = arrive_counter(q.counters + cf);
-                const uint32_t last = before == (uint32_t)(cl - cf) ? 1u : 0u;
-                if (last)
-                    q.counters[cf] = 0u;   // every contributor has counted in
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(L.last_flag()), "r"(last) : "memory");
-            }
-            epi_barrier();
-            uint32_t last;
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(last) : "r"(L.last_flag()));
-            if (last) {
-                // the last contributor adds every partial in CTA order
-                int32_t total[TC_N];
-#pragma unroll
-                for (int b = 0; b < TC_N; ++b)
-                    total[b] = 0;
-                bool valid = true;
-                if (e == u1 && all_ok) {
-                    // this CTA's last segment (and no role gave up): its stage ring
-                    // is idle, so every thread copies its row of each record (and
-                    // one header) into it with cp.async, all in flight at once
-                    const int cap = (int)((uint32_t)S * L.stage_bytes() / TC_REC_BYTES);
-                    for (int64_t c0 = cf; c0 <= cl; c0 += cap) {
-                        const int n = (int)min((int64_t)cap, cl - c0 + 1);
-                        for (int m = 0; m < n; ++m) {
-                            const int64_t c = c0 + m;
-                            const int64_t r = 2 * c + (part_begin(q, c, G) / UB == band ? 0 : 1);
-                            const char *src = q.records + r * TC_REC_BYTES;
-                            const uint32_t at = L.base + (uint32_t)m * TC_REC_BYTES;
-#pragma unroll
-                            for (int b = 0; b < TC_N; b += 4)
-                                cp_async16(at + TC_REC_HDR + (t * TC_N + b) * 4, src + TC_REC_HDR + (t * TC_N + b) * 4);
-                            if (t == 0)
-                                cp_async16(at, src);
-                        }
-                        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-                        epi_barrier();   // every thread's copies have landed
-                        for (int m = 0; m < n; ++m) {
-                            const uint32_t at = L.base + (uint32_t)m * TC_REC_BYTES;
-                            uint32_t hdr;
-                            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hdr) : "r"(at));
-                            valid &= hdr != 0;
-#pragma unroll
-                            for (int b = 0; b < TC_N; b += 4) {
-                                const int4 v4 = lds128(at + TC_REC_HDR + (t * TC_N + b) * 4);
-                                total[b] += v4.x;
-                                total[b + 1] += v4.y;
-                                total[b + 2] += v4.z;
-                                total[b + 3] += v4.w;
-                            }
-                        }
-                        epi_barrier();   // the ring is read before the next round lands
-                    }
-                } else {
-                    for (int64_t c = cf; c <= cl; ++c) {
-                        const int64_t r = 2 * c + (part_begin(q, c, G) / UB == band ? 0 : 1);
-                        const char *src = q.records + r * TC_REC_BYTES;
-                        const int hdr = __ldcg(reinterpret_cast<const int *>(src));
-                        const int4 *sp = reinterpret_cast<const int4 *>(src + TC_REC_HDR + t * TC_N * 4);
-#pragma unroll
-                        for (int b = 0; b < TC_N; b += 4) {
-                            const int4 v4 = __ldcg(sp + b / 4);
-                            total[b] += v4.x;
-                            total[b + 1] += v4.y;
-                            total[b + 2] += v4.z;
-                            total[b + 3] += v4.w;
-                        }
-                        valid &= hdr != 0;
-                    }
-                }
-                store_row(q, L, row, sw, total, valid);
-            }
-            u = e;
         }
     }
 
     // ---- teardown: tensor memory is freed only after every MMA has completed
     tc_fence_before();
     __syncthreads();
-    if (warp == TC_PRODUCER_WARP) {
-        if (lane == 0)
-            dev::mbar_wait_bounded(L.done(), 0, q.wait_ns);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the finishing kernel may start
+    if (p == 0 && w == PRODUCER) {
+        if (lane < q.pipes) {
+            Layout Lp = L;
+            Lp.base = base + q.cta_area + (uint32_t)lane * q.pipe_bytes;
+            dev::mbar_wait_bounded(Lp.done(), 0, q.wait_ns);
+        }
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(q.tmem_cols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
                      : "memory");
+    }
+    if (q.mode == TC_CLUSTER)
+        cluster_sync();   // no CTA leaves while another may still write its shared memory
+}
+
+// ---- finishing kernel for bands split between CTAs ------------------------------
+struct FinishParams {
+    const char *records;
+    const float *scale_w;
+    const float *scale_x;
+    float *y;
+    int32_t *acc;
+    int32_t n_rows, batch, y_stride;
+    int32_t units_per_band;
+    int64_t total_units;   // T of the streaming launch
+    int64_t grid;          // its CTA count
+    int64_t bands;
+};
+
+constexpr int TC_FIN_THREADS = 4 * TC_M;   // four threads per row, four vectors each
+
+// Band b of a streaming launch of G CTAs over T units (one unit per partition
+// step) is split when its first and last units belong to different CTAs;
+// each of them left a record of its partial sums (record 2c for the band of
+// CTA c's first unit, 2c + 1 for the other).  One CTA per band adds the
+// records in CTA order, scales and stores.
+__global__ void __launch_bounds__(TC_FIN_THREADS) dot_tc_finish_kernel(const FinishParams f)
+{
+    __shared__ int64_t span[3];   // first and last CTA of the band, and cf's record index
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the streaming kernel's records are complete
+    const int r_in = threadIdx.x >> 2;                    // row within the band
+    const int quad = threadIdx.x & 3;                      // vectors 4 quad .. 4 quad + 3
+    const int64_t T = f.total_units, G = f.grid;
+    const int64_t UB = f.units_per_band;
+    for (int64_t band = blockIdx.x; band < f.bands; band += gridDim.x) {
+        if (threadIdx.x == 0) {
+            const int64_t cf = owner_of(band * UB, T, G);
+            span[0] = cf;
+            span[1] = owner_of((band + 1) * UB - 1, T, G);
+            // the first CTA's record: its head if its range starts at the band, else its tail;
+            // every later CTA starts inside the band (its head record)
+            span[2] = 2 * cf + (T * cf / G == band * UB ? 0 : 1);
+        }
+        __syncthreads();
+        const int64_t cf = span[0], cl = span[1], r0 = span[2];
+        __syncthreads();
+        if (cf == cl)
+            continue;   // one CTA held the whole band and wrote its outputs
+        int32_t tot[4] = {0, 0, 0, 0};
+        bool valid = true;
+        for (int64_t c = cf; c <= cl; ++c) {
+            const int64_t r = c == cf ? r0 : 2 * c;
+            const char *rp = f.records + r * TC_REC_BYTES;
+            const int4 v = __ldcg(reinterpret_cast<const int4 *>(rp + TC_REC_HDR + (r_in * TC_N + 4 * quad) * 4));
+            valid &= __ldcg(reinterpret_cast<const int *>(rp)) != 0;
+            tot[0] += v.x;
+            tot[1] += v.y;
+            tot[2] += v.z;
+            tot[3] += v.w;
+        }
+        const int64_t row = band * TC_M + r_in;
+        if (row >= f.n_rows)
+            continue;
+        const float sw = __ldg(f.scale_w + row);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int b = 4 * quad + i;
+            if (b < f.batch) {
+                const int64_t o = row * f.y_stride + b;
+                f.y[o] = valid ? __fmul_rn(__int2float_rn(tot[i]), __fmul_rn(sw, __ldg(f.scale_x + b)))
+                               : __int_as_float(0x7fc00000);
+                if (f.acc)
+                    f.acc[o] = valid ? tot[i] : INT32_MIN;
+            }
+        }
     }
 }
 
@@ -711,7 +966,7 @@ EncodeTiled encoder()
     return fn;
 }
 
-bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+bool encode_2d_u8_uncached(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                   uint32_t box_outer, CUtensorMapSwizzle swizzle)
 {
     EncodeTiled enc = encoder();
@@ -726,16 +981,76 @@ bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t o
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shared memory per CTA, sized so that every CTA resident on an SM finds its
-// tensor memory free (tcgen05.alloc would otherwise wait for another CTA to
-// finish): with 256 columns each CTA asks for more than a third of the SM's
-// shared memory (at most two CTAs, which together fit the 512 columns); with
-// 512 columns, for more than half (one CTA per SM).
-constexpr uint32_t TC_MIN_SMEM_2 = 80u * 1024u;
-constexpr uint32_t TC_MAX_SMEM_2 = 113u * 1024u;
-constexpr uint32_t TC_MIN_SMEM_1 = 120u * 1024u;
-constexpr uint32_t TC_MAX_SMEM_1 = 227u * 1024u;
+// Host work per call is kept small: the last few tensor maps are reused while
+// their tensor and box are the same (encoding is a driver call).
+struct MapEntry {
+    const void *base;
+    uint64_t inner, outer;
+    uint32_t box_inner, box_outer;
+    CUtensorMapSwizzle swizzle;
+    CUtensorMap map;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[8];
+int g_maps_used = 0, g_maps_next = 0;
 
+bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle)
+{
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_maps_used; ++i) {
+        const MapEntry &m = g_maps[i];
+        if (m.base == base && m.inner == inner && m.outer == outer && m.box_inner == box_inner &&
+            m.box_outer == box_outer && m.swizzle == swizzle) {
+            *map = m.map;
+            return true;
+        }
+    }
+    if (!encode_2d_u8_uncached(map, base, inner, outer, box_inner, box_outer, swizzle))
+        return false;
+    MapEntry &m = g_maps[g_maps_next];
+    m = MapEntry{base, inner, outer, box_inner, box_outer, swizzle, *map};
+    g_maps_next = (g_maps_next + 1) % 8;
+    g_maps_used = g_maps_used < 8 ? g_maps_used + 1 : 8;
+    return true;
+}
+
+// The kernel's dynamic shared-memory limit, raised once per device to the
+// largest size asked for so far.
+std::atomic<int> g_smem_limit[64];
+
+cudaError_t ensure_smem_limit(uint32_t bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaFuncSetAttribute(dot_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    int cur = g_smem_limit[dev].load(std::memory_order_acquire);
+    if ((int)bytes <= cur)
+        return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(dot_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) {
+        while (cur < (int)bytes && !g_smem_limit[dev].compare_exchange_weak(cur, (int)bytes))
+            ;
+    }
+    return e;
+}
+
+// cudaOccupancyMaxActiveClusters answers, per device and launch shape.
+struct ClusterFit {
+    int dev;
+    uint32_t smem;
+    int threads, cluster, n;
+};
+std::mutex g_fit_mu;
+ClusterFit g_fits[16];
+int g_fits_used = 0;
+
+
+// Shared memory per CTA: at least 120 KiB, more than half of the SM's, so
+// that one CTA runs per SM and finds all 512 tensor-memory columns free
+// (tcgen05.alloc would otherwise wait for another CTA to finish).
+constexpr uint32_t TC_MIN_SMEM = 120u * 1024u;
+constexpr uint32_t TC_MAX_SMEM = 227u * 1024u;
 
 int64_t align256(int64_t b) { return (b + 255) & ~(int64_t)255; }
 
@@ -746,42 +1061,76 @@ bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass)
     return aligned && k >= 16 && (k % 16) == 0 && batch_pass >= 1 && batch_pass <= TC_N;
 }
 
-int dot_tc_threads() { return TC_THREADS; }
+int dot_tc_threads(int pipes) { return 32 * pipes * tc_pipe_warps(pipes == 2 ? 2 : TC_MAX_GROUPS); }
 
 int dot_tc_rows_per_band() { return TC_M; }
 
 // Resolve the schedule of one tensor-core launch.  cfg fields of 0 take the
-// defaults: two CTAs per SM, two units per stage, two stages, three A
-// buffers (the remaining tensor memory holds the accumulators).
+// defaults: two pipelines per CTA, two units per stage, two stages, three A
+// buffers per pipeline (the rest of its tensor memory holds accumulators).
+// Bands map onto CTAs in one of three ways (cfg.schedule, 0 = choose):
+//  * a cluster of C CTAs per band (C = 2..4) when that keeps every SM busy --
+//    or, with no workspace, at least three quarters of them: no cross-SM
+//    traffic at all;
+//  * equal shares of the whole unit list (stream-K) when a workspace is given;
+//  * whole bands per CTA otherwise.
 bool dot_tc_plan(int64_t n_rows, int32_t k, int64_t sm_count, const DotTcConfig &cfg, bool split,
                  DotTcPlan *out)
 {
-    const int cps = cfg.ctas_per_sm ? cfg.ctas_per_sm : 2;
-    const int ups = cfg.units_per_stage ? cfg.units_per_stage : 2;
-    if ((cps != 1 && cps != 2) || ups < 1 || ups > TC_MAX_UPS || sm_count < 1)
+    const int pipes = cfg.pipes ? cfg.pipes : 2;
+    if (pipes < 1 || pipes > TC_MAX_PIPES)
         return false;
-    const int depth = cfg.depth ? cfg.depth : (ups == 2 ? 2 : 4);
-    const uint32_t cols = cps == 2 ? 256u : 512u;
-    const int na = cfg.a_bufs ? cfg.a_bufs : (cps == 2 ? 3 : 4);
-    // two converter groups fill consecutive units at once: with one A buffer a
-    // group could wait on a barrier phase two ahead of the last it saw
-    if (depth < 1 || depth > LOOM_MAX_DEPTH || na < 2 || (uint32_t)na * TC_A_COLS + 2 * TC_ACC_COLS > cols)
+    const int groups = pipes == 2 ? 2 : TC_MAX_GROUPS;   // converter groups per pipeline
+    const int ups = cfg.units_per_stage ? cfg.units_per_stage : groups;
+    if (ups < 1 || ups > groups || sm_count < 1 || cfg.schedule < 0 || cfg.schedule > 3)
+        return false;
+    const int depth = cfg.depth ? cfg.depth : (ups >= 2 ? 2 : 4);
+    const uint32_t cols = TC_TMEM_COLS / (uint32_t)pipes;
+    const int na = cfg.a_bufs ? cfg.a_bufs : 2 * groups - 1;
+    // A group's consecutive units are at most 2 groups - 1 apart (a stage cut
+    // short by a band's end is skipped by the groups past its units); with
+    // fewer A buffers than that a group could wait on a barrier phase two
+    // ahead of the last one completed.
+    if (depth < 1 || depth > LOOM_MAX_DEPTH || na < 2 * groups - 1 ||
+        (uint32_t)na * TC_A_COLS + 2 * TC_ACC_COLS > cols)
         return false;
     int ng = (int)((cols - (uint32_t)na * TC_A_COLS) / TC_ACC_COLS);
     ng = ng > TC_MAX_ACC ? TC_MAX_ACC : ng;
-    uint32_t smem = tc_smem_bytes(depth, ups, na, ng);
-    const uint32_t lo = cps == 2 ? TC_MIN_SMEM_2 : TC_MIN_SMEM_1;
-    const uint32_t hi = cps == 2 ? TC_MAX_SMEM_2 : TC_MAX_SMEM_1;
-    if (smem > hi)
-        return false;
-    smem = smem < lo ? lo : smem;
     const int64_t bands = (n_rows + TC_M - 1) / TC_M;
     const int32_t ub = (k + TC_KU - 1) / TC_KU;
     const int64_t total = bands * ub;
-    const int32_t quantum = split ? 1 : ub;
+
+    // CTAs per band for the cluster schedule: each CTA keeps at least one unit per pipeline
+    int64_t c = bands > 0 ? sm_count / bands : 0;
+    c = c > TC_MAX_CLUSTER ? TC_MAX_CLUSTER : c;
+    c = c > ub / pipes ? ub / pipes : c;
+    int mode;
+    if (cfg.schedule == 1)
+        mode = TC_WHOLE;
+    else if (cfg.schedule == 2)
+        mode = TC_SPLIT;
+    else if (cfg.schedule == 3)
+        mode = TC_CLUSTER;
+    else if (c >= 2 && (split ? bands * c == sm_count : 4 * bands * c >= 3 * sm_count))
+        mode = TC_CLUSTER;   // every SM busy (or, with no workspace, most of them)
+    else
+        mode = split ? TC_SPLIT : TC_WHOLE;
+    if (mode == TC_SPLIT && !split)
+        return false;   // the split schedule needs the workspace
+    if (mode == TC_CLUSTER && c < 2)
+        mode = TC_WHOLE;   // one CTA per band already
+    const int cluster = mode == TC_CLUSTER ? (int)c : 1;
+
+    uint32_t smem = tc_smem_bytes(pipes, cluster, depth, ups, na, ng);
+    if (smem > TC_MAX_SMEM)
+        return false;
+    smem = smem < TC_MIN_SMEM ? TC_MIN_SMEM : smem;
+    const int32_t quantum = mode == TC_SPLIT ? 1 : ub;
     const int64_t steps = total / quantum;
-    const int64_t slots = (int64_t)cps * sm_count;
-    out->grid = steps < slots ? steps : slots;
+    if (mode == TC_CLUSTER)
+        out->grid = bands * cluster;
+    else
+        out->grid = steps < sm_count ? steps : sm_count;
     out->quantum = quantum;
     out->units_per_band = ub;
     out->total_units = total;
@@ -789,22 +1138,74 @@ bool dot_tc_plan(int64_t n_rows, int32_t k, int64_t sm_count, const DotTcConfig 
     out->ups = ups;
     out->na = na;
     out->ng = ng;
-    out->tmem_cols = cols;
+    out->pipes = pipes;
+    out->groups = groups;
+    out->mode = mode;
+    out->cluster = cluster;
+    out->cta_area = tc_cta_area(cluster);
+    out->pipe_cols = cols;
+    out->pipe_bytes = tc_pipe_bytes(depth, ups, na, ng);
     out->smem_bytes = smem;
-    out->split = split;
+    out->split = mode == TC_SPLIT;
     out->sm_count = sm_count;
     return true;
 }
 
-// Workspace of a split launch: arrival counters for the largest grid the
-// device runs (two CTAs per SM) at offset 0 -- a fixed place, so calls of
-// any shape find them at zero -- then two partial-sum records (validity
-// header + sums) per CTA of this grid, rewritten by every call.
-static int64_t tc_counter_bytes(int64_t sm_count) { return align256(2 * sm_count * 4); }
-
+// Workspace of a split launch: two partial-sum records (validity header +
+// sums) per CTA, every one written before it is read, so the workspace needs
+// no initialisation.
 int64_t dot_tc_workspace_bytes(const DotTcPlan &plan)
 {
-    return tc_counter_bytes(plan.sm_count) + align256(plan.grid * 2 * (int64_t)TC_REC_BYTES);
+    return plan.split ? align256(plan.grid * 2 * (int64_t)TC_REC_BYTES) : 0;
+}
+
+// Whether every cluster of a cluster-schedule plan is resident at once on the
+// current device (clusters need their CTAs' SMs inside one GPC, so fewer may
+// fit than SMs / cluster).
+bool dot_tc_cluster_fits(const DotTcPlan &plan)
+{
+    if (plan.mode != TC_CLUSTER)
+        return true;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const int threads = dot_tc_threads(plan.pipes);
+    {
+        std::lock_guard<std::mutex> lock(g_fit_mu);
+        for (int i = 0; i < g_fits_used; ++i) {
+            const ClusterFit &f = g_fits[i];
+            if (f.dev == dev && f.smem == plan.smem_bytes && f.threads == threads && f.cluster == plan.cluster)
+                return (int64_t)f.n * plan.cluster >= plan.grid;
+        }
+    }
+    if (ensure_smem_limit(plan.smem_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)dot_tc_threads(plan.pipes), 1, 1);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cudaLaunchAttribute ca[1];
+    ca[0].id = cudaLaunchAttributeClusterDimension;
+    ca[0].val.clusterDim.x = (unsigned)plan.cluster;
+    ca[0].val.clusterDim.y = 1;
+    ca[0].val.clusterDim.z = 1;
+    cfg.attrs = ca;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dot_tc_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_fit_mu);
+        if (g_fits_used < 16)
+            g_fits[g_fits_used++] = ClusterFit{dev, plan.smem_bytes, threads, plan.cluster, n};
+    }
+    return (int64_t)n * plan.cluster >= plan.grid;
 }
 
 cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream)
@@ -814,8 +1215,7 @@ cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_
     const int64_t k = (int64_t)p.k_words * 4;
     CUtensorMap tmw, tmx;
     if (!encode_2d_u8(&tmw, p.w, (uint64_t)k, (uint64_t)p.n_rows, TC_KU, TC_M, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d_u8(&tmx, p.x, (uint64_t)k, (uint64_t)p.batch, (uint32_t)(TC_KU * plan.ups), TC_N,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_2d_u8(&tmx, p.x, (uint64_t)k, (uint64_t)p.batch, TC_KU, TC_N, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     TcParams q;
     q.scale_w = p.scale_w;
@@ -823,14 +1223,11 @@ cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_
     q.y = p.y;
     q.acc = p.acc;
     q.error = p.error;
-    q.counters = nullptr;
     q.records = nullptr;
     if (plan.split) {
         if (!p.workspace || p.workspace_bytes < dot_tc_workspace_bytes(plan))
             return cudaErrorInvalidValue;
-        char *ws = static_cast<char *>(p.workspace);
-        q.counters = reinterpret_cast<uint32_t *>(ws);
-        q.records = ws + tc_counter_bytes(plan.sm_count);
+        q.records = static_cast<char *>(p.workspace);
     }
     q.n_rows = p.n_rows;
     q.batch = p.batch;
@@ -842,20 +1239,62 @@ cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_
     q.ups = plan.ups;
     q.na = plan.na;
     q.ng = plan.ng;
-    q.tmem_cols = plan.tmem_cols;
+    q.pipes = plan.pipes;
+    q.groups = plan.groups;
+    q.mode = plan.mode;
+    q.cluster = plan.cluster;
+    q.cta_area = plan.cta_area;
+    q.pipe_cols = plan.pipe_cols;
+    q.pipe_bytes = plan.pipe_bytes;
     q.wait_ns = p.wait_ns;
     q.inject_stall = p.inject_stall;
 
-    cudaError_t e = cudaFuncSetAttribute(dot_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)plan.smem_bytes);
+    cudaError_t e = ensure_smem_limit(plan.smem_bytes);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
-    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.blockDim = dim3((unsigned)dot_tc_threads(plan.pipes), 1, 1);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, dot_tc_kernel, tmw, tmx, q);
+    cudaLaunchAttribute ca[1];
+    if (plan.mode == TC_CLUSTER) {
+        ca[0].id = cudaLaunchAttributeClusterDimension;
+        ca[0].val.clusterDim.x = (unsigned)plan.cluster;
+        ca[0].val.clusterDim.y = 1;
+        ca[0].val.clusterDim.z = 1;
+        cfg.attrs = ca;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, dot_tc_kernel, tmw, tmx, q);
+    if (e != cudaSuccess || !plan.split)
+        return e;
+
+    // bands split between CTAs: the finishing kernel, a programmatic dependent
+    // (its CTAs are scheduled as the streaming CTAs retire)
+    FinishParams f;
+    f.records = q.records;
+    f.scale_w = p.scale_w;
+    f.scale_x = p.scale_x;
+    f.y = p.y;
+    f.acc = p.acc;
+    f.n_rows = p.n_rows;
+    f.batch = p.batch;
+    f.y_stride = p.y_stride;
+    f.units_per_band = plan.units_per_band;
+    f.total_units = plan.total_units;
+    f.grid = plan.grid;
+    f.bands = plan.total_units / plan.units_per_band;
+    cudaLaunchConfig_t fc = {};
+    fc.gridDim = dim3((unsigned)(f.bands < 4096 ? f.bands : 4096), 1, 1);
+    fc.blockDim = dim3(TC_FIN_THREADS, 1, 1);
+    fc.stream = stream;
+    cudaLaunchAttribute fa[1];
+    fa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    fa[0].val.programmaticStreamSerializationAllowed = 1;
+    fc.attrs = fa;
+    fc.numAttrs = 1;
+    return cudaLaunchKernelEx(&fc, dot_tc_finish_kernel, f);
 }
 
 }  // namespace loom

@@ -76,29 +76,33 @@ uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps);
 int dot_rows_per_warp(DotKernel kind, int tuned_rows_per_warp);
 cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream);
 
-// tensor-core path (dot_tc.cu): a persistent grid splits the list of
-// 128-row x 128-k weight units into equal contiguous ranges
+// tensor-core path (dot_tc.cu): a persistent grid of one CTA per SM splits
+// the list of 128-row x 128-k weight units into equal contiguous ranges; each
+// CTA runs one or two pipelines on the halves of its range
 struct DotTcConfig {
-    int32_t depth;            // shared-memory stages; 0 = default
-    int32_t units_per_stage;  // 1 or 2; 0 = default
-    int32_t a_bufs;           // f16 A buffers in tensor memory; 0 = default
-    int32_t ctas_per_sm;      // 1 or 2; 0 = default
+    int32_t depth;            // shared-memory stages per pipeline; 0 = default
+    int32_t units_per_stage;  // 1 .. converter groups per pipeline; 0 = default
+    int32_t a_bufs;           // f16 A buffers per pipeline in tensor memory; 0 = default
+    int32_t pipes;            // pipelines per CTA, 1 or 2; 0 = default
+    int32_t schedule;         // 0 choose, 1 whole bands, 2 split (workspace), 3 cluster per band
 };
 struct DotTcPlan {
     int64_t grid;
     int64_t total_units;
     int32_t units_per_band, quantum;
-    int32_t depth, ups, na, ng;
-    uint32_t tmem_cols, smem_bytes;
+    int32_t depth, ups, na, ng, pipes, groups;
+    int32_t mode, cluster;    // how bands map onto CTAs; CTAs per band (cluster schedule)
+    uint32_t cta_area, pipe_cols, pipe_bytes, smem_bytes;
     bool split;               // bands may be split between CTAs (needs the workspace)
     int64_t sm_count;         // SMs the grid was sized for
 };
 bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass);
-int dot_tc_threads();
+int dot_tc_threads(int pipes);
 int dot_tc_rows_per_band();
 bool dot_tc_plan(int64_t n_rows, int32_t k, int64_t sm_count, const DotTcConfig &cfg, bool split,
                  DotTcPlan *out);
 int64_t dot_tc_workspace_bytes(const DotTcPlan &plan);
+bool dot_tc_cluster_fits(const DotTcPlan &plan);
 cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream);
 
 // ---- unpack ----------------------------------------------------------------

@@ -69,15 +69,15 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
     out->chunk_bytes = 0;
     out->stall = 0;
     out->wait_ns = DEFAULT_WAIT_NS;
-    out->tc = DotTcConfig{0, 0, 0, 0};
+    out->tc = DotTcConfig{0, 0, 0, 0, 0};
     if (!t)
         return LOOM_OK;
     if (t->depth < 0 || t->depth > LOOM_MAX_DEPTH || t->path < 0 || t->path > 3 ||
         t->units_per_warp < 0 || t->units_per_warp > 32 || t->wait_ns < 0 ||
         (t->warps_per_cta != 0 && !valid_warps(t->warps_per_cta)) ||
         (t->chunk_bytes != 0 && !valid_chunk(t->chunk_bytes)) || t->tc_units_per_stage < 0 ||
-        t->tc_units_per_stage > 2 || t->tc_a_buffers < 0 || t->tc_a_buffers > 8 ||
-        t->tc_ctas_per_sm < 0 || t->tc_ctas_per_sm > 2 || t->reserved != 0)
+        t->tc_units_per_stage > 4 || t->tc_a_buffers < 0 || t->tc_a_buffers > 8 ||
+        t->tc_pipelines < 0 || t->tc_pipelines > 2 || t->tc_schedule < 0 || t->tc_schedule > 3)
         return LOOM_ERR_ARG;
     if (t->depth)
         out->depth = t->depth;
@@ -88,7 +88,7 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
     out->stall = t->inject_stall != 0;
     if (t->wait_ns)
         out->wait_ns = (uint64_t)t->wait_ns;
-    out->tc = DotTcConfig{t->depth, t->tc_units_per_stage, t->tc_a_buffers, t->tc_ctas_per_sm};
+    out->tc = DotTcConfig{t->depth, t->tc_units_per_stage, t->tc_a_buffers, t->tc_pipelines, t->tc_schedule};
     return LOOM_OK;
 }
 
@@ -162,9 +162,13 @@ loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned,
         if (!dot_tc_plan(n_rows, (int32_t)k, sms, c, split, &pl))
             return LOOM_ERR_ARG;
         const int64_t grid = batch == 0 ? 0 : pl.grid;
-        const int64_t per_cta = pl.grid ? pl.quantum * ceil_div(pl.total_units / pl.quantum, pl.grid) : 0;
-        fill_launch(out, grid, (uint32_t)dot_tc_threads(), pl.smem_bytes, (uint32_t)per_cta,
-                    LOOM_KERNEL_DOT_TENSOR);
+        // weight units per CTA (at most): a cluster's share of one band, or a share of the list
+        const int64_t per_cta = pl.grid == 0        ? 0
+                                : pl.cluster > 1    ? ceil_div(pl.units_per_band, pl.cluster)
+                                                    : pl.quantum * ceil_div(pl.total_units / pl.quantum, pl.grid);
+        fill_launch(out, grid, (uint32_t)dot_tc_threads(pl.pipes), pl.smem_bytes, (uint32_t)per_cta,
+                    pl.split ? LOOM_KERNEL_DOT_TENSOR_SPLIT : LOOM_KERNEL_DOT_TENSOR);
+        out->cluster[0] = (uint32_t)pl.cluster;
         if (plan)
             *plan = pl;
         return LOOM_OK;
@@ -254,11 +258,11 @@ loom_status row_sum_common(const float *values, int64_t num_segments, int64_t se
 // ---- dequantised dot ------------------------------------------------------
 
 // Workspace of the tensor-core path for n_rows x k on `sms` SMs: enough for
-// the largest persistent grid (two CTAs per SM) whatever the schedule.
+// the persistent grid (one CTA per SM) whatever the schedule.
 int64_t dot_workspace_bytes(int64_t n_rows, int64_t k, int64_t sms)
 {
     DotTcPlan pl;
-    DotTcConfig c{0, 1, 0, 2};
+    DotTcConfig c{0, 1, 0, 0, 2};   // the split schedule: the largest any schedule needs
     if (n_rows <= 0 || k < 16 || !dot_tc_plan(n_rows, (int32_t)k, sms, c, true, &pl))
         return 0;
     return dot_tc_workspace_bytes(pl);
@@ -333,13 +337,21 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
                           sms ? sms : 1, &L, &plan);
         if (st != LOOM_OK)
             return st;
+        const bool tensor = L.kernel == LOOM_KERNEL_DOT_TENSOR || L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT;
+        if (tensor && t.tc.schedule == 0 && !dot_tc_cluster_fits(plan)) {
+            // the clusters would not all be resident at once: share the units out instead
+            DotTcConfig c = t.tc;
+            c.schedule = split ? 2 : 1;
+            st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, engine, c, split, sms, &L, &plan);
+            if (st != LOOM_OK)
+                return st;
+        }
         // the first pass is the widest, so a short workspace stops the call before any launch
-        if (L.kernel == LOOM_KERNEL_DOT_TENSOR && split &&
-            workspace_bytes < dot_tc_workspace_bytes(plan))
+        if (L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT && workspace_bytes < dot_tc_workspace_bytes(plan))
             return LOOM_ERR_ARG;
         const int depth_used = (int)(t.depth ? t.depth : DOT_DEFAULT_DEPTH);
-        const DotKernel kind =
-            L.kernel == LOOM_KERNEL_DOT_TENSOR ? DotKernel::Tensor : dot_select(staged, k, nb);
+        const bool on_tc = L.kernel == LOOM_KERNEL_DOT_TENSOR || L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT;
+        const DotKernel kind = on_tc ? DotKernel::Tensor : dot_select(staged, k, nb);
         DotParams p;
         p.w = w;
         p.scale_w = scale_w;
@@ -368,10 +380,9 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
 }
 
 // ---- fixed device scratch of loom_i8_dequant_dot_noalloc ---------------------
-// One array per device, zero at module load like every static device
-// variable; the split-band protocol leaves its counters at zero after each
-// call, so it needs no clearing.  8 MiB covers the workspace of a grid of two
-// CTAs on each of up to 255 SMs.
+// One array per device; the streaming kernel writes every record of it that
+// the finishing kernel reads, so it needs no initialisation.  8 MiB covers the
+// workspace of a grid of one CTA on each of up to 511 SMs.
 constexpr int64_t NOALLOC_SCRATCH_BYTES = 8ll << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
@@ -472,7 +483,7 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
             if (st != LOOM_OK)
                 return st;
         }
-        const DotTcConfig tc{0, (int32_t)opt(10, 0), (int32_t)opt(11, 0), (int32_t)opt(12, 0)};
+        const DotTcConfig tc{0, (int32_t)opt(10, 0), (int32_t)opt(11, 0), (int32_t)opt(12, 0), (int32_t)opt(13, 0)};
         return dot_geometry(workload[0], workload[1], workload[2], aligned, opt(4, 0), opt(5, 0),
                             opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms ? sms : 1, out, nullptr);
     }

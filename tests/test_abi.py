@@ -87,12 +87,21 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
 SMS = 152   # SM count given to the launch configuration (no device is needed then)
 
 
-def tc_grid(n_rows, k, ctas_per_sm=2, split=True):
-    """Persistent tensor-core grid: one CTA per share of the 128-row x 128-k weight units
-    (whole 128-row bands without a workspace), at most ctas_per_sm per SM."""
+def tc_expect(n_rows, k, split=True, pipes=2):
+    """The tensor-core schedule: a cluster of c CTAs per 128-row band (c = 2..4) when that
+    keeps every SM busy -- or, without a workspace, at least three quarters of them; else
+    one CTA per SM over equal shares of the 128-row x 128-k units (of whole bands without
+    a workspace).  Returns (grid, cluster, units per CTA, split)."""
     bands = oracle.workgroups(n_rows, 128)
-    units = bands * oracle.workgroups(k, 128) if split else bands
-    return min(units, ctas_per_sm * SMS), units
+    ub = oracle.workgroups(k, 128)
+    c = min(4, SMS // bands, ub // pipes)
+    if c >= 2 and (bands * c == SMS if split else 4 * bands * c >= 3 * SMS):
+        return bands * c, c, oracle.workgroups(ub, c), False
+    if split:
+        grid = min(bands * ub, SMS)
+        return grid, 1, oracle.workgroups(bands * ub, grid), True
+    grid = min(bands, SMS)
+    return grid, 1, ub * oracle.workgroups(bands, grid), False
 
 
 def test_dot_launch(loom):
@@ -100,34 +109,42 @@ def test_dot_launch(loom):
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_K
     assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
     wl = [8192, 16384, 16, 1, 0, 0, 0, 0, 1, SMS]
+    # 64 bands: with a workspace, equal shares on every SM (streaming + finishing kernel)
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl)
-    assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR and L["cluster"] == (1, 1, 1)
-    assert L["grid"] == (304, 1, 1) and L["block"] == (448, 1, 1)
-    assert L["units_per_cta"] == oracle.workgroups(64 * 128, 304)
-    assert 80 * 1024 <= L["smem_bytes"] <= 113 * 1024          # two CTAs per SM, no third
-    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl[:8] + [0, SMS])
-    assert L["grid"] == (64, 1, 1) and L["units_per_cta"] == 128   # whole bands
-    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl + [0, 0, 1])
-    assert L["grid"] == (152, 1, 1) and L["smem_bytes"] >= 120 * 1024   # one CTA per SM
+    assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR_SPLIT
+    assert L["grid"] == (152, 1, 1) and L["cluster"] == (1, 1, 1) and L["units_per_cta"] == 54
+    assert L["block"] == (896, 1, 1)                            # two pipelines of 14 warps
+    assert 120 * 1024 <= L["smem_bytes"] <= 227 * 1024          # one CTA per SM
+    for ws, sched in ((0, 0), (1, 3)):   # no workspace, or asked for: a cluster of two per band
+        L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl[:8] + [ws, SMS, 0, 0, 0, sched])
+        assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR and L["cluster"] == (2, 1, 1)
+        assert L["grid"] == (128, 1, 1) and L["units_per_cta"] == 64
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl + [0, 0, 0, 1])   # whole bands
+    assert L["grid"] == (64, 1, 1) and L["units_per_cta"] == 128
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl + [0, 0, 1])      # one pipeline
+    assert L["grid"] == (152, 1, 1) and L["block"] == (704, 1, 1)   # four converter groups
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8191, 16384, 16, 1, 2, 0, 0, 1])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_B
     assert L["grid"][0] == oracle.workgroups(8191, L["units_per_cta"])
-    for n in (1, 127, 128, 129, 8192):
+    for n in (1, 127, 128, 129, 2049, 8192, 20000):
         for k in (16, 1024, 1040, 16384):
             for split in (0, 1):
                 L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT,
                                             [n, k, 5, 1, 0, 0, 0, 0, split, SMS])
-                grid, units = tc_grid(n, k, split=bool(split))
-                assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR
-                assert L["grid"][0] == grid and L["units_per_cta"] == oracle.workgroups(units, grid) * (
-                    1 if split else oracle.workgroups(k, 128))
+                grid, cl, per, two = tc_expect(n, k, split=bool(split))
+                assert L["kernel"] == (loom.LOOM_KERNEL_DOT_TENSOR_SPLIT if two else loom.LOOM_KERNEL_DOT_TENSOR)
+                assert (L["grid"][0], L["cluster"][0], L["units_per_cta"]) == (grid, cl, per), (n, k, split)
     with pytest.raises(loom.LoomError):   # tensor cores forced where k allows no tile
         loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [64, 8, 16, 1, 2, 0, 0, 2])
-    for bad in ([0, 0, 4], [0, 0, 1], [0, 3, 0], [0, 0, 0, 3], [3, 2, 0, 0]):   # stages, units per stage, A buffers, CTAs per SM
+    # stages, units per stage, A buffers, pipelines, schedule: out of range or not fitting
+    for bad in ([0, 0, 4], [0, 0, 2], [0, 3, 0], [0, 0, 0, 3], [3, 2, 0, 0], [0, 0, 0, 0, 4], [0, 0, 6, 1]):
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT,
                                     [8192, 16384, 16, 1, bad[0], 0, 0, 2, 1, SMS] + bad[1:])
         assert e.value.status == loom.LOOM_ERR_ARG
+    with pytest.raises(loom.LoomError) as e:   # the split schedule without a workspace
+        loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl[:8] + [0, SMS, 0, 0, 0, 2])
+    assert e.value.status == loom.LOOM_ERR_ARG
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16388, 16])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_DIRECT
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [77, 64, 0, 1, 0, 0, 0, 0, 1, SMS])

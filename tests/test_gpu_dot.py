@@ -141,25 +141,30 @@ def test_tensor_core_exact_at_group_bound(env):
     check(d, y, acc, "group bound")
 
 
-# (stages, units per stage, A buffers, CTAs per SM); 0 = default
-TC_SCHEDULES = [(0, 0, 0, 0), (1, 2, 0, 0), (1, 1, 0, 0), (2, 1, 0, 0), (5, 1, 0, 0), (2, 2, 2, 0),
-                (0, 0, 0, 1), (3, 2, 4, 1), (5, 2, 6, 1), (8, 1, 2, 1)]
+# (stages, units per stage, A buffers, pipelines per CTA, band schedule); 0 = default
+TC_SCHEDULES = [(0, 0, 0, 0, 0), (1, 2, 0, 0, 0), (1, 1, 0, 0, 0), (2, 1, 0, 0, 0), (4, 1, 0, 0, 0),
+                (0, 0, 0, 1, 0), (3, 2, 7, 1, 0), (1, 4, 0, 1, 0), (8, 1, 7, 1, 0), (3, 3, 0, 1, 0),
+                (0, 0, 0, 0, 1), (0, 0, 0, 0, 2), (0, 0, 0, 0, 3), (4, 1, 0, 0, 3), (0, 0, 0, 1, 3),
+                (1, 2, 0, 1, 2), (0, 0, 0, 1, 1)]
 
 
-@pytest.mark.parametrize("n,k,b", [(384, 8192, 16), (2049, 4112, 16), (128, 1024, 5), (3, 256, 9)])
+@pytest.mark.parametrize("n,k,b", [(384, 8192, 16), (2049, 4112, 16), (128, 1024, 5), (3, 256, 9),
+                                   (1024, 16384, 16)])
 def test_tensor_core_schedule_invariance(env, n, k, b):
-    # Every schedule -- split or whole bands, stage depth and width, A
-    # buffers, one or two CTAs per SM -- gives the same bits.
+    # Every schedule -- a cluster per band, split or whole bands, stage depth
+    # and width, A buffers, one or two pipelines per CTA -- gives the same bits.
     torch, loom = env
     d = small(n, k, b, seed=99 + n + k)
     ref_y, ref_acc = run_dot(loom, torch, d)
     check(d, ref_y, ref_acc, "tensor default")
     for ws in ("auto", None):
-        for depth, ups, na, cps in TC_SCHEDULES:
+        for depth, ups, na, pipes, sched in TC_SCHEDULES:
+            if sched == 2 and ws is None:
+                continue   # the split schedule needs the workspace
             t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_TENSOR, tc_units_per_stage=ups,
-                                 tc_a_buffers=na, tc_ctas_per_sm=cps)
+                                 tc_a_buffers=na, tc_pipelines=pipes, tc_schedule=sched)
             y, acc = run_dot(loom, torch, d, tuning=t, workspace=ws)
-            what = f"ws={ws} schedule={(depth, ups, na, cps)}"
+            what = f"ws={ws} schedule={(depth, ups, na, pipes, sched)}"
             assert np.array_equal(acc, ref_acc), what
             assert same_bits(y, ref_y), what
 
@@ -167,22 +172,27 @@ def test_tensor_core_schedule_invariance(env, n, k, b):
 def test_tensor_core_schedules_that_do_not_fit(env):
     torch, loom = env
     d = small(128, 1024, 16, seed=5)
-    for depth, ups, na, cps in [(3, 2, 0, 0), (0, 0, 4, 0), (0, 0, 8, 1), (2, 2, 1, 0)]:
+    for depth, ups, na, pipes, sched in [(3, 2, 0, 0, 0), (0, 0, 4, 0, 0), (0, 0, 8, 1, 0), (2, 2, 2, 0, 0),
+                                         (8, 2, 0, 1, 0), (0, 0, 6, 1, 0), (0, 3, 0, 0, 0)]:
         t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_TENSOR, tc_units_per_stage=ups,
-                             tc_a_buffers=na, tc_ctas_per_sm=cps)
+                             tc_a_buffers=na, tc_pipelines=pipes, tc_schedule=sched)
         with pytest.raises(loom.LoomError) as e:
             run_dot(loom, torch, d, tuning=t)
         assert e.value.status == loom.LOOM_ERR_ARG
+    with pytest.raises(loom.LoomError) as e:   # split schedule, no workspace
+        run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR, tc_schedule=2),
+                workspace=None)
+    assert e.value.status == loom.LOOM_ERR_ARG
 
 
 def test_tensor_core_workspace_reuse_and_size(env):
-    # One explicit workspace through many calls of different shapes (its
-    # counters must come back to zero after each), then one too short.
+    # One explicit workspace (garbage to start with) through many calls of
+    # different shapes, then one too short.
     torch, loom = env
     shapes = [(2049, 4112, 16), (300, 2064, 7), (8192 // 8, 16384, 16), (129, 1040, 3)]
     need = max(loom.loom_i8_dequant_dot_workspace_bytes(n, k, b) for n, k, b in shapes)
     assert need > 0
-    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")
     for rep in range(2):
         for i, (n, k, b) in enumerate(shapes):
             d = small(n, k, b, seed=11 * i + rep)
@@ -197,8 +207,8 @@ def test_tensor_core_workspace_reuse_and_size(env):
 
 
 def test_tensor_core_injected_stall(env):
-    # The stalled call reports a timeout and NaN outputs; the workspace it used
-    # is still clean, so the next call through it is exact.
+    # The stalled call reports a timeout and NaN outputs (its split bands'
+    # records are marked invalid); the next call through the same workspace is exact.
     torch, loom = env
     for n, k in ((256, 4096), (2049, 4112)):
         d = small(n, k, 16, seed=41 + n)
@@ -275,6 +285,10 @@ def test_batched_full_workload(env, weights):
     d = synth.dequant_batched()
     y, acc = run_dot(loom, torch, d)
     check(d, y, acc, "8192 x 16384 x 16")
+    # the same bits through the split schedule and through whole bands
+    for sched in (2, 1):
+        y2, acc2 = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR, tc_schedule=sched))
+        assert np.array_equal(acc2, acc) and same_bits(y2, y), sched
 
 
 def test_unpack_every_byte_and_over_dispatch(env):
