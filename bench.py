@@ -80,24 +80,35 @@ def measured_peak():
 
 
 def recorded_traffic():
-    """Per-kernel DRAM bytes per launch from the committed ncu summary, valid
-    only while the kernel sources hash to the value recorded with it."""
+    """Per-kernel DRAM bytes per launch from the committed ncu summary, each valid
+    only while the sources of that workload's kernels hash to the value recorded
+    with it."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return {}
-    if d.get("source_hash") != source_hash():
-        return {}
-    return d.get("bytes_per_launch", {})
+    out = {}
+    for name, rec in d.get("workloads", {}).items():
+        if rec.get("source_hash") == source_hash(name):
+            out[name] = rec.get("bytes_per_launch")
+    return out
 
 
-def source_hash() -> str:
+#: the source files each workload's kernels are built from
+KERNEL_SOURCES = {
+    "segments": ("row_sum.cu",), "wide": ("row_sum.cu",),
+    "gemv": ("dequant_dot.cu",), "batched": ("dot_tc.cu",),
+}
+SHARED_SOURCES = ("common.cuh", "internal.h", "loom_api.cu")
+
+
+def source_hash(workload: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int8_dequant_dot_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(KERNEL_SOURCES[workload] + SHARED_SOURCES):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -288,6 +299,9 @@ def run_ours(args, rank, world, dist):
     clocks.start()
     time.sleep(0.3)   # let the sampler attach before the timed work
     with torch.cuda.stream(stream):
+        # keep the device busy for ~1 ms while the host queues the first steps, so
+        # that no event below times host-side launch work on an idle device
+        torch.cuda._sleep(2_000_000)
         step_start.record(stream)
         for _ in range(args.steps):
             for name in ORDER:

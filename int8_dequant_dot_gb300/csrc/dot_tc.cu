@@ -383,24 +383,33 @@ __device__ __forceinline__ bool warp_wait(const CtaArea &L, const TcParams &q, u
 }
 
 // ---- work partition ----------------------------------------------------------
+// n / d for n >= 0, d > 0: one 32-bit division when both fit (64-bit division
+// is a long instruction sequence, and these sit on the start-up path).
+__device__ __forceinline__ int64_t div64(int64_t n, int64_t d)
+{
+    if ((((uint64_t)n) | ((uint64_t)d)) < (1ull << 32))
+        return (int64_t)((uint32_t)n / (uint32_t)d);
+    return n / d;
+}
+
 // CTA c of G takes units [begin(c), begin(c + 1)): equal shares of the unit
 // list, in steps of `quantum` units.
 __device__ __forceinline__ int64_t part_begin(const TcParams &q, int64_t c, int64_t G)
 {
-    const int64_t steps = q.total_units / q.quantum;
-    return q.quantum * (steps * c / G);
+    const int64_t steps = div64(q.total_units, q.quantum);
+    return q.quantum * div64(steps * c, G);
 }
 
 // The CTA whose range holds unit u (split partitions: quantum 1).  CTA c
 // starts at floor(T c / G), so it is the largest c with T c < (u + 1) G.
-__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t T, int64_t G) { return ((u + 1) * G - 1) / T; }
+__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t T, int64_t G) { return div64((u + 1) * G - 1, T); }
 
 // Walks a CTA's units stage by stage: up to `ups` units of one band.
 struct StageWalk {
     int64_t u, u1, band;
     int32_t kb, ub, ups;
     __device__ StageWalk(int64_t u0_, int64_t u1_, int32_t ub_, int32_t ups_)
-        : u(u0_), u1(u1_), band(u0_ / ub_), kb((int32_t)(u0_ - (u0_ / ub_) * ub_)), ub(ub_), ups(ups_)
+        : u(u0_), u1(u1_), band(div64(u0_, ub_)), kb((int32_t)(u0_ - div64(u0_, ub_) * ub_)), ub(ub_), ups(ups_)
     {
     }
     __device__ bool more() const { return u < u1; }
@@ -591,7 +600,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int g = 0;
             bool ok = true;
             for (int64_t u = u0; u < u1 && ok;) {
-                const int64_t e = min(u1, (u / UB + 1) * UB);   // end of this band's segment
+                const int64_t e = min(u1, (div64(u, UB) + 1) * UB);   // end of this band's segment
                 for (int64_t gu = u; gu < e && ok; gu += TC_UNITS_PER_GROUP) {
                     if (g >= NG && !role_wait(C, q, gfree0 + 8 * gs, gph ^ 1u)) {
                         ok = false;
@@ -725,7 +734,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         bool ok = true;
         int g = 0;
         for (int64_t u = u0; u < u1;) {
-            const int64_t band = u / UB;
+            const int64_t band = div64(u, UB);
             const int64_t blo = band * UB, bhi = blo + UB;
             const int64_t e = min(u1, bhi);
             const int64_t row = band * TC_M + t;
@@ -841,7 +850,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             // ---- a band split between CTAs: this CTA's record of it (the
             // finishing kernel adds the records of every CTA sharing the band)
-            const int64_t rec = 2 * cta + (band == U0 / UB ? 0 : 1);
+            const int64_t rec = 2 * cta + (band == div64(U0, UB) ? 0 : 1);
             char *rp = q.records + rec * TC_REC_BYTES;
             int4 *dst = reinterpret_cast<int4 *>(rp + TC_REC_HDR + t * TC_N * 4);
 #pragma unroll
@@ -908,36 +917,56 @@ __global__ void __launch_bounds__(TC_FIN_THREADS) dot_tc_finish_kernel(const Fin
             span[1] = owner_of((band + 1) * UB - 1, T, G);
             // the first CTA's record: its head if its range starts at the band, else its tail;
             // every later CTA starts inside the band (its head record)
-            span[2] = 2 * cf + (T * cf / G == band * UB ? 0 : 1);
+            span[2] = 2 * cf + (div64(T * cf, G) == band * UB ? 0 : 1);
         }
         __syncthreads();
         const int64_t cf = span[0], cl = span[1], r0 = span[2];
         __syncthreads();
         if (cf == cl)
             continue;   // one CTA held the whole band and wrote its outputs
+        const int64_t row = band * TC_M + r_in;
+        const bool live = row < f.n_rows;
+        // scales first: their loads overlap the records'
+        const float sw = live ? __ldg(f.scale_w + row) : 0.f;
+        float sx[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            sx[i] = 4 * quad + i < f.batch ? __ldg(f.scale_x + 4 * quad + i) : 0.f;
         int32_t tot[4] = {0, 0, 0, 0};
         bool valid = true;
-        for (int64_t c = cf; c <= cl; ++c) {
-            const int64_t r = c == cf ? r0 : 2 * c;
-            const char *rp = f.records + r * TC_REC_BYTES;
-            const int4 v = __ldcg(reinterpret_cast<const int4 *>(rp + TC_REC_HDR + (r_in * TC_N + 4 * quad) * 4));
-            valid &= __ldcg(reinterpret_cast<const int *>(rp)) != 0;
-            tot[0] += v.x;
-            tot[1] += v.y;
-            tot[2] += v.z;
-            tot[3] += v.w;
+        // the records of up to four CTAs at a time, all loads in flight together
+        for (int64_t c0 = cf; c0 <= cl; c0 += 4) {
+            int4 v[4];
+            int hdr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t c = c0 + i;
+                v[i] = make_int4(0, 0, 0, 0);
+                hdr[i] = 1;
+                if (c <= cl) {
+                    const int64_t r = c == cf ? r0 : 2 * c;
+                    const char *rp = f.records + r * TC_REC_BYTES;
+                    v[i] = __ldcg(reinterpret_cast<const int4 *>(rp + TC_REC_HDR + (r_in * TC_N + 4 * quad) * 4));
+                    hdr[i] = __ldcg(reinterpret_cast<const int *>(rp));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                tot[0] += v[i].x;
+                tot[1] += v[i].y;
+                tot[2] += v[i].z;
+                tot[3] += v[i].w;
+                valid &= hdr[i] != 0;
+            }
         }
-        const int64_t row = band * TC_M + r_in;
-        if (row >= f.n_rows)
+        if (!live)
             continue;
-        const float sw = __ldg(f.scale_w + row);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int b = 4 * quad + i;
             if (b < f.batch) {
                 const int64_t o = row * f.y_stride + b;
-                f.y[o] = valid ? __fmul_rn(__int2float_rn(tot[i]), __fmul_rn(sw, __ldg(f.scale_x + b)))
-                               : __int_as_float(0x7fc00000);
+                f.y[o] = valid ? __fmul_rn(__int2float_rn(tot[i]), __fmul_rn(sw, sx[i])) : __int_as_float(0x7fc00000);
                 if (f.acc)
                     f.acc[o] = valid ? tot[i] : INT32_MIN;
             }
