@@ -33,7 +33,7 @@ def build(force: bool = False) -> str:
     if force or stale:
         tmp = _LIB + ".tmp%d" % os.getpid()
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-                               "-fPIC", "-shared", "-o", tmp, _SRC])
+                               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -53,6 +53,10 @@ def _load():
         lib.oracle_unpack_word.restype = None
         lib.oracle_i8_dequant_dot.argtypes = [_ptr, _ptr, _i64, _i64, _ptr, _ptr, _i64, _i64, _i64,
                                               _ptr, _ptr]
+        lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_f32.restype = ctypes.c_float
+        lib.oracle_packed_dot.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, _ptr, _ptr, _i64,
+                                          _i64, _ptr]
         lib.oracle_workgroups.argtypes = [_i64, _i64]
         lib.oracle_workgroups.restype = _i64
         _lib = lib
@@ -204,3 +208,36 @@ def i8_dequant_dot(w: np.ndarray, scale_w: np.ndarray, x: np.ndarray, scale_x: n
 
 def workgroups(element_count: int, workgroup_size: int) -> int:
     return int(_load().oracle_workgroups(element_count, workgroup_size))
+
+
+def f16_to_f32(bits: int) -> float:
+    """Value of an IEEE binary16 bit pattern."""
+    return float(_load().oracle_f16_to_f32(ctypes.c_uint16(bits & 0xFFFF)))
+
+
+def packed_dot(fields: np.ndarray, scales: np.ndarray, rhs: np.ndarray, counts,
+               initial: np.ndarray | None = None, threads: int = 1) -> np.ndarray:
+    """The pages' packed signed-byte dot for every instance: ``out float32[P][lanes]``.
+
+    fields uint32/int32 [P][records][lanes]; scales f16 bit patterns (uint16) or
+    float16 [P][records][lanes]; rhs float32 [P][records][streams][4]; counts int [P];
+    initial float32 [P][lanes] or None.
+    """
+    f = np.ascontiguousarray(fields).view(np.uint32)
+    sc = np.ascontiguousarray(scales).view(np.uint16)
+    a = np.ascontiguousarray(rhs, dtype=np.float32)
+    P, R, L = f.shape
+    S = a.shape[2]
+    if sc.shape != f.shape or a.shape != (P, R, S, 4):
+        raise ValueError("packed_dot: shapes disagree")
+    c = np.ascontiguousarray(np.broadcast_to(np.asarray(counts, dtype=np.int32), (P,)))
+    init = None if initial is None else np.ascontiguousarray(initial, dtype=np.float32).reshape(P, L)
+    out = np.zeros((P, L), np.float32)
+    lib = _load()
+
+    def run(p0, p1):
+        _check(lib.oracle_packed_dot(_p(f), _p(sc), _p(a), P, R, L, S, _p(c), _p(init), p0, p1,
+                                     _p(out)), "packed_dot")
+
+    _run_spans(run, P, threads)
+    return out

@@ -18,6 +18,7 @@
  * Pinned by tests/test_oracle_*.py against closed forms, the pages' printed
  * check vectors, exhaustive small cases and independent formulations.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stddef.h>
 
@@ -182,6 +183,72 @@ int oracle_i8_dequant_dot(const int8_t *w, const float *scale_w, int64_t n_rows,
                 a += (int64_t)w[r * k + kk] * (int64_t)x[b * k + kk];
             acc[r * batch + b] = a;
             y[r * batch + b] = (double)scale_w[r] * (double)scale_x[b] * (double)a;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * IEEE binary16 bit pattern to its value (sign, 5-bit exponent biased by 15,
+ * 10-bit fraction; exponent 0 holds zero and the subnormals m * 2^-24,
+ * exponent 31 infinity and NaN).  Every binary16 value is exact in f32.
+ */
+float oracle_f16_to_f32(uint16_t h)
+{
+    const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    float v;
+    if (e == 0)
+        v = ldexpf((float)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(m + 1024), e - 25);
+    return sign ? -v : v;
+}
+
+/*
+ * The packed signed-byte dot of the pages' streaming example, for
+ * `problems` independent instances of it (one instance per dispatch).
+ * [P1] "Apply the same controls to a packed dot product": lane l of an
+ * instance owns one output; for every record r < count it loads the packed
+ * word fields[r][l], the f16 scale scales[r][l] and the four f32 activations
+ * rhs[r][l mod streams][0..3]; the four bytes are unpacked as signed
+ * integers (oracle_unpack_word's order), converted to f32 and multiplied by
+ * the scale (f32), and the dot product with the activations advances the
+ * lane's f32 sum, which starts from initial[l] (0 when initial is NULL).
+ * Reading taken for the dot step: the four products are added to the sum in
+ * element order, each as one fused multiply-add (one rounding per element):
+ *   sum = fmaf(scaled[j], rhs[j], sum),  j = 0, 1, 2, 3.
+ * Layouts: fields, scales [problems][records][lanes]; rhs
+ * [problems][records][streams][4]; counts [problems] (each in [0, records]);
+ * initial and out [problems][lanes].  Instances [p_begin, p_end) are done.
+ */
+int oracle_packed_dot(const uint32_t *fields, const uint16_t *scales, const float *rhs,
+                      int64_t problems, int64_t records, int64_t lanes, int64_t streams,
+                      const int32_t *counts, const float *initial, int64_t p_begin,
+                      int64_t p_end, float *out)
+{
+    if (problems < 0 || records < 0 || lanes < 0 || streams < 1 || p_begin < 0 ||
+        p_end > problems)
+        return ORACLE_ERR_SHAPE;
+    for (int64_t p = p_begin; p < p_end; ++p) {
+        const int64_t count = counts[p];
+        if (count < 0 || count > records)
+            return ORACLE_ERR_RANGE;
+        for (int64_t l = 0; l < lanes; ++l) {
+            float sum = initial ? initial[p * lanes + l] : 0.0f;
+            for (int64_t r = 0; r < count; ++r) {
+                const int64_t at = (p * records + r) * lanes + l;
+                int32_t ints[4];
+                oracle_unpack_word(fields[at], ints);
+                const float scale = oracle_f16_to_f32(scales[at]);
+                const float *a = rhs + ((p * records + r) * streams + l % streams) * 4;
+                for (int j = 0; j < 4; ++j) {
+                    const float scaled = (float)ints[j] * scale;
+                    sum = fmaf(scaled, a[j], sum);
+                }
+            }
+            out[p * lanes + l] = sum;
         }
     }
     return ORACLE_OK;

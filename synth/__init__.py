@@ -245,3 +245,24 @@ def dequant_batched(n_rows: int = 8192, k: int = 16384, batch: int = 16,
     d["scale_x"] = uniform_f32(stream_seed(s, 4), batch, 1e-3, 1e-2)
     d["batch"] = batch
     return d
+
+
+def packed_dot_case(problems: int = 128, records: int = 128, lanes: int = 2048, streams: int = 64,
+                    counts=None, seed: int | None = None) -> dict:
+    """Instances of the pages' packed-dot example: packed signed bytes ``[P][R][L]``
+    (int32 words of uniform bytes), f16 scales ``[P][R][L]`` uniform on
+    [2**-8, 2**-4) rounded to binary16 (returned as their bit patterns),
+    activations ``[P][R][S][4]`` N(0,1), initial sums ``[P][L]`` N(0,1) and one
+    record count per instance (all ``records`` unless given)."""
+    s = workload_seed(6) if seed is None else seed
+    n = problems * records * lanes
+    fields = int8_bytes(stream_seed(s, 0), 4 * n).view("<i4").reshape(problems, records, lanes)
+    scales = uniform_f32(stream_seed(s, 1), n, 2.0 ** -8, 2.0 ** -4).astype(np.float16)
+    rhs = normal_f32(stream_seed(s, 2), problems * records * streams * 4).reshape(problems, records, streams, 4)
+    initial = normal_f32(stream_seed(s, 3), problems * lanes).reshape(problems, lanes)
+    if counts is None:
+        counts = np.full(problems, records, np.int32)
+    counts = np.ascontiguousarray(np.broadcast_to(np.asarray(counts, np.int32), (problems,)))
+    return dict(fields=fields, scales=scales.view(np.uint16).reshape(problems, records, lanes), rhs=rhs,
+                initial=initial, counts=counts, problems=problems, records=records, lanes=lanes,
+                streams=streams)

@@ -33,6 +33,16 @@ MUTANTS = {
     "dot_operand_reversed": ("(int64_t)x[b * k + kk]", "(int64_t)x[b * k + (k - 1 - kk)]"),
     "dot_vector_scale": ("(double)scale_x[b]", "(double)scale_x[0]"),
     "ceil_division": ("(element_count + workgroup_size - 1)", "(element_count + workgroup_size)"),
+    "f16_exponent_bias": ("ldexpf((float)(m + 1024), e - 25)", "ldexpf((float)(m + 1024), e - 24)"),
+    "f16_subnormal_hidden_bit": ("v = ldexpf((float)m, -24);", "v = ldexpf((float)(m + 1024), -24);"),
+    "packed_unfused_step": ("sum = fmaf(scaled, a[j], sum);", "sum = sum + scaled * a[j];"),
+    "packed_stream_map": ("l % streams) * 4", "(l + 1) % streams) * 4"),
+    "packed_scale_lane": ("oracle_f16_to_f32(scales[at])", "oracle_f16_to_f32(scales[at - l])"),
+    "packed_last_record_dropped": ("for (int64_t r = 0; r < count; ++r) {\n                const int64_t at",
+                                   "for (int64_t r = 0; r + 1 < count; ++r) {\n                const int64_t at"),
+    "packed_initial_dropped": ("float sum = initial ? initial[p * lanes + l] : 0.0f;", "float sum = 0.0f;"),
+    "packed_element_order": ("sum = fmaf(scaled, a[j], sum);",
+                             "sum = fmaf((float)ints[3 - j] * scale, a[3 - j], sum);"),
 }
 
 
@@ -44,10 +54,12 @@ def test_planted_mistake_is_caught(name, tmp_path):
     src = tmp_path / "oracle.c"
     src.write_text(text.replace(before, after))
     lib = tmp_path / "liboracle_mutant.so"
-    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(lib), str(src)])
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                           "-shared", "-o", str(lib), str(src), "-lm"])
     env = dict(os.environ, ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_rowsum.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_dot.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_dot.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_packed_dot.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
