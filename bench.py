@@ -99,7 +99,7 @@ def recorded_traffic():
 #: the source files each workload's kernels are built from
 KERNEL_SOURCES = {
     "segments": ("row_sum.cu",), "wide": ("row_sum.cu",),
-    "gemv": ("dequant_dot.cu",), "batched": ("dot_tc.cu",),
+    "gemv": ("dequant_dot.cu",), "batched": ("dot_tc.cu",), "packed": ("packed_dot.cu",),
 }
 SHARED_SOURCES = ("common.cuh", "internal.h", "loom_api.cu")
 
@@ -344,6 +344,8 @@ def run_ours(args, rank, world, dist):
 
     # end to end through the public API: pinned host inputs -> device -> kernels -> host results
     e2e = run_e2e(args, inp, total, torch, loom, stream, work)
+    # the pages' own packed-dot example, timed on its own (not part of the step)
+    extras = {"packed_dot": measure_packed(args, torch, loom, stream, peak, peak_kind)}
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -358,11 +360,66 @@ def run_ours(args, rank, world, dist):
         "e2e": e2e,
         "gpu_launches": work.launches_per_step * args.steps,
         "clocks": clk,
+        "extras": extras,
     }
     if rank == 0:
         threads = os.cpu_count() or 1
         line["cpu_baseline"] = cpu_baseline(inp, total, threads)
         print(json.dumps(line), flush=True)
+
+
+PACKED_WORKLOAD = "packed dot: 128 instances x 128 records x 2048 lanes, 64 activation streams"
+
+
+def packed_alg_bytes(d) -> int:
+    """Per instance: the active records' words and scales, their activation rows,
+    the initial sums, the count and the outputs."""
+    c = d["counts"].astype(np.int64)
+    L, S = d["lanes"], d["streams"]
+    return int((c * L * 6).sum() + (c * S * 16).sum() + d["problems"] * (L * 8 + 4))
+
+
+def measure_packed(args, torch, loom, stream, peak, peak_kind):
+    """Single launches, each after a 512 MB read that leaves nothing of the
+    inputs in L2; CUDA events on the launching stream."""
+    import synth
+    d = synth.packed_dot_case()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    f, sc, rhs = t(d["fields"]), t(d["scales"].view(np.int16)), t(d["rhs"])
+    counts, init = t(d["counts"]), t(d["initial"])
+    out = torch.empty((d["problems"], d["lanes"]), dtype=torch.float32, device="cuda")
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros((), dtype=torch.int64, device="cuda")
+    alg = packed_alg_bytes(d)
+
+    def call():
+        loom.loom_packed_dot(f, sc, rhs, counts, 0, init, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            call()
+    stream.synchronize()
+    times = []
+    for _ in range(max(args.steps, 5)):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            sink.copy_(flush.view(torch.int32).sum())
+            torch.cuda._sleep(200_000)
+            a.record(stream)
+            call()
+            b.record(stream)
+        stream.synchronize()
+        times.append(a.elapsed_time(b))
+    avg = sum(times) / len(times)
+    gbs = alg / (avg * 1e-3) / 1e9
+    L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [d["problems"], d["records"], d["lanes"], d["streams"]])
+    del flush
+    return {"workload": PACKED_WORKLOAD, "alg_bytes": alg, "avg_ms": avg, "min_ms": min(times),
+            "launches": len(times), "l2": "512 MB read before each launch",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": peak_kind, "traffic": recorded_traffic().get("packed")},
+            "grid": L["grid"], "block": L["block"][0]}
 
 
 def run_e2e(args, inp, total, torch, loom, stream, work):
@@ -415,6 +472,17 @@ def run_profile(args):
     import synth
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
+    if args.profile == "packed":
+        d = synth.packed_dot_case()
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        f, sc, rhs, counts, init = (t(d["fields"]), t(d["scales"].view(np.int16)), t(d["rhs"]), t(d["counts"]),
+                                    t(d["initial"]))
+        with torch.cuda.stream(stream):
+            for _ in range(args.launches):
+                loom.loom_packed_dot(f, sc, rhs, counts, 0, init, stream=stream)
+        stream.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": args.launches}))
+        return
     if args.profile in ("segments", "wide"):
         inp = {"segments": synth.batched_segments() if args.profile == "segments" else None,
                "wide": synth.wide_rows() if args.profile == "wide" else None}
@@ -461,7 +529,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--depth", type=int, default=0, help="read-ahead depth (0 = library default)")
-    ap.add_argument("--profile", choices=ORDER, default=None)
+    ap.add_argument("--profile", choices=ORDER + ("packed",), default=None)
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3 and args.profile is None:

@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define LOOM_ABI_VERSION 2
+#define LOOM_ABI_VERSION 3
 
 typedef enum loom_status {
     LOOM_OK = 0,
@@ -58,11 +58,14 @@ typedef enum loom_op {
                                     chunk_bytes} */
     LOOM_OP_ROW_SUM_BATCHED = 2, /* workload {num_segments, rows, lanes, staged (0/1), depth,
                                     warps_per_cta, units_per_warp, chunk_bytes} */
-    LOOM_OP_I8_DEQUANT_DOT = 3   /* workload {n_rows, k, batch, staged (0/1), depth,
+    LOOM_OP_I8_DEQUANT_DOT = 3,  /* workload {n_rows, k, batch, staged (0/1), depth,
                                     warps_per_cta, rows_per_warp, engine (0 auto, 1 dp4a,
                                     2 tensor), workspace (0/1, default 1), sm_count (0 =
                                     the current device), tc_units_per_stage,
                                     tc_a_buffers, tc_pipelines, tc_schedule} */
+    LOOM_OP_PACKED_DOT = 4       /* workload {problems, records, lanes, streams, aligned (0/1:
+                                    inputs 16-byte aligned, default 1), depth,
+                                    records_per_stage} */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
@@ -95,6 +98,8 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_TENSOR_SPLIT 8 /* the same kernel over equal shares of all units, then
                                           a finishing kernel for the bands split between CTAs
                                           (two launches per pass) */
+#define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: 3-D TMA read-ahead ring per CTA */
+#define LOOM_KERNEL_PACKED_DIRECT 10 /* packed dot: plain loads */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8
@@ -212,6 +217,38 @@ loom_status loom_i8_dequant_dot_noalloc(const int32_t *d_w_packed, const float *
                                         int32_t n_rows, int32_t k, const int32_t *d_x_packed,
                                         const float *d_scale_x, int32_t batch, float *d_y,
                                         int32_t *d_acc, void *stream);
+
+/*
+ * The packed signed-byte dot of the pages' streaming example, for `problems`
+ * independent instances (the pages time one instance per dispatch over many
+ * dispatches; here one call takes them all).
+ * [P1] "Apply the same controls to a packed dot product": lane l of an
+ * instance owns one output.  For every record r < count it reads the packed
+ * word fields[r][l] (four signed bytes, element j = bits 8j..8j+7), the f16
+ * scale scales[r][l] and four f32 activations rhs[r][l mod streams][0..3];
+ * the bytes become f32, are multiplied by the scale, and the dot product
+ * with the activations advances the lane's f32 sum in record order.  Each of
+ * the four products enters the sum as one fused multiply-add, in element
+ * order (the reading taken of the pages' ordered dot step), so the result is
+ * defined to the bit.  The sum starts from d_initial (or 0).
+ * Layout (caller-owned device memory, row-major): d_fields int32
+ * [problems][records][lanes]; d_scales f16 bit patterns [problems][records]
+ * [lanes]; d_rhs f32 [problems][records][streams][4]; d_counts int32
+ * [problems] (NULL: `count` for every instance); d_initial f32
+ * [problems][lanes] (NULL: 0); d_out f32 [problems][lanes].
+ * Schedule: 256 lanes of one instance per CTA; with lanes a multiple of 8,
+ * at most 64 streams and 16-byte aligned inputs a read-ahead ring of 3-D TMA
+ * copies, else plain loads (same bits).
+ * Errors: NULL required pointer -> LOOM_ERR_NULL; pointers not 4-byte (fields,
+ * rhs, initial, out) or 2-byte (scales) aligned -> LOOM_ERR_ALIGN; negative
+ * sizes, streams < 1, or more than 65535 instances -> LOOM_ERR_SHAPE; host
+ * count outside [0, records] -> LOOM_ERR_RANGE.  Device counts outside
+ * [0, records] are clamped and flagged (LOOM_DEVERR_COUNT_RANGE, _ex only).
+ */
+loom_status loom_packed_dot(const int32_t *d_fields, const uint16_t *d_scales, const float *d_rhs,
+                            int32_t problems, int32_t records, int32_t lanes, int32_t streams,
+                            const int32_t *d_counts, int32_t count, const float *d_initial,
+                            float *d_out, void *stream);
 
 /*
  * Unpack and convert: d_out[4j + i] = (float) signed byte i of d_packed[j].

@@ -74,6 +74,16 @@ loom_status loom_i8_dequant_dot_ex(const int32_t *d_w_packed, const float *d_sca
                                    int32_t *d_acc, void *d_workspace, int64_t workspace_bytes,
                                    int32_t *d_error, const loom_tuning *tuning, void *stream);
 
+/* loom_packed_dot with tuning (NULL = defaults): depth = stages of the read-ahead
+ * ring (1 = the serial control), units_per_warp = records per stage (1..32),
+ * path = LOOM_PATH_STAGED / LOOM_PATH_DIRECT to force one (LOOM_ERR_ALIGN or
+ * LOOM_ERR_SHAPE when the staged path cannot take the inputs).  Extra errors:
+ * a tuning value out of range -> LOOM_ERR_ARG. */
+loom_status loom_packed_dot_ex(const int32_t *d_fields, const uint16_t *d_scales, const float *d_rhs,
+                               int32_t problems, int32_t records, int32_t lanes, int32_t streams,
+                               const int32_t *d_counts, int32_t count, const float *d_initial,
+                               float *d_out, int32_t *d_error, const loom_tuning *tuning, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

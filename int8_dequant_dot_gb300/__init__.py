@@ -34,6 +34,7 @@ LOOM_OP_I8_UNPACK = 0
 LOOM_OP_FULL_TILE_SUM = 1
 LOOM_OP_ROW_SUM_BATCHED = 2
 LOOM_OP_I8_DEQUANT_DOT = 3
+LOOM_OP_PACKED_DOT = 4
 
 LOOM_KERNEL_UNPACK = 1
 LOOM_KERNEL_ROWSUM_STAGED = 2
@@ -43,6 +44,8 @@ LOOM_KERNEL_DOT_STAGED_B = 5
 LOOM_KERNEL_DOT_DIRECT = 6
 LOOM_KERNEL_DOT_TENSOR = 7
 LOOM_KERNEL_DOT_TENSOR_SPLIT = 8
+LOOM_KERNEL_PACKED_STAGED = 9
+LOOM_KERNEL_PACKED_DIRECT = 10
 
 LOOM_MAX_DEPTH = 8
 LOOM_PATH_AUTO = 0
@@ -55,6 +58,7 @@ EXPORTS = (
     "loom_launch_config", "loom_full_tile_sum", "loom_row_sum_batched", "loom_i8_dequant_dot",
     "loom_i8_unpack", "loom_status_string", "loom_abi_version", "loom_row_sum_batched_ex",
     "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes", "loom_i8_dequant_dot_noalloc",
+    "loom_packed_dot", "loom_packed_dot_ex",
 )
 
 
@@ -102,6 +106,8 @@ def _bind() -> ctypes.CDLL:
                                    ctypes.POINTER(loom_tuning), P],
         "loom_i8_dequant_dot_workspace_bytes": [i32, i32, i32, ctypes.POINTER(i64)],
         "loom_i8_dequant_dot_noalloc": [P, P, i32, i32, P, P, i32, P, P, P],
+        "loom_packed_dot": [P, P, P, i32, i32, i32, i32, P, i32, P, P, P],
+        "loom_packed_dot_ex": [P, P, P, i32, i32, i32, i32, P, i32, P, P, P, ctypes.POINTER(loom_tuning), P],
         "loom_i8_unpack": [P, i64, P, P],
         "loom_status_string": [i32],
         "loom_abi_version": [],
@@ -324,6 +330,40 @@ def loom_i8_dequant_dot_noalloc(w_packed, scale_w, n_rows: int, k: int, x_packed
                                             _ptr(acc), _stream(stream, w_packed)),
            "loom_i8_dequant_dot_noalloc")
     return y, acc
+
+
+def loom_packed_dot(fields, scales, rhs, counts=None, count: int = 0, initial=None, *,
+                    problems: int | None = None, records: int | None = None, lanes: int | None = None,
+                    streams: int | None = None, out=None, stream=None):
+    """The pages' packed signed-byte dot for ``problems`` instances; returns ``out``
+    float32 ``[problems][lanes]``.  ``fields`` int32 ``[P][R][L]``, ``scales`` f16 (or
+    their int16 bit patterns) ``[P][R][L]``, ``rhs`` float32 ``[P][R][S][4]``; ``counts``
+    int32 ``[P]`` on the device, or None with ``count`` for every instance."""
+    return loom_packed_dot_ex(fields, scales, rhs, counts, count, initial, problems=problems,
+                              records=records, lanes=lanes, streams=streams, out=out, stream=stream,
+                              _name="loom_packed_dot")
+
+
+def loom_packed_dot_ex(fields, scales, rhs, counts=None, count: int = 0, initial=None, *,
+                       problems: int | None = None, records: int | None = None, lanes: int | None = None,
+                       streams: int | None = None, out=None, error=None, tuning=None, stream=None,
+                       _name: str = "loom_packed_dot_ex"):
+    import torch
+    if problems is None or records is None or lanes is None:
+        problems, records, lanes = fields.shape
+    if streams is None:
+        streams = rhs.shape[2]
+    if out is None:
+        out = _empty(fields, (int(problems), int(lanes)), torch.float32)
+    st = _stream(stream, fields)
+    args = (_ptr(fields), _ptr(scales), _ptr(rhs), int(problems), int(records), int(lanes), int(streams),
+            _ptr(counts), int(count), _ptr(initial), _ptr(out))
+    if _name == "loom_packed_dot":
+        _check(_lib.loom_packed_dot(*args, st), _name)
+    else:
+        tp = ctypes.byref(tuning) if tuning is not None else None
+        _check(_lib.loom_packed_dot_ex(*args, _ptr(error), tp, st), _name)
+    return out
 
 
 def loom_i8_unpack(packed, n_words: int, out=None, *, stream=None):

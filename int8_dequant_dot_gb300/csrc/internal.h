@@ -105,6 +105,32 @@ int64_t dot_tc_workspace_bytes(const DotTcPlan &plan);
 bool dot_tc_cluster_fits(const DotTcPlan &plan);
 cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream);
 
+// ---- the pages' packed-dot example (packed_dot.cu) ---------------------------
+constexpr int PD_DEFAULT_DEPTH = 2;        // stages of the read-ahead ring
+constexpr int PD_DEFAULT_RPS = 8;          // records per stage
+constexpr int PD_MAX_RPS = 32;
+constexpr int PD_MAX_STAGED_STREAMS = 64;  // one TMA box row holds every stream of a record
+constexpr int PD_LANES_PER_CTA = 256;
+
+struct PackedParams {
+    const int32_t *fields;     // [problems][records][lanes] packed signed bytes
+    const uint16_t *scales;    // [problems][records][lanes] f16 bit patterns
+    const float *rhs;          // [problems][records][streams][4]
+    int32_t problems, records, lanes, streams;
+    const int32_t *counts;     // [problems] or NULL (count for every instance)
+    int32_t count;
+    const float *initial;      // [problems][lanes] or NULL
+    float *out;                // [problems][lanes]
+    int32_t *error;
+    int32_t depth, rps;
+    uint64_t wait_ns;
+    int32_t inject_stall;
+};
+bool packed_dot_stageable(const PackedParams &q);
+uint32_t packed_dot_smem_bytes(bool staged, int depth, int rps, int streams);
+uint32_t packed_dot_threads(bool staged);
+cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_launch &L, cudaStream_t stream);
+
 // ---- unpack ----------------------------------------------------------------
 constexpr int UNPACK_BLOCK = 256;
 cudaError_t launch_unpack(const int32_t *packed, int64_t n_words, float *out, const loom_launch &L,

@@ -379,6 +379,88 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     return LOOM_OK;
 }
 
+// ---- the pages' packed-dot example ------------------------------------------------
+
+// `aligned`: the inputs meet the TMA path's alignment; the staged kernel is
+// taken when the shape allows it too (lanes a multiple of 8, <= 64 streams).
+loom_status packed_geometry(int64_t problems, int64_t records, int64_t lanes, int64_t streams, bool aligned,
+                            int64_t depth, int64_t rps, loom_launch *out)
+{
+    if (problems < 0 || problems > 65535 || records < 0 || lanes < 0 || streams < 1 ||
+        ceil_div(lanes, PD_LANES_PER_CTA) > 0x7fffffff)
+        return LOOM_ERR_SHAPE;
+    if (depth == 0)
+        depth = PD_DEFAULT_DEPTH;
+    if (rps == 0)
+        rps = PD_DEFAULT_RPS;
+    if (depth < 1 || depth > LOOM_MAX_DEPTH || rps < 1 || rps > PD_MAX_RPS)
+        return LOOM_ERR_ARG;
+    const bool staged = aligned && lanes % 8 == 0 && streams <= PD_MAX_STAGED_STREAMS;
+    const uint32_t smem = packed_dot_smem_bytes(staged, (int)depth, (int)rps, (int)streams);
+    if (smem > 227 * 1024)
+        return LOOM_ERR_ARG;
+    fill_launch(out, ceil_div(lanes, PD_LANES_PER_CTA), packed_dot_threads(staged), smem, PD_LANES_PER_CTA,
+                staged ? LOOM_KERNEL_PACKED_STAGED : LOOM_KERNEL_PACKED_DIRECT);
+    out->grid[1] = (uint32_t)problems;
+    return LOOM_OK;
+}
+
+loom_status packed_common(const int32_t *fields, const uint16_t *scales, const float *rhs, int32_t problems,
+                          int32_t records, int32_t lanes, int32_t streams, const int32_t *counts, int32_t count,
+                          const float *initial, float *out, int32_t *error, const loom_tuning *tuning,
+                          void *stream)
+{
+    Tuning t;
+    loom_status st = read_tuning(tuning, 0, &t);
+    if (st != LOOM_OK)
+        return st;
+    if (t.path == LOOM_PATH_TENSOR)
+        return LOOM_ERR_ARG;
+    if (problems < 0 || problems > 65535 || records < 0 || lanes < 0 || streams < 1)
+        return LOOM_ERR_SHAPE;
+    if (!counts && (count < 0 || count > records))
+        return LOOM_ERR_RANGE;
+    if (problems == 0 || lanes == 0)
+        return LOOM_OK;   // no outputs: no launch
+    if (!out || (records > 0 && (!fields || !scales || !rhs)))
+        return LOOM_ERR_NULL;
+    if (misaligned(fields, 4) || misaligned(scales, 2) || misaligned(rhs, 4) || misaligned(counts, 4) ||
+        misaligned(initial, 4) || misaligned(out, 4) || misaligned(error, 4))
+        return LOOM_ERR_ALIGN;
+    PackedParams q;
+    q.fields = fields;
+    q.scales = scales;
+    q.rhs = rhs;
+    q.problems = problems;
+    q.records = records;
+    q.lanes = lanes;
+    q.streams = streams;
+    q.counts = counts;
+    q.count = count;
+    q.initial = initial;
+    q.out = out;
+    q.error = error;
+    q.wait_ns = t.wait_ns;
+    q.inject_stall = t.stall;
+    const bool stageable = packed_dot_stageable(q);
+    if (t.path == LOOM_PATH_STAGED && !stageable)
+        return (lanes % 8 != 0 || streams > PD_MAX_STAGED_STREAMS) ? LOOM_ERR_SHAPE : LOOM_ERR_ALIGN;
+    const bool staged = stageable && t.path != LOOM_PATH_DIRECT;
+    loom_launch L;
+    st = packed_geometry(problems, records, lanes, streams, staged, t.depth, t.upw, &L);
+    if (st != LOOM_OK)
+        return st;
+    q.depth = t.depth ? t.depth : PD_DEFAULT_DEPTH;
+    q.rps = t.upw ? t.upw : PD_DEFAULT_RPS;
+    const cudaError_t e = launch_packed_dot(q, L.kernel == LOOM_KERNEL_PACKED_STAGED, L,
+                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    return LOOM_OK;
+}
+
 // ---- fixed device scratch of loom_i8_dequant_dot_noalloc ---------------------
 // One array per device; the streaming kernel writes every record of it that
 // the finishing kernel reads, so it needs no initialisation.  8 MiB covers the
@@ -487,6 +569,11 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         return dot_geometry(workload[0], workload[1], workload[2], aligned, opt(4, 0), opt(5, 0),
                             opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms ? sms : 1, out, nullptr);
     }
+    case LOOM_OP_PACKED_DOT:
+        if (n_workload < 4)
+            return LOOM_ERR_ARG;
+        return packed_geometry(workload[0], workload[1], workload[2], workload[3], opt(4, 1) != 0, opt(5, 0),
+                               opt(6, 0), out);
     default:
         return LOOM_ERR_ARG;
     }
@@ -593,6 +680,24 @@ loom_status loom_i8_dequant_dot_noalloc(const int32_t *d_w_packed, const float *
     }
     return dot_common(d_w_packed, d_scale_w, n_rows, k, d_x_packed, d_scale_x, batch, d_y, d_acc,
                       scratch, scratch ? NOALLOC_SCRATCH_BYTES : 0, nullptr, nullptr, stream);
+}
+
+loom_status loom_packed_dot(const int32_t *d_fields, const uint16_t *d_scales, const float *d_rhs,
+                            int32_t problems, int32_t records, int32_t lanes, int32_t streams,
+                            const int32_t *d_counts, int32_t count, const float *d_initial, float *d_out,
+                            void *stream)
+{
+    return packed_common(d_fields, d_scales, d_rhs, problems, records, lanes, streams, d_counts, count,
+                         d_initial, d_out, nullptr, nullptr, stream);
+}
+
+loom_status loom_packed_dot_ex(const int32_t *d_fields, const uint16_t *d_scales, const float *d_rhs,
+                               int32_t problems, int32_t records, int32_t lanes, int32_t streams,
+                               const int32_t *d_counts, int32_t count, const float *d_initial, float *d_out,
+                               int32_t *d_error, const loom_tuning *tuning, void *stream)
+{
+    return packed_common(d_fields, d_scales, d_rhs, problems, records, lanes, streams, d_counts, count,
+                         d_initial, d_out, d_error, tuning, stream);
 }
 
 loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)

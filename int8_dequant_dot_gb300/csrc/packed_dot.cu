@@ -1,0 +1,344 @@
+// packed_dot.cu -- the pages' own packed signed-byte dot: f16 per-record
+// scales, f32 activations, an ordered f32 accumulation per output lane.
+//
+// Method (Loom pages, "Tune loop unrolling and pipelining", section "Apply
+// the same controls to a packed dot product"): lane l of an instance owns one
+// output.  For each record r < count it reads the packed word fields[r][l]
+// (four signed bytes), the f16 scale scales[r][l] and four f32 activations
+// rhs[r][l mod streams][0..3]; the bytes are converted to f32 and scaled, and
+// the dot product with the activations advances the lane's f32 sum.  The
+// records are a recurrence: their order fixes the result.
+//
+// Reading of the dot step: the four products enter the sum in element order,
+// each as one fused multiply-add.  int8 x f16 fits in 19 significant bits,
+// so the scaled bytes are exact in f32 and only the fused steps round.
+//
+// GB300 design
+//  * Many independent instances per launch (the pages benchmark one instance
+//    per dispatch, many dispatches per measurement).  A CTA takes 256 lanes of
+//    one instance, one consumer thread per lane, and streams its records.
+//  * Staged path: one producer thread fills a ring of `depth` stages, each
+//    `rps` records of the CTA's words (1 KiB per record), scales (512 B) and
+//    the instance's whole activation row (16 B per stream), with three 3-D
+//    TMA copies completing on the stage's mbarrier (words and scales
+//    evict-first; activations, which every lane block of the instance reads,
+//    evict-last).  This is the read-ahead queue of the pages'
+//    pipeline(depth); depth 1 is the serial control and the depth never
+//    changes a result.  (Reading the activations through L1 instead left
+//    every CTA waiting on one load per record: measured 1.6x slower.)
+//  * Consumers read their word and scale from shared memory (consecutive
+//    lanes, consecutive addresses) and their stream's float4 (32 consecutive
+//    streams per warp: conflict-free), then run the four fused steps.
+//  * Direct path (inputs a TMA copy cannot take: lanes not a multiple of 8,
+//    more than 64 streams, unaligned pointers): plain loads, same order and
+//    arithmetic, identical bits.
+//  * Every wait is bounded; a wait that runs out sets LOOM_DEVERR_TIMEOUT and
+//    the affected outputs are NaN.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace loom {
+namespace {
+
+constexpr int PD_LANES = 256;                 // lanes (consumer threads) per CTA
+constexpr int PD_CONSUMER_WARPS = PD_LANES / 32;
+constexpr int PD_THREADS_STAGED = PD_LANES + 32;   // + the producer warp
+
+struct PackedDeviceParams {
+    const int32_t *fields;
+    const uint16_t *scales;
+    const float *rhs;
+    int32_t problems, records, lanes, streams;
+    const int32_t *counts;   // per instance, or NULL: count_scalar for all
+    int32_t count_scalar;
+    const float *initial;    // [problems][lanes] or NULL (0)
+    float *out;              // [problems][lanes]
+    int32_t *error;
+    int32_t depth;           // stages in the ring
+    int32_t rps;             // records per stage
+    uint64_t wait_ns;
+    int32_t inject_stall;
+};
+
+// Shared-memory layout of one stage: fields [rps][256] i32, scales [rps][256]
+// u16, activations [rps][streams][4] f32; each part 128-byte aligned.
+struct PdStage {
+    uint32_t fields_bytes, scales_bytes, rhs_bytes;
+    __host__ __device__ PdStage(int rps, int streams)
+        : fields_bytes((uint32_t)rps * PD_LANES * 4u), scales_bytes((uint32_t)rps * PD_LANES * 2u),
+          rhs_bytes(((uint32_t)rps * (uint32_t)streams * 16u + 127u) & ~127u)
+    {
+    }
+    __host__ __device__ uint32_t bytes() const { return fields_bytes + scales_bytes + rhs_bytes; }
+};
+
+uint32_t pd_smem_bytes(int depth, int rps, int streams)
+{
+    return 128u + (uint32_t)depth * PdStage(rps, streams).bytes() + 16u * (uint32_t)depth;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// One record of one lane: four signed bytes, scaled exactly, then four fused
+// steps in element order.
+__device__ __forceinline__ float record_step(float sum, uint32_t word, uint16_t scale_bits, const float4 &a)
+{
+    const float scale = __half2float(__ushort_as_half(scale_bits));
+    const float b0 = (float)(int32_t)(int8_t)(word & 0xFFu);
+    const float b1 = (float)(int32_t)(int8_t)((word >> 8) & 0xFFu);
+    const float b2 = (float)(int32_t)(int8_t)((word >> 16) & 0xFFu);
+    const float b3 = (float)(int32_t)(int8_t)(word >> 24);
+    sum = __fmaf_rn(__fmul_rn(b0, scale), a.x, sum);
+    sum = __fmaf_rn(__fmul_rn(b1, scale), a.y, sum);
+    sum = __fmaf_rn(__fmul_rn(b2, scale), a.z, sum);
+    sum = __fmaf_rn(__fmul_rn(b3, scale), a.w, sum);
+    return sum;
+}
+
+__device__ __forceinline__ int32_t instance_count(const PackedDeviceParams &p, int32_t inst)
+{
+    const int32_t raw = p.counts ? __ldg(p.counts + inst) : p.count_scalar;
+    const int32_t c = min(max(raw, 0), p.records);
+    if (c != raw)
+        dev::flag_error(p.error, LOOM_DEVERR_COUNT_RANGE);
+    return c;
+}
+
+// Staged path.  Block (blockIdx.x, blockIdx.y) = (lane block, instance).
+__global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel(
+    const __grid_constant__ CUtensorMap tm_fields, const __grid_constant__ CUtensorMap tm_scales,
+    const __grid_constant__ CUtensorMap tm_rhs, const PackedDeviceParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t base = (dev::smem_u32(smem_raw) + 127u) & ~127u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t inst = blockIdx.y;
+    const int32_t lane0 = blockIdx.x * PD_LANES;
+    const int D = p.depth, RPS = p.rps;
+    const PdStage st(RPS, p.streams);
+    const uint32_t bars = base + (uint32_t)D * st.bytes();
+    auto full = [&](int s) { return bars + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return bars + 8u * (uint32_t)(D + s); };
+    auto stage = [&](int s) { return base + (uint32_t)s * st.bytes(); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < D; ++s) {
+            dev::mbar_init(full(s), 1);
+            dev::mbar_init(empty(s), PD_CONSUMER_WARPS);
+        }
+        dev::fence_barrier_init();
+    }
+    __syncthreads();
+    const int32_t count = instance_count(p, inst);
+    const int nst = (count + RPS - 1) / RPS;
+
+    if (warp == PD_CONSUMER_WARPS) {
+        // ---- producer: three 3-D copies per stage (words, scales, activations)
+        if (lane == 0 && !p.inject_stall) {
+            const uint64_t once = dev::l2_evict_first_policy();   // words, scales: read once
+            const uint64_t shared = dev::l2_evict_last_policy();  // activations: every lane block
+            const uint32_t tx = st.fields_bytes + st.scales_bytes + (uint32_t)RPS * (uint32_t)p.streams * 16u;
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % D;
+                if (i >= D && !dev::mbar_wait_bounded(empty(s), ((i / D) - 1) & 1, p.wait_ns)) {
+                    dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int32_t r0 = i * RPS;
+                dev::mbar_arrive_expect_tx(full(s), tx);
+                tma_load_3d(stage(s), &tm_fields, lane0, r0, inst, full(s), once);
+                tma_load_3d(stage(s) + st.fields_bytes, &tm_scales, lane0, r0, inst, full(s), once);
+                tma_load_3d(stage(s) + st.fields_bytes + st.scales_bytes, &tm_rhs, 0, r0, inst, full(s), shared);
+                ++issued;
+            }
+            // every copy issued must land before the CTA may leave (bounded)
+            for (int j = issued > D ? issued - D : 0; j < issued; ++j)
+                dev::mbar_wait_bounded(full(j % D), (j / D) & 1, p.wait_ns);
+        }
+        return;
+    }
+
+    // ---- consumers: thread t owns lane lane0 + t
+    const int t = threadIdx.x;
+    const int32_t l = lane0 + t;
+    const bool live = l < p.lanes;
+    const int32_t sl = l % p.streams;
+    float sum = (live && p.initial) ? __ldg(p.initial + (int64_t)inst * p.lanes + l) : 0.f;
+    bool ok = true;
+    for (int i = 0; i < nst; ++i) {
+        const int s = i % D;
+        const bool landed = dev::mbar_wait_bounded(full(s), (i / D) & 1, p.wait_ns);
+        if (!__all_sync(dev::FULL_MASK, landed)) {
+            ok = false;
+            break;
+        }
+        const uint32_t f = stage(s), sc = f + st.fields_bytes, a = sc + st.scales_bytes;
+        const int n_here = min(RPS, count - i * RPS);
+        for (int k = 0; k < n_here; ++k) {
+            uint32_t word;
+            uint16_t sbits;
+            float4 v;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(word) : "r"(f + (uint32_t)(k * PD_LANES + t) * 4u));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sbits) : "r"(sc + (uint32_t)(k * PD_LANES + t) * 2u));
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                         : "r"(a + (uint32_t)(k * p.streams + sl) * 16u));
+            sum = record_step(sum, word, sbits, v);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty(s));
+    }
+    if (!ok)
+        dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+    if (live)
+        p.out[(int64_t)inst * p.lanes + l] = ok ? sum : __int_as_float(0x7fc00000);
+}
+
+// Direct path: plain loads, one thread per lane, records in order.
+__global__ void __launch_bounds__(PD_LANES) packed_dot_direct_kernel(const PackedDeviceParams p)
+{
+    const int32_t inst = blockIdx.y;
+    const int32_t l = blockIdx.x * PD_LANES + threadIdx.x;
+    const int32_t count = instance_count(p, inst);
+    if (l >= p.lanes)
+        return;   // over-dispatched lane: no loads, no stores
+    const int32_t sl = l % p.streams;
+    float sum = p.initial ? __ldg(p.initial + (int64_t)inst * p.lanes + l) : 0.f;
+    for (int32_t r = 0; r < count; ++r) {
+        const int64_t at = ((int64_t)inst * p.records + r) * p.lanes + l;
+        const float *ap = p.rhs + (((int64_t)inst * p.records + r) * p.streams + sl) * 4;
+        const float4 v = make_float4(__ldg(ap), __ldg(ap + 1), __ldg(ap + 2), __ldg(ap + 3));
+        sum = record_step(sum, (uint32_t)__ldg(p.fields + at), __ldg(p.scales + at), v);
+    }
+    p.out[(int64_t)inst * p.lanes + l] = sum;
+}
+
+// ---- host: 3-D tensor maps ----------------------------------------------------------
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled pd_encoder()
+{
+    static EncodeTiled fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<EncodeTiled>(f);
+    }();
+    return fn;
+}
+
+// [outer][mid][inner] elements of `esize` bytes, box {box_inner, box_mid, 1}.
+bool encode_3d(CUtensorMap *map, CUtensorMapDataType type, uint32_t esize, const void *base, uint64_t inner,
+               uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid)
+{
+    EncodeTiled enc = pd_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {inner, mid, outer};
+    const cuuint64_t strides[2] = {inner * esize, inner * mid * esize};
+    const cuuint32_t box[3] = {box_inner, box_mid, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, type, 3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+std::mutex g_pd_attr_mu;
+bool g_pd_attr_set[64];
+
+}  // namespace
+
+bool packed_dot_stageable(const PackedParams &q)
+{
+    const auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+    return q.lanes % 8 == 0 && q.streams >= 1 && q.streams <= PD_MAX_STAGED_STREAMS && al16(q.fields) &&
+           al16(q.scales) && al16(q.rhs);
+}
+
+uint32_t packed_dot_smem_bytes(bool staged, int depth, int rps, int streams)
+{
+    return staged ? pd_smem_bytes(depth, rps, streams) : 0u;
+}
+
+uint32_t packed_dot_threads(bool staged) { return staged ? PD_THREADS_STAGED : PD_LANES; }
+
+cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_launch &L, cudaStream_t stream)
+{
+    if (L.grid[0] == 0 || L.grid[1] == 0)
+        return cudaSuccess;
+    PackedDeviceParams p;
+    p.fields = q.fields;
+    p.scales = q.scales;
+    p.rhs = q.rhs;
+    p.problems = q.problems;
+    p.records = q.records;
+    p.lanes = q.lanes;
+    p.streams = q.streams;
+    p.counts = q.counts;
+    p.count_scalar = q.count;
+    p.initial = q.initial;
+    p.out = q.out;
+    p.error = q.error;
+    p.depth = q.depth;
+    p.rps = q.rps;
+    p.wait_ns = q.wait_ns;
+    p.inject_stall = q.inject_stall;
+    const dim3 grid(L.grid[0], L.grid[1], 1);
+    if (!staged) {
+        packed_dot_direct_kernel<<<grid, L.block[0], 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    CUtensorMap tf, ts, tr;
+    if (!encode_3d(&tf, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, q.fields, (uint64_t)q.lanes, (uint64_t)q.records,
+                   (uint64_t)q.problems, PD_LANES, (uint32_t)q.rps) ||
+        !encode_3d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, q.scales, (uint64_t)q.lanes, (uint64_t)q.records,
+                   (uint64_t)q.problems, PD_LANES, (uint32_t)q.rps) ||
+        !encode_3d(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q.rhs, (uint64_t)q.streams * 4, (uint64_t)q.records,
+                   (uint64_t)q.problems, (uint32_t)q.streams * 4, (uint32_t)q.rps))
+        return cudaErrorInvalidValue;
+    {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        std::lock_guard<std::mutex> lock(g_pd_attr_mu);
+        if (dev >= 0 && dev < 64 && !g_pd_attr_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(packed_dot_staged_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            if (e != cudaSuccess)
+                return e;
+            g_pd_attr_set[dev] = true;
+        }
+    }
+    packed_dot_staged_kernel<<<grid, L.block[0], L.smem_bytes, stream>>>(tf, ts, tr, p);
+    return cudaGetLastError();
+}
+
+}  // namespace loom

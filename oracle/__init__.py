@@ -57,6 +57,8 @@ def _load():
         lib.oracle_f16_to_f32.restype = ctypes.c_float
         lib.oracle_packed_dot.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, _ptr, _ptr, _i64,
                                           _i64, _ptr]
+        lib.oracle_lane_sums_f32.argtypes = [_ptr, _i64, _i64, _i64, _i64, _ptr, _i64, _i64, _ptr]
+        lib.oracle_guarded_rows_f32.argtypes = [_ptr, _i64, _i64, _i64, _ptr, _i64, _i64, _i64, _i64, _ptr]
         lib.oracle_workgroups.argtypes = [_i64, _i64]
         lib.oracle_workgroups.restype = _i64
         _lib = lib
@@ -240,4 +242,43 @@ def packed_dot(fields: np.ndarray, scales: np.ndarray, rhs: np.ndarray, counts,
                                      _p(out)), "packed_dot")
 
     _run_spans(run, P, threads)
+    return out
+
+
+def lane_sums(values: np.ndarray, counts, width: int = 1, threads: int = 1) -> np.ndarray:
+    """Per-lane f32 sums of segments ``values[S][rows][lanes]`` (width 1) or
+    ``values[S][rows][lanes][4]`` (width 4) over each segment's first ``counts[s]``
+    rows: ``float32[S][lanes]``."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    S, rows, lanes = v.shape[:3]
+    if (width == 1 and v.ndim != 3) or (width == 4 and (v.ndim != 4 or v.shape[3] != 4)):
+        raise ValueError("lane_sums: values do not match the width")
+    c = np.ascontiguousarray(np.broadcast_to(np.asarray(counts, np.int32), (S,)))
+    out = np.zeros((S, lanes), np.float32)
+    lib = _load()
+
+    def run(a, b):
+        _check(lib.oracle_lane_sums_f32(_p(v), rows * lanes * width, rows, lanes, width, _p(c), a, b, _p(out)),
+               "lane_sums")
+
+    _run_spans(run, S, threads)
+    return out
+
+
+def guarded_rows(values: np.ndarray, counts, columns: int, active_lanes: int, threads: int = 1) -> np.ndarray:
+    """The pages' guarded ragged rows over segments ``values[S][rows][lanes][4]``:
+    ``float32[S][lanes]``."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    S, rows, lanes = v.shape[:3]
+    if v.ndim != 4 or v.shape[3] != 4:
+        raise ValueError("guarded_rows: values must be [S][rows][lanes][4]")
+    c = np.ascontiguousarray(np.broadcast_to(np.asarray(counts, np.int32), (S,)))
+    out = np.zeros((S, lanes), np.float32)
+    lib = _load()
+
+    def run(a, b):
+        _check(lib.oracle_guarded_rows_f32(_p(v), rows * lanes * 4, rows, lanes, _p(c), columns, active_lanes,
+                                           a, b, _p(out)), "guarded_rows")
+
+    _run_spans(run, S, threads)
     return out

@@ -146,6 +146,82 @@ int oracle_sum_rows(const float *values, int64_t rows, int64_t lanes,
 }
 
 /*
+ * Per-lane f32 sums of independent segments, in the precision and order the
+ * pages write them.  Segment s starts at values + s * seg_stride and holds
+ * rows x lanes x width f32 (row-major); its first counts[s] rows are summed.
+ * [P1] "Keep one checked source for experiments" (width 1, sum_rows): each
+ * work-item sums its own column, the f32 carried sum starting at zero and
+ * adding one row per trip.  [P1] "Give each motif its own schedule" (width
+ * 4, sum_vector_rows): each row contributes a four-element vector reduced
+ * into the carried sum; reading taken: the elements are added to the sum one
+ * at a time in element order.  Segments [s_begin, s_end) are done; out is
+ * [segments][lanes].
+ */
+int oracle_lane_sums_f32(const float *values, int64_t seg_stride, int64_t rows, int64_t lanes,
+                         int64_t width, const int32_t *counts, int64_t s_begin, int64_t s_end,
+                         float *out)
+{
+    if (rows < 0 || lanes < 0 || (width != 1 && width != 4) || s_begin < 0 || s_end < s_begin)
+        return ORACLE_ERR_SHAPE;
+    for (int64_t s = s_begin; s < s_end; ++s) {
+        const int64_t count = counts[s];
+        if (count < 0 || count > rows)
+            return ORACLE_ERR_RANGE;
+        const float *seg = values + s * seg_stride;
+        for (int64_t lane = 0; lane < lanes; ++lane) {
+            float sum = 0.0f;
+            for (int64_t row = 0; row < count; ++row)
+                for (int64_t j = 0; j < width; ++j)
+                    sum = sum + seg[(row * lanes + lane) * width + j];
+            out[s * lanes + lane] = sum;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Guarded ragged rows of independent segments ([rows][lanes][4] f32 each).
+ * [P1] "Keep guards and inner loops in the source" (sum_guarded_rows): the
+ * row range is rounded up to a multiple of four; each trip adds to the f32
+ * carried sum the row's partial sum, which is the identity (0) for rows at or
+ * past the count, else the f32 sum, from the identity, of the row's first
+ * `columns` components, each of them the identity for lanes at or past
+ * `active_lanes`.  Rows at or past the count are never read.
+ */
+int oracle_guarded_rows_f32(const float *values, int64_t seg_stride, int64_t rows, int64_t lanes,
+                            const int32_t *counts, int64_t columns, int64_t active_lanes,
+                            int64_t s_begin, int64_t s_end, float *out)
+{
+    if (rows < 0 || lanes < 0 || columns < 0 || columns > 4 || active_lanes < 0 || s_begin < 0 ||
+        s_end < s_begin)
+        return ORACLE_ERR_SHAPE;
+    for (int64_t s = s_begin; s < s_end; ++s) {
+        const int64_t count = counts[s];
+        if (count < 0 || count > rows)
+            return ORACLE_ERR_RANGE;
+        const float *seg = values + s * seg_stride;
+        const int64_t end = ((count + 3) / 4) * 4;
+        for (int64_t lane = 0; lane < lanes; ++lane) {
+            float sum = 0.0f;
+            for (int64_t row = 0; row < end; ++row) {
+                float partial = 0.0f;
+                if (row < count) {
+                    float component_sum = 0.0f;
+                    for (int64_t column = 0; column < columns; ++column) {
+                        const float value = lane < active_lanes ? seg[(row * lanes + lane) * 4 + column] : 0.0f;
+                        component_sum = component_sum + value;
+                    }
+                    partial = component_sum;
+                }
+                sum = sum + partial;
+            }
+            out[s * lanes + lane] = sum;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * One packed 32-bit word to its four signed bytes.
  * [P1] "Apply the same controls to a packed dot product": the packed field
  * is unpacked into four 8-bit integers, which are then converted as signed

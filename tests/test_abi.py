@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(loom):
 
 
 def test_version_and_strings(loom):
-    assert loom.loom_abi_version() == 2
+    assert loom.loom_abi_version() == 3
     for st in range(-7, 1):
         assert loom.loom_status_string(st)
     assert loom.loom_status_string(-99) == "unknown status"
@@ -74,12 +74,13 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
         for warps in (1, 2, 4, 8):
             for chunk in (512, 4096, 8192):
                 wl = [10, rows, lanes, 1, depth, warps, 0, chunk]
-                if warps * depth * (chunk + 8) > 227 * 1024:   # more than a CTA may hold
+                want = warps * depth * (chunk + 8)   # depth stages of one chunk + one barrier each
+                if want > 227 * 1024:   # more than a CTA may hold
                     with pytest.raises(loom.LoomError):
                         loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, wl)
                     continue
                 L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, wl)
-                assert L["smem_bytes"] == warps * depth * (chunk + 8) and L["block"][0] == 32 * warps
+                assert L["smem_bytes"] == want and L["block"][0] == 32 * warps
     L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [10, rows, lanes, 1, 1, 1])
     assert L["smem_bytes"] == (4096 if rows * lanes <= 4096 else 8192) + 8
 
@@ -254,3 +255,52 @@ def test_unpack_validation(loom):
     assert lib.loom_i8_unpack(None, 5, A, None) == loom.LOOM_ERR_NULL
     assert lib.loom_i8_unpack(A, -1, A, None) == loom.LOOM_ERR_SHAPE
     assert lib.loom_i8_unpack(A + 2, 5, A, None) == loom.LOOM_ERR_ALIGN
+
+
+def test_packed_dot_launch(loom):
+    # 256 lanes of one instance per CTA; grid.y = instances.  Staged (TMA ring,
+    # 256 consumers + a producer warp) when lanes % 8 == 0 and streams <= 64.
+    L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [128, 128, 2048, 64])
+    assert L["kernel"] == loom.LOOM_KERNEL_PACKED_STAGED
+    assert L["grid"] == (8, 128, 1) and L["block"] == (288, 1, 1) and L["units_per_cta"] == 256
+    # default ring: 2 stages of 8 records x (1 KiB of words + 512 B of scales + 1 KiB of activations)
+    assert L["smem_bytes"] == 128 + 2 * 8 * (1024 + 512 + 64 * 16) + 16 * 2
+    for P, R, Ln, S in ((1, 128, 2048, 64), (3, 5, 1000, 7), (2, 0, 8, 1), (65535, 1, 1, 1)):
+        for aligned in (0, 1):
+            L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [P, R, Ln, S, aligned])
+            staged = aligned == 1 and Ln % 8 == 0 and S <= 64
+            assert L["kernel"] == (loom.LOOM_KERNEL_PACKED_STAGED if staged else loom.LOOM_KERNEL_PACKED_DIRECT)
+            assert L["grid"] == (oracle.workgroups(Ln, 256), P, 1)
+            assert L["block"][0] == (288 if staged else 256)
+    L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [1, 128, 2048, 128])   # too many streams to stage
+    assert L["kernel"] == loom.LOOM_KERNEL_PACKED_DIRECT and L["smem_bytes"] == 0
+    for bad in ([-1, 1, 8, 1], [1, -1, 8, 1], [1, 1, -8, 1], [1, 1, 8, 0], [65536, 1, 8, 1]):
+        with pytest.raises(loom.LoomError) as e:
+            loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, bad)
+        assert e.value.status == loom.LOOM_ERR_SHAPE
+    for bad in ([1, 8, 8, 1, 1, 9], [1, 8, 8, 1, 1, 0, 33], [1, 8, 8, 64, 1, 8, 32]):   # depth, rps, smem
+        with pytest.raises(loom.LoomError) as e:
+            loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, bad)
+        assert e.value.status == loom.LOOM_ERR_ARG
+
+
+def test_packed_dot_validation(loom):
+    lib = loom.library()
+    f = lambda *a: lib.loom_packed_dot(*a)
+    # empty work needs no pointers
+    assert f(None, None, None, 0, 128, 2048, 64, None, 0, None, None, None) == loom.LOOM_OK
+    assert f(None, None, None, 4, 128, 0, 64, None, 0, None, None, None) == loom.LOOM_OK
+    assert f(None, None, None, 4, 8, 16, 4, None, 3, None, None, None) == loom.LOOM_ERR_NULL
+    assert f(A, A, A, 4, 8, 16, 4, None, 3, None, None, None) == loom.LOOM_ERR_NULL     # no output
+    assert f(A, A + 1, A, 4, 8, 16, 4, None, 3, None, A, None) == loom.LOOM_ERR_ALIGN   # scales 2-byte
+    assert f(A + 2, A, A, 4, 8, 16, 4, None, 3, None, A, None) == loom.LOOM_ERR_ALIGN
+    assert f(A, A, A, 4, 8, 16, 4, None, 9, None, A, None) == loom.LOOM_ERR_RANGE      # count > records
+    assert f(A, A, A, 4, 8, 16, 4, None, -1, None, A, None) == loom.LOOM_ERR_RANGE
+    assert f(A, A, A, 4, 8, 16, 0, None, 3, None, A, None) == loom.LOOM_ERR_SHAPE      # no streams
+    assert f(A, A, A, -4, 8, 16, 4, None, 3, None, A, None) == loom.LOOM_ERR_SHAPE
+    t = loom.make_tuning(path=loom.LOOM_PATH_TENSOR)
+    assert lib.loom_packed_dot_ex(A, A, A, 4, 8, 16, 4, None, 3, None, A, None, ctypes.byref(t),
+                                  None) == loom.LOOM_ERR_ARG
+    t = loom.make_tuning(path=loom.LOOM_PATH_STAGED)   # 12 lanes cannot be staged
+    assert lib.loom_packed_dot_ex(A, A, A, 4, 8, 12, 4, None, 3, None, A, None, ctypes.byref(t),
+                                  None) == loom.LOOM_ERR_SHAPE

@@ -149,7 +149,7 @@ TC_SCHEDULES = [(0, 0, 0, 0, 0), (1, 2, 0, 0, 0), (1, 1, 0, 0, 0), (2, 1, 0, 0, 
 
 
 @pytest.mark.parametrize("n,k,b", [(384, 8192, 16), (2049, 4112, 16), (128, 1024, 5), (3, 256, 9),
-                                   (1024, 16384, 16)])
+                                   (1024, 16384, 16), (128, 16384, 16), (200, 65536, 16)])
 def test_tensor_core_schedule_invariance(env, n, k, b):
     # Every schedule -- a cluster per band, split or whole bands, stage depth
     # and width, A buffers, one or two pipelines per CTA -- gives the same bits.
