@@ -43,6 +43,20 @@ MUTANTS = {
     "packed_initial_dropped": ("float sum = initial ? initial[p * lanes + l] : 0.0f;", "float sum = 0.0f;"),
     "packed_element_order": ("sum = fmaf(scaled, a[j], sum);",
                              "sum = fmaf((float)ints[3 - j] * scale, a[3 - j], sum);"),
+    "lane_sum_row_order": ("sum = sum + seg[(row * lanes + lane) * width + j];",
+                           "sum = sum + seg[((count - 1 - row) * lanes + lane) * width + j];"),
+    "lane_sum_element_order": ("sum = sum + seg[(row * lanes + lane) * width + j];",
+                               "sum = sum + seg[(row * lanes + lane) * width + (width - 1 - j)];"),
+    "lane_sum_lane_index": ("sum = sum + seg[(row * lanes + lane) * width + j];",
+                            "sum = sum + seg[(row * lanes + 0) * width + j];"),
+    "lane_sum_last_row_dropped": ("for (int64_t row = 0; row < count; ++row)\n                for (int64_t j = 0;",
+                                  "for (int64_t row = 0; row + 1 < count; ++row)\n                for (int64_t j = 0;"),
+    "guarded_reads_past_count": ("                if (row < count) {\n                    float component_sum",
+                                 "                if (row < end) {\n                    float component_sum"),
+    "guarded_column_bound": ("for (int64_t column = 0; column < columns; ++column)",
+                             "for (int64_t column = 0; column <= columns && column < 4; ++column)"),
+    "guarded_active_bound": ("lane < active_lanes ? seg", "lane <= active_lanes ? seg"),
+    "guarded_row_order": ("? seg[(row * lanes + lane) * 4 + column]", "? seg[((count - 1 - row) * lanes + lane) * 4 + column]"),
 }
 
 
@@ -60,6 +74,7 @@ def test_planted_mistake_is_caught(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_rowsum.py"),
                         os.path.join(ROOT, "tests", "test_oracle_dot.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_packed_dot.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_packed_dot.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_lane_sums.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
