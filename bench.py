@@ -100,6 +100,7 @@ def recorded_traffic():
 KERNEL_SOURCES = {
     "segments": ("row_sum.cu",), "wide": ("row_sum.cu",),
     "gemv": ("dequant_dot.cu",), "batched": ("dot_tc.cu",), "packed": ("packed_dot.cu",),
+    "sum_rows": ("lane_sum.cu",), "sum_vector_rows": ("lane_sum.cu",), "guarded_rows": ("lane_sum.cu",),
 }
 SHARED_SOURCES = ("common.cuh", "internal.h", "loom_api.cu")
 
@@ -266,6 +267,22 @@ def run_reference(args, rank, world):
 # our arm
 # ----------------------------------------------------------------------------
 
+def slowest_rank_ms(elapsed_ms: float, dist, device) -> float:
+    """The timed region's length on the slowest rank (every rank gets it)."""
+    if dist is None:
+        return elapsed_ms
+    import torch
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Replicas: every rank moves the whole workload each step, so the job moves
+    world times the bytes in the slowest rank's step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import int8_dequant_dot_gb300 as loom
@@ -316,13 +333,9 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    elapsed_ms = step_start.elapsed_time(step_end)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = slowest_rank_ms(step_start.elapsed_time(step_end), dist, "cuda")
     ms_per_step = elapsed_ms / args.steps
-    value = world * total / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, total, ms_per_step)
 
     peak, peak_kind = measured_peak()
     traffic = recorded_traffic()
@@ -344,8 +357,8 @@ def run_ours(args, rank, world, dist):
 
     # end to end through the public API: pinned host inputs -> device -> kernels -> host results
     e2e = run_e2e(args, inp, total, torch, loom, stream, work)
-    # the pages' own packed-dot example, timed on its own (not part of the step)
-    extras = {"packed_dot": measure_packed(args, torch, loom, stream, peak, peak_kind)}
+    # the pages' other examples (packed dot, per-lane sums), each timed on its own (not part of the step)
+    extras = measure_extras(args, torch, loom, stream, peak, peak_kind)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -379,22 +392,16 @@ def packed_alg_bytes(d) -> int:
     return int((c * L * 6).sum() + (c * S * 16).sum() + d["problems"] * (L * 8 + 4))
 
 
-def measure_packed(args, torch, loom, stream, peak, peak_kind):
-    """Single launches, each after a 512 MB read that leaves nothing of the
-    inputs in L2; CUDA events on the launching stream."""
-    import synth
-    d = synth.packed_dot_case()
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    f, sc, rhs = t(d["fields"]), t(d["scales"].view(np.int16)), t(d["rhs"])
-    counts, init = t(d["counts"]), t(d["initial"])
-    out = torch.empty((d["problems"], d["lanes"]), dtype=torch.float32, device="cuda")
-    flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
-    sink = torch.zeros((), dtype=torch.int64, device="cuda")
-    alg = packed_alg_bytes(d)
+def lane_alg_bytes(d) -> int:
+    """Per segment: the active rows, the count and the outputs."""
+    c = d["counts"].astype(np.int64)
+    row = d["lanes"] * d["width"] * 4
+    return int((c * row).sum() + d["num_segments"] * (4 + d["lanes"] * 4))
 
-    def call():
-        loom.loom_packed_dot(f, sc, rhs, counts, 0, init, out=out, stream=stream)
 
+def _time_single(args, torch, stream, call, flush, sink):
+    """Single launches, each after a 512 MB read that leaves nothing of the inputs
+    in L2; CUDA events on the launching stream.  Returns the times in ms."""
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             call()
@@ -411,15 +418,55 @@ def measure_packed(args, torch, loom, stream, peak, peak_kind):
             b.record(stream)
         stream.synchronize()
         times.append(a.elapsed_time(b))
+    return times
+
+
+def _extra_line(workload, alg, times, peak, peak_kind, traffic, launch):
     avg = sum(times) / len(times)
     gbs = alg / (avg * 1e-3) / 1e9
-    L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [d["problems"], d["records"], d["lanes"], d["streams"]])
-    del flush
-    return {"workload": PACKED_WORKLOAD, "alg_bytes": alg, "avg_ms": avg, "min_ms": min(times),
-            "launches": len(times), "l2": "512 MB read before each launch",
+    return {"workload": workload, "alg_bytes": alg, "avg_ms": avg, "min_ms": min(times), "launches": len(times),
+            "l2": "512 MB read before each launch",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "peak_source": peak_kind, "traffic": recorded_traffic().get("packed")},
-            "grid": L["grid"], "block": L["block"][0]}
+                         "peak_source": peak_kind, "traffic": traffic},
+            "grid": launch["grid"], "block": launch["block"][0]}
+
+
+def measure_extras(args, torch, loom, stream, peak, peak_kind):
+    import synth
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros((), dtype=torch.int64, device="cuda")
+    traffic = recorded_traffic()
+    out = {}
+
+    d = synth.packed_dot_case()
+    f, sc, rhs = t(d["fields"]), t(d["scales"].view(np.int16)), t(d["rhs"])
+    counts, init = t(d["counts"]), t(d["initial"])
+    y = torch.empty((d["problems"], d["lanes"]), dtype=torch.float32, device="cuda")
+    times = _time_single(args, torch, stream,
+                         lambda: loom.loom_packed_dot(f, sc, rhs, counts, 0, init, out=y, stream=stream), flush, sink)
+    L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [d["problems"], d["records"], d["lanes"], d["streams"]])
+    out["packed_dot"] = _extra_line(PACKED_WORKLOAD, packed_alg_bytes(d), times, peak, peak_kind,
+                                    traffic.get("packed"), L)
+    del f, sc, rhs, counts, init, y, d
+
+    for name, S, R, W, guarded in (("sum_rows", 65536, 64, 1, False), ("sum_vector_rows", 16384, 64, 4, False),
+                                   ("guarded_rows", 16384, 63, 4, True)):
+        d = synth.lane_segments(num_segments=S, rows=R, lanes=32, width=W)
+        v, c = t(d["values"]), t(d["counts"])
+        o = torch.empty((S, 32), dtype=torch.float32, device="cuda")
+        if guarded:
+            call = lambda: loom.loom_sum_guarded_rows(v, S, R * 32 * 4, R, 32, c, 0, 4, 32, out=o, stream=stream)
+            what = f"guarded ragged rows: {S} segments x {R} rows x 32 lanes x 4, counts U[0,{R}], 4 columns, 32 lanes"
+        else:
+            call = lambda: loom.loom_sum_rows(v, S, R * 32 * W, R, 32, W, c, 0, out=o, stream=stream)
+            what = f"per-lane sums (width {W}): {S} segments x {R} rows x 32 lanes, counts U[0,{R}]"
+        times = _time_single(args, torch, stream, call, flush, sink)
+        L = loom.loom_launch_config(loom.LOOM_OP_LANE_SUMS, [S, R, 32, W])
+        out[name] = _extra_line(what, lane_alg_bytes(d), times, peak, peak_kind, traffic.get(name), L)
+        del v, c, o, d
+    del flush
+    return out
 
 
 def run_e2e(args, inp, total, torch, loom, stream, work):
@@ -483,6 +530,21 @@ def run_profile(args):
         stream.synchronize()
         print(json.dumps({"profile": args.profile, "launches": args.launches}))
         return
+    if args.profile in ("sum_rows", "sum_vector_rows", "guarded_rows"):
+        S, R, W = {"sum_rows": (65536, 64, 1), "sum_vector_rows": (16384, 64, 4),
+                   "guarded_rows": (16384, 63, 4)}[args.profile]
+        d = synth.lane_segments(num_segments=S, rows=R, lanes=32, width=W)
+        v = torch.from_numpy(d["values"]).cuda()
+        c = torch.from_numpy(d["counts"]).cuda()
+        with torch.cuda.stream(stream):
+            for _ in range(args.launches):
+                if args.profile == "guarded_rows":
+                    loom.loom_sum_guarded_rows(v, S, R * 128, R, 32, c, 0, 4, 32, stream=stream)
+                else:
+                    loom.loom_sum_rows(v, S, R * 32 * W, R, 32, W, c, 0, stream=stream)
+        stream.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": args.launches}))
+        return
     if args.profile in ("segments", "wide"):
         inp = {"segments": synth.batched_segments() if args.profile == "segments" else None,
                "wide": synth.wide_rows() if args.profile == "wide" else None}
@@ -529,7 +591,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--depth", type=int, default=0, help="read-ahead depth (0 = library default)")
-    ap.add_argument("--profile", choices=ORDER + ("packed",), default=None)
+    ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows"),
+                    default=None)
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3 and args.profile is None:

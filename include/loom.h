@@ -63,9 +63,12 @@ typedef enum loom_op {
                                     2 tensor), workspace (0/1, default 1), sm_count (0 =
                                     the current device), tc_units_per_stage,
                                     tc_a_buffers, tc_pipelines, tc_schedule} */
-    LOOM_OP_PACKED_DOT = 4       /* workload {problems, records, lanes, streams, aligned (0/1:
+    LOOM_OP_PACKED_DOT = 4,      /* workload {problems, records, lanes, streams, aligned (0/1:
                                     inputs 16-byte aligned, default 1), depth,
                                     records_per_stage} */
+    LOOM_OP_LANE_SUMS = 5        /* workload {num_segments, rows, lanes, width (1 or 4), aligned
+                                    (0/1, default 1), depth, warps_per_cta, units_per_warp,
+                                    chunk_bytes}; also the guarded rows (width 4) */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
@@ -100,6 +103,8 @@ typedef struct loom_launch {
                                           (two launches per pass) */
 #define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: 3-D TMA read-ahead ring per CTA */
 #define LOOM_KERNEL_PACKED_DIRECT 10 /* packed dot: plain loads */
+#define LOOM_KERNEL_LANESUM_STAGED 11 /* per-lane sums: bulk-copy read-ahead ring per warp */
+#define LOOM_KERNEL_LANESUM_DIRECT 12 /* per-lane sums: plain loads */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8
@@ -249,6 +254,44 @@ loom_status loom_packed_dot(const int32_t *d_fields, const uint16_t *d_scales, c
                             int32_t problems, int32_t records, int32_t lanes, int32_t streams,
                             const int32_t *d_counts, int32_t count, const float *d_initial,
                             float *d_out, void *stream);
+
+/*
+ * Per-lane f32 sums of independent segments: the pages' sum_rows (width 1)
+ * and sum_vector_rows (width 4).
+ * [P1] "Keep one checked source for experiments": work-item `lane` sums its
+ * column of rows [0, count), an f32 carried sum from zero, one row per trip
+ * in row order (the pages' check cases print the expected sums for an iota
+ * input).  [P1] "Give each motif its own schedule": each row holds a
+ * four-element vector per lane, reduced into the carried sum one element at
+ * a time in element order (the reading taken).  The results are defined to
+ * the bit.
+ * Layout: segment s at d_values + s * seg_stride, rows x lanes x width f32
+ * row-major (lanes 1..32); d_counts int32 [num_segments] (NULL: `count` for
+ * all); d_out f32 [num_segments][lanes].  One warp per segment, its active
+ * rows streamed through a ring of bulk copies (16-byte aligned values and
+ * segment starts, lanes * width a multiple of 4), else plain loads.
+ * Errors: NULL -> LOOM_ERR_NULL; pointers not 4-byte aligned ->
+ * LOOM_ERR_ALIGN; bad sizes or strides -> LOOM_ERR_SHAPE; host count outside
+ * [0, rows] -> LOOM_ERR_RANGE.  Device counts outside [0, rows] are clamped.
+ */
+loom_status loom_sum_rows(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                          int32_t lanes, int32_t width, const int32_t *d_counts, int32_t count, float *d_out,
+                          void *stream);
+
+/*
+ * Guarded ragged rows of independent segments: the pages' sum_guarded_rows.
+ * [P1] "Keep guards and inner loops in the source": the row range is
+ * rounded up to a multiple of four; each trip adds to the lane's f32 carried
+ * sum the identity for a row at or past the count (such rows are never
+ * read), else the f32 sum from zero of the row's first `columns` (0..4)
+ * components, each of them the identity on lanes at or past `active_lanes`.
+ * Layout: segment s at d_values + s * seg_stride, rows x lanes x 4 f32;
+ * d_counts / count, d_out and errors as loom_sum_rows; columns outside
+ * [0, 4] or active_lanes outside [0, lanes] -> LOOM_ERR_SHAPE.
+ */
+loom_status loom_sum_guarded_rows(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                                  int32_t lanes, const int32_t *d_counts, int32_t count, int32_t columns,
+                                  int32_t active_lanes, float *d_out, void *stream);
 
 /*
  * Unpack and convert: d_out[4j + i] = (float) signed byte i of d_packed[j].

@@ -84,6 +84,17 @@ loom_status loom_packed_dot_ex(const int32_t *d_fields, const uint16_t *d_scales
                                const int32_t *d_counts, int32_t count, const float *d_initial,
                                float *d_out, int32_t *d_error, const loom_tuning *tuning, void *stream);
 
+/* loom_sum_rows and loom_sum_guarded_rows with tuning (NULL = defaults): depth,
+ * warps_per_cta, units_per_warp (segments per warp), chunk_bytes and path as for
+ * the row sums; d_error gets LOOM_DEVERR_* bits. */
+loom_status loom_sum_rows_ex(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                             int32_t lanes, int32_t width, const int32_t *d_counts, int32_t count, float *d_out,
+                             int32_t *d_error, const loom_tuning *tuning, void *stream);
+loom_status loom_sum_guarded_rows_ex(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                                     int32_t lanes, const int32_t *d_counts, int32_t count, int32_t columns,
+                                     int32_t active_lanes, float *d_out, int32_t *d_error, const loom_tuning *tuning,
+                                     void *stream);
+
 #ifdef __cplusplus
 }
 #endif

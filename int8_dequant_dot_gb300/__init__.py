@@ -35,6 +35,7 @@ LOOM_OP_FULL_TILE_SUM = 1
 LOOM_OP_ROW_SUM_BATCHED = 2
 LOOM_OP_I8_DEQUANT_DOT = 3
 LOOM_OP_PACKED_DOT = 4
+LOOM_OP_LANE_SUMS = 5
 
 LOOM_KERNEL_UNPACK = 1
 LOOM_KERNEL_ROWSUM_STAGED = 2
@@ -46,6 +47,8 @@ LOOM_KERNEL_DOT_TENSOR = 7
 LOOM_KERNEL_DOT_TENSOR_SPLIT = 8
 LOOM_KERNEL_PACKED_STAGED = 9
 LOOM_KERNEL_PACKED_DIRECT = 10
+LOOM_KERNEL_LANESUM_STAGED = 11
+LOOM_KERNEL_LANESUM_DIRECT = 12
 
 LOOM_MAX_DEPTH = 8
 LOOM_PATH_AUTO = 0
@@ -58,7 +61,8 @@ EXPORTS = (
     "loom_launch_config", "loom_full_tile_sum", "loom_row_sum_batched", "loom_i8_dequant_dot",
     "loom_i8_unpack", "loom_status_string", "loom_abi_version", "loom_row_sum_batched_ex",
     "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes", "loom_i8_dequant_dot_noalloc",
-    "loom_packed_dot", "loom_packed_dot_ex",
+    "loom_packed_dot", "loom_packed_dot_ex", "loom_sum_rows", "loom_sum_rows_ex", "loom_sum_guarded_rows",
+    "loom_sum_guarded_rows_ex",
 )
 
 
@@ -108,6 +112,10 @@ def _bind() -> ctypes.CDLL:
         "loom_i8_dequant_dot_noalloc": [P, P, i32, i32, P, P, i32, P, P, P],
         "loom_packed_dot": [P, P, P, i32, i32, i32, i32, P, i32, P, P, P],
         "loom_packed_dot_ex": [P, P, P, i32, i32, i32, i32, P, i32, P, P, P, ctypes.POINTER(loom_tuning), P],
+        "loom_sum_rows": [P, i64, i64, i32, i32, i32, P, i32, P, P],
+        "loom_sum_rows_ex": [P, i64, i64, i32, i32, i32, P, i32, P, P, ctypes.POINTER(loom_tuning), P],
+        "loom_sum_guarded_rows": [P, i64, i64, i32, i32, P, i32, i32, i32, P, P],
+        "loom_sum_guarded_rows_ex": [P, i64, i64, i32, i32, P, i32, i32, i32, P, P, ctypes.POINTER(loom_tuning), P],
         "loom_i8_unpack": [P, i64, P, P],
         "loom_status_string": [i32],
         "loom_abi_version": [],
@@ -363,6 +371,43 @@ def loom_packed_dot_ex(fields, scales, rhs, counts=None, count: int = 0, initial
     else:
         tp = ctypes.byref(tuning) if tuning is not None else None
         _check(_lib.loom_packed_dot_ex(*args, _ptr(error), tp, st), _name)
+    return out
+
+
+def loom_sum_rows(values, num_segments: int, seg_stride: int, rows: int, lanes: int, width: int = 1,
+                  counts=None, count: int = 0, *, out=None, error=None, tuning=None, stream=None):
+    """Per-lane f32 sums (the pages' sum_rows, width 1, and sum_vector_rows, width 4):
+    returns ``out`` float32 ``[num_segments][lanes]``."""
+    import torch
+    if out is None:
+        out = _empty(values, (int(num_segments), int(lanes)), torch.float32)
+    st = _stream(stream, values)
+    args = (_ptr(values), int(num_segments), int(seg_stride), int(rows), int(lanes), int(width), _ptr(counts),
+            int(count), _ptr(out))
+    if tuning is None and error is None:
+        _check(_lib.loom_sum_rows(*args, st), "loom_sum_rows")
+    else:
+        tp = ctypes.byref(tuning) if tuning is not None else None
+        _check(_lib.loom_sum_rows_ex(*args, _ptr(error), tp, st), "loom_sum_rows_ex")
+    return out
+
+
+def loom_sum_guarded_rows(values, num_segments: int, seg_stride: int, rows: int, lanes: int, counts=None,
+                          count: int = 0, columns: int = 4, active_lanes: int = 32, *, out=None, error=None,
+                          tuning=None, stream=None):
+    """The pages' guarded ragged rows over segments ``[rows][lanes][4]``: returns ``out``
+    float32 ``[num_segments][lanes]``."""
+    import torch
+    if out is None:
+        out = _empty(values, (int(num_segments), int(lanes)), torch.float32)
+    st = _stream(stream, values)
+    args = (_ptr(values), int(num_segments), int(seg_stride), int(rows), int(lanes), _ptr(counts), int(count),
+            int(columns), int(active_lanes), _ptr(out))
+    if tuning is None and error is None:
+        _check(_lib.loom_sum_guarded_rows(*args, st), "loom_sum_guarded_rows")
+    else:
+        tp = ctypes.byref(tuning) if tuning is not None else None
+        _check(_lib.loom_sum_guarded_rows_ex(*args, _ptr(error), tp, st), "loom_sum_guarded_rows_ex")
     return out
 
 

@@ -105,6 +105,27 @@ int64_t dot_tc_workspace_bytes(const DotTcPlan &plan);
 bool dot_tc_cluster_fits(const DotTcPlan &plan);
 cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream);
 
+// ---- per-lane f32 sums (lane_sum.cu): sum_rows, sum_vector_rows, guarded rows ----
+struct LaneSumParams {
+    const float *values;
+    int64_t num_units;        // segments
+    int64_t unit_stride;      // elements between segment starts
+    int32_t rows, lanes;      // rows of lanes x width f32
+    const int32_t *counts;    // per segment, or NULL: count_scalar
+    int32_t count_scalar;
+    int32_t columns, active_lanes;   // guarded rows only
+    float *out;               // [segments][lanes]
+    int32_t *error;
+    int32_t depth;            // chunks in flight per warp (staged)
+    int32_t units_per_warp;
+    int32_t chunk_rows;       // rows per staged chunk
+    uint64_t wait_ns;
+    int32_t inject_stall;
+};
+uint32_t lane_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems);
+cudaError_t launch_lane_sum(const LaneSumParams &p, int width, bool guarded, bool staged, const loom_launch &L,
+                            cudaStream_t stream);
+
 // ---- the pages' packed-dot example (packed_dot.cu) ---------------------------
 constexpr int PD_DEFAULT_DEPTH = 2;        // stages of the read-ahead ring
 constexpr int PD_DEFAULT_RPS = 8;          // records per stage

@@ -379,6 +379,115 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     return LOOM_OK;
 }
 
+// ---- per-lane f32 sums ------------------------------------------------------------
+
+constexpr int LS_DEFAULT_DEPTH = 2;
+constexpr int64_t LS_DEFAULT_CHUNK_BYTES = 4096;
+
+// `aligned`: values 16-byte aligned and segment starts 16-byte apart; the
+// staged kernel also needs rows of a multiple of 16 bytes (lanes * width % 4).
+loom_status lane_sum_geometry(int64_t num_segments, int64_t rows, int64_t lanes, int64_t width, bool aligned,
+                              int64_t depth, int64_t warps, int64_t upw, int64_t chunk_bytes, loom_launch *out,
+                              int32_t *chunk_rows)
+{
+    if (num_segments < 0 || rows < 0 || lanes < 1 || lanes > 32 || (width != 1 && width != 4) ||
+        rows * lanes * width >= (1ll << 31))
+        return LOOM_ERR_SHAPE;
+    if (depth == 0)
+        depth = LS_DEFAULT_DEPTH;
+    if (warps == 0)
+        warps = 1;
+    if (chunk_bytes == 0)
+        chunk_bytes = LS_DEFAULT_CHUNK_BYTES;
+    if (depth < 1 || depth > LOOM_MAX_DEPTH || !valid_warps(warps) || upw < 0 || upw > 32 || !valid_chunk(chunk_bytes))
+        return LOOM_ERR_ARG;
+    if (upw == 0)
+        upw = row_sum_default_units_per_warp((int32_t)rows, (int32_t)(lanes * width));
+    const bool staged = aligned && (lanes * width) % 4 == 0;
+    // whole rows per chunk (staged rows are a multiple of 16 bytes, so is every chunk)
+    const int64_t row_bytes = lanes * width * 4;
+    int64_t crow = chunk_bytes / row_bytes;
+    if (crow < 1)
+        crow = 1;
+    const uint32_t smem = lane_sum_smem_bytes(staged, (int)depth, (int)warps, (int)(crow * lanes * width));
+    if (smem > 227 * 1024)
+        return LOOM_ERR_ARG;
+    const int64_t per_cta = warps * upw;
+    if (ceil_div(num_segments, per_cta) > 0x7fffffff)
+        return LOOM_ERR_SHAPE;
+    fill_launch(out, ceil_div(num_segments, per_cta), (uint32_t)(32 * warps), smem, (uint32_t)per_cta,
+                staged ? LOOM_KERNEL_LANESUM_STAGED : LOOM_KERNEL_LANESUM_DIRECT);
+    if (chunk_rows)
+        *chunk_rows = (int32_t)crow;
+    return LOOM_OK;
+}
+
+loom_status lane_sum_common(const float *values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                            int32_t lanes, int32_t width, bool guarded, const int32_t *counts, int32_t count,
+                            int32_t columns, int32_t active_lanes, float *out, int32_t *error,
+                            const loom_tuning *tuning, void *stream)
+{
+    Tuning t;
+    loom_status st = read_tuning(tuning, 0, &t);
+    if (st != LOOM_OK)
+        return st;
+    if (t.path == LOOM_PATH_TENSOR)
+        return LOOM_ERR_ARG;
+    if (num_segments < 0 || rows < 0 || lanes < 1 || lanes > 32 || (width != 1 && width != 4) || seg_stride < 0 ||
+        (int64_t)rows * lanes * width >= (1ll << 31))
+        return LOOM_ERR_SHAPE;
+    if (guarded && (columns < 0 || columns > 4 || active_lanes < 0 || active_lanes > lanes))
+        return LOOM_ERR_SHAPE;
+    if (num_segments > 1 && seg_stride < (int64_t)rows * lanes * width)
+        return LOOM_ERR_SHAPE;
+    if (num_segments > 1 && seg_stride > 0 &&
+        num_segments - 1 > (INT64_MAX - (int64_t)rows * lanes * width) / seg_stride)
+        return LOOM_ERR_SHAPE;
+    if (!counts && (count < 0 || count > rows))
+        return LOOM_ERR_RANGE;
+    if (num_segments == 0)
+        return LOOM_OK;
+    if (!out || (rows > 0 && !values))
+        return LOOM_ERR_NULL;
+    if (misaligned(values, 4) || misaligned(counts, 4) || misaligned(out, 4) || misaligned(error, 4))
+        return LOOM_ERR_ALIGN;
+    const bool can_stage = !misaligned(values, 16) && (seg_stride % 4 == 0 || num_segments == 1) &&
+                           (lanes * width) % 4 == 0;
+    if (t.path == LOOM_PATH_STAGED && !can_stage)
+        return LOOM_ERR_ALIGN;
+    const bool staged = can_stage && t.path != LOOM_PATH_DIRECT;
+    loom_launch L;
+    int32_t crow = 0;
+    st = lane_sum_geometry(num_segments, rows, lanes, width, staged, t.depth, t.warps, t.upw, t.chunk_bytes, &L,
+                           &crow);
+    if (st != LOOM_OK)
+        return st;
+    LaneSumParams p;
+    p.values = values;
+    p.num_units = num_segments;
+    p.unit_stride = seg_stride;
+    p.rows = rows;
+    p.lanes = lanes;
+    p.counts = counts;
+    p.count_scalar = count;
+    p.columns = guarded ? columns : width;
+    p.active_lanes = guarded ? active_lanes : lanes;
+    p.out = out;
+    p.error = error;
+    p.depth = t.depth ? t.depth : LS_DEFAULT_DEPTH;
+    p.units_per_warp = (int32_t)(L.units_per_cta / (L.block[0] / 32));
+    p.chunk_rows = crow;
+    p.wait_ns = t.wait_ns;
+    p.inject_stall = t.stall;
+    const cudaError_t e = launch_lane_sum(p, width, guarded, L.kernel == LOOM_KERNEL_LANESUM_STAGED, L,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    return LOOM_OK;
+}
+
 // ---- the pages' packed-dot example ------------------------------------------------
 
 // `aligned`: the inputs meet the TMA path's alignment; the staged kernel is
@@ -569,6 +678,11 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         return dot_geometry(workload[0], workload[1], workload[2], aligned, opt(4, 0), opt(5, 0),
                             opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms ? sms : 1, out, nullptr);
     }
+    case LOOM_OP_LANE_SUMS:
+        if (n_workload < 4)
+            return LOOM_ERR_ARG;
+        return lane_sum_geometry(workload[0], workload[1], workload[2], workload[3], opt(4, 1) != 0, opt(5, 0),
+                                 opt(6, 0), opt(7, 0), opt(8, 0), out, nullptr);
     case LOOM_OP_PACKED_DOT:
         if (n_workload < 4)
             return LOOM_ERR_ARG;
@@ -698,6 +812,39 @@ loom_status loom_packed_dot_ex(const int32_t *d_fields, const uint16_t *d_scales
 {
     return packed_common(d_fields, d_scales, d_rhs, problems, records, lanes, streams, d_counts, count,
                          d_initial, d_out, d_error, tuning, stream);
+}
+
+loom_status loom_sum_rows(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                          int32_t lanes, int32_t width, const int32_t *d_counts, int32_t count, float *d_out,
+                          void *stream)
+{
+    return lane_sum_common(d_values, num_segments, seg_stride, rows, lanes, width, false, d_counts, count, 0, 0,
+                           d_out, nullptr, nullptr, stream);
+}
+
+loom_status loom_sum_rows_ex(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                             int32_t lanes, int32_t width, const int32_t *d_counts, int32_t count, float *d_out,
+                             int32_t *d_error, const loom_tuning *tuning, void *stream)
+{
+    return lane_sum_common(d_values, num_segments, seg_stride, rows, lanes, width, false, d_counts, count, 0, 0,
+                           d_out, d_error, tuning, stream);
+}
+
+loom_status loom_sum_guarded_rows(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                                  int32_t lanes, const int32_t *d_counts, int32_t count, int32_t columns,
+                                  int32_t active_lanes, float *d_out, void *stream)
+{
+    return lane_sum_common(d_values, num_segments, seg_stride, rows, lanes, 4, true, d_counts, count, columns,
+                           active_lanes, d_out, nullptr, nullptr, stream);
+}
+
+loom_status loom_sum_guarded_rows_ex(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
+                                     int32_t lanes, const int32_t *d_counts, int32_t count, int32_t columns,
+                                     int32_t active_lanes, float *d_out, int32_t *d_error, const loom_tuning *tuning,
+                                     void *stream)
+{
+    return lane_sum_common(d_values, num_segments, seg_stride, rows, lanes, 4, true, d_counts, count, columns,
+                           active_lanes, d_out, d_error, tuning, stream);
 }
 
 loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)

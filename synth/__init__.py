@@ -266,3 +266,17 @@ def packed_dot_case(problems: int = 128, records: int = 128, lanes: int = 2048, 
     return dict(fields=fields, scales=scales.view(np.uint16).reshape(problems, records, lanes), rhs=rhs,
                 initial=initial, counts=counts, problems=problems, records=records, lanes=lanes,
                 streams=streams)
+
+
+def lane_segments(num_segments: int = 65536, rows: int = 64, lanes: int = 32, width: int = 1,
+                  count_max: int | None = None, seed: int | None = None) -> dict:
+    """Segments ``[S][rows][lanes]`` (width 1) or ``[S][rows][lanes][4]`` (width 4) of
+    values uniform on the 2**-23 grid in [-1, 1), with counts uniform in [0, count_max]
+    (``rows`` unless given)."""
+    s = workload_seed(7 if width == 1 else 8) if seed is None else seed
+    shape = (num_segments, rows, lanes) if width == 1 else (num_segments, rows, lanes, 4)
+    values = uniform_grid_f32(stream_seed(s, 0), int(np.prod(shape))).reshape(shape)
+    hi = rows if count_max is None else count_max
+    counts = uniform_int(stream_seed(s, 1), num_segments, 0, hi).astype(np.int32)
+    return dict(values=values, counts=counts, num_segments=num_segments, rows=rows, lanes=lanes, width=width,
+                seg_stride=rows * lanes * width)

@@ -304,3 +304,37 @@ def test_packed_dot_validation(loom):
     t = loom.make_tuning(path=loom.LOOM_PATH_STAGED)   # 12 lanes cannot be staged
     assert lib.loom_packed_dot_ex(A, A, A, 4, 8, 12, 4, None, 3, None, A, None, ctypes.byref(t),
                                   None) == loom.LOOM_ERR_SHAPE
+
+
+def test_lane_sum_launch(loom):
+    # one warp per segment; 64 x 32 rows of width 1: four segments per warp (32 KiB of rows)
+    L = loom.loom_launch_config(loom.LOOM_OP_LANE_SUMS, [65536, 64, 32, 1])
+    assert L["kernel"] == loom.LOOM_KERNEL_LANESUM_STAGED
+    assert L["block"] == (32, 1, 1) and L["units_per_cta"] == 4 and L["grid"] == (16384, 1, 1)
+    assert L["smem_bytes"] == 2 * (4096 + 8)
+    L = loom.loom_launch_config(loom.LOOM_OP_LANE_SUMS, [16384, 64, 32, 4])
+    assert L["units_per_cta"] == 1 and L["grid"] == (16384, 1, 1)
+    for S, R, Ln, W in ((0, 64, 32, 1), (1, 1, 1, 1), (1009, 63, 32, 4), (77, 5, 7, 1), (3, 2, 12, 1)):
+        for aligned in (0, 1):
+            L = loom.loom_launch_config(loom.LOOM_OP_LANE_SUMS, [S, R, Ln, W, aligned])
+            staged = aligned == 1 and (Ln * W) % 4 == 0
+            assert L["kernel"] == (loom.LOOM_KERNEL_LANESUM_STAGED if staged else loom.LOOM_KERNEL_LANESUM_DIRECT)
+            assert L["grid"][0] == oracle.workgroups(S, L["units_per_cta"])
+    for bad in ([1, 64, 33, 1], [1, 64, 0, 1], [1, 64, 32, 2], [-1, 64, 32, 1]):
+        with pytest.raises(loom.LoomError) as e:
+            loom.loom_launch_config(loom.LOOM_OP_LANE_SUMS, bad)
+        assert e.value.status == loom.LOOM_ERR_SHAPE
+
+
+def test_lane_sum_validation(loom):
+    lib = loom.library()
+    assert lib.loom_sum_rows(None, 0, 0, 64, 32, 1, None, 0, None, None) == loom.LOOM_OK
+    assert lib.loom_sum_rows(None, 4, 2048, 64, 32, 1, None, 3, None, None) == loom.LOOM_ERR_NULL
+    assert lib.loom_sum_rows(A + 2, 4, 2048, 64, 32, 1, None, 3, A, None) == loom.LOOM_ERR_ALIGN
+    assert lib.loom_sum_rows(A, 4, 2048, 64, 32, 1, None, 65, A, None) == loom.LOOM_ERR_RANGE
+    assert lib.loom_sum_rows(A, 4, 100, 64, 32, 1, None, 3, A, None) == loom.LOOM_ERR_SHAPE   # overlapping
+    assert lib.loom_sum_rows(A, 4, 2048, 64, 32, 3, None, 3, A, None) == loom.LOOM_ERR_SHAPE   # width
+    g = lib.loom_sum_guarded_rows
+    assert g(A, 4, 8064, 63, 32, None, 3, 5, 32, A, None) == loom.LOOM_ERR_SHAPE   # columns > 4
+    assert g(A, 4, 8064, 63, 32, None, 3, 4, 33, A, None) == loom.LOOM_ERR_SHAPE   # active > lanes
+    assert g(A, 4, 8064, 63, 32, None, 64, 4, 32, A, None) == loom.LOOM_ERR_RANGE
