@@ -18,6 +18,21 @@ namespace dev {
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may be scheduled while the previous kernel on its stream drains.
+// At entry it lets the next kernel be scheduled the same way, then waits
+// until the previous kernel has completed and its memory operations are
+// visible: nothing before this touches global memory, so stream order holds
+// for every input and output whatever the previous kernel was.
+__device__ __forceinline__ void follow_previous_kernel()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// The wait alone (for a kernel that lets its dependents start later).
+__device__ __forceinline__ void wait_previous_kernel() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

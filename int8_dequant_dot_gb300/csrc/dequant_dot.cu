@@ -118,6 +118,7 @@ struct Ring {
 template <int NB, int RPW>
 __global__ void __launch_bounds__(256) dot_staged_k_kernel(const DotParams p)
 {
+    dev::follow_previous_kernel();
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int S = DOT_K_CHUNK_WORDS / 128;  // slots per chunk
     const int lane = threadIdx.x & 31;
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(256) dot_staged_k_kernel(const DotParams p)
 template <int NB>
 __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
 {
+    dev::follow_previous_kernel();
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -355,6 +357,7 @@ __global__ void __launch_bounds__(256) dot_staged_b_kernel(const DotParams p)
 template <int NB>
 __global__ void __launch_bounds__(256, 1) dot_direct_kernel(const DotParams p)
 {
+    dev::follow_previous_kernel();
     const int lane = threadIdx.x & 31;
     const int32_t r = (int32_t)((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
     if (r >= p.n_rows)
@@ -396,6 +399,7 @@ cudaError_t launch_staged_k(const DotParams &p, const loom_launch &L, cudaStream
 __global__ void __launch_bounds__(UNPACK_BLOCK) unpack_kernel(const int32_t *__restrict__ packed,
                                                               int64_t n_words, float *__restrict__ out)
 {
+    dev::follow_previous_kernel();
     const int64_t j = (int64_t)blockIdx.x * UNPACK_BLOCK + threadIdx.x;
     if (j >= n_words)
         return;  // over-dispatched invocation: no load, no store

@@ -464,6 +464,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                   const TcParams q)
 {
     extern __shared__ unsigned char smem_raw[];
+    // the next kernel (the finishing kernel, when bands are split) is let in at teardown
+    dev::wait_previous_kernel();
     const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
     const CtaArea C{base};
     const int warp = threadIdx.x >> 5;
@@ -905,7 +907,7 @@ constexpr int TC_FIN_THREADS = 4 * TC_M;   // four threads per row, four vectors
 __global__ void __launch_bounds__(TC_FIN_THREADS) dot_tc_finish_kernel(const FinishParams f)
 {
     __shared__ int64_t span[3];   // first and last CTA of the band, and cf's record index
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // the streaming kernel's records are complete
+    dev::follow_previous_kernel();   // the streaming kernel's records are complete
     const int r_in = threadIdx.x >> 2;                    // row within the band
     const int quad = threadIdx.x & 3;                      // vectors 4 quad .. 4 quad + 3
     const int64_t T = f.total_units, G = f.grid;
@@ -1286,14 +1288,17 @@ cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_
     cfg.blockDim = dim3((unsigned)dot_tc_threads(plan.pipes), 1, 1);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute ca[1];
+    cudaLaunchAttribute ca[2];
+    ca[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see follow_previous_kernel
+    ca[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = ca;
+    cfg.numAttrs = 1;
     if (plan.mode == TC_CLUSTER) {
-        ca[0].id = cudaLaunchAttributeClusterDimension;
-        ca[0].val.clusterDim.x = (unsigned)plan.cluster;
-        ca[0].val.clusterDim.y = 1;
-        ca[0].val.clusterDim.z = 1;
-        cfg.attrs = ca;
-        cfg.numAttrs = 1;
+        ca[1].id = cudaLaunchAttributeClusterDimension;
+        ca[1].val.clusterDim.x = (unsigned)plan.cluster;
+        ca[1].val.clusterDim.y = 1;
+        ca[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     e = cudaLaunchKernelEx(&cfg, dot_tc_kernel, tmw, tmx, q);
     if (e != cudaSuccess || !plan.split)

@@ -157,7 +157,9 @@ constexpr int UNPACK_BLOCK = 256;
 cudaError_t launch_unpack(const int32_t *packed, int64_t n_words, float *out, const loom_launch &L,
                           cudaStream_t stream);
 
-// Launch a kernel with the geometry of L (grid.x, block.x, dynamic smem).
+// Launch a kernel with the geometry of L (grid, block, dynamic smem) as a
+// programmatic dependent of the previous kernel on the stream (the kernels
+// wait for it at entry: see follow_previous_kernel in common.cuh).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_with(void (*kernel)(KArgs...), const loom_launch &L, cudaStream_t stream,
                         Args &&...args)
@@ -173,6 +175,11 @@ cudaError_t launch_with(void (*kernel)(KArgs...), const loom_launch &L, cudaStre
     cfg.blockDim = dim3(L.block[0], L.block[1], L.block[2]);
     cfg.dynamicSmemBytes = L.smem_bytes;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -79,6 +79,7 @@ __device__ __forceinline__ void load_row(float (&v)[4], const float *row_base, i
 template <int WIDTH, bool GUARDED>
 __global__ void __launch_bounds__(256) lane_sum_staged_kernel(const LaneSumParams p)
 {
+    dev::follow_previous_kernel();
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(256) lane_sum_staged_kernel(const LaneSumParam
 template <int WIDTH, bool GUARDED>
 __global__ void __launch_bounds__(256) lane_sum_direct_kernel(const LaneSumParams p)
 {
+    dev::follow_previous_kernel();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t u0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + warp) * p.units_per_warp;

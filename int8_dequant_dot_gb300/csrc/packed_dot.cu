@@ -37,7 +37,6 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -127,6 +126,7 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel
     const __grid_constant__ CUtensorMap tm_fields, const __grid_constant__ CUtensorMap tm_scales,
     const __grid_constant__ CUtensorMap tm_rhs, const PackedDeviceParams p)
 {
+    dev::follow_previous_kernel();
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base = (dev::smem_u32(smem_raw) + 127u) & ~127u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel
 // Direct path: plain loads, one thread per lane, records in order.
 __global__ void __launch_bounds__(PD_LANES) packed_dot_direct_kernel(const PackedDeviceParams p)
 {
+    dev::follow_previous_kernel();
     const int32_t inst = blockIdx.y;
     const int32_t l = blockIdx.x * PD_LANES + threadIdx.x;
     const int32_t count = instance_count(p, inst);
@@ -272,9 +273,6 @@ bool encode_3d(CUtensorMap *map, CUtensorMapDataType type, uint32_t esize, const
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-std::mutex g_pd_attr_mu;
-bool g_pd_attr_set[64];
-
 }  // namespace
 
 bool packed_dot_stageable(const PackedParams &q)
@@ -312,11 +310,8 @@ cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_lau
     p.rps = q.rps;
     p.wait_ns = q.wait_ns;
     p.inject_stall = q.inject_stall;
-    const dim3 grid(L.grid[0], L.grid[1], 1);
-    if (!staged) {
-        packed_dot_direct_kernel<<<grid, L.block[0], 0, stream>>>(p);
-        return cudaGetLastError();
-    }
+    if (!staged)
+        return launch_with(packed_dot_direct_kernel, L, stream, p);
     CUtensorMap tf, ts, tr;
     if (!encode_3d(&tf, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, q.fields, (uint64_t)q.lanes, (uint64_t)q.records,
                    (uint64_t)q.problems, PD_LANES, (uint32_t)q.rps) ||
@@ -325,20 +320,7 @@ cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_lau
         !encode_3d(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q.rhs, (uint64_t)q.streams * 4, (uint64_t)q.records,
                    (uint64_t)q.problems, (uint32_t)q.streams * 4, (uint32_t)q.rps))
         return cudaErrorInvalidValue;
-    {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        std::lock_guard<std::mutex> lock(g_pd_attr_mu);
-        if (dev >= 0 && dev < 64 && !g_pd_attr_set[dev]) {
-            const cudaError_t e = cudaFuncSetAttribute(packed_dot_staged_kernel,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-            if (e != cudaSuccess)
-                return e;
-            g_pd_attr_set[dev] = true;
-        }
-    }
-    packed_dot_staged_kernel<<<grid, L.block[0], L.smem_bytes, stream>>>(tf, ts, tr, p);
-    return cudaGetLastError();
+    return launch_with(packed_dot_staged_kernel, L, stream, tf, ts, tr, p);
 }
 
 }  // namespace loom

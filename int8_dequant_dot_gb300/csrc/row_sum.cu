@@ -180,6 +180,7 @@ __device__ __forceinline__ void finish_group(const RowSumParams &p, int lane, in
 template <bool STAGED, int MINB>
 __global__ void __launch_bounds__(256, MINB) row_sum_kernel(const RowSumParams p)
 {
+    dev::follow_previous_kernel();
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
