@@ -59,6 +59,7 @@ def _load():
                                           _i64, _ptr]
         lib.oracle_lane_sums_f32.argtypes = [_ptr, _i64, _i64, _i64, _i64, _ptr, _i64, _i64, _ptr]
         lib.oracle_guarded_rows_f32.argtypes = [_ptr, _i64, _i64, _i64, _ptr, _i64, _i64, _i64, _i64, _ptr]
+        lib.oracle_routed_combine.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, _i64, _i64, _ptr]
         lib.oracle_workgroups.argtypes = [_i64, _i64]
         lib.oracle_workgroups.restype = _i64
         _lib = lib
@@ -281,4 +282,24 @@ def guarded_rows(values: np.ndarray, counts, columns: int, active_lanes: int, th
                                            a, b, _p(out)), "guarded_rows")
 
     _run_spans(run, S, threads)
+    return out
+
+
+def routed_combine(ids: np.ndarray, weights: np.ndarray, payload: np.ndarray, threads: int = 1) -> np.ndarray:
+    """Routed row combine: ``out float32[tokens][width]``; ``ids`` int32 ``[tokens][routes]``
+    (negative = missing), ``weights`` float32 ``[tokens][routes]``, ``payload`` float32
+    ``[rows][width]``."""
+    i = np.ascontiguousarray(ids, dtype=np.int32)
+    w = np.ascontiguousarray(weights, dtype=np.float32)
+    pl = np.ascontiguousarray(payload, dtype=np.float32)
+    T, R = i.shape
+    rows, width = pl.shape
+    out = np.zeros((T, width), np.float32)
+    lib = _load()
+
+    def run(a, b):
+        _check(lib.oracle_routed_combine(_p(i), _p(w), _p(pl), T, R, rows, width, a, b, _p(out)),
+               "routed_combine")
+
+    _run_spans(run, T, threads)
     return out

@@ -222,6 +222,45 @@ int oracle_guarded_rows_f32(const float *values, int64_t seg_stride, int64_t row
 }
 
 /*
+ * Routed row combine (a mixture-of-experts combine) for tokens
+ * [t_begin, t_end).
+ * [P1] "Separate route and payload lookahead": for each token the routes
+ * r = 0 .. routes-1 are visited in order; a route's row id selects a row of
+ * the payload matrix; a missing id (negative) suppresses the route's weight
+ * and payload reads and leaves the sum unchanged; otherwise the route's
+ * weight times the selected row (the weighted payload, one f32 product per
+ * element) is added to the token's f32 sum (one f32 addition per element),
+ * which starts at zero.  Reading taken: product and sum are rounded
+ * separately.  Layout: ids, weights [tokens][routes]; payload [rows][width];
+ * out [tokens][width].  An id >= rows is rejected.
+ */
+int oracle_routed_combine(const int32_t *ids, const float *weights, const float *payload, int64_t tokens,
+                          int64_t routes, int64_t rows, int64_t width, int64_t t_begin, int64_t t_end,
+                          float *out)
+{
+    if (tokens < 0 || routes < 0 || rows < 0 || width < 0 || t_begin < 0 || t_end > tokens)
+        return ORACLE_ERR_SHAPE;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        for (int64_t h = 0; h < width; ++h)
+            out[t * width + h] = 0.0f;
+        for (int64_t r = 0; r < routes; ++r) {
+            const int32_t id = ids[t * routes + r];
+            if (id < 0)
+                continue;   // a missing route: no weight, no payload
+            if (id >= rows)
+                return ORACLE_ERR_RANGE;
+            const float w = weights[t * routes + r];
+            const float *row = payload + (int64_t)id * width;
+            for (int64_t h = 0; h < width; ++h) {
+                const float weighted = w * row[h];
+                out[t * width + h] = out[t * width + h] + weighted;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * One packed 32-bit word to its four signed bytes.
  * [P1] "Apply the same controls to a packed dot product": the packed field
  * is unpacked into four 8-bit integers, which are then converted as signed

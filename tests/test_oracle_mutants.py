@@ -57,6 +57,12 @@ MUTANTS = {
                              "for (int64_t column = 0; column <= columns && column < 4; ++column)"),
     "guarded_active_bound": ("lane < active_lanes ? seg", "lane <= active_lanes ? seg"),
     "guarded_row_order": ("? seg[(row * lanes + lane) * 4 + column]", "? seg[((count - 1 - row) * lanes + lane) * 4 + column]"),
+    "routed_missing_not_skipped": ("            if (id < 0)\n                continue;   // a missing route",
+                                   "            if (id < -1000)\n                continue;   // a missing route"),
+    "routed_fused_step": ("                const float weighted = w * row[h];\n                out[t * width + h] = out[t * width + h] + weighted;",
+                          "                out[t * width + h] = fmaf(w, row[h], out[t * width + h]);"),
+    "routed_route_order": ("const int32_t id = ids[t * routes + r];", "const int32_t id = ids[t * routes + (routes - 1 - r)];"),
+    "routed_weight_index": ("const float w = weights[t * routes + r];", "const float w = weights[t * routes];"),
 }
 
 
@@ -75,6 +81,7 @@ def test_planted_mistake_is_caught(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_rowsum.py"),
                         os.path.join(ROOT, "tests", "test_oracle_dot.py"),
                         os.path.join(ROOT, "tests", "test_oracle_packed_dot.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_lane_sums.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_lane_sums.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_routed.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
