@@ -101,6 +101,7 @@ KERNEL_SOURCES = {
     "segments": ("row_sum.cu",), "wide": ("row_sum.cu",),
     "gemv": ("dequant_dot.cu",), "batched": ("dot_tc.cu",), "packed": ("packed_dot.cu",),
     "sum_rows": ("lane_sum.cu",), "sum_vector_rows": ("lane_sum.cu",), "guarded_rows": ("lane_sum.cu",),
+    "routed": ("routed.cu",),
 }
 SHARED_SOURCES = ("common.cuh", "internal.h", "loom_api.cu")
 
@@ -416,6 +417,16 @@ def lane_alg_bytes(d) -> int:
     return int((c * row).sum() + d["num_segments"] * (4 + d["lanes"] * 4))
 
 
+ROUTED_WORKLOAD = ("routed row combine: 4096 tokens x 8 routes (1 in 16 missing), payload rows of 2048 f32 "
+                   "each read once")
+
+
+def routed_alg_bytes(d) -> int:
+    """The ids, the present routes' weights and payload rows, and the outputs."""
+    valid = int((d["ids"] >= 0).sum())
+    return int(d["ids"].size * 4 + valid * 4 + valid * d["width"] * 4 + d["tokens"] * d["width"] * 4)
+
+
 def _time_single(args, torch, stream, call, flush, sink):
     """Single launches, each after a 512 MB read that leaves nothing of the inputs
     in L2; CUDA events on the launching stream.  Returns the times in ms."""
@@ -466,6 +477,16 @@ def measure_extras(args, torch, loom, stream, peak, peak_kind):
     out["packed_dot"] = _extra_line(PACKED_WORKLOAD, packed_alg_bytes(d), times, peak, peak_kind,
                                     traffic.get("packed"), L)
     del f, sc, rhs, counts, init, y, d
+
+    d = synth.routed_case()
+    ids, wts, pay = t(d["ids"]), t(d["weights"]), t(d["payload"])
+    o = torch.empty((d["tokens"], d["width"]), dtype=torch.float32, device="cuda")
+    times = _time_single(args, torch, stream, lambda: loom.loom_routed_combine(ids, wts, pay, out=o, stream=stream),
+                         flush, sink)
+    L = loom.loom_launch_config(loom.LOOM_OP_ROUTED_COMBINE, [d["tokens"], d["routes"], d["rows"], d["width"]])
+    out["routed_combine"] = _extra_line(ROUTED_WORKLOAD, routed_alg_bytes(d), times, peak, peak_kind,
+                                        traffic.get("routed"), L)
+    del ids, wts, pay, o, d
 
     for name, S, R, W, guarded in (("sum_rows", 65536, 64, 1, False), ("sum_vector_rows", 16384, 64, 4, False),
                                    ("guarded_rows", 16384, 63, 4, True)):
@@ -547,6 +568,16 @@ def run_profile(args):
         stream.synchronize()
         print(json.dumps({"profile": args.profile, "launches": args.launches}))
         return
+    if args.profile == "routed":
+        d = synth.routed_case()
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        ids, wts, pay = t(d["ids"]), t(d["weights"]), t(d["payload"])
+        with torch.cuda.stream(stream):
+            for _ in range(args.launches):
+                loom.loom_routed_combine(ids, wts, pay, stream=stream)
+        stream.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": args.launches}))
+        return
     if args.profile in ("sum_rows", "sum_vector_rows", "guarded_rows"):
         S, R, W = {"sum_rows": (65536, 64, 1), "sum_vector_rows": (16384, 64, 4),
                    "guarded_rows": (16384, 63, 4)}[args.profile]
@@ -608,7 +639,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--depth", type=int, default=0, help="read-ahead depth (0 = library default)")
-    ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows"),
+    ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows", "routed"),
                     default=None)
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()

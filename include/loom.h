@@ -66,9 +66,11 @@ typedef enum loom_op {
     LOOM_OP_PACKED_DOT = 4,      /* workload {problems, records, lanes, streams, aligned (0/1:
                                     inputs 16-byte aligned, default 1), depth,
                                     records_per_stage} */
-    LOOM_OP_LANE_SUMS = 5        /* workload {num_segments, rows, lanes, width (1 or 4), aligned
+    LOOM_OP_LANE_SUMS = 5,       /* workload {num_segments, rows, lanes, width (1 or 4), aligned
                                     (0/1, default 1), depth, warps_per_cta, units_per_warp,
                                     chunk_bytes}; also the guarded rows (width 4) */
+    LOOM_OP_ROUTED_COMBINE = 6   /* workload {tokens, routes, rows, width, aligned (0/1, default
+                                    1), depth, warps_per_cta} */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
@@ -105,6 +107,8 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_PACKED_DIRECT 10 /* packed dot: plain loads */
 #define LOOM_KERNEL_LANESUM_STAGED 11 /* per-lane sums: bulk-copy read-ahead ring per warp */
 #define LOOM_KERNEL_LANESUM_DIRECT 12 /* per-lane sums: plain loads */
+#define LOOM_KERNEL_ROUTED_STAGED 13  /* routed combine: bulk-copy ring of payload pieces per warp */
+#define LOOM_KERNEL_ROUTED_DIRECT 14  /* routed combine: plain loads */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8
@@ -292,6 +296,28 @@ loom_status loom_sum_rows(const float *d_values, int64_t num_segments, int64_t s
 loom_status loom_sum_guarded_rows(const float *d_values, int64_t num_segments, int64_t seg_stride, int32_t rows,
                                   int32_t lanes, const int32_t *d_counts, int32_t count, int32_t columns,
                                   int32_t active_lanes, float *d_out, void *stream);
+
+/*
+ * Routed row combine (a mixture-of-experts combine).
+ * [P1] "Separate route and payload lookahead": for each token the routes are
+ * visited in order; route r's row id selects a row of d_payload; a missing
+ * id (negative) suppresses the route's weight and payload reads and leaves
+ * the sum unchanged; otherwise every element of the selected row is
+ * multiplied by the route's weight (one f32 product) and added to the
+ * token's f32 sum (one f32 addition), which starts at zero.  Product and sum
+ * are rounded separately (the reading taken), so the result is defined to
+ * the bit.
+ * Layout (caller-owned device memory): d_ids int32 and d_weights f32
+ * [tokens][routes]; d_payload f32 [rows][width]; d_out f32 [tokens][width].
+ * One warp per token; its ids are read once, then its valid routes' row
+ * pieces stream through a ring of bulk copies (width a multiple of 4,
+ * 16-byte aligned payload and output, at most 32 routes), else plain loads.
+ * Errors: NULL -> LOOM_ERR_NULL; pointers not 4-byte aligned ->
+ * LOOM_ERR_ALIGN; negative sizes -> LOOM_ERR_SHAPE.  Ids at or past `rows`
+ * are treated as missing and flagged (LOOM_DEVERR_COUNT_RANGE, _ex only).
+ */
+loom_status loom_routed_combine(const int32_t *d_ids, const float *d_weights, const float *d_payload, int64_t tokens,
+                                int32_t routes, int32_t rows, int32_t width, float *d_out, void *stream);
 
 /*
  * Unpack and convert: d_out[4j + i] = (float) signed byte i of d_packed[j].

@@ -95,6 +95,13 @@ loom_status loom_sum_guarded_rows_ex(const float *d_values, int64_t num_segments
                                      int32_t active_lanes, float *d_out, int32_t *d_error, const loom_tuning *tuning,
                                      void *stream);
 
+/* loom_routed_combine with tuning (NULL = defaults): depth = row pieces in flight per
+ * warp, warps_per_cta, path (LOOM_PATH_STAGED on inputs it cannot take ->
+ * LOOM_ERR_SHAPE / LOOM_ERR_ALIGN); d_error gets LOOM_DEVERR_* bits. */
+loom_status loom_routed_combine_ex(const int32_t *d_ids, const float *d_weights, const float *d_payload,
+                                   int64_t tokens, int32_t routes, int32_t rows, int32_t width, float *d_out,
+                                   int32_t *d_error, const loom_tuning *tuning, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

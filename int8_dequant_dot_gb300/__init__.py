@@ -36,6 +36,7 @@ LOOM_OP_ROW_SUM_BATCHED = 2
 LOOM_OP_I8_DEQUANT_DOT = 3
 LOOM_OP_PACKED_DOT = 4
 LOOM_OP_LANE_SUMS = 5
+LOOM_OP_ROUTED_COMBINE = 6
 
 LOOM_KERNEL_UNPACK = 1
 LOOM_KERNEL_ROWSUM_STAGED = 2
@@ -49,6 +50,8 @@ LOOM_KERNEL_PACKED_STAGED = 9
 LOOM_KERNEL_PACKED_DIRECT = 10
 LOOM_KERNEL_LANESUM_STAGED = 11
 LOOM_KERNEL_LANESUM_DIRECT = 12
+LOOM_KERNEL_ROUTED_STAGED = 13
+LOOM_KERNEL_ROUTED_DIRECT = 14
 
 LOOM_MAX_DEPTH = 8
 LOOM_PATH_AUTO = 0
@@ -62,7 +65,7 @@ EXPORTS = (
     "loom_i8_unpack", "loom_status_string", "loom_abi_version", "loom_row_sum_batched_ex",
     "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes", "loom_i8_dequant_dot_noalloc",
     "loom_packed_dot", "loom_packed_dot_ex", "loom_sum_rows", "loom_sum_rows_ex", "loom_sum_guarded_rows",
-    "loom_sum_guarded_rows_ex",
+    "loom_sum_guarded_rows_ex", "loom_routed_combine", "loom_routed_combine_ex",
 )
 
 
@@ -116,6 +119,8 @@ def _bind() -> ctypes.CDLL:
         "loom_sum_rows_ex": [P, i64, i64, i32, i32, i32, P, i32, P, P, ctypes.POINTER(loom_tuning), P],
         "loom_sum_guarded_rows": [P, i64, i64, i32, i32, P, i32, i32, i32, P, P],
         "loom_sum_guarded_rows_ex": [P, i64, i64, i32, i32, P, i32, i32, i32, P, P, ctypes.POINTER(loom_tuning), P],
+        "loom_routed_combine": [P, P, P, i64, i32, i32, i32, P, P],
+        "loom_routed_combine_ex": [P, P, P, i64, i32, i32, i32, P, P, ctypes.POINTER(loom_tuning), P],
         "loom_i8_unpack": [P, i64, P, P],
         "loom_status_string": [i32],
         "loom_abi_version": [],
@@ -408,6 +413,29 @@ def loom_sum_guarded_rows(values, num_segments: int, seg_stride: int, rows: int,
     else:
         tp = ctypes.byref(tuning) if tuning is not None else None
         _check(_lib.loom_sum_guarded_rows_ex(*args, _ptr(error), tp, st), "loom_sum_guarded_rows_ex")
+    return out
+
+
+def loom_routed_combine(ids, weights, payload, *, tokens: int | None = None, routes: int | None = None,
+                        rows: int | None = None, width: int | None = None, out=None, error=None, tuning=None,
+                        stream=None):
+    """Routed row combine: ``out`` float32 ``[tokens][width]`` from ``ids`` int32 and
+    ``weights`` float32 ``[tokens][routes]`` (negative id = missing route) and
+    ``payload`` float32 ``[rows][width]``."""
+    import torch
+    if tokens is None or routes is None:
+        tokens, routes = ids.shape
+    if rows is None or width is None:
+        rows, width = payload.shape
+    if out is None:
+        out = _empty(payload, (int(tokens), int(width)), torch.float32)
+    st = _stream(stream, payload)
+    args = (_ptr(ids), _ptr(weights), _ptr(payload), int(tokens), int(routes), int(rows), int(width), _ptr(out))
+    if tuning is None and error is None:
+        _check(_lib.loom_routed_combine(*args, st), "loom_routed_combine")
+    else:
+        tp = ctypes.byref(tuning) if tuning is not None else None
+        _check(_lib.loom_routed_combine_ex(*args, _ptr(error), tp, st), "loom_routed_combine_ex")
     return out
 
 

@@ -126,6 +126,24 @@ uint32_t lane_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems)
 cudaError_t launch_lane_sum(const LaneSumParams &p, int width, bool guarded, bool staged, const loom_launch &L,
                             cudaStream_t stream);
 
+// ---- routed row combine (routed.cu) -------------------------------------------
+struct RoutedParams {
+    const int32_t *ids;       // [tokens][routes], negative = missing
+    const float *weights;     // [tokens][routes]
+    const float *payload;     // [rows][width]
+    float *out;               // [tokens][width]
+    int64_t tokens;
+    int32_t routes, rows, width;
+    int32_t *error;
+    int32_t depth;            // pieces in flight per warp (staged)
+    uint64_t wait_ns;
+    int32_t inject_stall;
+};
+constexpr int RC_DEFAULT_DEPTH = 4;
+constexpr int RC_MAX_STAGED_ROUTES = 32;
+uint32_t routed_smem_bytes(bool staged, int depth, int warps);
+cudaError_t launch_routed(const RoutedParams &p, bool staged, const loom_launch &L, cudaStream_t stream);
+
 // ---- the pages' packed-dot example (packed_dot.cu) ---------------------------
 constexpr int PD_DEFAULT_DEPTH = 2;        // stages of the read-ahead ring
 constexpr int PD_DEFAULT_RPS = 8;          // records per stage

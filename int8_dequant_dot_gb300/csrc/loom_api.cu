@@ -379,6 +379,77 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     return LOOM_OK;
 }
 
+// ---- routed row combine ----------------------------------------------------------
+
+loom_status routed_geometry(int64_t tokens, int64_t routes, int64_t rows, int64_t width, bool aligned, int64_t depth,
+                            int64_t warps, loom_launch *out)
+{
+    if (tokens < 0 || routes < 0 || rows < 0 || width < 0 || rows > 0x7fffffff || width > 0x7fffffff ||
+        routes > 0x7fffffff)
+        return LOOM_ERR_SHAPE;
+    if (depth == 0)
+        depth = RC_DEFAULT_DEPTH;
+    if (warps == 0)
+        warps = 2;
+    if (depth < 1 || depth > LOOM_MAX_DEPTH || !valid_warps(warps))
+        return LOOM_ERR_ARG;
+    const bool staged = aligned && width % 4 == 0 && routes <= RC_MAX_STAGED_ROUTES;
+    if (ceil_div(tokens, warps) > 0x7fffffff)
+        return LOOM_ERR_SHAPE;
+    fill_launch(out, ceil_div(tokens, warps), (uint32_t)(32 * warps), routed_smem_bytes(staged, (int)depth, (int)warps),
+                (uint32_t)warps, staged ? LOOM_KERNEL_ROUTED_STAGED : LOOM_KERNEL_ROUTED_DIRECT);
+    return LOOM_OK;
+}
+
+loom_status routed_common(const int32_t *ids, const float *weights, const float *payload, int64_t tokens,
+                          int32_t routes, int32_t rows, int32_t width, float *out, int32_t *error,
+                          const loom_tuning *tuning, void *stream)
+{
+    Tuning t;
+    loom_status st = read_tuning(tuning, 0, &t);
+    if (st != LOOM_OK)
+        return st;
+    if (t.path == LOOM_PATH_TENSOR)
+        return LOOM_ERR_ARG;
+    if (tokens < 0 || routes < 0 || rows < 0 || width < 0)
+        return LOOM_ERR_SHAPE;
+    if (tokens == 0 || width == 0)
+        return LOOM_OK;
+    if (!out || (routes > 0 && (!ids || !weights)) || (routes > 0 && rows > 0 && !payload))
+        return LOOM_ERR_NULL;
+    if (misaligned(ids, 4) || misaligned(weights, 4) || misaligned(payload, 4) || misaligned(out, 4) ||
+        misaligned(error, 4))
+        return LOOM_ERR_ALIGN;
+    const bool can_stage = !misaligned(payload, 16) && !misaligned(out, 16) && width % 4 == 0 &&
+                           routes <= RC_MAX_STAGED_ROUTES;
+    if (t.path == LOOM_PATH_STAGED && !can_stage)
+        return (width % 4 != 0 || routes > RC_MAX_STAGED_ROUTES) ? LOOM_ERR_SHAPE : LOOM_ERR_ALIGN;
+    const bool staged = can_stage && t.path != LOOM_PATH_DIRECT;
+    loom_launch L;
+    st = routed_geometry(tokens, routes, rows, width, staged, t.depth, t.warps, &L);
+    if (st != LOOM_OK)
+        return st;
+    RoutedParams p;
+    p.ids = ids;
+    p.weights = weights;
+    p.payload = payload;
+    p.out = out;
+    p.tokens = tokens;
+    p.routes = routes;
+    p.rows = rows;
+    p.width = width;
+    p.error = error;
+    p.depth = t.depth ? t.depth : RC_DEFAULT_DEPTH;
+    p.wait_ns = t.wait_ns;
+    p.inject_stall = t.stall;
+    const cudaError_t e = launch_routed(p, L.kernel == LOOM_KERNEL_ROUTED_STAGED, L, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    return LOOM_OK;
+}
+
 // ---- per-lane f32 sums ------------------------------------------------------------
 
 constexpr int LS_DEFAULT_DEPTH = 2;
@@ -678,6 +749,11 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         return dot_geometry(workload[0], workload[1], workload[2], aligned, opt(4, 0), opt(5, 0),
                             opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms ? sms : 1, out, nullptr);
     }
+    case LOOM_OP_ROUTED_COMBINE:
+        if (n_workload < 4)
+            return LOOM_ERR_ARG;
+        return routed_geometry(workload[0], workload[1], workload[2], workload[3], opt(4, 1) != 0, opt(5, 0),
+                               opt(6, 0), out);
     case LOOM_OP_LANE_SUMS:
         if (n_workload < 4)
             return LOOM_ERR_ARG;
@@ -845,6 +921,19 @@ loom_status loom_sum_guarded_rows_ex(const float *d_values, int64_t num_segments
 {
     return lane_sum_common(d_values, num_segments, seg_stride, rows, lanes, 4, true, d_counts, count, columns,
                            active_lanes, d_out, d_error, tuning, stream);
+}
+
+loom_status loom_routed_combine(const int32_t *d_ids, const float *d_weights, const float *d_payload, int64_t tokens,
+                                int32_t routes, int32_t rows, int32_t width, float *d_out, void *stream)
+{
+    return routed_common(d_ids, d_weights, d_payload, tokens, routes, rows, width, d_out, nullptr, nullptr, stream);
+}
+
+loom_status loom_routed_combine_ex(const int32_t *d_ids, const float *d_weights, const float *d_payload,
+                                   int64_t tokens, int32_t routes, int32_t rows, int32_t width, float *d_out,
+                                   int32_t *d_error, const loom_tuning *tuning, void *stream)
+{
+    return routed_common(d_ids, d_weights, d_payload, tokens, routes, rows, width, d_out, d_error, tuning, stream);
 }
 
 loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)

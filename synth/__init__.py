@@ -280,3 +280,21 @@ def lane_segments(num_segments: int = 65536, rows: int = 64, lanes: int = 32, wi
     counts = uniform_int(stream_seed(s, 1), num_segments, 0, hi).astype(np.int32)
     return dict(values=values, counts=counts, num_segments=num_segments, rows=rows, lanes=lanes, width=width,
                 seg_stride=rows * lanes * width)
+
+
+def routed_case(tokens: int = 4096, routes: int = 8, width: int = 2048, missing_every: int = 16,
+                seed: int | None = None) -> dict:
+    """A routed row combine: ``tokens x routes`` row ids that visit every payload row
+    once (a seeded permutation of ``tokens * routes`` rows), about one route in
+    ``missing_every`` marked missing (-1), weights uniform on [0, 1) and payload rows of
+    ``width`` N(0,1) values."""
+    s = workload_seed(9) if seed is None else seed
+    rows = tokens * routes
+    order = np.argsort(splitmix64(stream_seed(s, 0), 0, rows), kind="stable").astype(np.int32)
+    ids = order.reshape(tokens, routes).copy()
+    if missing_every:
+        miss = uniform_int(stream_seed(s, 1), rows, 0, missing_every - 1).reshape(tokens, routes) == 0
+        ids[miss] = -1
+    weights = uniform_f32(stream_seed(s, 2), rows, 0.0, 1.0).reshape(tokens, routes)
+    payload = normal_f32(stream_seed(s, 3), rows * width).reshape(rows, width)
+    return dict(ids=ids, weights=weights, payload=payload, tokens=tokens, routes=routes, rows=rows, width=width)

@@ -338,3 +338,22 @@ def test_lane_sum_validation(loom):
     assert g(A, 4, 8064, 63, 32, None, 3, 5, 32, A, None) == loom.LOOM_ERR_SHAPE   # columns > 4
     assert g(A, 4, 8064, 63, 32, None, 3, 4, 33, A, None) == loom.LOOM_ERR_SHAPE   # active > lanes
     assert g(A, 4, 8064, 63, 32, None, 64, 4, 32, A, None) == loom.LOOM_ERR_RANGE
+
+
+def test_routed_combine_launch_and_validation(loom):
+    L = loom.loom_launch_config(loom.LOOM_OP_ROUTED_COMBINE, [4096, 8, 32768, 2048])
+    assert L["kernel"] == loom.LOOM_KERNEL_ROUTED_STAGED and L["block"] == (64, 1, 1)
+    assert L["grid"] == (2048, 1, 1) and L["smem_bytes"] == 2 * 4 * (2048 + 8)
+    for T, R, W, aligned, staged in ((1, 8, 2048, 1, True), (7, 33, 64, 1, False), (7, 8, 62, 1, False),
+                                     (7, 8, 64, 0, False), (0, 8, 64, 1, True)):
+        L = loom.loom_launch_config(loom.LOOM_OP_ROUTED_COMBINE, [T, R, 100, W, aligned])
+        assert L["kernel"] == (loom.LOOM_KERNEL_ROUTED_STAGED if staged else loom.LOOM_KERNEL_ROUTED_DIRECT)
+        assert L["grid"][0] == oracle.workgroups(T, 2)
+    lib = loom.library()
+    f = lib.loom_routed_combine
+    assert f(None, None, None, 0, 8, 100, 64, None, None) == loom.LOOM_OK
+    assert f(A, A, A, 4, 8, 100, 64, None, None) == loom.LOOM_ERR_NULL
+    assert f(A + 2, A, A, 4, 8, 100, 64, A, None) == loom.LOOM_ERR_ALIGN
+    assert f(A, A, A, -4, 8, 100, 64, A, None) == loom.LOOM_ERR_SHAPE
+    t = loom.make_tuning(path=loom.LOOM_PATH_STAGED)
+    assert lib.loom_routed_combine_ex(A, A, A, 4, 40, 100, 64, A, None, ctypes.byref(t), None) == loom.LOOM_ERR_SHAPE
