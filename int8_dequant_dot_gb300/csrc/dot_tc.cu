@@ -464,8 +464,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                   const TcParams q)
 {
     extern __shared__ unsigned char smem_raw[];
-    // the next kernel (the finishing kernel, when bands are split) is let in at teardown
-    dev::wait_previous_kernel();
+    // Set-up (barriers, tensor memory, the tensor maps' prefetch) may run while
+    // the previous kernel on the stream drains; the first global access of each
+    // role -- the producer's first copy, the epilogue's first scale load -- waits
+    // for it (wait_previous_kernel).  The MMA and converter warps touch only
+    // shared and tensor memory.  The next kernel (the finishing kernel, when
+    // bands are split) is let in at teardown.
     const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
     const CtaArea C{base};
     const int warp = threadIdx.x >> 5;
@@ -514,10 +518,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint64_t xpol = dev::l2_evict_last_policy();
     int issued = 0;        // producer: stages issued
     if (w == PRODUCER && p < q.pipes) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+        }
         for (int i = lane; i < L.n_bars(); i += 32)
             L.bar_init(i);
         dev::fence_barrier_init();
         __syncwarp();
+        dev::wait_previous_kernel();
         if (lane == 0 && !q.inject_stall) {
             int i = 0;
             for (StageWalk sw(u0, u1, UB, q.ups); sw.more() && i < S; ++i) {
@@ -727,6 +736,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int t = 32 * sub + lane;   // tile row
         const uint32_t tlane = (uint32_t)(32 * sub) << 16;
         const bool leader = w == EPI0 && lane == 0;
+        dev::wait_previous_kernel();
         // the pass's vector scales, one copy per pipeline
         if (w == EPI0 && lane < TC_N) {
             const float v = lane < q.batch ? __ldg(q.scale_x + lane) : 0.f;
