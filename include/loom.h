@@ -69,8 +69,9 @@ typedef enum loom_op {
     LOOM_OP_LANE_SUMS = 5,       /* workload {num_segments, rows, lanes, width (1 or 4), aligned
                                     (0/1, default 1), depth, warps_per_cta, units_per_warp,
                                     chunk_bytes}; also the guarded rows (width 4) */
-    LOOM_OP_ROUTED_COMBINE = 6   /* workload {tokens, routes, rows, width, aligned (0/1, default
+    LOOM_OP_ROUTED_COMBINE = 6,  /* workload {tokens, routes, rows, width, aligned (0/1, default
                                     1), depth, warps_per_cta} */
+    LOOM_OP_STAGE_ROWS = 7       /* workload {num_segments, rows, lanes} */
 } loom_op;
 
 /* Launch geometry of one kernel launch.  `units_per_cta` logical work units
@@ -109,6 +110,7 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_LANESUM_DIRECT 12 /* per-lane sums: plain loads */
 #define LOOM_KERNEL_ROUTED_STAGED 13  /* routed combine: bulk-copy ring of payload pieces per warp */
 #define LOOM_KERNEL_ROUTED_DIRECT 14  /* routed combine: plain loads */
+#define LOOM_KERNEL_STAGE_ROWS 15     /* upload of ragged rows: one CTA per 8 KiB of a segment */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8
@@ -318,6 +320,26 @@ loom_status loom_sum_guarded_rows(const float *d_values, int64_t num_segments, i
  */
 loom_status loom_routed_combine(const int32_t *d_ids, const float *d_weights, const float *d_payload, int64_t tokens,
                                 int32_t routes, int32_t rows, int32_t width, float *d_out, void *stream);
+
+/*
+ * Upload of ragged row-sum inputs: only the rows the row sums read.  For each
+ * segment s, elements [0, count_s * lanes) at h_values + s * seg_stride are
+ * copied to the same offsets of d_values; the rest of d_values is not
+ * touched.  The pages have no counterpart (their inputs start on the
+ * device): the bytes past a segment's count are not inputs of the row sums,
+ * and on GB300 the SMs read host memory in place over the host link, so the
+ * upload moves only the active prefix of every segment.
+ * h_values: memory the device can read -- pinned host memory (cudaHostAlloc,
+ * cudaMallocHost, cudaHostRegister), device memory, or any host memory where
+ * the device has pageable-memory access; d_values: device memory; d_counts:
+ * int32 [num_segments] readable by the device, or NULL (`count` for every
+ * segment); counts are clamped to [0, rows].  Asynchronous on `stream`.
+ * Errors: NULL -> LOOM_ERR_NULL; pointers not 4-byte aligned ->
+ * LOOM_ERR_ALIGN; bad sizes or strides -> LOOM_ERR_SHAPE; host count outside
+ * [0, rows] -> LOOM_ERR_RANGE; memory the device cannot read -> LOOM_ERR_ARG.
+ */
+loom_status loom_stage_rows(const float *h_values, float *d_values, int64_t num_segments, int64_t seg_stride,
+                            int32_t rows, int32_t lanes, const int32_t *d_counts, int32_t count, void *stream);
 
 /*
  * Unpack and convert: d_out[4j + i] = (float) signed byte i of d_packed[j].

@@ -37,6 +37,7 @@ LOOM_OP_I8_DEQUANT_DOT = 3
 LOOM_OP_PACKED_DOT = 4
 LOOM_OP_LANE_SUMS = 5
 LOOM_OP_ROUTED_COMBINE = 6
+LOOM_OP_STAGE_ROWS = 7
 
 LOOM_KERNEL_UNPACK = 1
 LOOM_KERNEL_ROWSUM_STAGED = 2
@@ -52,6 +53,7 @@ LOOM_KERNEL_LANESUM_STAGED = 11
 LOOM_KERNEL_LANESUM_DIRECT = 12
 LOOM_KERNEL_ROUTED_STAGED = 13
 LOOM_KERNEL_ROUTED_DIRECT = 14
+LOOM_KERNEL_STAGE_ROWS = 15
 
 LOOM_MAX_DEPTH = 8
 LOOM_PATH_AUTO = 0
@@ -65,7 +67,7 @@ EXPORTS = (
     "loom_i8_unpack", "loom_status_string", "loom_abi_version", "loom_row_sum_batched_ex",
     "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes", "loom_i8_dequant_dot_noalloc",
     "loom_packed_dot", "loom_packed_dot_ex", "loom_sum_rows", "loom_sum_rows_ex", "loom_sum_guarded_rows",
-    "loom_sum_guarded_rows_ex", "loom_routed_combine", "loom_routed_combine_ex",
+    "loom_sum_guarded_rows_ex", "loom_routed_combine", "loom_routed_combine_ex", "loom_stage_rows",
 )
 
 
@@ -121,6 +123,7 @@ def _bind() -> ctypes.CDLL:
         "loom_sum_guarded_rows_ex": [P, i64, i64, i32, i32, P, i32, i32, i32, P, P, ctypes.POINTER(loom_tuning), P],
         "loom_routed_combine": [P, P, P, i64, i32, i32, i32, P, P],
         "loom_routed_combine_ex": [P, P, P, i64, i32, i32, i32, P, P, ctypes.POINTER(loom_tuning), P],
+        "loom_stage_rows": [P, P, i64, i64, i32, i32, P, i32, P],
         "loom_i8_unpack": [P, i64, P, P],
         "loom_status_string": [i32],
         "loom_abi_version": [],
@@ -437,6 +440,16 @@ def loom_routed_combine(ids, weights, payload, *, tokens: int | None = None, rou
         tp = ctypes.byref(tuning) if tuning is not None else None
         _check(_lib.loom_routed_combine_ex(*args, _ptr(error), tp, st), "loom_routed_combine_ex")
     return out
+
+
+def loom_stage_rows(h_values, d_values, num_segments: int, seg_stride: int, rows: int, lanes: int,
+                    counts=None, count: int = 0, *, stream=None):
+    """Copy only each segment's first ``counts[s]`` rows from ``h_values`` (pinned host
+    memory, or any memory the device can read) to the same offsets of ``d_values``."""
+    _check(_lib.loom_stage_rows(_ptr(h_values), _ptr(d_values), int(num_segments), int(seg_stride), int(rows),
+                                int(lanes), _ptr(counts), int(count), _stream(stream, d_values)),
+           "loom_stage_rows")
+    return d_values
 
 
 def loom_i8_unpack(packed, n_words: int, out=None, *, stream=None):

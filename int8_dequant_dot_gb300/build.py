@@ -21,7 +21,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libloom.so")
-SOURCES = ["loom_api.cu", "row_sum.cu", "dequant_dot.cu", "dot_tc.cu", "packed_dot.cu", "lane_sum.cu", "routed.cu"]
+SOURCES = ["loom_api.cu", "row_sum.cu", "dequant_dot.cu", "dot_tc.cu", "packed_dot.cu", "lane_sum.cu", "routed.cu", "stage.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -126,6 +126,19 @@ uint32_t lane_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems)
 cudaError_t launch_lane_sum(const LaneSumParams &p, int width, bool guarded, bool staged, const loom_launch &L,
                             cudaStream_t stream);
 
+// ---- upload of ragged rows (stage.cu) ------------------------------------------
+struct StageParams {
+    const float *src;          // readable by the device: pinned host memory or device memory
+    float *dst;                // device memory, same layout
+    int64_t num_units, unit_stride, chunks_per_unit;
+    int32_t rows, lanes;
+    const int32_t *counts;     // device counts, or NULL: count_scalar
+    int32_t count_scalar;
+    int32_t vec4;              // 16-byte copies (both bases and the stride allow them)
+};
+int64_t stage_chunks_per_unit(int64_t rows, int64_t lanes);
+cudaError_t launch_stage_rows(const StageParams &p, cudaStream_t stream);
+
 // ---- routed row combine (routed.cu) -------------------------------------------
 struct RoutedParams {
     const int32_t *ids;       // [tokens][routes], negative = missing

@@ -379,6 +379,39 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     return LOOM_OK;
 }
 
+// ---- upload of ragged rows ---------------------------------------------------------
+
+loom_status stage_geometry(int64_t num_segments, int64_t rows, int64_t lanes, loom_launch *out)
+{
+    if (num_segments < 0 || rows < 0 || lanes < 1 || rows * lanes >= (1ll << 31))
+        return LOOM_ERR_SHAPE;
+    const int64_t per = stage_chunks_per_unit(rows, lanes);
+    if (num_segments > 0x7fffffff / per)
+        return LOOM_ERR_SHAPE;
+    fill_launch(out, num_segments * per, 256, 0, 1, LOOM_KERNEL_STAGE_ROWS);
+    return LOOM_OK;
+}
+
+// The device can read `p` (device, managed or registered host memory, or any
+// host memory where the device has pageable-memory access).
+bool device_readable(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type != cudaMemoryTypeUnregistered)
+        return true;
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return pageable != 0;
+}
+
 // ---- routed row combine ----------------------------------------------------------
 
 loom_status routed_geometry(int64_t tokens, int64_t routes, int64_t rows, int64_t width, bool aligned, int64_t depth,
@@ -749,6 +782,10 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         return dot_geometry(workload[0], workload[1], workload[2], aligned, opt(4, 0), opt(5, 0),
                             opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms ? sms : 1, out, nullptr);
     }
+    case LOOM_OP_STAGE_ROWS:
+        if (n_workload < 3)
+            return LOOM_ERR_ARG;
+        return stage_geometry(workload[0], workload[1], workload[2], out);
     case LOOM_OP_ROUTED_COMBINE:
         if (n_workload < 4)
             return LOOM_ERR_ARG;
@@ -934,6 +971,48 @@ loom_status loom_routed_combine_ex(const int32_t *d_ids, const float *d_weights,
                                    int32_t *d_error, const loom_tuning *tuning, void *stream)
 {
     return routed_common(d_ids, d_weights, d_payload, tokens, routes, rows, width, d_out, d_error, tuning, stream);
+}
+
+loom_status loom_stage_rows(const float *h_values, float *d_values, int64_t num_segments, int64_t seg_stride,
+                            int32_t rows, int32_t lanes, const int32_t *d_counts, int32_t count, void *stream)
+{
+    if (num_segments < 0 || rows < 0 || lanes < 1 || seg_stride < 0 || (int64_t)rows * lanes >= (1ll << 31))
+        return LOOM_ERR_SHAPE;
+    if (num_segments > 1 && seg_stride < (int64_t)rows * lanes)
+        return LOOM_ERR_SHAPE;
+    if (num_segments > 1 && seg_stride > 0 && num_segments - 1 > (INT64_MAX - (int64_t)rows * lanes) / seg_stride)
+        return LOOM_ERR_SHAPE;
+    if (!d_counts && (count < 0 || count > rows))
+        return LOOM_ERR_RANGE;
+    loom_launch L;
+    loom_status st = stage_geometry(num_segments, rows, lanes, &L);
+    if (st != LOOM_OK)
+        return st;
+    if (num_segments == 0 || rows == 0)
+        return LOOM_OK;
+    if (!h_values || !d_values)
+        return LOOM_ERR_NULL;
+    if (misaligned(h_values, 4) || misaligned(d_values, 4) || misaligned(d_counts, 4))
+        return LOOM_ERR_ALIGN;
+    if (!device_readable(h_values) || (d_counts && !device_readable(d_counts)))
+        return LOOM_ERR_ARG;
+    StageParams p;
+    p.src = h_values;
+    p.dst = d_values;
+    p.num_units = num_segments;
+    p.unit_stride = seg_stride;
+    p.chunks_per_unit = stage_chunks_per_unit(rows, lanes);
+    p.rows = rows;
+    p.lanes = lanes;
+    p.counts = d_counts;
+    p.count_scalar = count;
+    p.vec4 = !misaligned(h_values, 16) && !misaligned(d_values, 16) && (seg_stride % 4 == 0 || num_segments == 1);
+    const cudaError_t e = launch_stage_rows(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    return LOOM_OK;
 }
 
 loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)

@@ -357,3 +357,18 @@ def test_routed_combine_launch_and_validation(loom):
     assert f(A, A, A, -4, 8, 100, 64, A, None) == loom.LOOM_ERR_SHAPE
     t = loom.make_tuning(path=loom.LOOM_PATH_STAGED)
     assert lib.loom_routed_combine_ex(A, A, A, 4, 40, 100, 64, A, None, ctypes.byref(t), None) == loom.LOOM_ERR_SHAPE
+
+
+def test_stage_rows_launch_and_validation(loom):
+    L = loom.loom_launch_config(loom.LOOM_OP_STAGE_ROWS, [65536, 63, 32])
+    assert L["kernel"] == loom.LOOM_KERNEL_STAGE_ROWS and L["grid"] == (65536, 1, 1) and L["block"] == (256, 1, 1)
+    L = loom.loom_launch_config(loom.LOOM_OP_STAGE_ROWS, [16384, 16384, 1])
+    assert L["grid"] == (16384 * 8, 1, 1)   # 8 KiB per CTA
+    lib = loom.library()
+    f = lib.loom_stage_rows
+    assert f(None, None, 0, 0, 63, 32, None, 0, None) == loom.LOOM_OK
+    assert f(None, A, 4, 2016, 63, 32, None, 3, None) == loom.LOOM_ERR_NULL
+    assert f(A + 2, A, 4, 2016, 63, 32, None, 3, None) == loom.LOOM_ERR_ALIGN
+    assert f(A, A, 4, 2016, 63, 32, None, 64, None) == loom.LOOM_ERR_RANGE
+    assert f(A, A, 4, 100, 63, 32, None, 3, None) == loom.LOOM_ERR_SHAPE
+    assert f(A, A, 4, 2016, 63, 0, None, 3, None) == loom.LOOM_ERR_SHAPE
