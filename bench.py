@@ -374,6 +374,7 @@ def run_ours(args, rank, world, dist):
     e2e = run_e2e(args, inp, total, torch, loom, stream, work)
     # the pages' other examples (packed dot, per-lane sums), each timed on its own (not part of the step)
     extras = measure_extras(args, torch, loom, stream, peak, peak_kind)
+    extras["read_ahead"] = read_ahead_study(torch, loom, stream, work, alg)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -503,6 +504,38 @@ def measure_extras(args, torch, loom, stream, peak, peak_kind):
         L = loom.loom_launch_config(loom.LOOM_OP_LANE_SUMS, [S, R, 32, W])
         out[name] = _extra_line(what, lane_alg_bytes(d), times, peak, peak_kind, traffic.get(name), L)
         del v, c, o, d
+    del flush
+    return out
+
+
+def read_ahead_study(torch, loom, stream, work, alg):
+    """The pages' own comparison: the serial control (read-ahead depth 1) against
+    the default depth, same kernels and workloads, alternated ABAB; single
+    launches after a 512 MB read, CUDA events.  Not part of the step."""
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros((), dtype=torch.int64, device="cuda")
+    serial = loom.make_tuning(depth=1)
+    out = {}
+    for name in ("segments", "wide", "gemv"):
+        times = {"depth1": [], "default": []}
+        for rep in range(6):
+            for label, tu in (("depth1", serial), ("default", None)):
+                saved = work.tuning
+                work.tuning = tu
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    sink.copy_(flush.view(torch.int32).sum())
+                    torch.cuda._sleep(200_000)
+                    a.record(stream)
+                    work.launch(name)
+                    b.record(stream)
+                stream.synchronize()
+                work.tuning = saved
+                if rep > 0:
+                    times[label].append(a.elapsed_time(b))
+        out[name] = {k: {"avg_ms": sum(v) / len(v), "GB/s": alg[name] / (sum(v) / len(v) * 1e-3) / 1e9}
+                     for k, v in times.items()}
     del flush
     return out
 

@@ -152,3 +152,20 @@ def test_guarded_full_workload_bitwise(env):
     d = synth.lane_segments(num_segments=16384, rows=63, lanes=32, width=4)
     got = run_guarded(loom, torch, d["values"], d["counts"], 4, 32)
     assert same_bits(got, oracle.guarded_rows(d["values"], d["counts"], 4, 32, threads=16))
+
+
+@pytest.mark.parametrize("width,path", [(1, 0), (4, 0), (1, 2), (4, 2)])
+def test_nan_past_the_active_rows_is_never_read(env, width, path):
+    torch, loom = env
+    d = synth.lane_segments(num_segments=500, rows=63, lanes=32, width=width, seed=91 + width)
+    v = d["values"].copy()
+    for s, c in enumerate(d["counts"]):
+        v[s, c:] = np.nan
+    t = loom.make_tuning(path=path)
+    got = run_rows(loom, torch, v, d["counts"], width, tuning=t)
+    assert np.isfinite(got).all()
+    assert same_bits(got, oracle.lane_sums(v, d["counts"], width=width))
+    if width == 4:   # the guarded rows also never read past the count
+        got = run_guarded(loom, torch, v, d["counts"], 4, 32, tuning=t)
+        assert np.isfinite(got).all()
+        assert same_bits(got, oracle.guarded_rows(v, d["counts"], 4, 32))

@@ -272,3 +272,29 @@ def test_wide_rows_full_workload(env):
                       to_dev(d["counts"], torch), None, 8)
     compare(got, want, "16384 x 16384")
     compare(got, want, "16384 x 16384, one rounding", rel=ULP_REL)
+
+
+@pytest.mark.parametrize("path", [0, 2])   # staged ring, plain loads
+def test_nan_past_the_active_rows_is_never_read(env, path):
+    # every value past a segment's count (or a wide row's length) is NaN: a
+    # stray read would turn its sum into NaN
+    torch, loom = env
+    d = _batched_case(2000, seed=0xACE)
+    v = d["values"].reshape(2000, 63, 32).copy()
+    for s, c in enumerate(d["counts"]):
+        v[s, c:] = np.nan
+    want = oracle.row_sum_batched(v, 2016, 63, 32, d["counts"], d["initial"], 8)
+    t = loom.make_tuning(path=path)
+    got = run_batched(loom, torch, to_dev(v, torch), 2000, 2016, 63, 32, to_dev(d["counts"], torch),
+                      to_dev(d["initial"], torch), 8, tuning=t)
+    assert np.isfinite(got[2]).all() and np.isfinite(got[3]).all()
+    compare(got, want, f"poisoned segments path {path}", rel=ULP_REL)
+    w = synth.wide_rows(n_rows=300, n_cols=5000, seed=0xACF)
+    vals = w["values"].copy()
+    for r, L in enumerate(w["counts"]):
+        vals[r, L:] = np.nan
+    want = oracle.row_sum_batched(vals, 5000, 5000, 1, w["counts"], None, 8)
+    got = run_batched(loom, torch, to_dev(vals, torch), 300, 5000, 5000, 1, to_dev(w["counts"], torch), None, 8,
+                      tuning=t)
+    assert np.isfinite(got[2]).all() and np.isfinite(got[3]).all()
+    compare(got, want, f"poisoned wide rows path {path}", rel=ULP_REL)
