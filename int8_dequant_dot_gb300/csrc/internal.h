@@ -152,17 +152,18 @@ struct RoutedParams {
     uint64_t wait_ns;
     int32_t inject_stall;
 };
-constexpr int RC_DEFAULT_DEPTH = 4;
+constexpr int RC_DEFAULT_DEPTH = 2;   // measured best: every CTA of the workload resident at once
 constexpr int RC_MAX_STAGED_ROUTES = 32;
 uint32_t routed_smem_bytes(bool staged, int depth, int warps);
 cudaError_t launch_routed(const RoutedParams &p, bool staged, const loom_launch &L, cudaStream_t stream);
 
 // ---- the pages' packed-dot example (packed_dot.cu) ---------------------------
-constexpr int PD_DEFAULT_DEPTH = 2;        // stages of the read-ahead ring
-constexpr int PD_DEFAULT_RPS = 8;          // records per stage
+constexpr int PD_DEFAULT_DEPTH = 2;        // stages of the read-ahead ring (measured best on GB300)
+constexpr int PD_DEFAULT_RPS = 12;         // records per stage: 48 KiB stages, two CTAs per SM
 constexpr int PD_MAX_RPS = 32;
 constexpr int PD_MAX_STAGED_STREAMS = 64;  // one TMA box row holds every stream of a record
-constexpr int PD_LANES_PER_CTA = 256;
+constexpr int PD_LANES_PER_CTA = 256;      // direct path
+constexpr int PD_STAGED_LANES_PER_CTA = 512;   // staged path: two lanes per consumer thread
 
 struct PackedParams {
     const int32_t *fields;     // [problems][records][lanes] packed signed bytes

@@ -612,7 +612,8 @@ loom_status packed_geometry(int64_t problems, int64_t records, int64_t lanes, in
     const uint32_t smem = packed_dot_smem_bytes(staged, (int)depth, (int)rps, (int)streams);
     if (smem > 227 * 1024)
         return LOOM_ERR_ARG;
-    fill_launch(out, ceil_div(lanes, PD_LANES_PER_CTA), packed_dot_threads(staged), smem, PD_LANES_PER_CTA,
+    const int64_t per = staged ? PD_STAGED_LANES_PER_CTA : PD_LANES_PER_CTA;
+    fill_launch(out, ceil_div(lanes, per), packed_dot_threads(staged), smem, (uint32_t)per,
                 staged ? LOOM_KERNEL_PACKED_STAGED : LOOM_KERNEL_PACKED_DIRECT);
     out->grid[1] = (uint32_t)problems;
     return LOOM_OK;

@@ -15,14 +15,21 @@
 //
 // GB300 design
 //  * Many independent instances per launch (the pages benchmark one instance
-//    per dispatch, many dispatches per measurement).  A CTA takes 256 lanes of
-//    one instance, one consumer thread per lane, and streams its records.
+//    per dispatch, many dispatches per measurement).  A staged CTA takes 512
+//    lanes of one instance, each of its 256 consumer threads two lanes 256
+//    apart (two independent recurrences; with 64 streams, or any count that
+//    divides 256, both lanes read the same activations).
 //  * Staged path: one producer thread fills a ring of `depth` stages, each
-//    `rps` records of the CTA's words (1 KiB per record), scales (512 B) and
+//    `rps` records of the CTA's words (2 KiB per record), scales (1 KiB) and
 //    the instance's whole activation row (16 B per stream), with three 3-D
-//    TMA copies completing on the stage's mbarrier (words and scales
-//    evict-first; activations, which every lane block of the instance reads,
-//    evict-last).  This is the read-ahead queue of the pages'
+//    TMA copies completing on the stage's mbarrier (words and scales counted
+//    as 64- and 32-bit pairs so that one 256-element box row holds 512 lanes;
+//    words and scales evict-first; activations, which every lane block of the
+//    instance reads, evict-last).  512 lanes per CTA halve the copies and the
+//    activation staging per byte against 256.  The hand-over of a stage
+//    costs more than a second wave of CTAs: measured best are two stages of
+//    12 records (two 98 KB CTAs per SM), against deeper rings of smaller
+//    stages that fit every CTA at once.  This is the read-ahead queue of the pages'
 //    pipeline(depth); depth 1 is the serial control and the depth never
 //    changes a result.  (Reading the activations through L1 instead left
 //    every CTA waiting on one load per record: measured 1.6x slower.)
@@ -44,7 +51,8 @@
 namespace loom {
 namespace {
 
-constexpr int PD_LANES = 256;                 // lanes (consumer threads) per CTA
+constexpr int PD_LANES = 256;                 // consumer threads per CTA (lanes per direct CTA)
+constexpr int PD_SLANES = 2 * PD_LANES;       // lanes per staged CTA: two per consumer thread
 constexpr int PD_CONSUMER_WARPS = PD_LANES / 32;
 constexpr int PD_THREADS_STAGED = PD_LANES + 32;   // + the producer warp
 
@@ -64,12 +72,12 @@ struct PackedDeviceParams {
     int32_t inject_stall;
 };
 
-// Shared-memory layout of one stage: fields [rps][256] i32, scales [rps][256]
+// Shared-memory layout of one stage: fields [rps][512] i32, scales [rps][512]
 // u16, activations [rps][streams][4] f32; each part 128-byte aligned.
 struct PdStage {
     uint32_t fields_bytes, scales_bytes, rhs_bytes;
     __host__ __device__ PdStage(int rps, int streams)
-        : fields_bytes((uint32_t)rps * PD_LANES * 4u), scales_bytes((uint32_t)rps * PD_LANES * 2u),
+        : fields_bytes((uint32_t)rps * PD_SLANES * 4u), scales_bytes((uint32_t)rps * PD_SLANES * 2u),
           rhs_bytes(((uint32_t)rps * (uint32_t)streams * 16u + 127u) & ~127u)
     {
     }
@@ -122,7 +130,7 @@ __device__ __forceinline__ int32_t instance_count(const PackedDeviceParams &p, i
 }
 
 // Staged path.  Block (blockIdx.x, blockIdx.y) = (lane block, instance).
-__global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel(
+__global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel(
     const __grid_constant__ CUtensorMap tm_fields, const __grid_constant__ CUtensorMap tm_scales,
     const __grid_constant__ CUtensorMap tm_rhs, const PackedDeviceParams p)
 {
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel
     const uint32_t base = (dev::smem_u32(smem_raw) + 127u) & ~127u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t inst = blockIdx.y;
-    const int32_t lane0 = blockIdx.x * PD_LANES;
+    const int32_t lane0 = blockIdx.x * PD_SLANES;
     const int D = p.depth, RPS = p.rps;
     const PdStage st(RPS, p.streams);
     const uint32_t bars = base + (uint32_t)D * st.bytes();
@@ -165,8 +173,8 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel
                 }
                 const int32_t r0 = i * RPS;
                 dev::mbar_arrive_expect_tx(full(s), tx);
-                tma_load_3d(stage(s), &tm_fields, lane0, r0, inst, full(s), once);
-                tma_load_3d(stage(s) + st.fields_bytes, &tm_scales, lane0, r0, inst, full(s), once);
+                tma_load_3d(stage(s), &tm_fields, lane0 / 2, r0, inst, full(s), once);   // lane pairs
+                tma_load_3d(stage(s) + st.fields_bytes, &tm_scales, lane0 / 2, r0, inst, full(s), once);
                 tma_load_3d(stage(s) + st.fields_bytes + st.scales_bytes, &tm_rhs, 0, r0, inst, full(s), shared);
                 ++issued;
             }
@@ -177,12 +185,14 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel
         return;
     }
 
-    // ---- consumers: thread t owns lane lane0 + t
+    // ---- consumers: thread t owns lanes lane0 + t and lane0 + 256 + t
     const int t = threadIdx.x;
-    const int32_t l = lane0 + t;
-    const bool live = l < p.lanes;
-    const int32_t sl = l % p.streams;
-    float sum = (live && p.initial) ? __ldg(p.initial + (int64_t)inst * p.lanes + l) : 0.f;
+    const int32_t la = lane0 + t, lb = la + PD_LANES;
+    const bool live_a = la < p.lanes, live_b = lb < p.lanes;
+    const int32_t sa = la % p.streams, sb = lb % p.streams;
+    const float *init = p.initial ? p.initial + (int64_t)inst * p.lanes : nullptr;
+    float sum_a = (live_a && init) ? __ldg(init + la) : 0.f;
+    float sum_b = (live_b && init) ? __ldg(init + lb) : 0.f;
     bool ok = true;
     for (int i = 0; i < nst; ++i) {
         const int s = i % D;
@@ -194,15 +204,22 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel
         const uint32_t f = stage(s), sc = f + st.fields_bytes, a = sc + st.scales_bytes;
         const int n_here = min(RPS, count - i * RPS);
         for (int k = 0; k < n_here; ++k) {
-            uint32_t word;
-            uint16_t sbits;
-            float4 v;
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(word) : "r"(f + (uint32_t)(k * PD_LANES + t) * 4u));
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sbits) : "r"(sc + (uint32_t)(k * PD_LANES + t) * 2u));
+            uint32_t wa, wb;
+            uint16_t ha, hb;
+            float4 va, vb;
+            const uint32_t row = (uint32_t)(k * PD_SLANES + t);
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(f + row * 4u));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(f + (row + PD_LANES) * 4u));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ha) : "r"(sc + row * 2u));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hb) : "r"(sc + (row + PD_LANES) * 2u));
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                         : "r"(a + (uint32_t)(k * p.streams + sl) * 16u));
-            sum = record_step(sum, word, sbits, v);
+                         : "=f"(va.x), "=f"(va.y), "=f"(va.z), "=f"(va.w)
+                         : "r"(a + (uint32_t)(k * p.streams + sa) * 16u));
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(vb.x), "=f"(vb.y), "=f"(vb.z), "=f"(vb.w)
+                         : "r"(a + (uint32_t)(k * p.streams + sb) * 16u));
+            sum_a = record_step(sum_a, wa, ha, va);
+            sum_b = record_step(sum_b, wb, hb, vb);
         }
         __syncwarp();
         if (lane == 0)
@@ -210,8 +227,11 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel
     }
     if (!ok)
         dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
-    if (live)
-        p.out[(int64_t)inst * p.lanes + l] = ok ? sum : __int_as_float(0x7fc00000);
+    const float nan = __int_as_float(0x7fc00000);
+    if (live_a)
+        p.out[(int64_t)inst * p.lanes + la] = ok ? sum_a : nan;
+    if (live_b)
+        p.out[(int64_t)inst * p.lanes + lb] = ok ? sum_b : nan;
 }
 
 // Direct path: plain loads, one thread per lane, records in order.
@@ -313,10 +333,11 @@ cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_lau
     if (!staged)
         return launch_with(packed_dot_direct_kernel, L, stream, p);
     CUtensorMap tf, ts, tr;
-    if (!encode_3d(&tf, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, q.fields, (uint64_t)q.lanes, (uint64_t)q.records,
-                   (uint64_t)q.problems, PD_LANES, (uint32_t)q.rps) ||
-        !encode_3d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, q.scales, (uint64_t)q.lanes, (uint64_t)q.records,
-                   (uint64_t)q.problems, PD_LANES, (uint32_t)q.rps) ||
+    // words as 64-bit and scales as 32-bit lane pairs: a box row of 256 pairs holds 512 lanes
+    if (!encode_3d(&tf, CU_TENSOR_MAP_DATA_TYPE_INT64, 8, q.fields, (uint64_t)q.lanes / 2, (uint64_t)q.records,
+                   (uint64_t)q.problems, PD_SLANES / 2, (uint32_t)q.rps) ||
+        !encode_3d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, q.scales, (uint64_t)q.lanes / 2, (uint64_t)q.records,
+                   (uint64_t)q.problems, PD_SLANES / 2, (uint32_t)q.rps) ||
         !encode_3d(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q.rhs, (uint64_t)q.streams * 4, (uint64_t)q.records,
                    (uint64_t)q.problems, (uint32_t)q.streams * 4, (uint32_t)q.rps))
         return cudaErrorInvalidValue;

@@ -262,15 +262,15 @@ def test_packed_dot_launch(loom):
     # 256 consumers + a producer warp) when lanes % 8 == 0 and streams <= 64.
     L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [128, 128, 2048, 64])
     assert L["kernel"] == loom.LOOM_KERNEL_PACKED_STAGED
-    assert L["grid"] == (8, 128, 1) and L["block"] == (288, 1, 1) and L["units_per_cta"] == 256
-    # default ring: 2 stages of 8 records x (1 KiB of words + 512 B of scales + 1 KiB of activations)
-    assert L["smem_bytes"] == 128 + 2 * 8 * (1024 + 512 + 64 * 16) + 16 * 2
+    assert L["grid"] == (4, 128, 1) and L["block"] == (288, 1, 1) and L["units_per_cta"] == 512
+    # default ring: 2 stages of 12 records x (2 KiB of words + 1 KiB of scales + 1 KiB of activations)
+    assert L["smem_bytes"] == 128 + 2 * 12 * (2048 + 1024 + 64 * 16) + 16 * 2
     for P, R, Ln, S in ((1, 128, 2048, 64), (3, 5, 1000, 7), (2, 0, 8, 1), (65535, 1, 1, 1)):
         for aligned in (0, 1):
             L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [P, R, Ln, S, aligned])
             staged = aligned == 1 and Ln % 8 == 0 and S <= 64
             assert L["kernel"] == (loom.LOOM_KERNEL_PACKED_STAGED if staged else loom.LOOM_KERNEL_PACKED_DIRECT)
-            assert L["grid"] == (oracle.workgroups(Ln, 256), P, 1)
+            assert L["grid"] == (oracle.workgroups(Ln, 512 if staged else 256), P, 1)
             assert L["block"][0] == (288 if staged else 256)
     L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [1, 128, 2048, 128])   # too many streams to stage
     assert L["kernel"] == loom.LOOM_KERNEL_PACKED_DIRECT and L["smem_bytes"] == 0
@@ -278,7 +278,7 @@ def test_packed_dot_launch(loom):
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, bad)
         assert e.value.status == loom.LOOM_ERR_SHAPE
-    for bad in ([1, 8, 8, 1, 1, 9], [1, 8, 8, 1, 1, 0, 33], [1, 8, 8, 64, 1, 8, 32]):   # depth, rps, smem
+    for bad in ([1, 8, 8, 1, 1, 9], [1, 8, 8, 1, 1, 0, 33], [1, 8, 8, 64, 1, 8, 16]):   # depth, rps, smem
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, bad)
         assert e.value.status == loom.LOOM_ERR_ARG
@@ -343,7 +343,7 @@ def test_lane_sum_validation(loom):
 def test_routed_combine_launch_and_validation(loom):
     L = loom.loom_launch_config(loom.LOOM_OP_ROUTED_COMBINE, [4096, 8, 32768, 2048])
     assert L["kernel"] == loom.LOOM_KERNEL_ROUTED_STAGED and L["block"] == (64, 1, 1)
-    assert L["grid"] == (2048, 1, 1) and L["smem_bytes"] == 2 * 4 * (2048 + 8)
+    assert L["grid"] == (2048, 1, 1) and L["smem_bytes"] == 2 * 2 * (2048 + 8)
     for T, R, W, aligned, staged in ((1, 8, 2048, 1, True), (7, 33, 64, 1, False), (7, 8, 62, 1, False),
                                      (7, 8, 64, 0, False), (0, 8, 64, 1, True)):
         L = loom.loom_launch_config(loom.LOOM_OP_ROUTED_COMBINE, [T, R, 100, W, aligned])
