@@ -1,5 +1,5 @@
 /*
- * loom.h -- C ABI of libloom, a GB300 (sm_103a) library for two streaming
+ * loom.h -- C ABI of libloom, a GB300 (sm_103a) library for the streaming
  * reductions described in the Loom documentation pages (ROCm hrx-system):
  *
  *   [P1] "Tune loop unrolling and pipelining"
@@ -10,12 +10,22 @@
  *     to a carried sum, and the partial final tile is summed separately
  *     ([P1] "Derive full tiles from a ragged loop");
  *  2. packed signed-byte dequantisation with dot accumulation
- *     ([P1] "Apply the same controls to a packed dot product").
+ *     ([P1] "Apply the same controls to a packed dot product");
+ *  3. the pages' other streaming examples: their own packed dot (f16 record
+ *     scales, f32 activations, an ordered f32 sum), per-lane column sums
+ *     (sum_rows, sum_vector_rows), guarded ragged rows and the routed row
+ *     combine -- each a fixed sequence of f32 operations, defined to the bit;
+ *  4. an upload of ragged row-sum inputs that moves only the active rows.
  *
  * Conventions for every entry point
  *  - Pointers prefixed d_ are device pointers owned by the caller; the library
- *    never allocates, frees or retains them and keeps no global mutable state,
- *    so calls may be made from several host threads.
+ *    never allocates, frees or retains them and keeps no global mutable state
+ *    (two exceptions, documented at their entry points: the fixed scratch of
+ *    loom_i8_dequant_dot_noalloc, and a process-wide cache of tensor maps and
+ *    device attributes), so calls may be made from several host threads.
+ *  - Every kernel is launched as a programmatic dependent of the previous
+ *    kernel on the stream and waits for it before touching memory: stream
+ *    order holds as for any launch.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously; the return value covers argument validation and
  *    the launch only.  Faults found on the device are reported through the
