@@ -124,6 +124,12 @@ __device__ __forceinline__ void flag_error(int32_t *word, int32_t bits)
         atomicOr(word, bits);
 }
 
+// The double word (hi, lo) rounded to f32.  Once the running sum has left the
+// finite range, hi alone carries the IEEE result (an infinity, or NaN for
+// opposite infinities or a NaN input) while lo, whose error terms subtract
+// infinities, is NaN: hi is returned then.
+__device__ __forceinline__ float dw_round(float hi, float lo) { return isfinite(hi) ? __fadd_rn(hi, lo) : hi; }
+
 // ---------------------------------------------------------------------------
 // Double-word f32 accumulator.  `hi + lo` carries the running sum; every
 // addition to `hi` is split exactly into a rounded sum and its rounding error
@@ -172,7 +178,7 @@ struct DW {
         lo = __fadd_rn(__fadd_rn(lo, l), e);
     }
 
-    __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
+    __device__ __forceinline__ float value() const { return dw_round(hi, lo); }
 };
 
 // ---------------------------------------------------------------------------

@@ -170,8 +170,8 @@ __device__ __forceinline__ void finish_group(const RowSumParams &p, int lane, in
         float h0, h1, l0, l1;
         dev::unpack2(k.hi, h0, h1);
         dev::unpack2(k.lo, l0, l1);
-        p.full_sum[ubase + j] = __fadd_rn(h0, l0);
-        p.tail_sum[ubase + j] = __fadd_rn(h1, l1);
+        p.full_sum[ubase + j] = dev::dw_round(h0, l0);
+        p.tail_sum[ubase + j] = dev::dw_round(h1, l1);
     }
 }
 

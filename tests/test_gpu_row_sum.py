@@ -298,3 +298,30 @@ def test_nan_past_the_active_rows_is_never_read(env, path):
                       tuning=t)
     assert np.isfinite(got[2]).all() and np.isfinite(got[3]).all()
     compare(got, want, f"poisoned wide rows path {path}", rel=ULP_REL)
+
+
+@pytest.mark.parametrize("path", [0, 2])
+def test_infinities_and_nan_follow_ieee(env, path):
+    # +inf, -inf, both, and NaN in the full-tile rows or in the tail rows:
+    # the sums are what IEEE addition gives (the oracle's double sums, rounded)
+    torch, loom = env
+    S = 64
+    d = _batched_case(S, seed=0xF00)
+    v = d["values"].reshape(S, 63, 32).copy()
+    c = np.full(S, 61, np.int32)                       # full-tile rows 0..55, tail rows 56..60
+    specials = [(1, 3, 5, np.inf), (2, 10, 0, -np.inf), (3, 4, 1, np.inf), (3, 50, 7, -np.inf),
+                (4, 20, 20, np.nan), (5, 58, 3, np.inf), (6, 57, 1, np.nan), (7, 62, 9, np.inf)]
+    for s, r, l, x in specials:                        # (row 62 of segment 7 is past its count)
+        v[s, r, l] = x
+    want = oracle.row_sum_batched(v, 2016, 63, 32, c, d["initial"], 8)
+    got = run_batched(loom, torch, to_dev(v, torch), S, 2016, 63, 32, to_dev(c, torch),
+                      to_dev(d["initial"], torch), 8, tuning=loom.make_tuning(path=path))
+    for g, w in ((got[2], want["full_sum"]), (got[3], want["tail_sum"])):
+        w32 = w.astype(np.float32)
+        assert np.array_equal(np.isnan(g), np.isnan(w32))
+        inf = np.isinf(w32)
+        assert np.array_equal(g[inf], w32[inf])
+        fin = np.isfinite(w32)
+        assert np.all(np.abs(g[fin] - w[fin]) <= ULP_REL * np.abs(w[fin]) + ULP_ATOL)
+    assert np.isinf(got[2][1]) and got[2][1] > 0 and np.isnan(got[2][3]) and np.isnan(got[2][4])
+    assert np.isinf(got[3][5]) and np.isnan(got[3][6]) and np.isfinite(got[2][7]) and np.isfinite(got[3][7])
