@@ -1,14 +1,18 @@
 """Benchmark of the streaming-reduction hot path on GB300.
 
-One step runs every kernel of the path once over its full synthetic workload,
-in this order (no kernel reads data the previous one could have left in the
-129 MB L2, since each input exceeds L2 and consecutive kernels read
-different arrays):
+One step runs every kernel of the path once over its full synthetic workload:
 
   gemv      packed-int8 dequant GEMV, W 8192 x 16384, one vector
   segments  ragged row sums of 65,536 segments of 63 x 32 f32
-  batched   packed-int8 dequant-dot, the same W against 16 vectors
+  batched   packed-int8 dequant-dot, its own W (same shape and values as the
+            GEMV's, a separate array) against 16 vectors
   wide      ragged row sums of a 16,384 x 16,384 f32 matrix
+
+The four workloads are independent, so a step runs them as two lanes (CUDA
+streams) that overlap: segments then batched on one, wide then gemv on the
+other; an event forks both lanes off the launching stream and the step ends
+when both have joined it again.  Each kernel reads its own arrays and every
+array exceeds the 129 MB L2, so no kernel finds another's data in L2.
 
 The metric is HBM GB/s over algorithmic bytes (only the bytes the method
 must move: active rows, metadata, outputs).  Prints ONE JSON line.
@@ -37,6 +41,10 @@ METRIC = "HBM GB/s and % of GB300 peak: ragged f32 row-sum, packed-int8 dequant-
 WORKLOAD = ("gemv 8192x16384 int8 + 65536 ragged 63x32 f32 segments + batched dot 8192x16384x16 "
             "int8 + 16384x16384 f32 ragged wide rows")
 ORDER = ("gemv", "segments", "batched", "wide")
+#: the step's concurrent lanes: each lane is a CUDA stream running its kernels in
+#: order; measured best of the two- and three-lane splits (segments is bound by
+#: instruction issue and leaves HBM time that the wide rows use)
+STEP_LANES = (("segments", "batched"), ("wide", "gemv"))
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -130,6 +138,7 @@ class DeviceWorkload:
             "wide_values": t(wide["values"]), "wide_counts": t(wide["counts"]),
             "w": t(gemv["w"].view("<i4")), "sw": t(gemv["scale_w"]),
             "x1": t(gemv["x"].view("<i4")), "sx1": t(gemv["scale_x"]),
+            "wb": t(bat["w"].view("<i4")), "swb": t(bat["scale_w"]),
             "x16": t(bat["x"].view("<i4")), "sx16": t(bat["scale_x"]),
         }
         i32, f32 = torch.int32, torch.float32
@@ -146,8 +155,9 @@ class DeviceWorkload:
         L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 16, 1, 0, 0, 0, 0, 1])
         self.launches_per_step = 3 + (2 if L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR_SPLIT else 1)
 
-    def launch(self, name):
-        L, d, o, s = self.loom, self.d, self.o, self.stream
+    def launch(self, name, stream=None):
+        L, d, o = self.loom, self.d, self.o
+        s = self.stream if stream is None else stream
         if name == "segments":
             L.loom_row_sum_batched_ex(d["seg_values"], 65536, 2016, 63, 32, d["seg_counts"], d["seg_init"],
                                       8, out=o["seg"], tuning=self.tuning, stream=s)
@@ -158,10 +168,31 @@ class DeviceWorkload:
             L.loom_i8_dequant_dot_ex(d["w"], d["sw"], 8192, 16384, d["x1"], d["sx1"], 1, y=o["y1"],
                                      tuning=self.tuning, stream=s)
         elif name == "batched":
-            L.loom_i8_dequant_dot_ex(d["w"], d["sw"], 8192, 16384, d["x16"], d["sx16"], 16, y=o["y16"],
+            L.loom_i8_dequant_dot_ex(d["wb"], d["swb"], 8192, 16384, d["x16"], d["sx16"], 16, y=o["y16"],
                                      tuning=self.tuning, stream=s)
         else:
             raise ValueError(name)
+
+
+class Step:
+    """One step: the lanes of STEP_LANES forked off the launching stream by an
+    event, each on a stream of its own, and joined back by one event per lane."""
+
+    def __init__(self, torch, work, lanes=STEP_LANES):
+        self.work, self.lanes = work, lanes
+        self.streams = [torch.cuda.Stream() for _ in lanes]
+        self.fork = torch.cuda.Event()
+        self.joins = [torch.cuda.Event() for _ in lanes]
+
+    def run(self, main):
+        self.fork.record(main)
+        for lane, s, j in zip(self.lanes, self.streams, self.joins):
+            s.wait_event(self.fork)
+            for name in lane:
+                self.work.launch(name, stream=s)
+            j.record(s)
+        for j in self.joins:
+            main.wait_event(j)
 
 
 # ----------------------------------------------------------------------------
@@ -304,6 +335,7 @@ def run_ours(args, rank, world, dist):
     alg = algorithmic_bytes(inp)
     total = sum(alg.values())
     work = DeviceWorkload(inp, torch, loom, stream, depth=args.depth)
+    step = Step(torch, work)
 
     def barrier():
         if dist is not None:
@@ -312,14 +344,13 @@ def run_ours(args, rank, world, dist):
     # warm-up
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            for name in ORDER:
-                work.launch(name)
+            step.run(stream)
     stream.synchronize()
 
     # timed region: K whole steps between two events on the launching stream.
-    # Nothing is recorded between the kernels: an event between two launches
-    # costs about 2 us of the step and stops the next kernel from being
-    # scheduled while the previous one drains (programmatic dependent launch).
+    # Within a lane nothing is recorded between the kernels: an event between two
+    # launches costs about 2 us and stops the next kernel from being scheduled
+    # while the previous one drains (programmatic dependent launch).
     step_start = torch.cuda.Event(enable_timing=True)
     step_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -333,15 +364,15 @@ def run_ours(args, rank, world, dist):
         torch.cuda._sleep(2_000_000)
         step_start.record(stream)
         for _ in range(args.steps):
-            for name in ORDER:
-                work.launch(name)
+            step.run(stream)
         step_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     barrier()
 
-    # per-kernel durations for the roofline: the same K steps again, each launch
-    # between two events of its own (so each kernel runs alone, as ncu sees it)
+    # per-kernel durations for the roofline: the same K steps again, the kernels
+    # one after another on one stream, each launch between two events of its own
+    # (so each kernel runs alone, as ncu sees it)
     ev = {name: [] for name in ORDER}
     with torch.cuda.stream(stream):
         torch.cuda._sleep(2_000_000)
@@ -393,9 +424,12 @@ def run_ours(args, rank, world, dist):
                    "l2": "inputs larger than L2 (each >= 134 MB vs 129 MB); consecutive kernels read "
                          "different arrays", "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
                    "depth": args.depth or "default",
-                   "timing": "value: K steps between two events, no event between kernels (each kernel "
-                             "may be scheduled while the previous drains); kernels: the same K steps again "
-                             "with an event pair around every launch"},
+                   "step_lanes": [list(lane) for lane in STEP_LANES],
+                   "timing": "value: K steps between two events; each step forks two lanes (CUDA streams: "
+                             "segments then batched, wide then gemv) off the launching stream and joins them; "
+                             "no event between the kernels of a lane (each may be scheduled while the previous "
+                             "drains); kernels: the same K steps again, serially on one stream, with an event "
+                             "pair around every launch"},
         "roofline": roofline,
         "kernels": kernels,
         "e2e": e2e,
@@ -560,7 +594,8 @@ def run_e2e(args, inp, total, torch, loom, stream, work):
     for key, arr in (("seg_counts", inp["segments"]["counts"]), ("seg_init", inp["segments"]["initial"]),
                      ("wide_counts", inp["wide"]["counts"]), ("w", inp["gemv"]["w"].view("<i4")),
                      ("sw", inp["gemv"]["scale_w"]), ("x1", inp["gemv"]["x"].view("<i4")),
-                     ("sx1", inp["gemv"]["scale_x"]), ("x16", inp["batched"]["x"].view("<i4")),
+                     ("sx1", inp["gemv"]["scale_x"]), ("wb", inp["batched"]["w"].view("<i4")),
+                     ("swb", inp["batched"]["scale_w"]), ("x16", inp["batched"]["x"].view("<i4")),
                      ("sx16", inp["batched"]["scale_x"])):
         dense[key] = torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
     seg, wide = inp["segments"], inp["wide"]
@@ -573,6 +608,7 @@ def run_e2e(args, inp, total, torch, loom, stream, work):
     d2h = sum(t.numel() * t.element_size() for grp in host_out for t in grp)
     steps = max(1, min(args.steps, 5))
     d = work.d
+    step = Step(torch, work)
 
     def one_step():
         for key, t in dense.items():
@@ -581,8 +617,7 @@ def run_e2e(args, inp, total, torch, loom, stream, work):
                              seg["lanes"], d["seg_counts"], stream=stream)
         loom.loom_stage_rows(h_wide, d["wide_values"], wide["num_segments"], wide["seg_stride"], wide["rows"],
                              wide["lanes"], d["wide_counts"], stream=stream)
-        for name in ORDER:
-            work.launch(name)
+        step.run(stream)
         for grp_h, grp_d in zip(host_out, outs):
             for h, dv in zip(grp_h, grp_d):
                 h.copy_(dv, non_blocking=True)
