@@ -200,9 +200,13 @@ class Step:
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of SM clock and throttle reasons every 20 ms; each
+    sample carries nvidia-smi's own timestamp, so that only the samples taken
+    inside the timed region are reported."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index: int):
         self.proc = None
@@ -212,12 +216,32 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def parse(out: str):
+        """(wall-clock seconds, sm MHz, max MHz, set of active reasons) per sample line."""
+        import datetime
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = {nm for nm, v in zip(ClockSampler.NAMES, parts[5:9]) if v.lower() == "active"}
+            rows.append((t, sm, mx, reasons))
+        return rows
+
+    def stop(self, window=None):
+        """Summary of the samples inside `window` (wall-clock start, end); when no
+        sample falls inside it, of all samples, marked as such."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -226,24 +250,22 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+        return self.summarise(self.parse(out), window)
+
+    @staticmethod
+    def summarise(rows, window=None):
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if window and window[0] <= r[0] <= window[1]]
+        use = inside or rows
+        reasons = set()
+        for r in use:
+            reasons |= r[3]
+        out = {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+               "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(inside)}
+        if window:
+            out["timed_region_ms"] = round((window[1] - window[0]) * 1e3, 1)
+        return out
 
 
 # ----------------------------------------------------------------------------
@@ -358,6 +380,7 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)   # let the sampler attach before the timed work
+    t_region = time.time()
     with torch.cuda.stream(stream):
         # keep the device busy for ~1 ms while the host queues the first steps, so
         # that the events below never time host-side launch work on an idle device
@@ -367,6 +390,7 @@ def run_ours(args, rank, world, dist):
             step.run(stream)
         step_end.record(stream)
     stream.synchronize()
+    region = (t_region, time.time())
     torch.cuda.synchronize()
     barrier()
 
@@ -385,7 +409,7 @@ def run_ours(args, rank, world, dist):
                 b.record(stream)
                 ev[name].append((a, b))
     stream.synchronize()
-    clk = clocks.stop()
+    clk = clocks.stop(region)
     elapsed_ms = slowest_rank_ms(step_start.elapsed_time(step_end), dist, "cuda")
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_gbs(world, total, ms_per_step)
@@ -479,7 +503,7 @@ def _time_single(args, torch, stream, call, flush, sink):
             call()
     stream.synchronize()
     times = []
-    for _ in range(max(args.steps, 5)):
+    for _ in range(min(max(args.steps, 5), 200)):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -724,7 +748,7 @@ class _SingleWorkload:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)   # ~0.35 s timed: 16+ clock samples inside it
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--depth", type=int, default=0, help="read-ahead depth (0 = library default)")
