@@ -293,6 +293,12 @@ __device__ __forceinline__ DW2 warp_allreduce4(const DW2 &a, const DW2 &b, const
     return k;
 }
 
+// ceil(a / b) for 0 <= a <= INT32_MAX and b >= 1, with no overflow near INT32_MAX.
+__host__ __device__ __forceinline__ int32_t ceil_div_i32(int32_t a, int32_t b)
+{
+    return a / b + (a % b != 0);
+}
+
 __device__ __forceinline__ int32_t warp_sum_i32(int32_t v)
 {
 #pragma unroll

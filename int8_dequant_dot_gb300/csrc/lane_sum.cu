@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256) lane_sum_staged_kernel(const LaneSumParam
         if (c != raw)
             dev::flag_error(p.error, LOOM_DEVERR_COUNT_RANGE);
     }
-    const int32_t nchunks = (c + p.chunk_rows - 1) / p.chunk_rows;
+    const int32_t nchunks = dev::ceil_div_i32(c, p.chunk_rows);
 
     if (lane == 0) {
         for (int s = 0; s < D; ++s)

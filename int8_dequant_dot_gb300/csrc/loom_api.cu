@@ -329,8 +329,8 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
             return st;
     }
     const bool split = workspace != nullptr;
-    for (int32_t b0 = 0; b0 < batch; b0 += DOT_MAX_BATCH_PER_PASS) {
-        const int32_t nb = (batch - b0) < DOT_MAX_BATCH_PER_PASS ? (batch - b0) : DOT_MAX_BATCH_PER_PASS;
+    for (int64_t b0 = 0; b0 < batch; b0 += DOT_MAX_BATCH_PER_PASS) {
+        const int32_t nb = (int32_t)((batch - b0) < DOT_MAX_BATCH_PER_PASS ? (batch - b0) : DOT_MAX_BATCH_PER_PASS);
         loom_launch L;
         DotTcPlan plan;
         st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, engine, t.tc, split,

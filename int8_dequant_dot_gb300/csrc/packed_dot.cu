@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel
     }
     __syncthreads();
     const int32_t count = instance_count(p, inst);
-    const int nst = (count + RPS - 1) / RPS;
+    const int nst = dev::ceil_div_i32(count, RPS);
 
     if (warp == PD_CONSUMER_WARPS) {
         // ---- producer: three 3-D copies per stage (words, scales, activations)

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(256) routed_staged_kernel(const RoutedParams p
     }
     const uint32_t valid = __ballot_sync(FULL_MASK, id >= 0);
     const int nv = __popc(valid);
-    const int nb = (p.width + RC_BLOCK - 1) / RC_BLOCK;
+    const int nb = dev::ceil_div_i32(p.width, RC_BLOCK);
     const int total = nb * nv;   // pieces: block-major, valid routes in order
 
     if (lane == 0) {
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(256) routed_direct_kernel(const RoutedParams p
     if (t >= p.tokens)
         return;
     float *out_row = p.out + t * p.width;
-    for (int32_t c = lane; c < p.width; c += 32)
+    for (int64_t c = lane; c < p.width; c += 32)
         out_row[c] = 0.f;
     for (int r = 0; r < p.routes; ++r) {
         const int32_t id = route_id(p, t, r);
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256) routed_direct_kernel(const RoutedParams p
             continue;   // a missing route: no weight, no payload
         const float w = __ldg(p.weights + t * p.routes + r);
         const float *row = p.payload + (int64_t)id * p.width;
-        for (int32_t c = lane; c < p.width; c += 32)
+        for (int64_t c = lane; c < p.width; c += 32)
             out_row[c] = weighted_add(out_row[c], w, __ldg(row + c));
     }
 }

@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256, MINB) row_sum_kernel(const RowSumParams p
     const int32_t n_active = c * p.lanes;     // active elements
     const int32_t split = F * p.lanes;        // first tail element
     const int32_t nbulk = n_active & ~3;      // elements moved as 16-byte blocks
-    const int32_t nchunks = (nbulk + CH - 1) / CH;
+    const int32_t nchunks = dev::ceil_div_i32(nbulk, CH);
 
     const int D = p.depth;
     float *ring = reinterpret_cast<float *>(smem) + (size_t)warp * D * CH;
