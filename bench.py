@@ -637,60 +637,90 @@ def read_ahead_study(torch, loom, stream, work, alg):
     return out
 
 
-def run_e2e(args, inp, total, torch, loom, stream, work):
-    """Same metric through the binding with host buffers.  Every step moves its
-    inputs from pinned host memory to the device -- the dense ones (weights,
+#: the inputs and outputs of each workload on the end-to-end path
+E2E_INPUTS = {"segments": ("seg_counts", "seg_init"), "wide": ("wide_counts",),
+              "gemv": ("w", "sw", "x1", "sx1"), "batched": ("wb", "swb", "x16", "sx16")}
+E2E_OUTPUTS = {"segments": "seg", "wide": "wide", "gemv": "y1", "batched": "y16"}
+
+
+class E2EStep:
+    """One end-to-end step through the binding with host buffers.  The step moves
+    its inputs from pinned host memory to the device -- the dense ones (weights,
     vectors, scales, counts, initial sums) with copies, the two ragged f32 arrays
-    with loom_stage_rows, which moves only the rows the row sums read -- runs
-    the four kernels and reads the results back; all of it inside the timed
-    region."""
-    dense = {}
-    for key, arr in (("seg_counts", inp["segments"]["counts"]), ("seg_init", inp["segments"]["initial"]),
-                     ("wide_counts", inp["wide"]["counts"]), ("w", inp["gemv"]["w"].view("<i4")),
-                     ("sw", inp["gemv"]["scale_w"]), ("x1", inp["gemv"]["x"].view("<i4")),
-                     ("sx1", inp["gemv"]["scale_x"]), ("wb", inp["batched"]["w"].view("<i4")),
-                     ("swb", inp["batched"]["scale_w"]), ("x16", inp["batched"]["x"].view("<i4")),
-                     ("sx16", inp["batched"]["scale_x"])):
-        dense[key] = torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
-    seg, wide = inp["segments"], inp["wide"]
-    h_seg = torch.from_numpy(np.ascontiguousarray(seg["values"]).reshape(-1)).pin_memory()
-    h_wide = torch.from_numpy(np.ascontiguousarray(wide["values"]).reshape(-1)).pin_memory()
-    outs = [work.o["seg"], work.o["wide"], (work.o["y1"],), (work.o["y16"],)]
-    host_out = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in grp) for grp in outs]
-    staged = 4 * (int(seg["counts"].astype(np.int64).sum()) * seg["lanes"] + int(wide["counts"].astype(np.int64).sum()))
-    h2d = sum(t.numel() * t.element_size() for t in dense.values()) + staged
-    d2h = sum(t.numel() * t.element_size() for grp in host_out for t in grp)
+    with loom_stage_rows, which moves only the rows the row sums read -- runs the
+    four kernels and reads the results back into pinned host buffers.  Each lane
+    of the step (STEP_LANES) uploads, runs and reads back its own workloads in
+    order, so one lane's kernels overlap the other's uploads."""
+
+    def __init__(self, inp, torch, loom, work):
+        self.loom, self.work = loom, work
+        self.dense = {}
+        for key, arr in (("seg_counts", inp["segments"]["counts"]), ("seg_init", inp["segments"]["initial"]),
+                         ("wide_counts", inp["wide"]["counts"]), ("w", inp["gemv"]["w"].view("<i4")),
+                         ("sw", inp["gemv"]["scale_w"]), ("x1", inp["gemv"]["x"].view("<i4")),
+                         ("sx1", inp["gemv"]["scale_x"]), ("wb", inp["batched"]["w"].view("<i4")),
+                         ("swb", inp["batched"]["scale_w"]), ("x16", inp["batched"]["x"].view("<i4")),
+                         ("sx16", inp["batched"]["scale_x"])):
+            self.dense[key] = torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
+        seg, wide = inp["segments"], inp["wide"]
+        self.ragged = {
+            "segments": (torch.from_numpy(np.ascontiguousarray(seg["values"]).reshape(-1)).pin_memory(),
+                         "seg_values", "seg_counts", seg),
+            "wide": (torch.from_numpy(np.ascontiguousarray(wide["values"]).reshape(-1)).pin_memory(),
+                     "wide_values", "wide_counts", wide)}
+        self.outs = {"seg": work.o["seg"], "wide": work.o["wide"], "y1": (work.o["y1"],), "y16": (work.o["y16"],)}
+        self.host_out = {k: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in grp)
+                         for k, grp in self.outs.items()}
+        staged = 4 * (int(seg["counts"].astype(np.int64).sum()) * seg["lanes"] +
+                      int(wide["counts"].astype(np.int64).sum()))
+        self.h2d = sum(t.numel() * t.element_size() for t in self.dense.values()) + staged
+        self.d2h = sum(t.numel() * t.element_size() for grp in self.host_out.values() for t in grp)
+        self.torch = torch
+        self.streams = [torch.cuda.Stream() for _ in STEP_LANES]
+        self.fork = torch.cuda.Event()
+        self.joins = [torch.cuda.Event() for _ in STEP_LANES]
+
+    def run(self, main):
+        torch, d = self.torch, self.work.d
+        self.fork.record(main)
+        for lane, s, j in zip(STEP_LANES, self.streams, self.joins):
+            s.wait_event(self.fork)
+            with torch.cuda.stream(s):
+                for name in lane:
+                    for key in E2E_INPUTS[name]:
+                        d[key].copy_(self.dense[key], non_blocking=True)
+                    if name in self.ragged:
+                        h, dv, dc, g = self.ragged[name]
+                        self.loom.loom_stage_rows(h, d[dv], g["num_segments"], g["seg_stride"], g["rows"],
+                                                  g["lanes"], d[dc], stream=s)
+                    self.work.launch(name, stream=s)
+                    key = E2E_OUTPUTS[name]
+                    for hb, db in zip(self.host_out[key], self.outs[key]):
+                        hb.copy_(db, non_blocking=True)
+            j.record(s)
+        for j in self.joins:
+            main.wait_event(j)
+
+
+def run_e2e(args, inp, total, torch, loom, stream, work):
+    """The metric end to end (E2EStep), every step inside the timed region."""
+    e2e = E2EStep(inp, torch, loom, work)
     steps = max(1, min(args.steps, 5))
-    d = work.d
-    step = Step(torch, work)
-
-    def one_step():
-        for key, t in dense.items():
-            d[key].copy_(t, non_blocking=True)
-        loom.loom_stage_rows(h_seg, d["seg_values"], seg["num_segments"], seg["seg_stride"], seg["rows"],
-                             seg["lanes"], d["seg_counts"], stream=stream)
-        loom.loom_stage_rows(h_wide, d["wide_values"], wide["num_segments"], wide["seg_stride"], wide["rows"],
-                             wide["lanes"], d["wide_counts"], stream=stream)
-        step.run(stream)
-        for grp_h, grp_d in zip(host_out, outs):
-            for h, dv in zip(grp_h, grp_d):
-                h.copy_(dv, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        one_step()
+    e2e.run(stream)
     stream.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         a.record(stream)
         for _ in range(steps):
-            one_step()
+            e2e.run(stream)
         b.record(stream)
     stream.synchronize()
     ms = a.elapsed_time(b) / steps
-    return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
-            "h2d": "dense inputs by copy; the ragged f32 arrays by loom_stage_rows (active rows only)"}
+    return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": e2e.h2d,
+            "d2h_bytes_per_step": e2e.d2h, "ms_per_step": ms, "steps": steps,
+            "h2d": "dense inputs by copy; the ragged f32 arrays by loom_stage_rows (active rows only); "
+                   "each lane of the step uploads, runs and reads back its own workloads"}
 
 
 def run_profile(args):

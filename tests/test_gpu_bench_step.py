@@ -1,7 +1,8 @@
 """The benchmark's step at full size: the four workloads run as two concurrent
 lanes (CUDA streams forked and joined by events) return the same bits as the
 same kernels run one at a time on one stream, step after step, and sampled
-outputs agree with the oracle."""
+outputs agree with the oracle.  The end-to-end step (uploads from pinned host
+memory, the kernels, read-back, per lane) returns the same bits to the host."""
 import numpy as np
 import pytest
 
@@ -23,6 +24,7 @@ def poison(work, torch):
     o = work.o
     for t in list(o["seg"]) + list(o["wide"]) + [o["y1"], o["y16"]]:
         t.fill_(-1 if not t.dtype.is_floating_point else float("nan"))
+    torch.cuda.synchronize()   # the fills run on torch's current stream, the step on its own
 
 
 def same_bits(a, b):
@@ -74,3 +76,16 @@ def test_two_lane_step_matches_serial_kernels_and_oracle():
     g = inp["gemv"]
     acc, y = oracle.i8_dequant_dot(g["w"], g["scale_w"], g["x"], g["scale_x"], rows=rows)
     assert_rel(serial[8][rows], y, Y_REL, "gemv y")
+
+    # end to end: with every device input poisoned first, one step must upload the
+    # inputs (the ragged arrays' active rows only), run and read back the same bits
+    for t in work.d.values():
+        t.fill_(float("nan") if t.dtype.is_floating_point else -1)
+    poison(work, torch)   # (synchronises the fills above too)
+    e2e = bench.E2EStep(inp, torch, loom, work)
+    with torch.cuda.stream(s):
+        e2e.run(s)
+    s.synchronize()
+    host = [t.numpy() for k in ("seg", "wide", "y1", "y16") for t in e2e.host_out[k]]
+    for i, (a, b) in enumerate(zip(host, serial)):
+        assert same_bits(a, b), ("e2e", i)
