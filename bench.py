@@ -45,6 +45,8 @@ ORDER = ("gemv", "segments", "batched", "wide")
 #: order; measured best of the two- and three-lane splits (segments is bound by
 #: instruction issue and leaves HBM time that the wide rows use)
 STEP_LANES = (("segments", "batched"), ("wide", "gemv"))
+#: the same step on one stream (`--lanes 1`), for comparison
+ONE_LANE = (ORDER,)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -184,7 +186,7 @@ class DeviceWorkload:
 
 
 class Step:
-    """One step: the lanes of STEP_LANES forked off the launching stream by an
+    """One step: the lanes (STEP_LANES by default) forked off the launching stream by an
     event, each on a stream of its own, and joined back by one event per lane."""
 
     def __init__(self, torch, work, lanes=STEP_LANES):
@@ -387,7 +389,8 @@ def run_ours(args, rank, world, dist):
     alg = algorithmic_bytes(inp)
     total = sum(alg.values())
     work = DeviceWorkload(inp, torch, loom, stream, depth=args.depth)
-    step = Step(torch, work)
+    lanes = STEP_LANES if args.lanes == 2 else ONE_LANE
+    step = Step(torch, work, lanes)
 
     def barrier():
         if dist is not None:
@@ -478,12 +481,11 @@ def run_ours(args, rank, world, dist):
                    "l2": "inputs larger than L2 (each >= 134 MB vs 129 MB); consecutive kernels read "
                          "different arrays", "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
                    "depth": args.depth or "default",
-                   "step_lanes": [list(lane) for lane in STEP_LANES],
-                   "timing": "value: K steps between two events; each step forks two lanes (CUDA streams: "
-                             "segments then batched, wide then gemv) off the launching stream and joins them; "
-                             "no event between the kernels of a lane (each may be scheduled while the previous "
-                             "drains); kernels: the same K steps again, serially on one stream, with an event "
-                             "pair around every launch"},
+                   "step_lanes": [list(lane) for lane in lanes],
+                   "timing": "value: K steps between two events; each step forks its lanes (CUDA streams, "
+                             "step_lanes) off the launching stream and joins them; no event between the "
+                             "kernels of a lane (each may be scheduled while the previous drains); kernels: the "
+                             "same K steps again, serially on one stream, with an event pair around every launch"},
         "roofline": roofline,
         "kernels": kernels,
         "e2e": e2e,
@@ -649,11 +651,11 @@ class E2EStep:
     vectors, scales, counts, initial sums) with copies, the two ragged f32 arrays
     with loom_stage_rows, which moves only the rows the row sums read -- runs the
     four kernels and reads the results back into pinned host buffers.  Each lane
-    of the step (STEP_LANES) uploads, runs and reads back its own workloads in
+    of the step uploads, runs and reads back its own workloads in
     order, so one lane's kernels overlap the other's uploads."""
 
-    def __init__(self, inp, torch, loom, work):
-        self.loom, self.work = loom, work
+    def __init__(self, inp, torch, loom, work, lanes=STEP_LANES):
+        self.loom, self.work, self.lanes = loom, work, lanes
         self.dense = {}
         for key, arr in (("seg_counts", inp["segments"]["counts"]), ("seg_init", inp["segments"]["initial"]),
                          ("wide_counts", inp["wide"]["counts"]), ("w", inp["gemv"]["w"].view("<i4")),
@@ -676,14 +678,14 @@ class E2EStep:
         self.h2d = sum(t.numel() * t.element_size() for t in self.dense.values()) + staged
         self.d2h = sum(t.numel() * t.element_size() for grp in self.host_out.values() for t in grp)
         self.torch = torch
-        self.streams = [torch.cuda.Stream() for _ in STEP_LANES]
+        self.streams = [torch.cuda.Stream() for _ in lanes]
         self.fork = torch.cuda.Event()
-        self.joins = [torch.cuda.Event() for _ in STEP_LANES]
+        self.joins = [torch.cuda.Event() for _ in lanes]
 
     def run(self, main):
         torch, d = self.torch, self.work.d
         self.fork.record(main)
-        for lane, s, j in zip(STEP_LANES, self.streams, self.joins):
+        for lane, s, j in zip(self.lanes, self.streams, self.joins):
             s.wait_event(self.fork)
             with torch.cuda.stream(s):
                 for name in lane:
@@ -704,7 +706,7 @@ class E2EStep:
 
 def run_e2e(args, inp, total, torch, loom, stream, work):
     """The metric end to end (E2EStep), every step inside the timed region."""
-    e2e = E2EStep(inp, torch, loom, work)
+    e2e = E2EStep(inp, torch, loom, work, STEP_LANES if args.lanes == 2 else ONE_LANE)
     steps = max(1, min(args.steps, 5))
     e2e.run(stream)
     stream.synchronize()
@@ -815,6 +817,8 @@ def main():
     ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows", "routed"),
                     default=None)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--lanes", type=int, choices=(1, 2), default=2,
+                    help="2: the step's two concurrent stream lanes; 1: every kernel on one stream")
     args = ap.parse_args()
     if args.warmup < 3 and args.profile is None:
         ap.error("--warmup must be at least 3")
