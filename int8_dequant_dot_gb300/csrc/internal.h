@@ -12,7 +12,7 @@ namespace loom {
 
 // ---- row sum -------------------------------------------------------------
 constexpr int RS_DEFAULT_WARPS = 1;    // warps per CTA (a CTA's slot frees when its warp ends)
-constexpr int RS_DEFAULT_WARPS_WIDE = 2;  // lanes = 1 (wide rows)
+constexpr int RS_DEFAULT_WARPS_WIDE = 1;  // lanes = 1 (wide rows): a CTA slot frees when its row ends
 constexpr int RS_DEFAULT_CHUNK_ELEMS = 1024;       // one staged chunk: 4 KiB of f32 ...
 constexpr int RS_DEFAULT_CHUNK_ELEMS_LONG = 2048;  // ... 8 KiB for units above 4096 elements
 constexpr int RS_SLOT_ELEMS = 128;      // one warp-wide read: 32 lanes x float4
