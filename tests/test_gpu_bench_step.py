@@ -59,6 +59,16 @@ def test_two_lane_step_matches_serial_kernels_and_oracle():
         for i, (a, b) in enumerate(zip(outputs(work), serial)):
             assert same_bits(a, b), (rep, i)
 
+    # the one-stream schedule (bench.py --lanes 1) through the same Step
+    one = bench.Step(torch, work, bench.ONE_LANE)
+    poison(work, torch)
+    with torch.cuda.stream(s):
+        one.run(s)
+        one.run(s)
+    s.synchronize()
+    for i, (a, b) in enumerate(zip(outputs(work), serial)):
+        assert same_bits(a, b), ("one lane", i)
+
     # sampled outputs against the oracle
     rng = np.random.default_rng(12)
     seg = inp["segments"]
