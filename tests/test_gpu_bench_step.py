@@ -59,6 +59,17 @@ def test_two_lane_step_matches_serial_kernels_and_oracle():
         for i, (a, b) in enumerate(zip(outputs(work), serial)):
             assert same_bits(a, b), (rep, i)
 
+    # the two-lane step captured as a CUDA graph (fork and join become graph edges)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step.run(s)
+    poison(work, torch)
+    g.replay()
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(outputs(work), serial)):
+        assert same_bits(a, b), ("graph", i)
+    del g
+
     # the one-stream schedule (bench.py --lanes 1) through the same Step
     one = bench.Step(torch, work, bench.ONE_LANE)
     poison(work, torch)
