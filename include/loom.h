@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define LOOM_ABI_VERSION 3
+#define LOOM_ABI_VERSION 4
 
 typedef enum loom_status {
     LOOM_OK = 0,
@@ -206,7 +206,9 @@ loom_status loom_i8_dequant_dot(const int32_t *d_w_packed, const float *d_scale_
  * of W between CTAs that are not in one cluster, on the current device (0
  * when the tensor-core kernel is not taken: batch < 3, k < 16 or k % 16 !=
  * 0).  It is the most any schedule uses; with few bands the call gives each
- * band a cluster of CTAs and uses none of it.  With many bands, splitting
+ * band a cluster of CTAs and uses none of it.  The size grows with the CTAs
+ * of the launch, at most one per SM, so the query for the largest problem
+ * (n_rows = INT32_MAX) gives a workspace that serves every call on the device.  With many bands, splitting
  * spreads the weights evenly over the SMs; without a workspace each CTA then
  * takes whole bands.
  * The workspace (d_workspace, caller-owned device memory, 256-byte aligned,
@@ -227,8 +229,11 @@ loom_status loom_i8_dequant_dot_workspace_bytes(int32_t n_rows, int32_t k, int32
  * allocation.  The Loom pages have no counterpart of this entry point: it is
  * a deployment variant of the call above.  The bands of W are split between
  * CTAs through scratch that the library holds in a fixed device array (8 MiB
- * on each device, its address looked up once per device); results are the
- * same bits as loom_i8_dequant_dot.  The scratch is
+ * on each device that loads the library, held until the process exits);
+ * results are the same bits as loom_i8_dequant_dot.  The first call on a
+ * device (and again after its context has been re-created) looks up the
+ * array's device address with cudaGetSymbolAddress, which may load the
+ * module: make that first call before any stream capture.  The scratch is
  * shared by every call on a device, so calls that may run at the same time
  * (other streams, other host threads) must be serialised by the caller.
  * Errors: as loom_i8_dequant_dot; a problem whose split workspace would not

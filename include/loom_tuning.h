@@ -4,7 +4,8 @@
  * The _ex entry points take the same arguments as their plain counterparts
  * in loom.h, plus a device error word and an optional loom_tuning.  They
  * exist for schedule experiments (read-ahead depth, serial control, plain
- * loads) and for fault tests; none of these controls changes a result.
+ * loads) and for the limit of device waits; none of these controls changes a
+ * result.
  * [P1] = "Tune loop unrolling and pipelining" (Loom pages): the depth is the
  * read-ahead depth of its pipeline(depth) ("Separate depth from unrolling"),
  * depth 1 being the serial control.
@@ -35,10 +36,9 @@ typedef struct loom_tuning {
     int32_t warps_per_cta;  /* 1, 2, 4 or 8; 0 = default */
     int32_t chunk_bytes;    /* row sums: bytes per staged chunk, a multiple of 512 in
                                [512, 32768]; 0 = default */
-    int32_t inject_stall;   /* fault test: issue no bulk copies, so every staged wait runs
-                               out after wait_ns; results become NaN, the error word gets
-                               LOOM_DEVERR_TIMEOUT, and the device stays usable */
-    int64_t wait_ns;        /* limit of each device wait in ns; 0 = default (1 s) */
+    int64_t wait_ns;        /* limit of each device wait in ns; 0 = default (1 s).  A wait
+                               that runs out ends the kernel with NaN results and
+                               LOOM_DEVERR_TIMEOUT in the error word; the device stays usable */
     /* tensor-core dot schedule (depth above = its shared-memory stages) */
     int32_t tc_units_per_stage; /* 128-k weight units per stage, 1 .. converter groups of a
                                    pipeline; 0 = default (one per group) */

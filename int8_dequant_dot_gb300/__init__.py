@@ -14,9 +14,12 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libloom.so")
+#: the library this instance of the binding loads (the fault tests load a second
+#: instance of this module bound to libloom_test.so, by setting LIB_PATH first)
+LIB_PATH = globals().get("LIB_PATH") or os.path.join(HERE, "libloom.so")
 
 LOOM_OK = 0
 LOOM_ERR_NULL = -1
@@ -92,8 +95,8 @@ class loom_launch(ctypes.Structure):
 class loom_tuning(ctypes.Structure):
     _fields_ = [("depth", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("units_per_warp", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
-                ("chunk_bytes", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
-                ("wait_ns", ctypes.c_int64), ("tc_units_per_stage", ctypes.c_int32),
+                ("chunk_bytes", ctypes.c_int32), ("wait_ns", ctypes.c_int64),
+                ("tc_units_per_stage", ctypes.c_int32),
                 ("tc_a_buffers", ctypes.c_int32), ("tc_pipelines", ctypes.c_int32),
                 ("tc_schedule", ctypes.c_int32)]
 
@@ -225,12 +228,12 @@ def loom_row_sum_batched(values, num_segments: int, seg_stride: int, rows: int, 
 
 
 def make_tuning(depth: int = 0, path: int = LOOM_PATH_AUTO, units_per_warp: int = 0,
-                warps_per_cta: int = 0, chunk_bytes: int = 0, inject_stall: bool = False,
-                wait_ns: int = 0, tc_units_per_stage: int = 0, tc_a_buffers: int = 0,
-                tc_pipelines: int = 0, tc_schedule: int = 0) -> loom_tuning:
+                warps_per_cta: int = 0, chunk_bytes: int = 0, wait_ns: int = 0,
+                tc_units_per_stage: int = 0, tc_a_buffers: int = 0, tc_pipelines: int = 0,
+                tc_schedule: int = 0) -> loom_tuning:
     return loom_tuning(int(depth), int(path), int(units_per_warp), int(warps_per_cta),
-                       int(chunk_bytes), int(bool(inject_stall)), int(wait_ns),
-                       int(tc_units_per_stage), int(tc_a_buffers), int(tc_pipelines), int(tc_schedule))
+                       int(chunk_bytes), int(wait_ns), int(tc_units_per_stage), int(tc_a_buffers),
+                       int(tc_pipelines), int(tc_schedule))
 
 
 def loom_row_sum_batched_ex(values, num_segments: int, seg_stride: int, rows: int, lanes: int,
@@ -276,10 +279,16 @@ def dot_workspace(n_rows: int, k: int, batch: int, device=None):
 #: workspace="auto": one workspace per (device, stream), kept for reuse
 AUTO = "auto"
 _workspaces: dict = {}
+_workspaces_lock = threading.Lock()
+#: the largest problem the workspace query accepts: its workspace is the most any
+#: call on the device uses (the size grows with the CTAs, at most one per SM)
+_MAX_PROBLEM = (0x7FFFFFFF, 16, 16)
 
 
 def _workspace(workspace, like, n_rows, k, batch, stream_handle):
-    """(address, bytes) of the workspace argument."""
+    """(address, bytes) of the workspace argument.  "auto" keeps one workspace per
+    (device, stream), allocated once at its first use with the most any call on that
+    device needs, so it never grows and no call waits for the device."""
     if workspace is None:
         return None, 0
     if not (isinstance(workspace, str) and workspace == AUTO):
@@ -287,19 +296,27 @@ def _workspace(workspace, like, n_rows, k, batch, stream_handle):
             return workspace
         return _ptr(workspace), workspace.numel() * workspace.element_size()
     import torch
-    nbytes = loom_i8_dequant_dot_workspace_bytes(n_rows, k, batch)
-    if nbytes == 0:
+    if loom_i8_dequant_dot_workspace_bytes(n_rows, k, batch) == 0:
         return None, 0
     dev = like.device if hasattr(like, "device") else torch.device("cuda", torch.cuda.current_device())
     key = (dev.index, stream_handle)
-    ws = _workspaces.get(key)
-    if ws is None or ws.numel() < nbytes:
-        # calls on stream_handle may still use an outgrown workspace: let them
-        # finish before torch may hand its memory to anyone else
-        torch.cuda.synchronize(dev)
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        _workspaces[key] = ws
+    with _workspaces_lock:
+        ws = _workspaces.get(key)
+        if ws is None:
+            nbytes = loom_i8_dequant_dot_workspace_bytes(*_MAX_PROBLEM)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            _workspaces[key] = ws
     return ws.data_ptr(), ws.numel()
+
+
+def _on_device(t):
+    """The device of tensor `t` made current for the call (the library sizes the
+    tensor-core grid and finds its scratch on the current device)."""
+    import contextlib
+    if hasattr(t, "device") and getattr(t.device, "type", None) == "cuda":
+        import torch
+        return torch.cuda.device(t.device)
+    return contextlib.nullcontext()
 
 
 def loom_i8_dequant_dot(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_x, batch: int, *,
@@ -310,11 +327,12 @@ def loom_i8_dequant_dot(w_packed, scale_w, n_rows: int, k: int, x_packed, scale_
     if y is None:
         y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
         acc = acc if acc is not None else acc2
-    st = _stream(stream, w_packed)
-    wp, wb = _workspace(workspace, w_packed, n_rows, k, batch, st)
-    _check(_lib.loom_i8_dequant_dot(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
-                                    _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
-                                    wp, int(wb), st), "loom_i8_dequant_dot")
+    with _on_device(w_packed):
+        st = _stream(stream, w_packed)
+        wp, wb = _workspace(workspace, w_packed, n_rows, k, batch, st)
+        _check(_lib.loom_i8_dequant_dot(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
+                                        _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
+                                        wp, int(wb), st), "loom_i8_dequant_dot")
     return y, acc
 
 
@@ -325,12 +343,13 @@ def loom_i8_dequant_dot_ex(w_packed, scale_w, n_rows: int, k: int, x_packed, sca
         y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
         acc = acc if acc is not None else acc2
     tp = ctypes.byref(tuning) if tuning is not None else None
-    st = _stream(stream, w_packed)
-    wp, wb = _workspace(workspace, w_packed, n_rows, k, batch, st)
-    _check(_lib.loom_i8_dequant_dot_ex(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
-                                       _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
-                                       wp, int(wb), _ptr(error), tp, st),
-           "loom_i8_dequant_dot_ex")
+    with _on_device(w_packed):
+        st = _stream(stream, w_packed)
+        wp, wb = _workspace(workspace, w_packed, n_rows, k, batch, st)
+        _check(_lib.loom_i8_dequant_dot_ex(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
+                                           _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y), _ptr(acc),
+                                           wp, int(wb), _ptr(error), tp, st),
+               "loom_i8_dequant_dot_ex")
     return y, acc
 
 
@@ -341,10 +360,11 @@ def loom_i8_dequant_dot_noalloc(w_packed, scale_w, n_rows: int, k: int, x_packed
     if y is None:
         y, acc2 = _dot_outputs(w_packed, n_rows, batch, want_acc and acc is None)
         acc = acc if acc is not None else acc2
-    _check(_lib.loom_i8_dequant_dot_noalloc(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
-                                            _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y),
-                                            _ptr(acc), _stream(stream, w_packed)),
-           "loom_i8_dequant_dot_noalloc")
+    with _on_device(w_packed):
+        _check(_lib.loom_i8_dequant_dot_noalloc(_ptr(w_packed), _ptr(scale_w), int(n_rows), int(k),
+                                                _ptr(x_packed), _ptr(scale_x), int(batch), _ptr(y),
+                                                _ptr(acc), _stream(stream, w_packed)),
+               "loom_i8_dequant_dot_noalloc")
     return y, acc
 
 

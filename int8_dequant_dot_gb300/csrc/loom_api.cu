@@ -8,9 +8,12 @@
 // grid is the ceiling division of the workload by the units one CTA owns,
 // and every entry point launches with exactly the geometry this routine
 // returns, so the division lives in one place.
+#include <cuda.h>
+
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 #include "../../include/loom_tuning.h"
@@ -51,6 +54,16 @@ struct Tuning {
     DotTcConfig tc;
 };
 
+#ifdef LOOM_TEST_HOOKS
+// Test build only (libloom_test.so): while set, the staged kernels issue no
+// copies, so every wait on them runs out after the tuning's wait limit.  The
+// shipping library has no way to turn this on.
+std::atomic<int32_t> g_test_stall{0};
+int32_t test_stall() { return g_test_stall.load(std::memory_order_relaxed); }
+#else
+int32_t test_stall() { return 0; }
+#endif
+
 bool valid_warps(int64_t w) { return w == 1 || w == 2 || w == 4 || w == 8; }
 bool valid_chunk(int64_t b) { return b >= 512 && b <= 32768 && b % 512 == 0; }
 
@@ -67,7 +80,7 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
     out->upw = 0;
     out->warps = 0;
     out->chunk_bytes = 0;
-    out->stall = 0;
+    out->stall = test_stall();
     out->wait_ns = DEFAULT_WAIT_NS;
     out->tc = DotTcConfig{0, 0, 0, 0, 0};
     if (!t)
@@ -85,7 +98,6 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
     out->upw = t->units_per_warp;
     out->warps = t->warps_per_cta;
     out->chunk_bytes = t->chunk_bytes;
-    out->stall = t->inject_stall != 0;
     if (t->wait_ns)
         out->wait_ns = (uint64_t)t->wait_ns;
     out->tc = DotTcConfig{t->depth, t->tc_units_per_stage, t->tc_a_buffers, t->tc_pipelines, t->tc_schedule};
@@ -683,10 +695,39 @@ constexpr int64_t NOALLOC_SCRATCH_BYTES = 8ll << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
-std::atomic<void *> g_noalloc_addr[NOALLOC_MAX_DEVICES];
 
-// Device address of the scratch array on the current device, looked up once
-// per device with cudaGetSymbolAddress.
+// The scratch address of each device, with the context it was looked up in: a
+// context destroyed and created again (cudaDeviceReset) may load the module at
+// another address, so the address is looked up again when the context differs.
+struct ScratchAddr {
+    CUcontext ctx;
+    void *addr;
+};
+std::mutex g_noalloc_mu;
+ScratchAddr g_noalloc_addr[NOALLOC_MAX_DEVICES];
+
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+
+CUcontext current_context()
+{
+    static CtxGetCurrent fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetCurrent>(p);
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS)
+        return nullptr;
+    return c;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// cudaGetSymbolAddress once per device and context (the first call on a device
+// makes the lookup, which may load the module).
 loom_status noalloc_scratch(void **out)
 {
     int dev = 0;
@@ -694,14 +735,20 @@ loom_status noalloc_scratch(void **out)
         cudaGetLastError();
         return LOOM_ERR_CUDA;
     }
-    void *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return LOOM_ERR_CUDA;
-        }
-        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    ScratchAddr &a = g_noalloc_addr[dev];
+    CUcontext ctx = current_context();
+    if (ctx && a.ctx == ctx && a.addr) {
+        *out = a.addr;
+        return LOOM_OK;
     }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    a.ctx = current_context();   // the lookup makes the device's primary context current
+    a.addr = p;
     *out = p;
     return LOOM_OK;
 }
@@ -712,6 +759,11 @@ loom_status noalloc_scratch(void **out)
 using namespace loom;
 
 extern "C" {
+
+#ifdef LOOM_TEST_HOOKS
+// Exported by the test build only (declared in csrc/test_hooks.h).
+void loom_test_inject_stall(int32_t on) { g_test_stall.store(on != 0, std::memory_order_relaxed); }
+#endif
 
 int32_t loom_abi_version(void) { return LOOM_ABI_VERSION; }
 

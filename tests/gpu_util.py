@@ -1,4 +1,6 @@
 """Helpers shared by the GPU parity tests (no test functions here)."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -18,6 +20,47 @@ def loom_module():
     __graft_entry__.build()
     import int8_dequant_dot_gb300 as loom
     return loom
+
+
+_test_binding = None
+
+
+def loom_test_module():
+    """A second instance of the binding, bound to libloom_test.so: the library
+    built with the fault-test hook (the same kernels; its host layer also exports
+    loom_test_inject_stall).  The shipping libloom.so cannot stall on purpose."""
+    global _test_binding
+    if _test_binding is None:
+        import importlib.util
+        import os
+        import __graft_entry__
+        __graft_entry__.build()
+        pkg = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "int8_dequant_dot_gb300")
+        spec = importlib.util.spec_from_file_location("loom_with_test_hooks", os.path.join(pkg, "__init__.py"))
+        mod = importlib.util.module_from_spec(spec)
+        mod.LIB_PATH = os.path.join(pkg, "libloom_test.so")
+        spec.loader.exec_module(mod)
+        lib = mod.library()
+        lib.loom_test_inject_stall.argtypes = [ctypes.c_int32]
+        lib.loom_test_inject_stall.restype = None
+        _test_binding = mod
+    return _test_binding
+
+
+class injected_stall:
+    """Context manager: the staged kernels that the test binding launches inside it
+    issue no copies, so every wait of theirs runs out after the tuning's wait limit."""
+
+    def __init__(self, mod):
+        self.lib = mod.library()
+
+    def __enter__(self):
+        self.lib.loom_test_inject_stall(1)
+        return self
+
+    def __exit__(self, *exc):
+        self.lib.loom_test_inject_stall(0)
+        return False
 
 
 def to_dev(a: np.ndarray, torch):

@@ -43,8 +43,21 @@ def test_every_declared_symbol_is_exported(loom):
         assert getattr(loom.library(), name)
 
 
+def test_fault_hook_only_in_the_test_build(loom):
+    # The shipping library exports the declared entry points and nothing that can
+    # stall a kernel on purpose; the test build adds exactly that one hook.
+    def exported(path):
+        nm = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True)
+        return set(re.findall(r"\sT\s(loom_\w+)$", nm.stdout, re.M))
+    ship = exported(loom.LIB_PATH)
+    test = exported(os.path.join(os.path.dirname(loom.LIB_PATH), "libloom_test.so"))
+    assert "loom_test_inject_stall" not in ship
+    assert test == ship | {"loom_test_inject_stall"}
+    assert not hasattr(loom.make_tuning(), "inject_stall")
+
+
 def test_version_and_strings(loom):
-    assert loom.loom_abi_version() == 3
+    assert loom.loom_abi_version() == 4
     for st in range(-7, 1):
         assert loom.loom_status_string(st)
     assert loom.loom_status_string(-99) == "unknown status"

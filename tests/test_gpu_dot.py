@@ -9,7 +9,8 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import assert_rel, check_guard, guarded, loom_module, require_gpu, to_dev
+from gpu_util import (assert_rel, check_guard, guarded, injected_stall, loom_module, loom_test_module, require_gpu,
+                      to_dev)
 
 pytestmark = pytest.mark.gpu
 Y_REL = 1e-5
@@ -214,8 +215,10 @@ def test_tensor_core_injected_stall(env):
         d = small(n, k, 16, seed=41 + n)
         ws = loom.dot_workspace(n, k, 16)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000, path=loom.LOOM_PATH_TENSOR)
-        y, acc = run_dot(loom, torch, d, tuning=t, error=err, workspace=ws)
+        hooks = loom_test_module()
+        t = hooks.make_tuning(wait_ns=2_000_000, path=loom.LOOM_PATH_TENSOR)
+        with injected_stall(hooks):
+            y, acc = run_dot(hooks, torch, d, tuning=t, error=err, workspace=ws)
         assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
         assert np.isnan(y).all() and (acc == np.iinfo(np.int32).min).all()
         y, acc = run_dot(loom, torch, d, workspace=ws)
@@ -260,8 +263,10 @@ def test_dot_injected_stall(env):
     for b in (1, 16):
         d = small(64, 4096, b, seed=5 + b)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000, path=loom.LOOM_PATH_STAGED)
-        y, acc = run_dot(loom, torch, d, tuning=t, error=err)
+        hooks = loom_test_module()
+        t = hooks.make_tuning(wait_ns=2_000_000, path=loom.LOOM_PATH_STAGED)
+        with injected_stall(hooks):
+            y, acc = run_dot(hooks, torch, d, tuning=t, error=err)
         assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
         assert np.isnan(y).all()
         y, acc = run_dot(loom, torch, d)

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check_guard, guarded, loom_module, require_gpu, to_dev
+from gpu_util import check_guard, guarded, injected_stall, loom_module, loom_test_module, require_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -105,8 +105,9 @@ def test_injected_stall(env):
     d = synth.lane_segments(num_segments=40, rows=64, lanes=32, width=4, seed=71)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     counts = np.maximum(d["counts"], 1)
-    got = run_rows(loom, torch, d["values"], counts, 4, error=err,
-                   tuning=loom.make_tuning(inject_stall=True, wait_ns=2_000_000))
+    hooks = loom_test_module()
+    with injected_stall(hooks):
+        got = run_rows(hooks, torch, d["values"], counts, 4, error=err, tuning=hooks.make_tuning(wait_ns=2_000_000))
     assert np.isnan(got).all() and int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
     assert same_bits(run_rows(loom, torch, d["values"], counts, 4), oracle.lane_sums(d["values"], counts, width=4))
 

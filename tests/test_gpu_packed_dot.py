@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check_guard, guarded, loom_module, require_gpu, to_dev
+from gpu_util import check_guard, guarded, injected_stall, loom_module, loom_test_module, require_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -121,8 +121,9 @@ def test_injected_stall_reports_and_recovers(env):
     torch, loom = env
     d = synth.packed_dot_case(problems=2, records=32, lanes=512, streams=64, counts=[32, 20], seed=606)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000)
-    got = run(loom, torch, d, tuning=t, error=err)
+    hooks = loom_test_module()
+    with injected_stall(hooks):
+        got = run(hooks, torch, d, tuning=hooks.make_tuning(wait_ns=2_000_000), error=err)
     assert np.isnan(got).all()
     assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
     assert same_bits(run(loom, torch, d), want(d))   # the context is still usable

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check_guard, guarded, loom_module, require_gpu, to_dev
+from gpu_util import check_guard, guarded, injected_stall, loom_module, loom_test_module, require_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -96,7 +96,9 @@ def test_injected_stall(env):
     torch, loom = env
     d = synth.routed_case(tokens=16, routes=8, width=1024, missing_every=0, seed=43)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    got = run(loom, torch, d, error=err, tuning=loom.make_tuning(inject_stall=True, wait_ns=2_000_000))
+    hooks = loom_test_module()
+    with injected_stall(hooks):
+        got = run(hooks, torch, d, error=err, tuning=hooks.make_tuning(wait_ns=2_000_000))
     assert np.isnan(got).all() and int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
     assert same_bits(run(loom, torch, d), want(d))
 

@@ -11,7 +11,8 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import REL_TOL, assert_rel, check_guard, guarded, loom_module, require_gpu, to_dev
+from gpu_util import (REL_TOL, assert_rel, check_guard, guarded, injected_stall, loom_module, loom_test_module,
+                      require_gpu, to_dev)
 
 pytestmark = pytest.mark.gpu
 ULP_REL = 2.0**-23   # within one f32 rounding of the exact sum, with margin
@@ -228,8 +229,10 @@ def test_injected_stall_times_out_and_device_stays_usable(env):
     d = _batched_case(S, seed=12)
     dv, dc, di = to_dev(d["values"], torch), to_dev(d["counts"], torch), to_dev(d["initial"], torch)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    t = loom.make_tuning(inject_stall=True, wait_ns=2_000_000, path=loom.LOOM_PATH_STAGED)
-    fr, tc, fs, ts = run_batched(loom, torch, dv, S, 2016, 63, 32, dc, di, 8, tuning=t, error=err)
+    hooks = loom_test_module()
+    t = hooks.make_tuning(wait_ns=2_000_000, path=loom.LOOM_PATH_STAGED)
+    with injected_stall(hooks):
+        fr, tc, fs, ts = run_batched(hooks, torch, dv, S, 2016, 63, 32, dc, di, 8, tuning=t, error=err)
     assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
     has_data = d["counts"] > 0
     assert np.isnan(fs[has_data]).all()

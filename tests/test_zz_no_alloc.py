@@ -39,9 +39,11 @@ def test_noalloc_matches_workspace_entry_on_two_calls(loom):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    # two calls through the same scratch: a grid of uneven band splits, then the
-    # full 8192 x 16384 x 16 workload
-    for n, k, b, seed in ((2049, 4112, 16, 7), (8192, 16384, 16, None)):
+    # calls through the same scratch: a grid of uneven band splits; 33 vectors
+    # (three passes, the last of one vector below the tensor-core threshold, each
+    # pass's streaming kernel following the previous pass's finishing kernel);
+    # then the full 8192 x 16384 x 16 workload
+    for n, k, b, seed in ((2049, 4112, 16, 7), (1500, 2048, 33, 8), (8192, 16384, 16, None)):
         d = synth.dequant_batched() if seed is None else synth.dequant_batched(n_rows=n, k=k, batch=b, seed=seed)
         need = loom.loom_i8_dequant_dot_workspace_bytes(n, k, b)
         assert 0 < need <= 8 << 20
