@@ -298,6 +298,51 @@ def oracle_step(inp, threads, frac: float = 1.0):
     oracle.row_sum_batched(wide["values"][:m], 16384, 16384, 1, wide["counts"][:m], None, 8, threads=threads)
 
 
+def oracle_workload(inp, name, threads, frac: float = 1.0):
+    """One oracle pass over one workload (frac < 1: its leading segments / rows)."""
+    import oracle
+    if name in ("gemv", "batched"):
+        d = inp[name]
+        n = leading(d["w"].shape[0], frac)
+        oracle.i8_dequant_dot(d["w"][:n], d["scale_w"][:n], d["x"], d["scale_x"], threads=threads)
+    elif name == "segments":
+        d = inp["segments"]
+        m = leading(d["num_segments"], frac)
+        oracle.row_sum_batched(d["values"][:m], 2016, 63, 32, d["counts"][:m], d["initial"][:m], 8,
+                               threads=threads)
+    else:
+        d = inp["wide"]
+        m = leading(d["num_segments"], frac)
+        oracle.row_sum_batched(d["values"][:m], 16384, 16384, 1, d["counts"][:m], None, 8, threads=threads)
+
+
+def cpu_per_workload(inp, threads, budget_s: float = 1.5) -> dict:
+    """The oracle on each workload alone, single-threaded and on `threads` host
+    threads: GB/s over the algorithmic bytes of a leading sample of the workload
+    sized so that the single-threaded pass takes about `budget_s` seconds."""
+    out = {}
+    for name in ORDER:
+        probe = 1.0 / 64
+        t0 = time.perf_counter()
+        oracle_workload(inp, name, 1, probe)
+        t_probe = max(time.perf_counter() - t0, 1e-6)
+        frac = min(1.0, probe * budget_s / t_probe)
+        nbytes = algorithmic_bytes(inp, frac)[name]
+        t0 = time.perf_counter()
+        oracle_workload(inp, name, 1, frac)
+        t1 = time.perf_counter() - t0
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle_workload(inp, name, threads, frac)
+            reps += 1
+            tn = (time.perf_counter() - t0) / reps
+            if time.perf_counter() - t0 >= budget_s / 2 or reps >= 50:
+                break
+        out[name] = {"gbs_1_thread": nbytes / t1 / 1e9, f"gbs_{threads}_threads": nbytes / tn / 1e9,
+                     "sample_fraction": frac, "sample_bytes": nbytes}
+    return out
+
+
 def cpu_baseline(inp, total_bytes, threads, budget_s: float = 10.0):
     """The oracle as it stands on the host cores: whole steps (all four
     workloads) repeated until about `budget_s` seconds of work have run."""
@@ -313,7 +358,11 @@ def cpu_baseline(inp, total_bytes, threads, budget_s: float = 10.0):
     return {"value": total_bytes / per / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{steps} full steps (all four workloads, {total_bytes / 1e9:.2f} GB of algorithmic bytes "
                       f"each), fp64/int64 C oracle, {threads} threads over independent segments/rows; "
-                      f"{dt:.1f} s"}
+                      f"{dt:.1f} s",
+            "per_workload": cpu_per_workload(inp, threads),
+            "per_workload_sample": "each workload alone: a leading sample of its segments / rows sized so that "
+                                   "one single-threaded pass takes about 1.5 s, timed on 1 thread and on all "
+                                   "host threads"}
 
 
 #: wall-clock budget of the reference arm's K timed steps
@@ -472,6 +521,8 @@ def run_ours(args, rank, world, dist):
     # the pages' other examples (packed dot, per-lane sums), each timed on its own (not part of the step)
     extras = measure_extras(args, torch, loom, stream, peak, peak_kind)
     extras["read_ahead"] = read_ahead_study(torch, loom, stream, work, alg)
+    extras["stream_floor"] = stream_floor(torch, loom, stream, work, alg, extras)
+    extras["batched_engines"] = engine_study(torch, loom, stream, work, alg)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -552,7 +603,8 @@ def _time_single(args, torch, stream, call, flush, sink):
 def _extra_line(workload, alg, times, peak, peak_kind, traffic, launch):
     avg = sum(times) / len(times)
     gbs = alg / (avg * 1e-3) / 1e9
-    return {"workload": workload, "alg_bytes": alg, "avg_ms": avg, "min_ms": min(times), "launches": len(times),
+    return {"workload": workload, "alg_bytes": alg, "avg_ms": avg, "median_ms": statistics.median(times),
+            "min_ms": min(times), "launches": len(times),
             "l2": "512 MB read before each launch",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": peak_kind, "traffic": traffic},
@@ -605,6 +657,90 @@ def measure_extras(args, torch, loom, stream, peak, peak_kind):
         del v, c, o, d
     del flush
     return out
+
+
+#: read-only probe schedules (kind, depth, CTAs per SM) tried for every byte count
+FLOOR_SCHEDULES = ((0, 4, 4), (0, 8, 4), (0, 8, 2), (1, 4, 4), (1, 8, 4), (1, 8, 8), (2, 2, 12), (2, 4, 6))
+FLOOR_KINDS = ("grid_stride", "warp_range", "bulk_ring")
+
+
+def _after_flush(torch, stream, flush, sink, call):
+    """One launch after a 512 MB read, timed by events on the stream; ms."""
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        sink.copy_(flush.view(torch.int32).sum())
+        torch.cuda._sleep(200_000)
+        a.record(stream)
+        call()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b)
+
+
+def stream_floor(torch, loom, stream, work, alg, extras, reps: int = 21):
+    """The single-launch streaming floor: for the algorithmic byte count of every
+    workload, the best median over FLOOR_SCHEDULES of a launch that only reads
+    that many bytes (loom_stream_floor), beside the kernel's own single-launch
+    median; both after a 512 MB read, all launches interleaved."""
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros((), dtype=torch.int64, device="cuda")
+    word = torch.zeros(1, dtype=torch.int64, device="cuda")
+    sizes = dict(alg)
+    for name, line in extras.items():
+        if isinstance(line, dict) and "alg_bytes" in line:
+            sizes[name] = line["alg_bytes"]
+    src = torch.empty(max(sizes.values()) + 16, dtype=torch.uint8, device="cuda")
+    floor_t = {(n, sc): [] for n in sizes for sc in FLOOR_SCHEDULES}
+    kern_t = {n: [] for n in alg}
+    for rep in range(reps + 1):
+        for n, nbytes in sizes.items():
+            nb = nbytes // 16 * 16
+            for sc in FLOOR_SCHEDULES:
+                t = _after_flush(torch, stream, flush, sink,
+                                 lambda: loom.loom_stream_floor(src, nb, sc[0], sc[1], sc[2], word, stream=stream))
+                if rep:
+                    floor_t[(n, sc)].append(t)
+        for n in alg:
+            t = _after_flush(torch, stream, flush, sink, lambda: work.launch(n))
+            if rep:
+                kern_t[n].append(t)
+    out = {}
+    for n, nbytes in sizes.items():
+        meds = {sc: statistics.median(floor_t[(n, sc)]) for sc in FLOOR_SCHEDULES}
+        best = min(meds, key=meds.get)
+        k_ms = statistics.median(kern_t[n]) if n in kern_t else extras[n]["median_ms"]
+        out[n] = {"bytes": nbytes, "floor_us": meds[best] * 1e3,
+                  "floor_schedule": {"kind": FLOOR_KINDS[best[0]], "depth": best[1], "ctas_per_sm": best[2]},
+                  "floor_GB/s": nbytes / (meds[best] * 1e-3) / 1e9, "kernel_us": k_ms * 1e3,
+                  "kernel_over_floor": k_ms / meds[best]}
+    del flush, src
+    return {"note": "single launches after a 512 MB read, medians of %d; floor = best schedule of a read-only "
+                    "launch over the same byte count (loom_stream_floor)" % reps, "workloads": out}
+
+
+def engine_study(torch, loom, stream, work, alg, reps: int = 21):
+    """The batched dot (8192 x 16384 x 16) on both engines, alternated: the
+    tensor-core kernel against the dp4a kernel with lanes across the batch."""
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros((), dtype=torch.int64, device="cuda")
+    d, o = work.d, work.o
+    ys = {}
+    tunings = {"tensor": loom.make_tuning(path=loom.LOOM_PATH_TENSOR),
+               "dp4a": loom.make_tuning(path=loom.LOOM_PATH_STAGED)}
+    times = {k: [] for k in tunings}
+    for rep in range(reps + 1):
+        for k, tu in tunings.items():
+            y = torch.empty((8192, 16), dtype=torch.float32, device="cuda")
+            t = _after_flush(torch, stream, flush, sink, lambda: loom.loom_i8_dequant_dot_ex(
+                d["wb"], d["swb"], 8192, 16384, d["x16"], d["sx16"], 16, y=y, tuning=tu, stream=stream))
+            if rep:
+                times[k].append(t)
+            ys[k] = y
+    same = bool(torch.equal(ys["tensor"].view(torch.int32), ys["dp4a"].view(torch.int32)))
+    del flush
+    return {k: {"median_us": statistics.median(v) * 1e3, "GB/s": alg["batched"] / (statistics.median(v) * 1e-3) / 1e9}
+            for k, v in times.items()} | {"same_bits": same, "auto_picks": "tensor"}
 
 
 def read_ahead_study(torch, loom, stream, work, alg):

@@ -102,6 +102,30 @@ loom_status loom_routed_combine_ex(const int32_t *d_ids, const float *d_weights,
                                    int64_t tokens, int32_t routes, int32_t rows, int32_t width, float *d_out,
                                    int32_t *d_error, const loom_tuning *tuning, void *stream);
 
+/* Schedules of loom_stream_floor. */
+#define LOOM_FLOOR_GRID_STRIDE 0 /* grid-stride 16-byte loads, `depth` (4 or 8) in flight per thread */
+#define LOOM_FLOOR_WARP_RANGE 1  /* one contiguous range per warp, 16-byte loads, `depth` (4 or 8) in
+                                    flight per lane */
+#define LOOM_FLOOR_BULK_RING 2   /* one warp per CTA, a ring of `depth` (1..8) 8 KiB stages filled by
+                                    bulk copies */
+
+/* Measurement probe, not a step of the method: one launch that reads `bytes`
+ * of device memory at d_src once (16-byte loads or bulk copies) and keeps
+ * nothing of it.  Its time is what one launch that
+ * moves that many bytes takes on this device -- launch, ramp and tail
+ * included -- and is the reference each kernel's single-launch time is set
+ * against.  `ctas_per_sm` (1..32) CTAs per SM of the current device, 256
+ * threads each (32 for LOOM_FLOOR_BULK_RING).  d_sink: a device word that is
+ * written only when the checksum of the loaded words equals a fixed constant
+ * (so that no load can be dropped); d_error (may be NULL) gets
+ * LOOM_DEVERR_TIMEOUT if a bulk copy did not land within the default wait.
+ * Errors: NULL d_sink or d_src (bytes > 0) -> LOOM_ERR_NULL; d_src not 16-byte
+ * or d_sink not 8-byte aligned -> LOOM_ERR_ALIGN; bytes < 0 or not a multiple
+ * of 16 -> LOOM_ERR_SHAPE; unknown schedule, depth or ctas_per_sm ->
+ * LOOM_ERR_ARG. */
+loom_status loom_stream_floor(const void *d_src, int64_t bytes, int32_t schedule, int32_t depth,
+                              int32_t ctas_per_sm, uint64_t *d_sink, int32_t *d_error, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

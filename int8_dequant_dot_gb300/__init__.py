@@ -64,6 +64,10 @@ LOOM_PATH_STAGED = 1
 LOOM_PATH_DIRECT = 2
 LOOM_PATH_TENSOR = 3
 
+LOOM_FLOOR_GRID_STRIDE = 0
+LOOM_FLOOR_WARP_RANGE = 1
+LOOM_FLOOR_BULK_RING = 2
+
 #: every extern "C" symbol the headers declare
 EXPORTS = (
     "loom_launch_config", "loom_full_tile_sum", "loom_row_sum_batched", "loom_i8_dequant_dot",
@@ -71,6 +75,7 @@ EXPORTS = (
     "loom_i8_dequant_dot_ex", "loom_i8_dequant_dot_workspace_bytes", "loom_i8_dequant_dot_noalloc",
     "loom_packed_dot", "loom_packed_dot_ex", "loom_sum_rows", "loom_sum_rows_ex", "loom_sum_guarded_rows",
     "loom_sum_guarded_rows_ex", "loom_routed_combine", "loom_routed_combine_ex", "loom_stage_rows",
+    "loom_stream_floor",
 )
 
 
@@ -128,6 +133,7 @@ def _bind() -> ctypes.CDLL:
         "loom_routed_combine_ex": [P, P, P, i64, i32, i32, i32, P, P, ctypes.POINTER(loom_tuning), P],
         "loom_stage_rows": [P, P, i64, i64, i32, i32, P, i32, P],
         "loom_i8_unpack": [P, i64, P, P],
+        "loom_stream_floor": [P, i64, i32, i32, i32, P, P, P],
         "loom_status_string": [i32],
         "loom_abi_version": [],
     }
@@ -480,3 +486,11 @@ def loom_i8_unpack(packed, n_words: int, out=None, *, stream=None):
     _check(_lib.loom_i8_unpack(_ptr(packed), int(n_words), _ptr(out), _stream(stream, packed)),
            "loom_i8_unpack")
     return out
+
+
+def loom_stream_floor(src, nbytes: int, schedule: int, depth: int, ctas_per_sm: int, sink, *, error=None,
+                      stream=None):
+    """The read-only streaming probe: one launch reading ``nbytes`` at ``src`` (a device
+    tensor or address); ``sink`` is a device int64 word."""
+    _check(_lib.loom_stream_floor(_ptr(src), int(nbytes), int(schedule), int(depth), int(ctas_per_sm),
+                                  _ptr(sink), _ptr(error), _stream(stream, sink)), "loom_stream_floor")

@@ -184,6 +184,11 @@ uint32_t packed_dot_smem_bytes(bool staged, int depth, int rps, int streams);
 uint32_t packed_dot_threads(bool staged);
 cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_launch &L, cudaStream_t stream);
 
+// ---- read-only streaming probe (stream_floor.cu) --------------------------------
+cudaError_t launch_stream_floor(const void *src, int64_t bytes, int32_t kind, int32_t depth, int32_t ctas_per_sm,
+                                int32_t sm_count, uint64_t *sink, int32_t *error, uint64_t wait_ns,
+                                cudaStream_t stream);
+
 // ---- unpack ----------------------------------------------------------------
 constexpr int UNPACK_BLOCK = 256;
 cudaError_t launch_unpack(const int32_t *packed, int64_t n_words, float *out, const loom_launch &L,

@@ -1068,6 +1068,34 @@ loom_status loom_stage_rows(const float *h_values, float *d_values, int64_t num_
     return LOOM_OK;
 }
 
+loom_status loom_stream_floor(const void *d_src, int64_t bytes, int32_t schedule, int32_t depth,
+                              int32_t ctas_per_sm, uint64_t *d_sink, int32_t *d_error, void *stream)
+{
+    if (bytes < 0 || bytes % 16 != 0)
+        return LOOM_ERR_SHAPE;
+    const bool loads = schedule == LOOM_FLOOR_GRID_STRIDE || schedule == LOOM_FLOOR_WARP_RANGE;
+    if ((!loads && schedule != LOOM_FLOOR_BULK_RING) || (loads && depth != 4 && depth != 8) ||
+        (!loads && (depth < 1 || depth > LOOM_MAX_DEPTH)) || ctas_per_sm < 1 || ctas_per_sm > 32)
+        return LOOM_ERR_ARG;
+    if (!d_sink || (bytes > 0 && !d_src))
+        return LOOM_ERR_NULL;
+    if (misaligned(d_src, 16) || misaligned(d_sink, 8) || misaligned(d_error, 4))
+        return LOOM_ERR_ALIGN;
+    if (bytes == 0)
+        return LOOM_OK;
+    int64_t sms = 0;
+    const loom_status st = current_sm_count(&sms);
+    if (st != LOOM_OK)
+        return st;
+    const cudaError_t e = launch_stream_floor(d_src, bytes, schedule, depth, ctas_per_sm, (int32_t)sms, d_sink,
+                                              d_error, DEFAULT_WAIT_NS, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return LOOM_ERR_CUDA;
+    }
+    return LOOM_OK;
+}
+
 loom_status loom_i8_unpack(const int32_t *d_packed, int64_t n_words, float *d_out, void *stream)
 {
     if (n_words < 0)

@@ -385,3 +385,22 @@ def test_stage_rows_launch_and_validation(loom):
     assert f(A, A, 4, 2016, 63, 32, None, 64, None) == loom.LOOM_ERR_RANGE
     assert f(A, A, 4, 100, 63, 32, None, 3, None) == loom.LOOM_ERR_SHAPE
     assert f(A, A, 4, 2016, 63, 0, None, 3, None) == loom.LOOM_ERR_SHAPE
+
+
+def test_stream_floor_validation(loom):
+    # the read-only probe: every rejection happens on the host, before any device access
+    lib = loom.library()
+    A = 1 << 20
+    f = lambda src, n, kind, depth, cps, sink=A + 8: lib.loom_stream_floor(src, n, kind, depth, cps, sink, None, None)
+    assert f(A, 0, 0, 4, 4) == loom.LOOM_OK                       # nothing to read: no launch
+    assert f(A, -16, 0, 4, 4) == loom.LOOM_ERR_SHAPE
+    assert f(A, 24, 0, 4, 4) == loom.LOOM_ERR_SHAPE                # not whole 16-byte words
+    assert f(A, 64, 3, 4, 4) == loom.LOOM_ERR_ARG                  # unknown schedule
+    assert f(A, 64, 0, 6, 4) == loom.LOOM_ERR_ARG                  # loads: 4 or 8 in flight
+    assert f(A, 64, 2, 9, 4) == loom.LOOM_ERR_ARG                  # bulk ring: 1..8 stages
+    assert f(A, 64, 1, 8, 0) == loom.LOOM_ERR_ARG
+    assert f(A, 64, 1, 8, 33) == loom.LOOM_ERR_ARG
+    assert f(None, 64, 0, 4, 4) == loom.LOOM_ERR_NULL
+    assert f(A, 64, 0, 4, 4, None) == loom.LOOM_ERR_NULL
+    assert f(A + 4, 64, 0, 4, 4) == loom.LOOM_ERR_ALIGN
+    assert f(A, 64, 0, 4, 4, A + 4) == loom.LOOM_ERR_ALIGN
