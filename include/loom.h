@@ -121,6 +121,9 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_ROUTED_STAGED 13  /* routed combine: bulk-copy ring of payload pieces per warp */
 #define LOOM_KERNEL_ROUTED_DIRECT 14  /* routed combine: plain loads */
 #define LOOM_KERNEL_STAGE_ROWS 15     /* upload of ragged rows: one CTA per 8 KiB of a segment */
+#define LOOM_KERNEL_DOT_TENSOR_ROWS 16 /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass; one
+                                          CTA per SM owning whole rows (units_per_cta = rows),
+                                          two k ranges per MMA; one launch, no workspace */
 
 /* Maximum read-ahead depth (staged chunks in flight per warp or CTA). */
 #define LOOM_MAX_DEPTH 8

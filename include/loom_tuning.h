@@ -48,11 +48,15 @@ typedef struct loom_tuning {
     int32_t tc_pipelines;       /* pipelines per CTA (one CTA per SM): 1 (four converter groups,
                                    all 512 tensor-memory columns) or 2 (two groups and 256
                                    columns each, the halves of the CTA's units); 0 = 2 */
-    int32_t tc_schedule;        /* how 128-row bands of W map onto CTAs: 0 choose; 1 whole
+    int32_t tc_schedule;        /* how rows of W map onto CTAs: 0 choose; 1 whole 128-row
                                    bands per CTA; 2 equal shares of all units, split bands
                                    finished by a second kernel (needs the workspace, else
                                    LOOM_ERR_ARG); 3 a cluster of CTAs per band (when the SMs
-                                   allow at least two per band, else as 1) */
+                                   allow at least two per band, else as 1); 4 ceil(n_rows /
+                                   SMs) whole rows per CTA, in blocks of up to 64 (depth even,
+                                   2..8; tc_a_buffers 2 or 3; tc_units_per_stage 0 or 1 and
+                                   tc_pipelines 0 or 2, else LOOM_ERR_ARG).  Choosing takes 4
+                                   where blocks hold 32 rows or more and k >= 2048 */
 } loom_tuning;
 
 /* loom_row_sum_batched with tuning (NULL = defaults).  Extra errors:

@@ -25,7 +25,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libloom.so")
 TEST_LIB = os.path.join(HERE, "libloom_test.so")
-SOURCES = ["loom_api.cu", "row_sum.cu", "dequant_dot.cu", "dot_tc.cu", "packed_dot.cu", "lane_sum.cu", "routed.cu", "stage.cu", "stream_floor.cu"]
+SOURCES = ["loom_api.cu", "row_sum.cu", "dequant_dot.cu", "dot_tc.cu", "dot_tc_rows.cu", "packed_dot.cu", "lane_sum.cu", "routed.cu", "stage.cu", "stream_floor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -56,9 +56,17 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace loom {
 namespace {
+
+using tc::i8x4_to_f16x4;
+using tc::lds128;
+using tc::mbar_arrive;
+using tc::smem_desc_sw128;
+using tc::sts128;
+using tc::tma_load_2d;
 
 constexpr int TC_M = 128;                    // rows per band (MMA M)
 constexpr int TC_N = 16;                     // vectors per pass (MMA N)
@@ -88,7 +96,7 @@ constexpr uint32_t TC_EPI_BAR = 1;                   // named barriers 1, 2: epi
 constexpr uint32_t TC_REC_HDR = 16;                   // record header: validity word + padding
 constexpr uint32_t TC_REC_BYTES = TC_REC_HDR + 128 * 16 * 4;   // one split segment's partial sums
 // instruction descriptor: D f32, A/B f16, both K-major, N = 16, M = 128
-constexpr uint32_t TC_IDESC = (1u << 4) | ((TC_N >> 3) << 17) | ((TC_M >> 4) << 24);
+constexpr uint32_t TC_IDESC = tc::idesc_f16(TC_M, TC_N);
 
 struct TcParams {
     const float *scale_w;
@@ -184,21 +192,6 @@ uint32_t tc_smem_bytes(int pipes, int cluster, int S, int ups, int na, int ng)
 }
 
 // ---- PTX wrappers ----------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
-                                            uint32_t bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_rank()
 {
     uint32_t r;
@@ -245,9 +238,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void epi_barrier(int p)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(TC_EPI_BAR + p), "n"(32 * TC_EPI_WARPS) : "memory");
@@ -264,27 +254,6 @@ __device__ __forceinline__ bool epi_barrier_and(int p, bool v)
         : "r"(v ? 1u : 0u), "r"(TC_EPI_BAR + p), "n"(32 * TC_EPI_WARPS)
         : "memory");
     return r != 0;
-}
-
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t accumulate)
@@ -304,82 +273,18 @@ __device__ __forceinline__ void tc_mma_acc(uint32_t d, uint32_t a, uint64_t bdes
                  : "memory");
 }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar)
+__device__ __forceinline__ bool aborted(const CtaArea &C) { return tc::aborted(C.abort_flag()); }
+
+__device__ __forceinline__ void set_abort(const CtaArea &C, const TcParams &q) { tc::set_abort(C.abort_flag(), q.error); }
+
+__device__ __forceinline__ bool role_wait(const CtaArea &C, const TcParams &q, uint32_t bar, uint32_t parity)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    return tc::role_wait(C.abort_flag(), q.error, q.wait_ns, bar, parity);
 }
 
-// Shared-memory descriptor of a K-major operand with 128-byte swizzle:
-// start address, leading offset (unused here, 16 B), stride between 8-row
-// groups 1024 B, descriptor version 1, layout "128-byte swizzle".
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start)
+__device__ __forceinline__ bool warp_wait(const CtaArea &C, const TcParams &q, uint32_t bar, uint32_t parity)
 {
-    return (uint64_t)((start >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Four signed bytes -> two f16x2 words (elements 0,1 and 2,3; low half first).
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi)
-{
-    const uint32_t u = w ^ 0x80808080u;   // b + 128 as an unsigned byte
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));   // - 1152
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
-}
-
-__device__ __forceinline__ int4 lds128(uint32_t addr)
-{
-    int4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-__device__ __forceinline__ bool aborted(const CtaArea &C)
-{
-    uint32_t v;
-    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(C.abort_flag()));
-    return v != 0;
-}
-
-__device__ __forceinline__ void set_abort(const CtaArea &C, const TcParams &q)
-{
-    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(C.abort_flag()), "r"(1u) : "memory");
-    dev::flag_error(q.error, LOOM_DEVERR_TIMEOUT);
-}
-
-// Wait for a phase of `bar`; false once the CTA has aborted or the limit
-// has passed (which aborts the CTA).
-__device__ __forceinline__ bool role_wait(const CtaArea &L, const TcParams &q, uint32_t bar, uint32_t parity)
-{
-    if (dev::mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = dev::global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (dev::mbar_try_wait(bar, parity))
-            return true;
-        if ((i & 15u) == 0) {
-            if (aborted(L))
-                return false;
-            if (dev::global_ns() - t0 > q.wait_ns) {
-                set_abort(L, q);
-                return false;
-            }
-        }
-    }
-}
-
-// The same, agreed by every lane of the warp.
-__device__ __forceinline__ bool warp_wait(const CtaArea &L, const TcParams &q, uint32_t bar, uint32_t parity)
-{
-    return __all_sync(dev::FULL_MASK, role_wait(L, q, bar, parity));
+    return tc::warp_wait(C.abort_flag(), q.error, q.wait_ns, bar, parity);
 }
 
 // ---- work partition ----------------------------------------------------------
@@ -556,9 +461,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    tc_fence_before();
+    tc::fence_before();
     __syncthreads();
-    tc_fence_after();
+    tc::fence_after();
     if (q.mode == TC_CLUSTER)
         cluster_sync();   // rank 0's barrier is initialised before any rank arrives on it
     uint32_t tmem;
@@ -624,14 +529,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
+                        tc::fence_after();
                         const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)a * (TC_B_BYTES >> 4));
                         const uint32_t ta = tmem + (uint32_t)a * TC_A_COLS;
                         tc_mma(d, ta, bd, m != 0 ? 1u : 0u);
 #pragma unroll
                         for (int kk = 1; kk < TC_KSLICES; ++kk)
                             tc_mma_acc(d, ta + kk * 8, bd + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4));
-                        tc_commit(afree0 + 8 * a);   // A/B buffer a is free once these MMAs complete
+                        tc::commit(afree0 + 8 * a);   // A/B buffer a is free once these MMAs complete
                         if (++a == NA) {
                             a = 0;
                             aph ^= 1u;
@@ -639,7 +544,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     if (!ok)
                         break;
-                    tc_commit(gfull0 + 8 * gs);   // accumulator gs is final once these complete
+                    tc::commit(gfull0 + 8 * gs);   // accumulator gs is final once these complete
                     ++g;
                     if (++gs == NG) {
                         gs = 0;
@@ -648,7 +553,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 u = e;
             }
-            tc_commit(L.done());   // every MMA issued by this thread has completed
+            tc::commit(L.done());   // every MMA issued by this thread has completed
         }
         __syncwarp();
     } else if (w < CONV) {
@@ -691,7 +596,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     ok = false;
                     break;
                 }
-                tc_fence_after();
+                tc::fence_after();
                 // A operand: 128 f16 of row t -> 64 TMEM columns of buffer a
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
@@ -704,7 +609,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         i8x4_to_f16x4((uint32_t)v.z, r[c2 * 8 + 4], r[c2 * 8 + 5]);
                         i8x4_to_f16x4((uint32_t)v.w, r[c2 * 8 + 6], r[c2 * 8 + 7]);
                     }
-                    tc_st16(tmem + tlane + a * TC_A_COLS + part * 16, r);
+                    tc::st16(tmem + tlane + a * TC_A_COLS + part * 16, r);
                 }
                 // B operand: the activation piece into the K-major 128-byte-swizzled
                 // f16 tile (two 64-k atoms of 16 rows)
@@ -720,9 +625,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     sts128(atom + (((c0) ^ (n & 7)) << 4), hx[0], hx[1], hx[2], hx[3]);
                     sts128(atom + (((c0 + 1) ^ (n & 7)) << 4), hx[4], hx[5], hx[6], hx[7]);
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                fence_async_smem();
-                tc_fence_before();
+                tc::wait_st();
+                tc::fence_async_smem();
+                tc::fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(L.aready(a));
@@ -763,13 +668,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     ok = false;
                     continue;
                 }
-                tc_fence_after();
+                tc::fence_after();
                 uint32_t v[16];
-                tc_ld16(tmem + tlane + acc_col + gs * TC_ACC_COLS, v);
+                tc::ld16(tmem + tlane + acc_col + gs * TC_ACC_COLS, v);
 #pragma unroll
                 for (int b = 0; b < TC_N; ++b)
                     isum[b] += __float2int_rn(__uint_as_float(v[b]));
-                tc_fence_before();
+                tc::fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(L.gfree(gs));
@@ -875,7 +780,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 
     // ---- teardown: tensor memory is freed only after every MMA has completed
-    tc_fence_before();
+    tc::fence_before();
     __syncthreads();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the finishing kernel may start
     if (p == 0 && w == PRODUCER) {
@@ -885,7 +790,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             dev::mbar_wait_bounded(Lp.done(), 0, q.wait_ns);
         }
         __syncwarp();
-        tc_fence_after();
+        tc::fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
                      : "memory");
     }
@@ -1035,8 +940,10 @@ std::mutex g_map_mu;
 MapEntry g_maps[8];
 int g_maps_used = 0, g_maps_next = 0;
 
-bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                  uint32_t box_outer, CUtensorMapSwizzle swizzle)
+}  // namespace
+
+bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                             uint32_t box_outer, CUtensorMapSwizzle swizzle)
 {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_maps_used; ++i) {
@@ -1055,6 +962,8 @@ bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t o
     g_maps_used = g_maps_used < 8 ? g_maps_used + 1 : 8;
     return true;
 }
+
+namespace {
 
 // The kernel's dynamic shared-memory limit, raised once per device to the
 // largest size asked for so far.
@@ -1109,7 +1018,10 @@ int dot_tc_rows_per_band() { return TC_M; }
 // Resolve the schedule of one tensor-core launch.  cfg fields of 0 take the
 // defaults: two pipelines per CTA, two units per stage, two stages, three A
 // buffers per pipeline (the rest of its tensor memory holds accumulators).
-// Bands map onto CTAs in one of three ways (cfg.schedule, 0 = choose):
+// Rows map onto CTAs in one of four ways (cfg.schedule, 0 = choose):
+//  * whole rows per CTA (dot_tc_rows.cu) when n_rows / SMs fills at least half
+//    of the 64 rows of a block and k has 16 units or more: no partial sums
+//    leave a CTA;
 //  * a cluster of C CTAs per band (C = 2..4) when that keeps every SM busy --
 //    or, with no workspace, at least three quarters of them: no cross-SM
 //    traffic at all;
@@ -1118,12 +1030,17 @@ int dot_tc_rows_per_band() { return TC_M; }
 bool dot_tc_plan(int64_t n_rows, int32_t k, int64_t sm_count, const DotTcConfig &cfg, bool split,
                  DotTcPlan *out)
 {
+    // whole rows per CTA, where the rows fill the tensor-memory lanes well (dot_tc_rows.cu)
+    if (cfg.schedule == 4)
+        return dot_tc_rows_plan(n_rows, k, sm_count, cfg, true, out);
+    if (cfg.schedule == 0 && dot_tc_rows_plan(n_rows, k, sm_count, cfg, false, out))
+        return true;
     const int pipes = cfg.pipes ? cfg.pipes : 2;
     if (pipes < 1 || pipes > TC_MAX_PIPES)
         return false;
     const int groups = pipes == 2 ? 2 : TC_MAX_GROUPS;   // converter groups per pipeline
     const int ups = cfg.units_per_stage ? cfg.units_per_stage : groups;
-    if (ups < 1 || ups > groups || sm_count < 1 || cfg.schedule < 0 || cfg.schedule > 3)
+    if (ups < 1 || ups > groups || sm_count < 1 || cfg.schedule < 0 || cfg.schedule > 4)
         return false;
     const int depth = cfg.depth ? cfg.depth : (ups >= 2 ? 2 : 4);
     const uint32_t cols = TC_TMEM_COLS / (uint32_t)pipes;
@@ -1251,12 +1168,14 @@ bool dot_tc_cluster_fits(const DotTcPlan &plan)
 
 cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream)
 {
+    if (plan.mode == DOT_TC_ROWS)
+        return launch_dot_tc_rows(p, plan, stream);
     if (plan.grid == 0)
         return cudaSuccess;
     const int64_t k = (int64_t)p.k_words * 4;
     CUtensorMap tmw, tmx;
-    if (!encode_2d_u8(&tmw, p.w, (uint64_t)k, (uint64_t)p.n_rows, TC_KU, TC_M, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d_u8(&tmx, p.x, (uint64_t)k, (uint64_t)p.batch, TC_KU, TC_N, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_tensor_map_2d_u8(&tmw, p.w, (uint64_t)k, (uint64_t)p.n_rows, TC_KU, TC_M, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d_u8(&tmx, p.x, (uint64_t)k, (uint64_t)p.batch, TC_KU, TC_N, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     TcParams q;
     q.scale_w = p.scale_w;

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/loom.h"
@@ -84,7 +85,8 @@ struct DotTcConfig {
     int32_t units_per_stage;  // 1 .. converter groups per pipeline; 0 = default
     int32_t a_bufs;           // f16 A buffers per pipeline in tensor memory; 0 = default
     int32_t pipes;            // pipelines per CTA, 1 or 2; 0 = default
-    int32_t schedule;         // 0 choose, 1 whole bands, 2 split (workspace), 3 cluster per band
+    int32_t schedule;         // 0 choose, 1 whole bands, 2 split (workspace), 3 cluster per band,
+                              // 4 whole rows per CTA (dot_tc_rows.cu)
 };
 struct DotTcPlan {
     int64_t grid;
@@ -95,7 +97,13 @@ struct DotTcPlan {
     uint32_t cta_area, pipe_cols, pipe_bytes, smem_bytes;
     bool split;               // bands may be split between CTAs (needs the workspace)
     int64_t sm_count;         // SMs the grid was sized for
+    // row-block schedule (mode DOT_TC_ROWS, dot_tc_rows.cu)
+    int32_t rows_per_cta, block_rows, units_per_quarter;
+    uint32_t wbox, stage_bytes;
 };
+// mode of a DotTcPlan whose CTAs each own whole rows (dot_tc_rows.cu); the
+// band schedules of dot_tc.cu use the modes below it
+constexpr int DOT_TC_ROWS = 3;
 bool dot_tc_eligible(bool aligned, int32_t k, int32_t batch_pass);
 int dot_tc_threads(int pipes);
 int dot_tc_rows_per_band();
@@ -104,6 +112,13 @@ bool dot_tc_plan(int64_t n_rows, int32_t k, int64_t sm_count, const DotTcConfig 
 int64_t dot_tc_workspace_bytes(const DotTcPlan &plan);
 bool dot_tc_cluster_fits(const DotTcPlan &plan);
 cudaError_t launch_dot_tc(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream);
+bool dot_tc_rows_plan(int64_t n_rows, int32_t k, int64_t sm_count, const DotTcConfig &cfg, bool forced,
+                      DotTcPlan *out);
+int dot_tc_rows_threads();
+cudaError_t launch_dot_tc_rows(const DotParams &p, const DotTcPlan &plan, cudaStream_t stream);
+// 2-D tensor map of a row-major u8 array [outer][inner] (recently used maps are reused)
+bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                             uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
 // ---- per-lane f32 sums (lane_sum.cu): sum_rows, sum_vector_rows, guarded rows ----
 struct LaneSumParams {

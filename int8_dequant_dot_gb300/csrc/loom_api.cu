@@ -90,7 +90,7 @@ loom_status read_tuning(const loom_tuning *t, int default_depth, Tuning *out)
         (t->warps_per_cta != 0 && !valid_warps(t->warps_per_cta)) ||
         (t->chunk_bytes != 0 && !valid_chunk(t->chunk_bytes)) || t->tc_units_per_stage < 0 ||
         t->tc_units_per_stage > 4 || t->tc_a_buffers < 0 || t->tc_a_buffers > 8 ||
-        t->tc_pipelines < 0 || t->tc_pipelines > 2 || t->tc_schedule < 0 || t->tc_schedule > 3)
+        t->tc_pipelines < 0 || t->tc_pipelines > 2 || t->tc_schedule < 0 || t->tc_schedule > 4)
         return LOOM_ERR_ARG;
     if (t->depth)
         out->depth = t->depth;
@@ -174,12 +174,16 @@ loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned,
         if (!dot_tc_plan(n_rows, (int32_t)k, sms, c, split, &pl))
             return LOOM_ERR_ARG;
         const int64_t grid = batch == 0 ? 0 : pl.grid;
-        // weight units per CTA (at most): a cluster's share of one band, or a share of the list
-        const int64_t per_cta = pl.grid == 0        ? 0
-                                : pl.cluster > 1    ? ceil_div(pl.units_per_band, pl.cluster)
-                                                    : pl.quantum * ceil_div(pl.total_units / pl.quantum, pl.grid);
-        fill_launch(out, grid, (uint32_t)dot_tc_threads(pl.pipes), pl.smem_bytes, (uint32_t)per_cta,
-                    pl.split ? LOOM_KERNEL_DOT_TENSOR_SPLIT : LOOM_KERNEL_DOT_TENSOR);
+        // per CTA (at most): rows of W for the row-block schedule; else 128 x 128 weight
+        // units, a cluster's share of one band or a share of the list
+        const int64_t per_cta = pl.grid == 0                ? 0
+                                : pl.mode == DOT_TC_ROWS    ? pl.rows_per_cta
+                                : pl.cluster > 1            ? ceil_div(pl.units_per_band, pl.cluster)
+                                                            : pl.quantum * ceil_div(pl.total_units / pl.quantum, pl.grid);
+        const uint32_t id = pl.mode == DOT_TC_ROWS ? LOOM_KERNEL_DOT_TENSOR_ROWS
+                            : pl.split             ? LOOM_KERNEL_DOT_TENSOR_SPLIT
+                                                   : LOOM_KERNEL_DOT_TENSOR;
+        fill_launch(out, grid, (uint32_t)dot_tc_threads(pl.pipes), pl.smem_bytes, (uint32_t)per_cta, id);
         out->cluster[0] = (uint32_t)pl.cluster;
         if (plan)
             *plan = pl;
@@ -349,7 +353,8 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
                           sms ? sms : 1, &L, &plan);
         if (st != LOOM_OK)
             return st;
-        const bool tensor = L.kernel == LOOM_KERNEL_DOT_TENSOR || L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT;
+        const bool tensor = L.kernel == LOOM_KERNEL_DOT_TENSOR || L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT ||
+                            L.kernel == LOOM_KERNEL_DOT_TENSOR_ROWS;
         if (tensor && t.tc.schedule == 0 && !dot_tc_cluster_fits(plan)) {
             // the clusters would not all be resident at once: share the units out instead
             DotTcConfig c = t.tc;
@@ -362,8 +367,7 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         if (L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT && workspace_bytes < dot_tc_workspace_bytes(plan))
             return LOOM_ERR_ARG;
         const int depth_used = (int)(t.depth ? t.depth : DOT_DEFAULT_DEPTH);
-        const bool on_tc = L.kernel == LOOM_KERNEL_DOT_TENSOR || L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT;
-        const DotKernel kind = on_tc ? DotKernel::Tensor : dot_select(staged, k, nb);
+        const DotKernel kind = tensor ? DotKernel::Tensor : dot_select(staged, k, nb);
         DotParams p;
         p.w = w;
         p.scale_w = scale_w;

@@ -102,20 +102,26 @@ SMS = 152   # SM count given to the launch configuration (no device is needed th
 
 
 def tc_expect(n_rows, k, split=True, pipes=2):
-    """The tensor-core schedule: a cluster of c CTAs per 128-row band (c = 2..4) when that
-    keeps every SM busy -- or, without a workspace, at least three quarters of them; else
-    one CTA per SM over equal shares of the 128-row x 128-k units (of whole bands without
-    a workspace).  Returns (grid, cluster, units per CTA, split)."""
+    """The tensor-core schedule: ceil(n_rows / SMs) whole rows per CTA when the CTA's
+    blocks (at most 64 rows each) hold 32 rows or more and k has 16 or more 128-byte
+    units; else a cluster of c CTAs per 128-row band (c = 2..4) when that keeps every SM
+    busy -- or, without a workspace, at least three quarters of them; else one CTA per SM
+    over equal shares of the 128-row x 128-k units (of whole bands without a workspace).
+    Returns (grid, cluster, units per CTA, kind)."""
     bands = oracle.workgroups(n_rows, 128)
     ub = oracle.workgroups(k, 128)
+    rpc = oracle.workgroups(n_rows, SMS)
+    blocks = oracle.workgroups(rpc, 64)
+    if pipes == 2 and oracle.workgroups(rpc, blocks) >= 32 and ub >= 16:
+        return oracle.workgroups(n_rows, rpc), 1, rpc, "rows"
     c = min(4, SMS // bands, ub // pipes)
     if c >= 2 and (bands * c == SMS if split else 4 * bands * c >= 3 * SMS):
-        return bands * c, c, oracle.workgroups(ub, c), False
+        return bands * c, c, oracle.workgroups(ub, c), "bands"
     if split:
         grid = min(bands * ub, SMS)
-        return grid, 1, oracle.workgroups(bands * ub, grid), True
+        return grid, 1, oracle.workgroups(bands * ub, grid), "split"
     grid = min(bands, SMS)
-    return grid, 1, ub * oracle.workgroups(bands, grid), False
+    return grid, 1, ub * oracle.workgroups(bands, grid), "bands"
 
 
 def test_dot_launch(loom):
@@ -123,13 +129,18 @@ def test_dot_launch(loom):
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_K
     assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
     wl = [8192, 16384, 16, 1, 0, 0, 0, 0, 1, SMS]
-    # 64 bands: with a workspace, equal shares on every SM (streaming + finishing kernel)
-    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl)
+    # 8192 rows on 152 SMs: 54 whole rows per CTA (one launch, with or without a workspace)
+    for ws in (1, 0):
+        L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl[:8] + [ws, SMS])
+        assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR_ROWS
+        assert L["grid"] == (152, 1, 1) and L["cluster"] == (1, 1, 1) and L["units_per_cta"] == 54
+        assert L["block"] == (896, 1, 1)                            # two pipelines of 14 warps
+        assert 120 * 1024 <= L["smem_bytes"] <= 227 * 1024          # one CTA per SM
+    # asked for: equal shares of the 128 x 128 units on every SM (streaming + finishing kernel)
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl + [0, 0, 0, 2])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR_SPLIT
     assert L["grid"] == (152, 1, 1) and L["cluster"] == (1, 1, 1) and L["units_per_cta"] == 54
-    assert L["block"] == (896, 1, 1)                            # two pipelines of 14 warps
-    assert 120 * 1024 <= L["smem_bytes"] <= 227 * 1024          # one CTA per SM
-    for ws, sched in ((0, 0), (1, 3)):   # no workspace, or asked for: a cluster of two per band
+    for ws, sched in ((0, 3), (1, 3)):   # asked for: a cluster of two per band
         L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl[:8] + [ws, SMS, 0, 0, 0, sched])
         assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR and L["cluster"] == (2, 1, 1)
         assert L["grid"] == (128, 1, 1) and L["units_per_cta"] == 64
@@ -137,6 +148,13 @@ def test_dot_launch(loom):
     assert L["grid"] == (64, 1, 1) and L["units_per_cta"] == 128
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, wl + [0, 0, 1])      # one pipeline
     assert L["grid"] == (152, 1, 1) and L["block"] == (704, 1, 1)   # four converter groups
+    assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR_SPLIT
+    # whole rows asked for where they fill few lanes: 16384 rows -> 108 per CTA, two blocks
+    # of 54; 1000 rows -> 7 per CTA, 143 CTAs
+    for n, grid, per in ((16384, 152, 108), (1000, 143, 7), (9729, 150, 65)):
+        L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [n, 4096, 16, 1, 0, 0, 0, 2, 0, SMS, 0, 0, 0, 4])
+        assert L["kernel"] == loom.LOOM_KERNEL_DOT_TENSOR_ROWS
+        assert (L["grid"][0], L["units_per_cta"]) == (grid, per) == (oracle.workgroups(n, per), per)
     L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8191, 16384, 16, 1, 2, 0, 0, 1])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_B
     assert L["grid"][0] == oracle.workgroups(8191, L["units_per_cta"])
@@ -145,13 +163,15 @@ def test_dot_launch(loom):
             for split in (0, 1):
                 L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT,
                                             [n, k, 5, 1, 0, 0, 0, 0, split, SMS])
-                grid, cl, per, two = tc_expect(n, k, split=bool(split))
-                assert L["kernel"] == (loom.LOOM_KERNEL_DOT_TENSOR_SPLIT if two else loom.LOOM_KERNEL_DOT_TENSOR)
+                grid, cl, per, kind = tc_expect(n, k, split=bool(split))
+                assert L["kernel"] == {"split": loom.LOOM_KERNEL_DOT_TENSOR_SPLIT, "rows": loom.LOOM_KERNEL_DOT_TENSOR_ROWS,
+                                       "bands": loom.LOOM_KERNEL_DOT_TENSOR}[kind], (n, k, split)
                 assert (L["grid"][0], L["cluster"][0], L["units_per_cta"]) == (grid, cl, per), (n, k, split)
     with pytest.raises(loom.LoomError):   # tensor cores forced where k allows no tile
         loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [64, 8, 16, 1, 2, 0, 0, 2])
     # stages, units per stage, A buffers, pipelines, schedule: out of range or not fitting
-    for bad in ([0, 0, 4], [0, 0, 2], [0, 3, 0], [0, 0, 0, 3], [3, 2, 0, 0], [0, 0, 0, 0, 4], [0, 0, 6, 1]):
+    for bad in ([0, 0, 4], [0, 0, 2, 0, 2], [0, 3, 0], [0, 0, 0, 3], [3, 2, 0, 0], [0, 0, 0, 0, 5], [0, 0, 6, 1],
+                [3, 0, 0, 0, 4], [0, 2, 0, 0, 4], [0, 0, 4, 0, 4], [0, 0, 0, 1, 4], [10, 0, 0, 0, 4]):
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT,
                                     [8192, 16384, 16, 1, bad[0], 0, 0, 2, 1, SMS] + bad[1:])

@@ -146,7 +146,8 @@ def test_tensor_core_exact_at_group_bound(env):
 TC_SCHEDULES = [(0, 0, 0, 0, 0), (1, 2, 0, 0, 0), (1, 1, 0, 0, 0), (2, 1, 0, 0, 0), (4, 1, 0, 0, 0),
                 (0, 0, 0, 1, 0), (3, 2, 7, 1, 0), (1, 4, 0, 1, 0), (8, 1, 7, 1, 0), (3, 3, 0, 1, 0),
                 (0, 0, 0, 0, 1), (0, 0, 0, 0, 2), (0, 0, 0, 0, 3), (4, 1, 0, 0, 3), (0, 0, 0, 1, 3),
-                (1, 2, 0, 1, 2), (0, 0, 0, 1, 1)]
+                (1, 2, 0, 1, 2), (0, 0, 0, 1, 1),
+                (0, 0, 0, 0, 4), (2, 0, 0, 0, 4), (4, 1, 3, 2, 4), (8, 0, 2, 0, 4), (6, 0, 3, 0, 4)]
 
 
 @pytest.mark.parametrize("n,k,b", [(384, 8192, 16), (2049, 4112, 16), (128, 1024, 5), (3, 256, 9),
@@ -170,11 +171,34 @@ def test_tensor_core_schedule_invariance(env, n, k, b):
             assert same_bits(y, ref_y), what
 
 
+@pytest.mark.parametrize("n,k,b", [(9729, 2048, 16), (9729, 2048, 5), (10000, 4112, 16), (4864, 2048, 3),
+                                   (1, 16384, 16), (153, 1152, 16)])
+def test_tensor_core_whole_rows(env, n, k, b):
+    # CTAs owning whole rows: two blocks per CTA (9729 rows: 65 per CTA, blocks of 33),
+    # a short last CTA, k tails and k quarters that end past k (zero-filled units), one
+    # row, one row per CTA; the bits of the dp4a kernels and the oracle's integers.
+    torch, loom = env
+    d = small(n, k, b, seed=7 * n + k + b)
+    y, acc = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR, tc_schedule=4))
+    check(d, y, acc, f"rows {n}x{k}x{b}")
+    y2, acc2 = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_STAGED))
+    assert np.array_equal(acc2, acc) and same_bits(y2, y)
+
+
+def test_tensor_core_whole_rows_batches_over_16(env):
+    # Passes of 16, 16 and 1 vectors through the row-block kernel (y rows 33 wide).
+    torch, loom = env
+    d = small(4864, 2048, 33, seed=333)
+    y, acc = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR, tc_schedule=4))
+    check(d, y, acc, "rows b=33")
+
+
 def test_tensor_core_schedules_that_do_not_fit(env):
     torch, loom = env
     d = small(128, 1024, 16, seed=5)
     for depth, ups, na, pipes, sched in [(3, 2, 0, 0, 0), (0, 0, 4, 0, 0), (0, 0, 8, 1, 0), (2, 2, 2, 0, 0),
-                                         (8, 2, 0, 1, 0), (0, 0, 6, 1, 0), (0, 3, 0, 0, 0)]:
+                                         (8, 2, 0, 1, 0), (0, 0, 6, 1, 0), (0, 3, 0, 0, 0), (3, 0, 0, 0, 4),
+                                         (0, 0, 4, 0, 4), (0, 2, 0, 0, 4), (0, 0, 0, 1, 4)]:
         t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_TENSOR, tc_units_per_stage=ups,
                              tc_a_buffers=na, tc_pipelines=pipes, tc_schedule=sched)
         with pytest.raises(loom.LoomError) as e:
@@ -211,12 +235,12 @@ def test_tensor_core_injected_stall(env):
     # The stalled call reports a timeout and NaN outputs (its split bands'
     # records are marked invalid); the next call through the same workspace is exact.
     torch, loom = env
-    for n, k in ((256, 4096), (2049, 4112)):
+    for n, k, sched in ((256, 4096, 0), (2049, 4112, 0), (9729, 2048, 4)):
         d = small(n, k, 16, seed=41 + n)
         ws = loom.dot_workspace(n, k, 16)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         hooks = loom_test_module()
-        t = hooks.make_tuning(wait_ns=2_000_000, path=loom.LOOM_PATH_TENSOR)
+        t = hooks.make_tuning(wait_ns=2_000_000, path=loom.LOOM_PATH_TENSOR, tc_schedule=sched)
         with injected_stall(hooks):
             y, acc = run_dot(hooks, torch, d, tuning=t, error=err, workspace=ws)
         assert int(err.item()) & loom.LOOM_DEVERR_TIMEOUT
@@ -291,7 +315,7 @@ def test_batched_full_workload(env, weights):
     y, acc = run_dot(loom, torch, d)
     check(d, y, acc, "8192 x 16384 x 16")
     # the same bits through the split schedule and through whole bands
-    for sched in (2, 1):
+    for sched in (2, 1, 3):
         y2, acc2 = run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_TENSOR, tc_schedule=sched))
         assert np.array_equal(acc2, acc) and same_bits(y2, y), sched
 
