@@ -69,7 +69,7 @@ typedef enum loom_op {
     LOOM_OP_ROW_SUM_BATCHED = 2, /* workload {num_segments, rows, lanes, staged (0/1), depth,
                                     warps_per_cta, units_per_warp, chunk_bytes} */
     LOOM_OP_I8_DEQUANT_DOT = 3,  /* workload {n_rows, k, batch, staged (0/1), depth,
-                                    warps_per_cta, rows_per_warp, engine (0 auto, 1 dp4a,
+                                    warps_per_cta, ctas_per_sm (batch <= 2 kernel), engine (0 auto, 1 dp4a,
                                     2 tensor), workspace (0/1, default 1), sm_count (0 =
                                     the current device), tc_units_per_stage,
                                     tc_a_buffers, tc_pipelines, tc_schedule} */
@@ -106,7 +106,8 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_UNPACK 1
 #define LOOM_KERNEL_ROWSUM_STAGED 2 /* bulk-copy read-ahead ring per warp */
 #define LOOM_KERNEL_ROWSUM_DIRECT 3 /* plain loads (unaligned inputs) */
-#define LOOM_KERNEL_DOT_STAGED_K 4  /* lanes across k, batch <= 2 */
+#define LOOM_KERNEL_DOT_STAGED_K 4  /* lanes across k, batch <= 2: a block of rows per CTA (units_per_cta =
+                                       rows), its 8 KiB row pieces shared out evenly over the warps */
 #define LOOM_KERNEL_DOT_STAGED_B 5  /* lanes across the batch, batch > 2 */
 #define LOOM_KERNEL_DOT_DIRECT 6    /* plain loads (unaligned or k % 16 != 0) */
 #define LOOM_KERNEL_DOT_TENSOR 7    /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass;

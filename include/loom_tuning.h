@@ -31,8 +31,9 @@ typedef struct loom_tuning {
     int32_t depth;          /* staged chunks in flight per warp (per CTA for the tensor-core
                                dot), 1..LOOM_MAX_DEPTH; 0 = default */
     int32_t path;           /* LOOM_PATH_* */
-    int32_t units_per_warp; /* row sums: segments per warp, 1..32; dot: rows per warp
-                               of the batch <= 2 kernel, 1, 2 or 4; 0 = default */
+    int32_t units_per_warp; /* row sums: segments per warp, 1..32; dot: CTAs per SM of
+                               the batch <= 2 kernel, 1..32 (its rows are spread over
+                               that many CTAs on every SM); 0 = default */
     int32_t warps_per_cta;  /* 1, 2, 4 or 8; 0 = default */
     int32_t chunk_bytes;    /* row sums: bytes per staged chunk, a multiple of 512 in
                                [512, 32768]; 0 = default */

@@ -15,9 +15,11 @@
 //  * Weights stream once through HBM.  Each warp owns its rows and a private
 //    ring of `depth` shared-memory stages filled by bulk copies (the
 //    read-ahead queue); activations are small and stay in L1/L2.
-//  * batch <= 2 ("lanes across k"): every lane takes one 16-byte group of a
-//    row per 512-byte slot, dp4a against the matching activation words held
-//    in registers for several rows, and the warp sums its lanes per row.
+//  * batch <= 2 ("lanes across k"): each CTA owns a block of rows whose 8 KiB
+//    pieces its warps share out evenly; every lane takes one 16-byte group of
+//    a piece per 512-byte slot, dp4a against the matching activation words,
+//    and each warp's share of a row is summed across the warp and added into
+//    the row's total in shared memory.
 //  * batch > 2 ("lanes across the batch"): eight rows per unit; lane b of
 //    each half-warp owns vector b and keeps a slice of its activations in
 //    registers, reused for all eight rows; weight words are read from the
@@ -107,54 +109,84 @@ struct Ring {
 };
 
 // ---------------------------------------------------------------------------
-// batch <= 2: lanes across k.  A warp owns RPW consecutive rows and walks k in
-// chunks of DOT_K_CHUNK_WORDS words; for each chunk it holds the activation
-// words of its lanes in registers (the next chunk's are fetched while the
-// current one is used) and streams that chunk of every row through the ring,
-// so each activation word is loaded once per RPW rows.
-// Lane l takes words 4l..4l+3 of every 128-word slot; each row's partial dot
-// products are summed across the warp at the end.
+// batch <= 2: lanes across k.  CTA c owns rows [c RPC, (c + 1) RPC) for the
+// whole of k.  Its rows are cut into pieces of at most DOT_K_PIECE_WORDS words
+// (8 KiB) of one row, in row order, and warp w of the CTA takes an equal
+// contiguous share of the pieces: every warp of every CTA moves the same
+// number of bytes, whatever k and the number of rows.  A warp streams its
+// pieces through its own ring of `depth` bulk-copied stages.  Lane l takes
+// words 4l..4l+3 of every 128-word slot of a piece, with the matching
+// activation words.  The activations (batch x k bytes, shared by every row)
+// are copied once into the CTA's shared memory when they fit (p.x_in_smem);
+// else they are read through L1, which measured 2 us slower on 8192 x 16384.
+// A warp's share of a row ends in one warp-wide sum, added into the row's
+// int32 total in shared memory; a row that two warps share gets two integer
+// additions, whose order cannot change the sum.
 // ---------------------------------------------------------------------------
-template <int NB, int RPW>
-__global__ void __launch_bounds__(256) dot_staged_k_kernel(const DotParams p)
+template <int NB>
+__global__ void __launch_bounds__(256) dot_rows_k_kernel(const DotParams p)
 {
     dev::follow_previous_kernel();
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int S = DOT_K_CHUNK_WORDS / 128;  // slots per chunk
+    constexpr int SLOTS = DOT_K_PIECE_WORDS / 128;   // 128-word slots per piece
+    constexpr int DOT_K_SLOT_GROUP = 8 / NB;          // slots whose loads are in flight together
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int warps = blockDim.x >> 5;
-    const int32_t r0 = (int32_t)(((int64_t)blockIdx.x * warps + warp) * RPW);
+    const int32_t r0 = (int32_t)blockIdx.x * p.rows_per_cta;
     if (r0 >= p.n_rows)
-        return;
-    const int n = min(RPW, p.n_rows - r0);
+        return;   // over-dispatched CTA
+    const int nr = min(p.rows_per_cta, p.n_rows - r0);
     const int32_t kw = p.k_words;
-    const int32_t nchunks = (kw + DOT_K_CHUNK_WORDS - 1) / DOT_K_CHUNK_WORDS;
+    const int32_t P = (kw + DOT_K_PIECE_WORDS - 1) / DOT_K_PIECE_WORDS;   // pieces per row
+    const int32_t T = nr * P;
+    const int32_t t0 = (int32_t)((int64_t)T * warp / warps);
+    const int32_t t1 = (int32_t)((int64_t)T * (warp + 1) / warps);
     const int D = p.depth;
-    const uint32_t stage_bytes = DOT_K_CHUNK_WORDS * 4;
+    constexpr uint32_t stage_bytes = DOT_K_PIECE_WORDS * 4;
 
+    // shared memory: the warps' rings, their barriers, the activations' barrier,
+    // the row totals [rows_per_cta][NB], then (x_in_smem) the activations
     Ring ring;
     ring.depth = D;
     ring.stage_bytes = stage_bytes;
     ring.data0 = dev::smem_u32(smem) + warp * D * stage_bytes;
     ring.bar0 = dev::smem_u32(smem) + warps * D * stage_bytes + warp * D * 8;
+    const uint32_t xbar = dev::smem_u32(smem) + warps * D * (stage_bytes + 8);
+    int32_t *rsum = reinterpret_cast<int32_t *>(smem + warps * D * (stage_bytes + 8) + 8);
+    const int4 *xs = reinterpret_cast<const int4 *>(smem + dot_k_x_offset(warps, D, p.rows_per_cta));
+    for (int i = threadIdx.x; i < nr * NB; i += blockDim.x)
+        rsum[i] = 0;
     ring.init(lane);
     const uint64_t policy = dev::l2_evict_first_policy();
-    const int32_t total = n * nchunks;   // copy t: chunk t / n of row t % n
+    const uint32_t xbytes = (uint32_t)p.batch * (uint32_t)kw * 4u;
+    if (threadIdx.x == 0 && p.x_in_smem) {
+        dev::mbar_init(xbar, 1);
+        dev::fence_barrier_init();
+        if (!p.inject_stall && xbytes) {
+            dev::mbar_arrive_expect_tx(xbar, xbytes);
+            dev::bulk_g2s(dev::smem_u32(xs), p.x, xbytes, xbar, dev::l2_evict_last_policy());
+        }
+    }
+    __syncthreads();
 
-    int pt = 0;
+    // the first piece of this warp: row rs of the CTA, piece ps of the row
+    const int32_t rs = P ? t0 / P : 0, ps = t0 - rs * P;
+    int32_t pt = t0, pr = rs, pc = ps;   // the producer's next piece
     auto produce = [&]() {
-        if (pt >= total)
+        if (pt >= t1)
             return;
-        const int j = pt / n;
-        const int r = pt - j * n;
-        const int32_t off = j * DOT_K_CHUNK_WORDS;
+        const int32_t off = pc * DOT_K_PIECE_WORDS;
         if (lane == 0 && !p.inject_stall) {
-            const uint32_t bytes = (uint32_t)min(DOT_K_CHUNK_WORDS, kw - off) * 4u;
+            const uint32_t bytes = (uint32_t)min(DOT_K_PIECE_WORDS, kw - off) * 4u;
             dev::mbar_arrive_expect_tx(ring.pbar(), bytes);
-            dev::bulk_g2s(ring.pstage(), p.w + (int64_t)(r0 + r) * kw + off, bytes, ring.pbar(), policy);
+            dev::bulk_g2s(ring.pstage(), p.w + (int64_t)(r0 + pr) * kw + off, bytes, ring.pbar(), policy);
         }
         ++pt;
+        if (++pc == P) {
+            pc = 0;
+            ++pr;
+        }
         ring.pnext();
     };
     for (int s = 0; s < D; ++s)
@@ -164,79 +196,86 @@ __global__ void __launch_bounds__(256) dot_staged_k_kernel(const DotParams p)
     const int4 *x4[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
-        x4[b] = reinterpret_cast<const int4 *>(p.x + (int64_t)(b < p.batch ? b : 0) * kw);
+        x4[b] = (p.x_in_smem ? xs : reinterpret_cast<const int4 *>(p.x)) + (int64_t)(b < p.batch ? b : 0) * (kw >> 2);
     const unsigned char *ring_base = smem + (size_t)warp * D * stage_bytes;
-
-    auto load_x = [&](int j, int4 (&xv)[NB][S]) {
-        const int32_t off = j * DOT_K_CHUNK_WORDS;
-        const int32_t m = min(DOT_K_CHUNK_WORDS, kw - off);
+    int32_t acc[NB];
 #pragma unroll
-        for (int s = 0; s < S; ++s) {
-            const int32_t e = lane * 4 + 128 * s;
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                xv[b][s] = e < m ? __ldg(x4[b] + ((off + e) >> 2)) : make_int4(0, 0, 0, 0);
+    for (int b = 0; b < NB; ++b)
+        acc[b] = 0;
+    int32_t cr = rs, cc = ps;   // the consumer's piece
+    bool failed = false;
+    // the activations must have landed (a stalled test run issued no copy: its wait runs out)
+    if (p.x_in_smem && t0 < t1 && xbytes && !__all_sync(FULL_MASK, dev::mbar_wait_bounded(xbar, 0, p.wait_ns)))
+        failed = true;
+    for (int32_t t = t0; t < t1 && !failed; ++t) {
+        if (!ring.wait(p.wait_ns)) {
+            failed = true;
+            break;
         }
-    };
-
-    int32_t acc[RPW][NB];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
+        const int32_t off = cc * DOT_K_PIECE_WORDS;
+        const int32_t m = min(DOT_K_PIECE_WORDS, kw - off);
+        const int4 *s4 = reinterpret_cast<const int4 *>(ring_base + ring.cs * stage_bytes) + lane;
+        const int4 *xl[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b)
-            acc[r][b] = 0;
-
-    int4 xv[NB][S];
-    if (nchunks > 0)
-        load_x(0, xv);
-    bool failed = false;
-    for (int j = 0; j < nchunks && !failed; ++j) {
-        const int32_t m = min(DOT_K_CHUNK_WORDS, kw - j * DOT_K_CHUNK_WORDS);
-        int4 xn[NB][S];
-        if (j + 1 < nchunks)
-            load_x(j + 1, xn);   // next chunk's activations, in flight during this one
+            xl[b] = x4[b] + (off >> 2) + lane;
+        // activation words: from shared memory, or through L1
+        auto xload = [&](const int4 *a) { return p.x_in_smem ? *a : __ldg(a); };
+        if (m == DOT_K_PIECE_WORDS) {
+            // a whole piece: no bounds tests, so the loads of a group of slots issue together
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            if (r < n && !failed) {
-                if (!ring.wait(p.wait_ns)) {
-                    failed = true;
-                } else {
-                    const int4 *s4 = reinterpret_cast<const int4 *>(ring_base + ring.cs * stage_bytes);
+            for (int g = 0; g < SLOTS; g += DOT_K_SLOT_GROUP) {
+                int4 wv[DOT_K_SLOT_GROUP], xv[NB][DOT_K_SLOT_GROUP];
 #pragma unroll
-                    for (int s = 0; s < S; ++s) {
-                        const int32_t e = lane * 4 + 128 * s;
-                        if (e < m) {
-                            const int4 wv = s4[e >> 2];
+                for (int s = 0; s < DOT_K_SLOT_GROUP; ++s) {
+                    wv[s] = s4[32 * (g + s)];
 #pragma unroll
-                            for (int b = 0; b < NB; ++b)
-                                dp4a4(acc[r][b], wv, xv[b][s]);
-                        }
-                    }
-                    ring.cnext();
-                    produce();
+                    for (int b = 0; b < NB; ++b)
+                        xv[b][s] = xload(xl[b] + 32 * (g + s));
+                }
+#pragma unroll
+                for (int s = 0; s < DOT_K_SLOT_GROUP; ++s)
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        dp4a4(acc[b], wv[s], xv[b][s]);
+            }
+        } else {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                if (lane * 4 + 128 * s < m) {
+                    const int4 wv = s4[32 * s];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        dp4a4(acc[b], wv, xload(xl[b] + 32 * s));
                 }
             }
         }
-        if (j + 1 < nchunks) {
+        ring.cnext();
+        produce();
+        // this warp's share of row cr ends here: add it to the row's total
+        if (cc + 1 == P || t + 1 == t1) {
 #pragma unroll
-            for (int s = 0; s < S; ++s)
-#pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    xv[b][s] = xn[b][s];
+            for (int b = 0; b < NB; ++b) {
+                const int32_t sum = dev::warp_sum_i32(acc[b]);
+                if (lane == 0)
+                    atomicAdd(rsum + cr * NB + b, sum);
+                acc[b] = 0;
+            }
+        }
+        if (++cc == P) {
+            cc = 0;
+            ++cr;
         }
     }
     if (failed) {
         dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
         ring.drain(p.wait_ns, !p.inject_stall);
     }
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int32_t sum = dev::warp_sum_i32(acc[r][b]);
-            if (r < n && lane == b && b < p.batch)
-                store_result(p, r0 + r, b, sum, !failed);
-        }
+    const bool valid = !__syncthreads_or(failed);
+    for (int i = threadIdx.x; i < nr * NB; i += blockDim.x) {
+        const int r = i / NB, b = i - r * NB;
+        if (b < p.batch)
+            store_result(p, r0 + r, b, rsum[i], valid);
     }
 }
 
@@ -383,16 +422,6 @@ __global__ void __launch_bounds__(256, 1) dot_direct_kernel(const DotParams p)
     }
 }
 
-template <int NB>
-cudaError_t launch_staged_k(const DotParams &p, const loom_launch &L, cudaStream_t stream)
-{
-    if (p.rows_per_warp >= 4)
-        return launch_with(dot_staged_k_kernel<NB, 4>, L, stream, p);
-    if (p.rows_per_warp == 2 || p.rows_per_warp == 3)
-        return launch_with(dot_staged_k_kernel<NB, 2>, L, stream, p);
-    return launch_with(dot_staged_k_kernel<NB, 1>, L, stream, p);
-}
-
 // ---------------------------------------------------------------------------
 // Unpack: one thread per packed word, 256-thread CTAs.
 // ---------------------------------------------------------------------------
@@ -426,23 +455,28 @@ DotKernel dot_select(bool aligned, int32_t k, int32_t batch_pass)
     return batch_pass <= 2 ? DotKernel::StagedK : DotKernel::StagedB;
 }
 
-int dot_rows_per_warp(DotKernel kind, int tuned)
+int64_t dot_rows_per_cta(DotKernel kind, int64_t n_rows, int warps, int ctas_per_sm, int64_t sms)
 {
     switch (kind) {
-    case DotKernel::StagedK:   // 1, 2 or 4 rows (other requests round down)
-        return tuned >= 4 ? 4 : tuned >= 2 ? 2 : tuned == 1 ? 1 : DOT_K_DEFAULT_ROWS;
+    case DotKernel::StagedK: {
+        // ceil(n_rows / (CTAs per SM x SMs)) rows, so that one wave holds every row
+        const int64_t ctas = (int64_t)(ctas_per_sm ? ctas_per_sm : DOT_K_DEFAULT_CTAS_PER_SM) * (sms > 0 ? sms : 1);
+        int64_t rpc = (n_rows + ctas - 1) / ctas;
+        rpc = rpc < 1 ? 1 : rpc;
+        return rpc > DOT_K_MAX_ROWS_PER_CTA ? DOT_K_MAX_ROWS_PER_CTA : rpc;
+    }
     case DotKernel::StagedB:
-        return DOT_B_ROWS;
+        return (int64_t)warps * DOT_B_ROWS;
     default:
-        return 1;
+        return warps;
     }
 }
 
-uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps)
+uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps, int64_t rows_per_cta)
 {
     switch (kind) {
-    case DotKernel::StagedK:
-        return (uint32_t)(warps * depth * (DOT_K_CHUNK_WORDS * 4 + 8));
+    case DotKernel::StagedK:   // rings, barriers, row totals (the activations are added by the caller)
+        return dot_k_x_offset(warps, depth, rows_per_cta);
     case DotKernel::StagedB:
         return (uint32_t)(warps * depth * ((DOT_B_ROWS + DOT_MAX_BATCH_PER_PASS) * DOT_B_CHUNK_WORDS * 4 + 8));
     default:
@@ -459,7 +493,7 @@ cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L,
     case DotKernel::Tensor:
         return cudaErrorInvalidValue;   // launched by launch_dot_tc with its schedule
     case DotKernel::StagedK:
-        return nb == 1 ? launch_staged_k<1>(p, L, stream) : launch_staged_k<2>(p, L, stream);
+        return nb == 1 ? launch_with(dot_rows_k_kernel<1>, L, stream, p) : launch_with(dot_rows_k_kernel<2>, L, stream, p);
     case DotKernel::StagedB:
         return launch_with(dot_staged_b_kernel<16>, L, stream, p);
     default:

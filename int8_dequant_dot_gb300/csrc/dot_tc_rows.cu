@@ -19,12 +19,14 @@
 //    another.  The B operand has 32 columns, the 16 vectors over the first
 //    range and then over the second; of a lane's 32 accumulator columns the
 //    16 of its own range are the wanted sums, the other 16 (cross terms) are
-//    never read.  k is cut into four quarters of whole 128-byte units;
-//    pipeline p of the CTA's two takes quarters 2p (lanes 0..63) and 2p + 1
-//    (lanes 64..127).
-//  * A pipeline: a producer thread (per stage, 2-D TMA copies of one 128-byte
-//    unit of k of the block's rows in both of its quarters, 128-byte swizzle,
-//    and the two matching 16 x 128-byte activation boxes); two converter
+//    never read.  k is cut into two halves of whole 128-byte units, one per
+//    pipeline of the CTA; a stage of a pipeline holds two neighbouring units
+//    of its half, the first for lanes 0..63 and the second for lanes 64..127
+//    (each row then reads 256 contiguous bytes per stage), so over the stages
+//    each lane half sums every other unit of the pipeline's half.
+//  * A pipeline: a producer thread (per stage, 2-D TMA copies of the two
+//    128-byte units of k of the block's rows, 128-byte swizzle, and the two
+//    matching 16 x 128-byte activation boxes); two converter
 //    groups of four warps taking alternate stages (each thread one tensor-
 //    memory lane: int8 -> f16 of one row's 128 bytes into tensor memory with
 //    tcgen05.st, and two 16-byte pieces of activations into the 128-byte-
@@ -36,8 +38,8 @@
 //    every integer); the epilogue converts each finished accumulator to int32
 //    and adds it to its running sums, so acc is exact for any k.
 //  * At the end of a block the eight epilogue warps of the CTA put their
-//    int32 sums of the four quarters in shared memory; each row's four are
-//    added, scaled and stored.
+//    int32 sums of the four parts of k (two pipelines x two lane halves) in
+//    shared memory; each row's four are added, scaled and stored.
 //  * Every wait is bounded; a wait that runs out sets LOOM_DEVERR_TIMEOUT,
 //    every role stops at its next wait, issued copies and MMAs are allowed to
 //    finish, tensor memory is freed and the affected outputs are NaN (acc
@@ -71,7 +73,7 @@ constexpr uint32_t RB_ACC_COLS = RB_N;          // one f32 accumulator
 constexpr uint32_t RB_X_BOX = RB_VEC * RB_KU;   // 2 KiB of activations per range and unit
 constexpr uint32_t RB_B_BYTES = RB_N * RB_KU * 2;   // f16 B tile of one stage, 8 KiB
 constexpr uint32_t RB_B_KBLOCK = RB_N * 128;        // bytes of one 64-k block of the B tile
-constexpr uint32_t RB_MERGE_BYTES = 4 * RB_MAX_ROWS * RB_VEC * 4;   // int32 [quarter][row][vector]
+constexpr uint32_t RB_MERGE_BYTES = 4 * RB_MAX_ROWS * RB_VEC * 4;   // int32 [part of k][row][vector]
 constexpr uint32_t RB_AREA = 1024;              // tensor-memory slot, abort word, vector scales
 constexpr uint32_t RB_EPI_BAR = 1;              // named barrier of the CTA's eight epilogue warps
 constexpr uint32_t RB_IDESC = tc::idesc_f16(128, RB_N);
@@ -87,7 +89,7 @@ struct RowsParams {
     int32_t n_rows, batch, y_stride;
     int32_t rpc;          // rows per CTA
     int32_t br;           // rows per block (the weight boxes' height), <= 64
-    int32_t uq;           // 128-byte units of k per quarter
+    int32_t uq;           // stages per block of each pipeline (two 128-byte units of k each)
     int32_t depth;        // shared-memory stages per pipeline (even)
     int32_t na, ng;       // f16 A buffers and f32 accumulators per pipeline
     uint32_t wbox;        // shared memory of one weight box (1024-aligned)
@@ -149,19 +151,27 @@ __device__ __forceinline__ bool epi_barrier_and(bool v)
     return r != 0;
 }
 
-// A 16-byte piece of activations (16 int8 of vector row nn at k = 16 c8 of the
-// unit) -> f16 into row nn of the K-major 128-byte-swizzled B tile.
-__device__ __forceinline__ void put_b(uint32_t btile, int nn, int c8, const int4 &v)
+// Where a 16-byte piece of activations -- 16 int8 of B row nn at k = 16 c8 of
+// the unit -- goes as f16 in the K-major 128-byte-swizzled B tile: the row's
+// offset in the tile and the offsets of its two 16-byte chunks within the row.
+struct BPiece {
+    uint32_t row, c0, c1;
+    __device__ BPiece(int nn, int c8)
+        : row((uint32_t)(c8 >> 2) * RB_B_KBLOCK + (uint32_t)(nn >> 3) * 1024 + (uint32_t)(nn & 7) * 128),
+          c0((uint32_t)((2 * (c8 & 3)) ^ (nn & 7)) << 4), c1((uint32_t)((2 * (c8 & 3) + 1) ^ (nn & 7)) << 4)
+    {
+    }
+};
+
+__device__ __forceinline__ void put_b(uint32_t at, const BPiece &bp, const int4 &v)
 {
     uint32_t h[8];
     tc::i8x4_to_f16x4((uint32_t)v.x, h[0], h[1]);
     tc::i8x4_to_f16x4((uint32_t)v.y, h[2], h[3]);
     tc::i8x4_to_f16x4((uint32_t)v.z, h[4], h[5]);
     tc::i8x4_to_f16x4((uint32_t)v.w, h[6], h[7]);
-    const uint32_t row = btile + (uint32_t)(c8 >> 2) * RB_B_KBLOCK + (uint32_t)(nn >> 3) * 1024 + (uint32_t)(nn & 7) * 128;
-    const int c0 = 2 * (c8 & 3);
-    tc::sts128(row + (((c0) ^ (nn & 7)) << 4), h[0], h[1], h[2], h[3]);
-    tc::sts128(row + (((c0 + 1) ^ (nn & 7)) << 4), h[4], h[5], h[6], h[7]);
+    tc::sts128(at + bp.c0, h[0], h[1], h[2], h[3]);
+    tc::sts128(at + bp.c1, h[4], h[5], h[6], h[7]);
 }
 
 __global__ void __launch_bounds__(RB_THREADS, 1)
@@ -188,8 +198,7 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
     const int32_t rc = min(q.rpc, q.n_rows - r0);
     const int nblk = (rc + BR - 1) / BR;
     const int J = nblk * UQ;
-    const int32_t kq0 = (2 * p) * UQ * RB_KU;       // first byte of k of this pipeline's two quarters
-    const int32_t kq1 = (2 * p + 1) * UQ * RB_KU;
+    const int32_t kp = p * (2 * UQ) * RB_KU;     // first byte of k of this pipeline's half
 
     // ---- set-up: barriers, flags, tensor memory ------------------------------
     // Each producer initialises its pipeline's barriers and at once issues the
@@ -199,16 +208,25 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
     // kernel on the stream has completed (wait_previous_kernel).
     const uint64_t wpol = dev::l2_evict_first_policy();
     const uint64_t xpol = dev::l2_evict_last_policy();   // activations: re-read by every CTA
-    auto issue = [&](int j) {
-        const int s = j % S;
-        const int b = j / UQ;
-        const int32_t xu = (j - b * UQ) * RB_KU;
-        const int32_t row = r0 + b * BR;
-        dev::mbar_arrive_expect_tx(P.full(s), 2u * (uint32_t)BR * RB_KU + 2u * RB_X_BOX);
-        tc::tma_load_2d(P.wtile(s, 0), &tmw, kq0 + xu, row, P.full(s), wpol);
-        tc::tma_load_2d(P.wtile(s, 1), &tmw, kq1 + xu, row, P.full(s), wpol);
-        tc::tma_load_2d(P.xtile(s, 0), &tmx, kq0 + xu, 0, P.full(s), xpol);
-        tc::tma_load_2d(P.xtile(s, 1), &tmx, kq1 + xu, 0, P.full(s), xpol);
+    // The producer's cursor: slot, block and unit of the next stage.  Every
+    // role walks the stages with counters like these (no division per stage).
+    int ps = 0, pb = 0, pu = 0;
+    auto issue_next = [&]() {
+        const int32_t k0 = kp + 2 * pu * RB_KU;   // the stage's two units of k, side by side
+        const int32_t row = r0 + pb * BR;
+        if (!q.inject_stall) {
+            dev::mbar_arrive_expect_tx(P.full(ps), 2u * (uint32_t)BR * RB_KU + 2u * RB_X_BOX);
+            tc::tma_load_2d(P.wtile(ps, 0), &tmw, k0, row, P.full(ps), wpol);
+            tc::tma_load_2d(P.wtile(ps, 1), &tmw, k0 + RB_KU, row, P.full(ps), wpol);
+            tc::tma_load_2d(P.xtile(ps, 0), &tmx, k0, 0, P.full(ps), xpol);
+            tc::tma_load_2d(P.xtile(ps, 1), &tmx, k0 + RB_KU, 0, P.full(ps), xpol);
+        }
+        if (++pu == UQ) {
+            pu = 0;
+            ++pb;
+        }
+        if (++ps == S)
+            ps = 0;
     };
     int issued = 0;
     if (w == PRODUCER) {
@@ -221,9 +239,11 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
         dev::fence_barrier_init();
         __syncwarp();
         dev::wait_previous_kernel();
-        if (lane == 0 && !q.inject_stall)
-            for (; issued < S && issued < J; ++issued)
-                issue(issued);
+        if (lane == 0)
+            for (int j = 0; j < S && j < J; ++j) {
+                issue_next();
+                issued += q.inject_stall ? 0 : 1;
+            }
     }
     if (threadIdx.x == 0)
         asm volatile("st.shared.u32 [%0], 0;" ::"r"(abort_word) : "memory");
@@ -242,20 +262,20 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
     const uint32_t acc_col = (uint32_t)NA * RB_A_COLS;
     const uint32_t tl = (uint32_t)(32 * sub) << 16;   // this warp's lanes in a tensor-memory address
     const int L = 32 * sub + lane;                     // this thread's lane
-    const int half = L >> 6;                           // lanes 0..63: the first quarter, 64..127: the second
+    const int half = L >> 6;                           // lanes 0..63: a stage's first unit, 64..127: its second
     const int r = L & 63;                              // row within the block
 
     if (w == PRODUCER) {
         // ---- producer: the stages past the first S as the converters free them ----
         if (lane == 0) {
+            uint32_t eph = 0;   // parity of the converters' release of slot ps: ((j / S) - 1) & 1
             for (int j = S; j < J; ++j) {
-                const int s = j % S;
-                if (!tc::role_wait(abort_word, q.error, q.wait_ns, P.empty(s), ((j / S) - 1) & 1))
+                if (!tc::role_wait(abort_word, q.error, q.wait_ns, P.empty(ps), eph))
                     break;
-                if (!q.inject_stall) {
-                    issue(j);
-                    ++issued;
-                }
+                issue_next();
+                issued += q.inject_stall ? 0 : 1;
+                if (ps == 0)
+                    eph ^= 1u;
             }
             // every copy issued must land before the CTA may leave (bounded)
             for (int j = issued > S ? issued - S : 0; j < issued; ++j)
@@ -311,32 +331,35 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
         __syncwarp();
     } else if (w < EPI0) {
         // ---- converters: group h takes stages h, h + 2, ...; thread = lane L ------
-        // Weight row r of quarter (2p + half), and the activation pieces
-        // (vector L / 8, 16-byte chunk L % 8) of both quarters.
+        // Weight row r of the stage's unit `half`, and the activation pieces
+        // (vector L / 8, 16-byte chunk L % 8) of both units.
         const int h = w >> 2;
         const int n = L >> 3, c8 = L & 7;
+        const uint32_t roff = (uint32_t)r * RB_KU, rsw = (uint32_t)(r & 7) << 4;   // 128-byte swizzle
+        const uint32_t xoff = (uint32_t)n * RB_KU + (uint32_t)c8 * 16;
+        const BPiece bp(n, c8);   // rows n and 16 + n: the same chunk offsets, 2 KiB apart
+        int s = h, a = h, qa = 0;   // slot (j % S), A buffer (j % NA) and j / NA of stage j
+        uint32_t fph = 0;           // (j / S) & 1
         for (int j = h; j < J; j += RB_GROUPS) {
-            const int s = j % S;
-            if (!tc::warp_wait(abort_word, q.error, q.wait_ns, P.full(s), (j / S) & 1))
+            if (!tc::warp_wait(abort_word, q.error, q.wait_ns, P.full(s), fph))
                 break;
             int4 wv[8];
             if (r < BR) {
-                const uint32_t wrow = P.wtile(s, half) + (uint32_t)r * RB_KU;   // 128-byte swizzle
+                const uint32_t wrow = P.wtile(s, half) + roff;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    wv[c] = tc::lds128(wrow + ((c ^ (r & 7)) << 4));
+                    wv[c] = tc::lds128(wrow + (((uint32_t)c << 4) ^ rsw));
             } else {
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     wv[c] = make_int4(0, 0, 0, 0);
             }
-            const int4 xa = tc::lds128(P.xtile(s, 0) + (uint32_t)n * RB_KU + c8 * 16);
-            const int4 xb = tc::lds128(P.xtile(s, 1) + (uint32_t)n * RB_KU + c8 * 16);
+            const int4 xa = tc::lds128(P.xtile(s, 0) + xoff);
+            const int4 xb = tc::lds128(P.xtile(s, 1) + xoff);
             __syncwarp();
             if (lane == 0)
                 tc::mbar_arrive(P.empty(s));   // this warp is done with stage s
-            const int a = j % NA;
-            if (j >= NA && !tc::warp_wait(abort_word, q.error, q.wait_ns, P.afree(a), ((j / NA) - 1) & 1))
+            if (j >= NA && !tc::warp_wait(abort_word, q.error, q.wait_ns, P.afree(a), (uint32_t)(qa & 1) ^ 1u))
                 break;
             tc::fence_after();
             // A operand: 128 f16 of this lane's row -> 64 columns of buffer a
@@ -353,20 +376,30 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
                 }
                 tc::st16(tmem + tl + (uint32_t)a * RB_A_COLS + part * 16, v);
             }
-            // B operand: vector n over the first quarter is row n, over the second row 16 + n
-            put_b(P.btile(a), n, c8, xa);
-            put_b(P.btile(a), RB_VEC + n, c8, xb);
+            // B operand: vector n over the first unit is row n, over the second row 16 + n
+            put_b(P.btile(a) + bp.row, bp, xa);
+            put_b(P.btile(a) + bp.row + 2 * 1024, bp, xb);
             tc::wait_st();
             tc::fence_async_smem();
             tc::fence_before();
             __syncwarp();
             if (lane == 0)
                 tc::mbar_arrive(P.aready(a));
+            s += RB_GROUPS;
+            if (s >= S) {
+                s -= S;
+                fph ^= 1u;
+            }
+            a += RB_GROUPS;
+            if (a >= NA) {
+                a -= NA;
+                ++qa;
+            }
         }
     } else {
-        // ---- epilogue warps: accumulators -> int32 sums -> the four quarters
+        // ---- epilogue warps: accumulators -> int32 sums -> the four parts of k
         // of each row added in shared memory -> scaled outputs ---------------------
-        const int qtr = 2 * p + half;
+        const int part = 2 * p + half;   // which part of k this lane summed
         const int t = p * (32 * RB_EPI_WARPS) + (w - EPI0) * 32 + lane;   // 0..255 over the CTA
         const int orow = t >> 2;          // output row within the block
         const int ovec = 4 * (t & 3);     // its first of four vectors
@@ -376,7 +409,8 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
             asm volatile("st.shared.f32 [%0], %1;" ::"r"(sx_at + 4 * lane), "f"(v) : "memory");
         }
         bool ok = true;
-        int g = 0;
+        int gs = 0;            // accumulator of the next group (g % NG)
+        uint32_t gph = 0;      // (g / NG) & 1
         for (int b = 0; b < nblk; ++b) {
             const int32_t row = r0 + b * BR + orow;
             const bool live = orow < BR && b * BR + orow < rc;
@@ -385,26 +419,31 @@ __global__ void __launch_bounds__(RB_THREADS, 1)
 #pragma unroll
             for (int v = 0; v < RB_VEC; ++v)
                 isum[v] = 0;
-            for (int u0 = 0; u0 < UQ; u0 += RB_UNITS_PER_GROUP, ++g) {
+            for (int u0 = 0; u0 < UQ; u0 += RB_UNITS_PER_GROUP) {
+                const int cur = gs;
+                const uint32_t ph = gph;
+                if (++gs == NG) {
+                    gs = 0;
+                    gph ^= 1u;
+                }
                 if (!ok)
                     continue;
-                const int gs = g % NG;
-                if (!tc::warp_wait(abort_word, q.error, q.wait_ns, P.gfull(gs), (g / NG) & 1)) {
+                if (!tc::warp_wait(abort_word, q.error, q.wait_ns, P.gfull(cur), ph)) {
                     ok = false;
                     continue;
                 }
                 tc::fence_after();
                 uint32_t v[16];
-                tc::ld16(tmem + tl + acc_col + (uint32_t)gs * RB_ACC_COLS + RB_VEC * half, v);
+                tc::ld16(tmem + tl + acc_col + (uint32_t)cur * RB_ACC_COLS + RB_VEC * half, v);
 #pragma unroll
                 for (int i = 0; i < RB_VEC; ++i)
                     isum[i] += __float2int_rn(__uint_as_float(v[i]));
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    tc::mbar_arrive(P.gfree(gs));
+                    tc::mbar_arrive(P.gfree(cur));
             }
-            const uint32_t mine = merge + (uint32_t)((qtr * RB_MAX_ROWS + r) * RB_VEC) * 4;
+            const uint32_t mine = merge + (uint32_t)((part * RB_MAX_ROWS + r) * RB_VEC) * 4;
 #pragma unroll
             for (int i = 0; i < RB_VEC; i += 4)
                 tc::sts128(mine + 4 * i, (uint32_t)isum[i], (uint32_t)isum[i + 1], (uint32_t)isum[i + 2],
@@ -478,8 +517,8 @@ cudaError_t rows_smem_limit()
 // (even, 2..8; 0 = the deepest of 4 and 2 that fits), a_bufs (2 or 3; 0 = 2);
 // units_per_stage must be 0 or 1 and pipes 0 or 2.  Unless `forced`, the
 // schedule is taken only where it fills at least half the tensor-memory
-// lanes (32 or more rows per block) and k has at least 16 units (each quarter
-// at least four).
+// lanes (32 or more rows per block) and k has at least 16 units (each
+// pipeline at least four stages).
 bool dot_tc_rows_plan(int64_t n_rows, int32_t k, int64_t sms, const DotTcConfig &cfg, bool forced,
                       DotTcPlan *out)
 {
@@ -490,7 +529,7 @@ bool dot_tc_rows_plan(int64_t n_rows, int32_t k, int64_t sms, const DotTcConfig 
     const int64_t nblk = (rpc + RB_MAX_ROWS - 1) / RB_MAX_ROWS;
     const int64_t br = (rpc + nblk - 1) / nblk;
     const int32_t ub = (k + RB_KU - 1) / RB_KU;
-    const int32_t uq = (ub + 3) / 4;
+    const int32_t uq = (ub + 3) / 4;   // stages per block: two units each, in each of two pipelines
     if (!forced && (br < RB_MAX_ROWS / 2 || ub < 16))
         return false;
     const int na = cfg.a_bufs ? cfg.a_bufs : 2;
@@ -532,7 +571,7 @@ bool dot_tc_rows_plan(int64_t n_rows, int32_t k, int64_t sms, const DotTcConfig 
     out->sm_count = sms;
     out->rows_per_cta = (int32_t)rpc;
     out->block_rows = (int32_t)br;
-    out->units_per_quarter = uq;
+    out->stages_per_block = uq;
     out->wbox = wbox;
     out->stage_bytes = stage;
     return true;
@@ -561,7 +600,7 @@ cudaError_t launch_dot_tc_rows(const DotParams &p, const DotTcPlan &plan, cudaSt
     q.y_stride = p.y_stride;
     q.rpc = plan.rows_per_cta;
     q.br = plan.block_rows;
-    q.uq = plan.units_per_quarter;
+    q.uq = plan.stages_per_block;
     q.depth = plan.depth;
     q.na = plan.na;
     q.ng = plan.ng;

@@ -44,9 +44,13 @@ cudaError_t launch_row_sum(const RowSumParams &p, bool staged, const loom_launch
                            cudaStream_t stream);
 
 // ---- dequantised dot -----------------------------------------------------
-constexpr int DOT_DEFAULT_WARPS = 2;     // warps per CTA of the staged kernels
-constexpr int DOT_K_DEFAULT_ROWS = 4;     // lanes-across-k path: rows per warp
-constexpr int DOT_K_CHUNK_WORDS = 1024;   // lanes-across-k path: 4 KiB of one row
+constexpr int DOT_DEFAULT_WARPS = 2;     // warps per CTA of the lanes-across-batch kernel
+constexpr int DOT_K_DEFAULT_WARPS = 8;    // lanes-across-k kernel: warps per CTA ...
+constexpr int DOT_K_DEFAULT_CTAS_PER_SM = 2;   // ... and CTAs per SM, and ...
+constexpr int DOT_K_DEFAULT_DEPTH = 1;    // ... stages per warp: 16 one-stage rings of 8 KiB per SM
+constexpr uint32_t DOT_K_X_SMEM_MAX = 64 * 1024;   // activations staged in shared memory up to this
+constexpr int DOT_K_PIECE_WORDS = 2048;   // lanes-across-k kernel: a piece is 8 KiB of one row
+constexpr int DOT_K_MAX_ROWS_PER_CTA = 1024;
 constexpr int DOT_B_ROWS = 8;             // lanes-across-batch path: rows per warp
 constexpr int DOT_B_CHUNK_WORDS = 128;    // ... 512 B of each of those rows per chunk
 constexpr int DOT_MAX_BATCH_PER_PASS = 16;
@@ -63,7 +67,8 @@ struct DotParams {
     int32_t *acc;          // same layout as y, or NULL
     int32_t *error;
     int32_t depth;
-    int32_t rows_per_warp;  // lanes-across-k path
+    int32_t rows_per_cta;   // lanes-across-k kernel
+    int32_t x_in_smem;      // lanes-across-k kernel: activations copied into shared memory
     uint64_t wait_ns;
     int32_t inject_stall;
     void *workspace;        // tensor-core path: split-band workspace, or NULL
@@ -73,8 +78,25 @@ struct DotParams {
 enum class DotKernel { StagedK, StagedB, Direct, Tensor };
 
 DotKernel dot_select(bool aligned, int32_t k, int32_t batch_pass);
-uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps);
-int dot_rows_per_warp(DotKernel kind, int tuned_rows_per_warp);
+uint32_t dot_smem_bytes(DotKernel kind, int depth, int warps, int64_t rows_per_cta);
+// Default ring depth of a dp4a kernel.
+inline int dot_default_depth(DotKernel kind) { return kind == DotKernel::StagedK ? DOT_K_DEFAULT_DEPTH : DOT_DEFAULT_DEPTH; }
+// Lanes-across-k kernel: whether batch x k activation bytes are staged in shared
+// memory behind `smem` bytes of rings and totals.
+inline bool dot_k_x_fits(uint32_t smem, int64_t batch, int64_t k)
+{
+    return batch * k <= (int64_t)DOT_K_X_SMEM_MAX && smem + batch * k <= 227 * 1024;
+}
+// Lanes-across-k kernel: offset of the activations in shared memory (rings,
+// barriers, row totals in front), also the size of everything before them.
+__host__ __device__ inline uint32_t dot_k_x_offset(int warps, int depth, int64_t rows_per_cta)
+{
+    return ((uint32_t)(warps * depth * (DOT_K_PIECE_WORDS * 4 + 8) + 8 + rows_per_cta * 2 * 4) + 15u) & ~15u;
+}
+// Rows per CTA of a dp4a kernel: the lanes-across-k kernel spreads the rows over
+// ctas_per_sm (0 = default) CTAs on each of `sms` SMs; the others take a fixed
+// number of rows per warp.
+int64_t dot_rows_per_cta(DotKernel kind, int64_t n_rows, int warps, int ctas_per_sm, int64_t sms);
 cudaError_t launch_dot(const DotParams &p, DotKernel kind, const loom_launch &L, cudaStream_t stream);
 
 // tensor-core path (dot_tc.cu): a persistent grid of one CTA per SM splits
@@ -98,7 +120,7 @@ struct DotTcPlan {
     bool split;               // bands may be split between CTAs (needs the workspace)
     int64_t sm_count;         // SMs the grid was sized for
     // row-block schedule (mode DOT_TC_ROWS, dot_tc_rows.cu)
-    int32_t rows_per_cta, block_rows, units_per_quarter;
+    int32_t rows_per_cta, block_rows, stages_per_block;
     uint32_t wbox, stage_bytes;
 };
 // mode of a DotTcPlan whose CTAs each own whole rows (dot_tc_rows.cu); the

@@ -148,8 +148,10 @@ loom_status row_sum_geometry(int64_t num_segments, int64_t rows, int64_t lanes, 
 
 // engine: 0 = automatic, 1 = dp4a kernels only, 2 = tensor cores.  For the
 // tensor-core kernel `tc` holds its schedule (tc.depth = stages), `split`
-// whether a workspace lets bands be split between CTAs, and `sms` the SM
-// count the persistent grid is sized for; *plan receives the schedule.
+// whether a workspace lets bands be split between CTAs.  `sms` is the SM
+// count the grid is sized for (0 = the current device's, read when the
+// kernel needs it); *plan receives the tensor-core schedule.  For the
+// lanes-across-k kernel `rows_per_warp` is its CTAs per SM (0 = default).
 loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned, int64_t depth,
                          int64_t warps, int64_t rows_per_warp, int64_t engine, const DotTcConfig &tc,
                          bool split, int64_t sms, loom_launch *out, DotTcPlan *plan)
@@ -157,16 +159,20 @@ loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned,
     if (n_rows < 0 || n_rows > 0x7fffffff || k < 0 || k > MAX_K || (k % 4) != 0 || batch < 0 ||
         batch > 0x7fffffff)
         return LOOM_ERR_SHAPE;
-    if (warps == 0)
-        warps = DOT_DEFAULT_WARPS;
-    if (depth < 0 || depth > LOOM_MAX_DEPTH || !valid_warps(warps) || rows_per_warp < 0 ||
-        rows_per_warp > 32 || engine < 0 || engine > 2)
+    if (depth < 0 || depth > LOOM_MAX_DEPTH || (warps != 0 && !valid_warps(warps)) || rows_per_warp < 0 ||
+        rows_per_warp > 32 || engine < 0 || engine > 2 || sms < 0)
         return LOOM_ERR_ARG;
     const int32_t pass = (int32_t)(batch < DOT_MAX_BATCH_PER_PASS ? batch : DOT_MAX_BATCH_PER_PASS);
     const bool tc_ok = dot_tc_eligible(aligned, (int32_t)k, pass);
     const bool use_tc = (engine == 2 || (engine == 0 && pass >= 3)) && tc_ok;
     if (engine == 2 && !tc_ok)
         return aligned ? LOOM_ERR_SHAPE : LOOM_ERR_ALIGN;
+    const DotKernel kind = use_tc ? DotKernel::Tensor : dot_select(aligned, (int32_t)k, pass);
+    if (sms == 0 && (kind == DotKernel::Tensor || kind == DotKernel::StagedK)) {
+        const loom_status st = current_sm_count(&sms);   // both grids are sized by the device
+        if (st != LOOM_OK)
+            return st;
+    }
     if (use_tc) {
         DotTcPlan pl;
         DotTcConfig c = tc;
@@ -190,15 +196,23 @@ loom_status dot_geometry(int64_t n_rows, int64_t k, int64_t batch, bool aligned,
         return LOOM_OK;
     }
     if (depth == 0)
-        depth = DOT_DEFAULT_DEPTH;
-    const DotKernel kind = dot_select(aligned, (int32_t)k, pass);
-    const int64_t rows_per_cta = warps * dot_rows_per_warp(kind, (int)rows_per_warp);
+        depth = dot_default_depth(kind);
+    if (warps == 0)   // lanes across k: at most 128 KiB of rings per CTA whatever the depth
+        warps = kind != DotKernel::StagedK ? DOT_DEFAULT_WARPS
+                : depth <= 2               ? DOT_K_DEFAULT_WARPS
+                : depth <= 4               ? DOT_K_DEFAULT_WARPS / 2
+                                           : DOT_K_DEFAULT_WARPS / 4;
+    const int64_t rows_per_cta = dot_rows_per_cta(kind, n_rows, (int)warps, (int)rows_per_warp, sms);
     const int64_t grid = (batch == 0) ? 0 : ceil_div(n_rows, rows_per_cta);
+    uint32_t smem = dot_smem_bytes(kind, (int)depth, (int)warps, rows_per_cta);
+    if (kind == DotKernel::StagedK && dot_k_x_fits(smem, pass, k))
+        smem += (uint32_t)(pass * k);   // the activations, staged in shared memory
+    if (smem > 227 * 1024)
+        return LOOM_ERR_ARG;
     const uint32_t id = kind == DotKernel::StagedK   ? LOOM_KERNEL_DOT_STAGED_K
                         : kind == DotKernel::StagedB ? LOOM_KERNEL_DOT_STAGED_B
                                                      : LOOM_KERNEL_DOT_DIRECT;
-    fill_launch(out, grid, (uint32_t)warps * 32, dot_smem_bytes(kind, (int)depth, (int)warps),
-                (uint32_t)rows_per_cta, id);
+    fill_launch(out, grid, (uint32_t)warps * 32, smem, (uint32_t)rows_per_cta, id);
     return LOOM_OK;
 }
 
@@ -339,8 +353,8 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
     }
     const int32_t kw = k / 4;
     int64_t sms = 0;
-    if (staged && k >= 16 && (k % 16) == 0 && engine != 1) {
-        st = current_sm_count(&sms);   // the tensor-core grid is sized by the device
+    if (staged) {
+        st = current_sm_count(&sms);   // the tensor-core and lanes-across-k grids are sized by the device
         if (st != LOOM_OK)
             return st;
     }
@@ -349,8 +363,7 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         const int32_t nb = (int32_t)((batch - b0) < DOT_MAX_BATCH_PER_PASS ? (batch - b0) : DOT_MAX_BATCH_PER_PASS);
         loom_launch L;
         DotTcPlan plan;
-        st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, engine, t.tc, split,
-                          sms ? sms : 1, &L, &plan);
+        st = dot_geometry(n_rows, k, nb, staged, t.depth, t.warps, t.upw, engine, t.tc, split, sms, &L, &plan);
         if (st != LOOM_OK)
             return st;
         const bool tensor = L.kernel == LOOM_KERNEL_DOT_TENSOR || L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT ||
@@ -366,8 +379,8 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         // the first pass is the widest, so a short workspace stops the call before any launch
         if (L.kernel == LOOM_KERNEL_DOT_TENSOR_SPLIT && workspace_bytes < dot_tc_workspace_bytes(plan))
             return LOOM_ERR_ARG;
-        const int depth_used = (int)(t.depth ? t.depth : DOT_DEFAULT_DEPTH);
         const DotKernel kind = tensor ? DotKernel::Tensor : dot_select(staged, k, nb);
+        const int depth_used = (int)(t.depth ? t.depth : dot_default_depth(kind));
         DotParams p;
         p.w = w;
         p.scale_w = scale_w;
@@ -381,7 +394,9 @@ loom_status dot_common(const int32_t *w, const float *scale_w, int32_t n_rows, i
         p.acc = acc ? acc + b0 : nullptr;
         p.error = error;
         p.depth = depth_used;
-        p.rows_per_warp = kind == DotKernel::Tensor ? 0 : (int32_t)(L.units_per_cta / (L.block[0] / 32));
+        p.rows_per_cta = kind == DotKernel::Tensor ? 0 : (int32_t)L.units_per_cta;
+        p.x_in_smem = kind == DotKernel::StagedK &&
+                      dot_k_x_fits(dot_smem_bytes(kind, depth_used, (int)(L.block[0] / 32), L.units_per_cta), nb, k);
         p.wait_ns = t.wait_ns;
         p.inject_stall = t.stall;
         p.workspace = workspace;
@@ -828,16 +843,9 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         if (sms < 0 || sms > 4096)
             return LOOM_ERR_ARG;
         const bool aligned = opt(3, 1) != 0;
-        const int64_t pass = workload[2] < DOT_MAX_BATCH_PER_PASS ? workload[2] : DOT_MAX_BATCH_PER_PASS;
-        if (sms == 0 && aligned && workload[1] % 16 == 0 && workload[1] >= 16 &&
-            (opt(7, 0) == 2 || (opt(7, 0) == 0 && pass >= 3))) {
-            const loom_status st = current_sm_count(&sms);
-            if (st != LOOM_OK)
-                return st;
-        }
         const DotTcConfig tc{0, (int32_t)opt(10, 0), (int32_t)opt(11, 0), (int32_t)opt(12, 0), (int32_t)opt(13, 0)};
         return dot_geometry(workload[0], workload[1], workload[2], aligned, opt(4, 0), opt(5, 0),
-                            opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms ? sms : 1, out, nullptr);
+                            opt(6, 0), opt(7, 0), tc, opt(8, 1) != 0, sms, out, nullptr);
     }
     case LOOM_OP_STAGE_ROWS:
         if (n_workload < 3)

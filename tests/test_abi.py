@@ -125,9 +125,16 @@ def tc_expect(n_rows, k, split=True, pipes=2):
 
 
 def test_dot_launch(loom):
-    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 1])
+    # one vector: 2 CTAs of 8 one-stage warps on every SM, ceil(8192 / 304) = 27 rows each;
+    # shared memory: 8 rings of 8 KiB and their barriers, the activations' barrier, the
+    # row totals (rounded to 16 bytes) and the 16 KiB of activations
+    L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [8192, 16384, 1, 1, 0, 0, 0, 0, 1, SMS])
     assert L["kernel"] == loom.LOOM_KERNEL_DOT_STAGED_K
-    assert L["grid"][0] == oracle.workgroups(8192, L["units_per_cta"])
+    assert L["units_per_cta"] == 27 and L["grid"][0] == oracle.workgroups(8192, 27) == 304
+    assert L["block"] == (256, 1, 1) and L["smem_bytes"] == 8 * (8192 + 8) + 8 + 27 * 2 * 4 + 16384
+    for n, ctas, rows in ((8192, 1, 54), (8192, 2, 27), (37, 3, 1), (10**6, 3, 1024)):
+        L = loom.loom_launch_config(loom.LOOM_OP_I8_DEQUANT_DOT, [n, 4096, 2, 1, 0, 0, ctas, 0, 1, SMS])
+        assert (L["units_per_cta"], L["grid"][0]) == (rows, oracle.workgroups(n, rows)), (n, ctas)
     wl = [8192, 16384, 16, 1, 0, 0, 0, 0, 1, SMS]
     # 8192 rows on 152 SMs: 54 whole rows per CTA (one launch, with or without a workspace)
     for ws in (1, 0):

@@ -112,6 +112,21 @@ def test_dot_path_and_depth_invariance(env):
         assert np.array_equal(acc, ref_acc) and np.array_equal(y.view(np.int32), ref_y.view(np.int32))
 
 
+@pytest.mark.parametrize("n,k,b", [(37, 16400, 1), (300, 8192, 2), (5, 48, 1), (1000, 4096, 1), (2, 32784, 2)])
+def test_lanes_across_k_schedule_invariance(env, n, k, b):
+    # Blocks of rows per CTA whose 8 KiB pieces the warps share out (rows split between
+    # warps, ragged last pieces, fewer pieces than warps): any warps per CTA, CTAs per SM
+    # and ring depth give the default's bits and the oracle's integers.
+    torch, loom = env
+    d = small(n, k, b, seed=5 * n + k + b)
+    ref_y, ref_acc = run_dot(loom, torch, d)
+    check(d, ref_y, ref_acc, f"lanes across k {n}x{k}x{b}")
+    for warps, ctas, depth in ((1, 1, 1), (2, 3, 2), (4, 1, 4), (8, 2, 2), (4, 7, 3), (8, 32, 1), (1, 16, 8)):
+        t = loom.make_tuning(depth=depth, warps_per_cta=warps, units_per_warp=ctas, path=loom.LOOM_PATH_STAGED)
+        y, acc = run_dot(loom, torch, d, tuning=t)
+        assert np.array_equal(acc, ref_acc) and same_bits(y, ref_y), (warps, ctas, depth)
+
+
 @pytest.mark.parametrize("n,k,b", [(128, 1024, 16), (129, 1040, 3), (300, 2064, 7), (5, 16, 16),
                                    (257, 16384, 16), (64, 131056, 16), (130, 128, 4), (2049, 4112, 16)])
 def test_tensor_core_matches_dp4a_bitwise(env, n, k, b):
