@@ -122,6 +122,9 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_ROUTED_STAGED 13  /* routed combine: bulk-copy ring of payload pieces per warp */
 #define LOOM_KERNEL_ROUTED_DIRECT 14  /* routed combine: plain loads */
 #define LOOM_KERNEL_STAGE_ROWS 15     /* upload of ragged rows: one CTA per 8 KiB of a segment */
+#define LOOM_KERNEL_ROWSUM_SEGMENTS 17 /* 32-lane segments of at most 64 rows: one bulk copy and
+                                          one wait per segment, a ring of `depth` 8 KiB stages
+                                          per warp; the same bits as LOOM_KERNEL_ROWSUM_STAGED */
 #define LOOM_KERNEL_DOT_TENSOR_ROWS 16 /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass; one
                                           CTA per SM owning whole rows (units_per_cta = rows),
                                           two k ranges per MMA; one launch, no workspace */

@@ -58,6 +58,7 @@ LOOM_KERNEL_ROUTED_STAGED = 13
 LOOM_KERNEL_ROUTED_DIRECT = 14
 LOOM_KERNEL_STAGE_ROWS = 15
 LOOM_KERNEL_DOT_TENSOR_ROWS = 16
+LOOM_KERNEL_ROWSUM_SEGMENTS = 17
 
 LOOM_MAX_DEPTH = 8
 LOOM_PATH_AUTO = 0

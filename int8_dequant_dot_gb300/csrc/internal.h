@@ -38,8 +38,14 @@ struct RowSumParams {
     int32_t inject_stall;   // test hook: issue no copies (every wait runs out)
 };
 
+// One-copy-per-segment kernel (32-lane rows): a byte ring per warp holding whole
+// segments, `depth` of them in flight.
+constexpr int RS_SEG_RING_BYTES = 8192;         // default ring: one segment of up to 64 rows, or several shorter
+constexpr int RS_SEG_DEFAULT_DEPTH = 4;
+constexpr int RS_SEG_DEFAULT_UNITS_PER_WARP = 8;
 int row_sum_default_units_per_warp(int32_t rows, int32_t lanes);
 uint32_t row_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems);
+uint32_t row_sum_seg_smem_bytes(int depth, int warps, int ring_bytes);
 cudaError_t launch_row_sum(const RowSumParams &p, bool staged, const loom_launch &L,
                            cudaStream_t stream);
 

@@ -119,30 +119,42 @@ loom_status current_sm_count(int64_t *sms)
 
 // ---- geometry of each op ----------------------------------------------------
 
+// depth or chunk_bytes of 0 take the kernel's default; *depth_out and
+// *chunk_out (may be NULL) receive the values used.
 loom_status row_sum_geometry(int64_t num_segments, int64_t rows, int64_t lanes, bool staged,
                              int64_t depth, int64_t upw, int64_t warps, int64_t chunk_bytes,
-                             loom_launch *out)
+                             loom_launch *out, int32_t *depth_out = nullptr, int32_t *chunk_out = nullptr)
 {
     if (num_segments < 0 || rows < 0 || (lanes != 1 && lanes != 32) || rows * lanes >= (1ll << 31))
         return LOOM_ERR_SHAPE;
     if (warps == 0)
         warps = lanes == 1 ? RS_DEFAULT_WARPS_WIDE : RS_DEFAULT_WARPS;
+    // 32-lane segments whose active rows fit the ring (chunk_bytes, default 8 KiB) take
+    // one copy each; with a smaller chunk size they stream in chunks
+    const bool segs = staged && lanes == 32 && rows * 128 <= (chunk_bytes ? chunk_bytes : RS_SEG_RING_BYTES);
     if (chunk_bytes == 0)
-        chunk_bytes = default_chunk_bytes(rows, lanes);
+        chunk_bytes = segs ? RS_SEG_RING_BYTES : default_chunk_bytes(rows, lanes);
+    if (depth == 0)
+        depth = segs ? RS_SEG_DEFAULT_DEPTH : RS_DEFAULT_DEPTH;
     if (depth < 1 || depth > LOOM_MAX_DEPTH || upw < 0 || upw > 32 || !valid_warps(warps) ||
         !valid_chunk(chunk_bytes))
         return LOOM_ERR_ARG;
     if (upw == 0)
-        upw = row_sum_default_units_per_warp((int32_t)rows, (int32_t)lanes);
+        upw = segs ? RS_SEG_DEFAULT_UNITS_PER_WARP : row_sum_default_units_per_warp((int32_t)rows, (int32_t)lanes);
     const int64_t per_cta = warps * upw;
     const int64_t grid = ceil_div(num_segments, per_cta);
     if (grid > 0x7fffffff)
         return LOOM_ERR_SHAPE;
-    const uint32_t smem = row_sum_smem_bytes(staged, (int)depth, (int)warps, (int)(chunk_bytes / 4));
+    const uint32_t smem = segs ? row_sum_seg_smem_bytes((int)depth, (int)warps, (int)chunk_bytes)
+                               : row_sum_smem_bytes(staged, (int)depth, (int)warps, (int)(chunk_bytes / 4));
     if (smem > 227 * 1024)
         return LOOM_ERR_ARG;
     fill_launch(out, grid, (uint32_t)warps * 32, smem, (uint32_t)per_cta,
-                staged ? LOOM_KERNEL_ROWSUM_STAGED : LOOM_KERNEL_ROWSUM_DIRECT);
+                segs ? LOOM_KERNEL_ROWSUM_SEGMENTS : staged ? LOOM_KERNEL_ROWSUM_STAGED : LOOM_KERNEL_ROWSUM_DIRECT);
+    if (depth_out)
+        *depth_out = (int32_t)depth;
+    if (chunk_out)
+        *chunk_out = (int32_t)chunk_bytes;
     return LOOM_OK;
 }
 
@@ -232,7 +244,7 @@ loom_status row_sum_common(const float *values, int64_t num_segments, int64_t se
     if (num_segments > 1 && seg_stride > 0 && num_segments - 1 > (INT64_MAX - rows * (int64_t)lanes) / seg_stride)
         return LOOM_ERR_SHAPE;
     Tuning t;
-    loom_status st = read_tuning(tuning, RS_DEFAULT_DEPTH, &t);
+    loom_status st = read_tuning(tuning, 0, &t);   // depth 0: the kernel's own default
     if (st != LOOM_OK)
         return st;
     if (num_segments == 0)
@@ -256,7 +268,9 @@ loom_status row_sum_common(const float *values, int64_t num_segments, int64_t se
         staged = can_stage;
     }
     loom_launch L;
-    st = row_sum_geometry(num_segments, rows, lanes, staged, t.depth, t.upw, t.warps, t.chunk_bytes, &L);
+    int32_t depth = 0, chunk_bytes = 0;
+    st = row_sum_geometry(num_segments, rows, lanes, staged, t.depth, t.upw, t.warps, t.chunk_bytes, &L, &depth,
+                          &chunk_bytes);
     if (st != LOOM_OK)
         return st;
 
@@ -276,9 +290,9 @@ loom_status row_sum_common(const float *values, int64_t num_segments, int64_t se
     p.full_sum = full_sum;
     p.tail_sum = tail_sum;
     p.error = error;
-    p.depth = t.depth;
+    p.depth = depth;
     p.units_per_warp = (int32_t)(L.units_per_cta / (L.block[0] / 32));
-    p.chunk_elems = (int32_t)((t.chunk_bytes ? t.chunk_bytes : default_chunk_bytes(rows, lanes)) / 4);
+    p.chunk_elems = chunk_bytes / 4;
     p.wait_ns = t.wait_ns;
     p.inject_stall = t.stall;
     cudaError_t e = launch_row_sum(p, staged, L, static_cast<cudaStream_t>(stream));
@@ -830,12 +844,12 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         if (n_workload < 2)
             return LOOM_ERR_ARG;
         return row_sum_geometry(1, workload[0], workload[1], opt(2, 1) != 0,
-                                opt(3, RS_DEFAULT_DEPTH), 1, opt(4, 0), opt(5, 0), out);
+                                opt(3, 0), 1, opt(4, 0), opt(5, 0), out);
     case LOOM_OP_ROW_SUM_BATCHED:
         if (n_workload < 3)
             return LOOM_ERR_ARG;
         return row_sum_geometry(workload[0], workload[1], workload[2], opt(3, 1) != 0,
-                                opt(4, RS_DEFAULT_DEPTH), opt(6, 0), opt(5, 0), opt(7, 0), out);
+                                opt(4, 0), opt(6, 0), opt(5, 0), opt(7, 0), out);
     case LOOM_OP_I8_DEQUANT_DOT: {
         if (n_workload < 3)
             return LOOM_ERR_ARG;

@@ -329,6 +329,179 @@ __global__ void __launch_bounds__(256, MINB) row_sum_kernel(const RowSumParams p
     }
 }
 
+// ---------------------------------------------------------------------------
+// Segments of 32-lane rows that fit the ring (128 * rows <= ring bytes): one
+// bulk copy per segment.  A warp owns `units_per_warp` consecutive segments
+// and a byte ring of p.chunk_elems floats in shared memory.  The active prefix
+// of each segment (128 c bytes) goes whole into the ring behind the previous
+// one, or at the ring's start when it would cross the end; up to `depth`
+// segments are in flight (one mbarrier each, so depth 1 is the serial
+// control), so short segments keep more copies in flight than fixed stages
+// would, and the small ring leaves room for many warps per SM.  The warp
+// waits once per segment and issues the next copies as soon as space frees.
+// Lane l takes float4 l & 7 of rows (l >> 3) + 4i, i.e. the float4s at byte
+// 16 l + 512 i of the segment -- the element-to-lane mapping and per-lane
+// order of LaneSums::chunk -- with rows below F going to the full-tile sums
+// and the others to the tail sums; the folding and the warp reduction are
+// those of row_sum_kernel, so both kernels (and the direct path) return
+// identical bits.  Error-free sums make the kernel bound by instruction
+// issue, so the per-segment work is kept to one wait, two row loops and the
+// ring bookkeeping.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256, 3) row_sum_seg_kernel(const RowSumParams p)
+{
+    dev::follow_previous_kernel();
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int warps = blockDim.x >> 5;
+    const int64_t u0 = ((int64_t)blockIdx.x * warps + warp) * p.units_per_warp;
+    if (u0 >= p.num_units)
+        return;  // over-dispatched warp: no loads, no stores
+    const int n = (int)min((int64_t)p.units_per_warp, p.num_units - u0);
+
+    // Lane k describes segment u0 + k (units_per_warp <= 32).
+    int32_t c = 0, F = 0;
+    float init = 0.f;
+    if (lane < n) {
+        const int32_t raw = p.counts ? __ldg(p.counts + u0 + lane) : p.count_scalar;
+        c = min(max(raw, 0), p.rows);
+        if (c != raw)
+            dev::flag_error(p.error, LOOM_DEVERR_COUNT_RANGE);
+        init = p.initial ? __ldg(p.initial + u0 + lane) : p.initial_scalar;
+        F = (c / p.tile) * p.tile;   // full-tile rows
+    }
+
+    const int Q = p.depth;                          // segments in flight
+    const uint32_t R = (uint32_t)p.chunk_elems * 4u;   // ring bytes
+    unsigned char *ring = smem + (size_t)warp * (R + ((8u * Q + 15u) & ~15u));   // 16-byte aligned rings
+    const uint32_t ring0 = dev::smem_u32(ring);
+    const uint32_t bar0 = ring0 + R;
+    if (lane == 0) {
+        for (int s = 0; s < Q; ++s)
+            dev::mbar_init(bar0 + 8 * s, 1);
+        dev::fence_barrier_init();
+    }
+    __syncwarp();
+    const uint64_t policy = dev::l2_evict_first_policy();
+
+    // Where a segment of `sz` bytes goes after the byte `cur`: behind it, or
+    // at the start when it would cross the end.  Producer and consumer apply
+    // the same rule, so the consumer finds every segment without a record.
+    auto place = [R](uint32_t cur, uint32_t sz) { return cur + sz > R ? 0u : cur; };
+    uint32_t wpos = 0;     // producer: end of the last segment issued
+    int pj = 0, ps = 0;    // producer: next segment, its barrier
+    uint32_t rpos = 0;     // start of the oldest segment not yet summed (segment k)
+    int k = 0;
+    // Issue every next segment that fits: at most Q in flight, and its bytes
+    // clear of the segments not yet summed (those occupy [rpos, wpos) around
+    // the ring).  An empty segment moves nothing; its barrier phase is
+    // completed by an arrival that expects no bytes.
+    auto produce = [&]() {
+        while (pj < n && pj - k < Q) {
+            const uint32_t sz = (uint32_t)__shfl_sync(FULL_MASK, c, pj) * 128u;
+            const uint32_t pos = place(wpos, sz);
+            const bool fits = pj == k || (rpos < wpos ? (pos == wpos || sz <= rpos)
+                                                      : (pos == wpos && wpos + sz <= rpos));
+            if (!fits)
+                break;
+            if (lane == 0) {
+                if (sz == 0) {
+                    dev::mbar_arrive_expect_tx(bar0 + 8 * ps, 0);
+                } else if (!p.inject_stall) {
+                    dev::mbar_arrive_expect_tx(bar0 + 8 * ps, sz);
+                    dev::bulk_g2s(ring0 + pos, p.values + (u0 + pj) * p.unit_stride, sz, bar0 + 8 * ps, policy);
+                }
+            }
+            wpos = pos + sz;
+            ++pj;
+            ps = (ps + 1 == Q) ? 0 : ps + 1;
+        }
+    };
+    produce();
+
+    int cs = 0;            // consumer's barrier
+    uint32_t cphase = 0;   // parity of the phase the consumer waits for
+    int failed_at = n;     // first segment whose data never arrived
+    DW2 pend0{0, 0}, pend1{0, 0}, pend2{0, 0}, pend3{0, 0};   // folded partials of a group of 4
+    const int g = lane >> 3;   // this lane's rows: g, g + 4, ...
+    for (; k < n;) {
+        const int32_t kc = __shfl_sync(FULL_MASK, c, k);
+        const int32_t kF = __shfl_sync(FULL_MASK, F, k);
+        const float kinit = __shfl_sync(FULL_MASK, init, k);
+        LaneSums acc;
+        acc.reset(lane == 0 ? kinit : 0.f);
+        const bool landed = dev::mbar_wait_bounded(bar0 + 8 * cs, cphase, p.wait_ns);
+        if (!__all_sync(FULL_MASK, landed)) {
+            failed_at = k;
+            break;
+        }
+        const float4 *s4 = reinterpret_cast<const float4 *>(ring + rpos) + lane;
+        const int nf = kF > g ? (kF - g + 3) >> 2 : 0;   // this lane's full-tile rows
+        const int na = kc > g ? (kc - g + 3) >> 2 : 0;   // ... and all its active rows
+        int i = 0;
+#pragma unroll 2
+        for (; i < nf; ++i)
+            acc.full4(s4[32 * i]);
+#pragma unroll 2
+        for (; i < na; ++i)
+            acc.tail4(s4[32 * i]);
+        __syncwarp();
+        // segment k is summed: its bytes are free, the next one is the oldest
+        const uint32_t end = rpos + (uint32_t)kc * 128u;
+        ++k;
+        rpos = k < n ? place(end, (uint32_t)__shfl_sync(FULL_MASK, c, k) * 128u) : end;
+        cs = (cs + 1 == Q) ? 0 : cs + 1;
+        cphase ^= (cs == 0) ? 1u : 0u;
+        produce();
+        const DW2 ft = acc.fold();
+        const int q = (k - 1) & 3;
+        if (q == 0)
+            pend0 = ft;
+        else if (q == 1)
+            pend1 = ft;
+        else if (q == 2)
+            pend2 = ft;
+        else
+            pend3 = ft;
+        if (q == 3 || k == n) {
+            const DW2 z{0, 0};
+            finish_group(p, lane, u0 + ((k - 1) & ~3), q + 1, pend0, q >= 1 ? pend1 : z, q >= 2 ? pend2 : z,
+                         q >= 3 ? pend3 : z);
+        }
+    }
+
+    if (failed_at < n) {
+        dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+        // Segments of the unfinished group before the failure still get their sums.
+        const int q = failed_at & 3;
+        if (q > 0) {
+            const DW2 z{0, 0};
+            finish_group(p, lane, u0 + (failed_at & ~3), q, pend0, q >= 2 ? pend1 : z, q >= 3 ? pend2 : z, z);
+        }
+        // Let copies already in flight land before the warp leaves (bounded).
+        if (!p.inject_stall) {
+            int s = cs;
+            uint32_t ph = cphase;
+            for (int j = failed_at; j < pj; ++j) {
+                dev::mbar_wait_bounded(bar0 + 8 * s, ph, p.wait_ns);
+                s = (s + 1 == Q) ? 0 : s + 1;
+                ph ^= (s == 0) ? 1u : 0u;
+            }
+        }
+        if (lane >= failed_at && lane < n) {
+            p.full_sum[u0 + lane] = __int_as_float(0x7fc00000);
+            p.tail_sum[u0 + lane] = __int_as_float(0x7fc00000);
+        }
+    }
+
+    if (lane < n) {
+        const int64_t u = u0 + lane;
+        p.final_row[u] = F;
+        p.tail_count[u] = c - F;
+    }
+}
+
 }  // namespace
 
 int row_sum_default_units_per_warp(int32_t rows, int32_t lanes)
@@ -354,11 +527,18 @@ uint32_t row_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems)
     return (uint32_t)(warps * depth * (chunk_elems * 4 + 8));
 }
 
+uint32_t row_sum_seg_smem_bytes(int depth, int warps, int ring_bytes)
+{
+    return (uint32_t)(warps * (ring_bytes + ((8 * depth + 15) & ~15)));
+}
+
 cudaError_t launch_row_sum(const RowSumParams &p, bool staged, const loom_launch &L,
                            cudaStream_t stream)
 {
     if (L.grid[0] == 0)
         return cudaSuccess;
+    if (L.kernel == LOOM_KERNEL_ROWSUM_SEGMENTS)
+        return launch_with(row_sum_seg_kernel, L, stream, p);
     const bool small_units = (int64_t)p.rows * p.lanes <= 4096;
     if (staged)
         return small_units ? launch_with(row_sum_kernel<true, 3>, L, stream, p)

@@ -79,7 +79,11 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
         L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes])
         assert L["grid"][0] == oracle.workgroups(s, L["units_per_cta"])
         assert L["block"][0] % 32 == 0 and L["subgroup_size"] == 32
-        assert L["kernel"] == loom.LOOM_KERNEL_ROWSUM_STAGED
+        # 32-lane segments of at most 64 rows: one bulk copy per segment, 8 per warp
+        segs = lanes == 32 and rows <= 64
+        assert L["kernel"] == (loom.LOOM_KERNEL_ROWSUM_SEGMENTS if segs else loom.LOOM_KERNEL_ROWSUM_STAGED)
+        if segs:   # a ring of 8 KiB and four barriers: four segments in flight
+            assert L["units_per_cta"] == 8 and L["smem_bytes"] == 8192 + 4 * 8
         d = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes, 0])
         assert d["kernel"] == loom.LOOM_KERNEL_ROWSUM_DIRECT and d["smem_bytes"] == 0
     # one stage of 4 KiB plus one barrier per warp and depth
@@ -87,7 +91,10 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
         for warps in (1, 2, 4, 8):
             for chunk in (512, 4096, 8192):
                 wl = [10, rows, lanes, 1, depth, warps, 0, chunk]
-                want = warps * depth * (chunk + 8)   # depth stages of one chunk + one barrier each
+                if lanes == 32 and rows * 128 <= chunk:   # one ring of `chunk` bytes, `depth` barriers
+                    want = warps * (chunk + (8 * depth + 15) // 16 * 16)   # rings 16-byte aligned
+                else:                                     # depth stages of one chunk + one barrier each
+                    want = warps * depth * (chunk + 8)
                 if want > 227 * 1024:   # more than a CTA may hold
                     with pytest.raises(loom.LoomError):
                         loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, wl)
@@ -95,7 +102,8 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
                 L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, wl)
                 assert L["smem_bytes"] == want and L["block"][0] == 32 * warps
     L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [10, rows, lanes, 1, 1, 1])
-    assert L["smem_bytes"] == (4096 if rows * lanes <= 4096 else 8192) + 8
+    segs = lanes == 32 and rows <= 64   # an 8 KiB ring and one barrier (16-byte aligned); else chunks
+    assert L["smem_bytes"] == (8192 + 16 if segs else (4096 if rows * lanes <= 4096 else 8192) + 8)
 
 
 SMS = 152   # SM count given to the launch configuration (no device is needed then)
