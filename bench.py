@@ -118,7 +118,8 @@ def recorded_traffic():
 #: the source files each workload's kernels are built from
 KERNEL_SOURCES = {
     "segments": ("row_sum.cu",), "wide": ("row_sum.cu",),
-    "gemv": ("dequant_dot.cu",), "batched": ("dot_tc.cu",), "packed": ("packed_dot.cu",),
+    "gemv": ("dequant_dot.cu",), "batched": ("dot_tc.cu", "dot_tc_rows.cu", "tc_ptx.cuh"),
+    "packed": ("packed_dot.cu",),
     "sum_rows": ("lane_sum.cu",), "sum_vector_rows": ("lane_sum.cu",), "guarded_rows": ("lane_sum.cu",),
     "routed": ("routed.cu",),
 }

@@ -75,7 +75,7 @@ typedef enum loom_op {
                                     tc_a_buffers, tc_pipelines, tc_schedule} */
     LOOM_OP_PACKED_DOT = 4,      /* workload {problems, records, lanes, streams, aligned (0/1:
                                     inputs 16-byte aligned, default 1), depth,
-                                    records_per_stage} */
+                                    records_per_stage, sm_count (0 = the current device)} */
     LOOM_OP_LANE_SUMS = 5,       /* workload {num_segments, rows, lanes, width (1 or 4), aligned
                                     (0/1, default 1), depth, warps_per_cta, units_per_warp,
                                     chunk_bytes}; also the guarded rows (width 4) */
@@ -115,7 +115,8 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_TENSOR_SPLIT 8 /* the same kernel over equal shares of all units, then
                                           a finishing kernel for the bands split between CTAs
                                           (two launches per pass) */
-#define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: 3-D TMA read-ahead ring per CTA */
+#define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: one CTA per SM over tiles of 256 lanes
+                                        (units_per_cta = tiles), one 3-D TMA read-ahead ring */
 #define LOOM_KERNEL_PACKED_DIRECT 10 /* packed dot: plain loads */
 #define LOOM_KERNEL_LANESUM_STAGED 11 /* per-lane sums: bulk-copy read-ahead ring per warp */
 #define LOOM_KERNEL_LANESUM_DIRECT 12 /* per-lane sums: plain loads */

@@ -42,7 +42,7 @@ struct RowSumParams {
 // segments, `depth` of them in flight.
 constexpr int RS_SEG_RING_BYTES = 8192;         // default ring: one segment of up to 64 rows, or several shorter
 constexpr int RS_SEG_DEFAULT_DEPTH = 4;
-constexpr int RS_SEG_DEFAULT_UNITS_PER_WARP = 8;
+constexpr int RS_SEG_DEFAULT_UNITS_PER_WARP = 4;   // measured best of 1..32 (4.3 waves of resident warps)
 int row_sum_default_units_per_warp(int32_t rows, int32_t lanes);
 uint32_t row_sum_smem_bytes(bool staged, int depth, int warps, int chunk_elems);
 uint32_t row_sum_seg_smem_bytes(int depth, int warps, int ring_bytes);
@@ -201,12 +201,11 @@ uint32_t routed_smem_bytes(bool staged, int depth, int warps);
 cudaError_t launch_routed(const RoutedParams &p, bool staged, const loom_launch &L, cudaStream_t stream);
 
 // ---- the pages' packed-dot example (packed_dot.cu) ---------------------------
-constexpr int PD_DEFAULT_DEPTH = 2;        // stages of the read-ahead ring (measured best on GB300)
-constexpr int PD_DEFAULT_RPS = 12;         // records per stage: 48 KiB stages, two CTAs per SM
+constexpr int PD_DEFAULT_DEPTH = 3;        // stages of the read-ahead ring ...
+constexpr int PD_DEFAULT_RPS = 12;         // ... of 12 records (30 KiB): two CTAs per SM (measured best)
 constexpr int PD_MAX_RPS = 32;
 constexpr int PD_MAX_STAGED_STREAMS = 64;  // one TMA box row holds every stream of a record
-constexpr int PD_LANES_PER_CTA = 256;      // direct path
-constexpr int PD_STAGED_LANES_PER_CTA = 512;   // staged path: two lanes per consumer thread
+constexpr int PD_LANES_PER_CTA = 256;      // direct path; staged path: lanes per tile
 
 struct PackedParams {
     const int32_t *fields;     // [problems][records][lanes] packed signed bytes
@@ -225,6 +224,7 @@ struct PackedParams {
 bool packed_dot_stageable(const PackedParams &q);
 uint32_t packed_dot_smem_bytes(bool staged, int depth, int rps, int streams);
 uint32_t packed_dot_threads(bool staged);
+int64_t packed_dot_tiles(int64_t problems, int64_t lanes);   // staged path: tiles of 256 lanes
 cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_launch &L, cudaStream_t stream);
 
 // ---- read-only streaming probe (stream_floor.cu) --------------------------------

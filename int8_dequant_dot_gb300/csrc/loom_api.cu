@@ -641,8 +641,10 @@ loom_status lane_sum_common(const float *values, int64_t num_segments, int64_t s
 
 // `aligned`: the inputs meet the TMA path's alignment; the staged kernel is
 // taken when the shape allows it too (lanes a multiple of 8, <= 64 streams).
+// It runs one or two CTAs per SM (as many as their rings allow) over tiles of
+// 256 lanes (`sms`: the SM count, 0 = the current device's).
 loom_status packed_geometry(int64_t problems, int64_t records, int64_t lanes, int64_t streams, bool aligned,
-                            int64_t depth, int64_t rps, loom_launch *out)
+                            int64_t depth, int64_t rps, int64_t sms, loom_launch *out)
 {
     if (problems < 0 || problems > 65535 || records < 0 || lanes < 0 || streams < 1 ||
         ceil_div(lanes, PD_LANES_PER_CTA) > 0x7fffffff)
@@ -657,10 +659,24 @@ loom_status packed_geometry(int64_t problems, int64_t records, int64_t lanes, in
     const uint32_t smem = packed_dot_smem_bytes(staged, (int)depth, (int)rps, (int)streams);
     if (smem > 227 * 1024)
         return LOOM_ERR_ARG;
-    const int64_t per = staged ? PD_STAGED_LANES_PER_CTA : PD_LANES_PER_CTA;
-    fill_launch(out, ceil_div(lanes, per), packed_dot_threads(staged), smem, (uint32_t)per,
-                staged ? LOOM_KERNEL_PACKED_STAGED : LOOM_KERNEL_PACKED_DIRECT);
-    out->grid[1] = (uint32_t)problems;
+    if (!staged) {
+        fill_launch(out, ceil_div(lanes, PD_LANES_PER_CTA), packed_dot_threads(false), 0, PD_LANES_PER_CTA,
+                    LOOM_KERNEL_PACKED_DIRECT);
+        out->grid[1] = (uint32_t)problems;
+        return LOOM_OK;
+    }
+    if (sms == 0) {
+        const loom_status st = current_sm_count(&sms);
+        if (st != LOOM_OK)
+            return st;
+    }
+    // two CTAs per SM when their rings fit (each SM then keeps 16 consumer warps busy)
+    const int64_t per_sm = smem <= 113 * 1024 ? 2 : 1;
+    const int64_t tiles = packed_dot_tiles(problems, lanes);
+    const int64_t grid = tiles < per_sm * sms ? tiles : per_sm * sms;
+    // units per CTA: tiles (of 256 lanes of one instance), at most
+    fill_launch(out, grid, packed_dot_threads(true), smem, (uint32_t)(grid ? ceil_div(tiles, grid) : 0),
+                LOOM_KERNEL_PACKED_STAGED);
     return LOOM_OK;
 }
 
@@ -706,7 +722,7 @@ loom_status packed_common(const int32_t *fields, const uint16_t *scales, const f
         return (lanes % 8 != 0 || streams > PD_MAX_STAGED_STREAMS) ? LOOM_ERR_SHAPE : LOOM_ERR_ALIGN;
     const bool staged = stageable && t.path != LOOM_PATH_DIRECT;
     loom_launch L;
-    st = packed_geometry(problems, records, lanes, streams, staged, t.depth, t.upw, &L);
+    st = packed_geometry(problems, records, lanes, streams, staged, t.depth, t.upw, 0, &L);
     if (st != LOOM_OK)
         return st;
     q.depth = t.depth ? t.depth : PD_DEFAULT_DEPTH;
@@ -879,7 +895,7 @@ loom_status loom_launch_config(loom_op op, const int64_t *workload, int32_t n_wo
         if (n_workload < 4)
             return LOOM_ERR_ARG;
         return packed_geometry(workload[0], workload[1], workload[2], workload[3], opt(4, 1) != 0, opt(5, 0),
-                               opt(6, 0), out);
+                               opt(6, 0), opt(7, 0), out);
     default:
         return LOOM_ERR_ARG;
     }

@@ -15,24 +15,21 @@
 //
 // GB300 design
 //  * Many independent instances per launch (the pages benchmark one instance
-//    per dispatch, many dispatches per measurement).  A staged CTA takes 512
-//    lanes of one instance, each of its 256 consumer threads two lanes 256
-//    apart (two independent recurrences; with 64 streams, or any count that
-//    divides 256, both lanes read the same activations).
-//  * Staged path: one producer thread fills a ring of `depth` stages, each
-//    `rps` records of the CTA's words (2 KiB per record), scales (1 KiB) and
-//    the instance's whole activation row (16 B per stream), with three 3-D
-//    TMA copies completing on the stage's mbarrier (words and scales counted
-//    as 64- and 32-bit pairs so that one 256-element box row holds 512 lanes;
-//    words and scales evict-first; activations, which every lane block of the
-//    instance reads, evict-last).  512 lanes per CTA halve the copies and the
-//    activation staging per byte against 256.  The hand-over of a stage
-//    costs more than a second wave of CTAs: measured best are two stages of
-//    12 records (two 98 KB CTAs per SM), against deeper rings of smaller
-//    stages that fit every CTA at once.  This is the read-ahead queue of the pages'
-//    pipeline(depth); depth 1 is the serial control and the depth never
-//    changes a result.  (Reading the activations through L1 instead left
-//    every CTA waiting on one load per record: measured 1.6x slower.)
+//    per dispatch, many dispatches per measurement).  The staged path cuts
+//    them into tiles of 256 lanes of one instance and runs a persistent grid
+//    of one CTA per SM over the tile list (tile c, c + G, ...): 1024 tiles
+//    of the 128 x 2048-lane workload give every SM 6 or 7, where CTAs of 512
+//    lanes ran in 1.7 waves.
+//  * One producer thread streams every stage of every tile of its CTA
+//    through one ring of `depth` stages -- `rps` records of the tile's words
+//    (1 KiB per record), scales (512 B) and the instance's activation row
+//    (16 B per stream) as three 3-D TMA copies on the stage's mbarrier;
+//    words and scales evict-first, activations (read by every tile of the
+//    instance) evict-last -- so a CTA's next tile is already in flight while
+//    its consumers finish the current one.  This is the read-ahead queue of
+//    the pages' pipeline(depth); depth 1 is the serial control and the depth
+//    never changes a result.  (Reading the activations through L1 instead
+//    left every CTA waiting on one load per record: measured 1.6x slower.)
 //  * Consumers read their word and scale from shared memory (consecutive
 //    lanes, consecutive addresses) and their stream's float4 (32 consecutive
 //    streams per warp: conflict-free), then run the four fused steps.
@@ -51,10 +48,10 @@
 namespace loom {
 namespace {
 
-constexpr int PD_LANES = 256;                 // consumer threads per CTA (lanes per direct CTA)
-constexpr int PD_SLANES = 2 * PD_LANES;       // lanes per staged CTA: two per consumer thread
-constexpr int PD_CONSUMER_WARPS = PD_LANES / 32;
-constexpr int PD_THREADS_STAGED = PD_LANES + 32;   // + the producer warp
+constexpr int PD_LANES = 256;                 // lanes per direct CTA
+constexpr int PD_TILE = 256;                  // staged path: lanes per tile, one per consumer thread
+constexpr int PD_CONSUMER_WARPS = PD_TILE / 32;
+constexpr int PD_THREADS_STAGED = PD_TILE + 32;   // + the producer warp
 
 struct PackedDeviceParams {
     const int32_t *fields;
@@ -72,12 +69,12 @@ struct PackedDeviceParams {
     int32_t inject_stall;
 };
 
-// Shared-memory layout of one stage: fields [rps][512] i32, scales [rps][512]
+// Shared-memory layout of one stage: fields [rps][256] i32, scales [rps][256]
 // u16, activations [rps][streams][4] f32; each part 128-byte aligned.
 struct PdStage {
     uint32_t fields_bytes, scales_bytes, rhs_bytes;
     __host__ __device__ PdStage(int rps, int streams)
-        : fields_bytes((uint32_t)rps * PD_SLANES * 4u), scales_bytes((uint32_t)rps * PD_SLANES * 2u),
+        : fields_bytes((uint32_t)rps * PD_TILE * 4u), scales_bytes(((uint32_t)rps * PD_TILE * 2u + 127u) & ~127u),
           rhs_bytes(((uint32_t)rps * (uint32_t)streams * 16u + 127u) & ~127u)
     {
     }
@@ -129,7 +126,12 @@ __device__ __forceinline__ int32_t instance_count(const PackedDeviceParams &p, i
     return c;
 }
 
-// Staged path.  Block (blockIdx.x, blockIdx.y) = (lane block, instance).
+// Staged path: a persistent grid of one or two CTAs per SM.  The work is a
+// list of tiles -- 256 lanes of one instance, instance-major -- and CTA c
+// takes tiles c, c + G, c + 2G, ... (1024 tiles of the 128 x 2048-lane
+// workload: 6 or 7 per SM).  The producer streams every stage of every tile of the CTA through one
+// ring, so the copies of a CTA's next tile are in flight while its consumers
+// finish the current one; consumer thread t owns lane t of the tile.
 __global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel(
     const __grid_constant__ CUtensorMap tm_fields, const __grid_constant__ CUtensorMap tm_scales,
     const __grid_constant__ CUtensorMap tm_rhs, const PackedDeviceParams p)
@@ -138,14 +140,14 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base = (dev::smem_u32(smem_raw) + 127u) & ~127u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int32_t inst = blockIdx.y;
-    const int32_t lane0 = blockIdx.x * PD_SLANES;
     const int D = p.depth, RPS = p.rps;
     const PdStage st(RPS, p.streams);
     const uint32_t bars = base + (uint32_t)D * st.bytes();
     auto full = [&](int s) { return bars + 8u * (uint32_t)s; };
     auto empty = [&](int s) { return bars + 8u * (uint32_t)(D + s); };
     auto stage = [&](int s) { return base + (uint32_t)s * st.bytes(); };
+    const int32_t lblocks = (p.lanes + PD_TILE - 1) / PD_TILE;
+    const int32_t tiles = p.problems * lblocks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < D; ++s) {
@@ -155,28 +157,37 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel
         dev::fence_barrier_init();
     }
     __syncthreads();
-    const int32_t count = instance_count(p, inst);
-    const int nst = dev::ceil_div_i32(count, RPS);
 
     if (warp == PD_CONSUMER_WARPS) {
         // ---- producer: three 3-D copies per stage (words, scales, activations)
         if (lane == 0 && !p.inject_stall) {
             const uint64_t once = dev::l2_evict_first_policy();   // words, scales: read once
             const uint64_t shared = dev::l2_evict_last_policy();  // activations: every lane block
-            const uint32_t tx = st.fields_bytes + st.scales_bytes + (uint32_t)RPS * (uint32_t)p.streams * 16u;
-            int issued = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % D;
-                if (i >= D && !dev::mbar_wait_bounded(empty(s), ((i / D) - 1) & 1, p.wait_ns)) {
-                    dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
-                    break;
+            const uint32_t tx = (uint32_t)RPS * PD_TILE * 6u + (uint32_t)RPS * (uint32_t)p.streams * 16u;
+            int s = 0, issued = 0;
+            uint32_t eph = 0;   // parity of the consumers' release of stage s
+            bool ok = true;
+            for (int32_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int32_t inst = t / lblocks;
+                const int32_t l0 = (t - inst * lblocks) * PD_TILE;
+                const int32_t count = instance_count(p, inst);
+                for (int32_t r0 = 0; r0 < count; r0 += RPS) {
+                    if (issued >= D && !dev::mbar_wait_bounded(empty(s), eph, p.wait_ns)) {
+                        dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    dev::mbar_arrive_expect_tx(full(s), tx);
+                    tma_load_3d(stage(s), &tm_fields, l0, r0, inst, full(s), once);
+                    tma_load_3d(stage(s) + st.fields_bytes, &tm_scales, l0, r0, inst, full(s), once);
+                    tma_load_3d(stage(s) + st.fields_bytes + st.scales_bytes, &tm_rhs, 0, r0, inst, full(s), shared);
+                    ++issued;
+                    if (++s == D) {
+                        s = 0;
+                        if (issued > D)
+                            eph ^= 1u;
+                    }
                 }
-                const int32_t r0 = i * RPS;
-                dev::mbar_arrive_expect_tx(full(s), tx);
-                tma_load_3d(stage(s), &tm_fields, lane0 / 2, r0, inst, full(s), once);   // lane pairs
-                tma_load_3d(stage(s) + st.fields_bytes, &tm_scales, lane0 / 2, r0, inst, full(s), once);
-                tma_load_3d(stage(s) + st.fields_bytes + st.scales_bytes, &tm_rhs, 0, r0, inst, full(s), shared);
-                ++issued;
             }
             // every copy issued must land before the CTA may leave (bounded)
             for (int j = issued > D ? issued - D : 0; j < issued; ++j)
@@ -185,53 +196,51 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel
         return;
     }
 
-    // ---- consumers: thread t owns lanes lane0 + t and lane0 + 256 + t
+    // ---- consumers: thread t owns lane t of each tile
     const int t = threadIdx.x;
-    const int32_t la = lane0 + t, lb = la + PD_LANES;
-    const bool live_a = la < p.lanes, live_b = lb < p.lanes;
-    const int32_t sa = la % p.streams, sb = lb % p.streams;
-    const float *init = p.initial ? p.initial + (int64_t)inst * p.lanes : nullptr;
-    float sum_a = (live_a && init) ? __ldg(init + la) : 0.f;
-    float sum_b = (live_b && init) ? __ldg(init + lb) : 0.f;
+    int s = 0;
+    uint32_t fph = 0;   // parity of the copies into stage s
     bool ok = true;
-    for (int i = 0; i < nst; ++i) {
-        const int s = i % D;
-        const bool landed = dev::mbar_wait_bounded(full(s), (i / D) & 1, p.wait_ns);
-        if (!__all_sync(dev::FULL_MASK, landed)) {
-            ok = false;
-            break;
+    for (int32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int32_t inst = tile / lblocks;
+        const int32_t l = (tile - inst * lblocks) * PD_TILE + t;
+        const bool live = l < p.lanes;
+        const int32_t sl = l % p.streams;
+        const int32_t count = instance_count(p, inst);
+        float sum = (live && p.initial) ? __ldg(p.initial + (int64_t)inst * p.lanes + l) : 0.f;
+        for (int32_t r0 = 0; r0 < count && ok; r0 += RPS) {
+            const bool landed = dev::mbar_wait_bounded(full(s), fph, p.wait_ns);
+            if (!__all_sync(dev::FULL_MASK, landed)) {
+                ok = false;
+                break;
+            }
+            const uint32_t f = stage(s), sc = f + st.fields_bytes, a = sc + st.scales_bytes;
+            const int n_here = min(RPS, count - r0);
+            for (int k = 0; k < n_here; ++k) {
+                uint32_t w;
+                uint16_t h;
+                float4 v;
+                const uint32_t row = (uint32_t)(k * PD_TILE + t);
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(f + row * 4u));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(sc + row * 2u));
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                             : "r"(a + (uint32_t)(k * p.streams + sl) * 16u));
+                sum = record_step(sum, w, h, v);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty(s));
+            if (++s == D) {
+                s = 0;
+                fph ^= 1u;
+            }
         }
-        const uint32_t f = stage(s), sc = f + st.fields_bytes, a = sc + st.scales_bytes;
-        const int n_here = min(RPS, count - i * RPS);
-        for (int k = 0; k < n_here; ++k) {
-            uint32_t wa, wb;
-            uint16_t ha, hb;
-            float4 va, vb;
-            const uint32_t row = (uint32_t)(k * PD_SLANES + t);
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(f + row * 4u));
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(f + (row + PD_LANES) * 4u));
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ha) : "r"(sc + row * 2u));
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hb) : "r"(sc + (row + PD_LANES) * 2u));
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(va.x), "=f"(va.y), "=f"(va.z), "=f"(va.w)
-                         : "r"(a + (uint32_t)(k * p.streams + sa) * 16u));
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(vb.x), "=f"(vb.y), "=f"(vb.z), "=f"(vb.w)
-                         : "r"(a + (uint32_t)(k * p.streams + sb) * 16u));
-            sum_a = record_step(sum_a, wa, ha, va);
-            sum_b = record_step(sum_b, wb, hb, vb);
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(empty(s));
+        if (!ok)
+            dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
+        if (live)
+            p.out[(int64_t)inst * p.lanes + l] = ok ? sum : __int_as_float(0x7fc00000);
     }
-    if (!ok)
-        dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
-    const float nan = __int_as_float(0x7fc00000);
-    if (live_a)
-        p.out[(int64_t)inst * p.lanes + la] = ok ? sum_a : nan;
-    if (live_b)
-        p.out[(int64_t)inst * p.lanes + lb] = ok ? sum_b : nan;
 }
 
 // Direct path: plain loads, one thread per lane, records in order.
@@ -309,6 +318,8 @@ uint32_t packed_dot_smem_bytes(bool staged, int depth, int rps, int streams)
 
 uint32_t packed_dot_threads(bool staged) { return staged ? PD_THREADS_STAGED : PD_LANES; }
 
+int64_t packed_dot_tiles(int64_t problems, int64_t lanes) { return problems * ((lanes + PD_TILE - 1) / PD_TILE); }
+
 cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_launch &L, cudaStream_t stream)
 {
     if (L.grid[0] == 0 || L.grid[1] == 0)
@@ -333,11 +344,11 @@ cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_lau
     if (!staged)
         return launch_with(packed_dot_direct_kernel, L, stream, p);
     CUtensorMap tf, ts, tr;
-    // words as 64-bit and scales as 32-bit lane pairs: a box row of 256 pairs holds 512 lanes
-    if (!encode_3d(&tf, CU_TENSOR_MAP_DATA_TYPE_INT64, 8, q.fields, (uint64_t)q.lanes / 2, (uint64_t)q.records,
-                   (uint64_t)q.problems, PD_SLANES / 2, (uint32_t)q.rps) ||
-        !encode_3d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, q.scales, (uint64_t)q.lanes / 2, (uint64_t)q.records,
-                   (uint64_t)q.problems, PD_SLANES / 2, (uint32_t)q.rps) ||
+    // a box of 256 lanes x rps records of words, and of scales
+    if (!encode_3d(&tf, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, q.fields, (uint64_t)q.lanes, (uint64_t)q.records,
+                   (uint64_t)q.problems, PD_TILE, (uint32_t)q.rps) ||
+        !encode_3d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, q.scales, (uint64_t)q.lanes, (uint64_t)q.records,
+                   (uint64_t)q.problems, PD_TILE, (uint32_t)q.rps) ||
         !encode_3d(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q.rhs, (uint64_t)q.streams * 4, (uint64_t)q.records,
                    (uint64_t)q.problems, (uint32_t)q.streams * 4, (uint32_t)q.rps))
         return cudaErrorInvalidValue;

@@ -79,11 +79,11 @@ def test_row_sum_launch_is_ceiling_division(loom, rows, lanes):
         L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes])
         assert L["grid"][0] == oracle.workgroups(s, L["units_per_cta"])
         assert L["block"][0] % 32 == 0 and L["subgroup_size"] == 32
-        # 32-lane segments of at most 64 rows: one bulk copy per segment, 8 per warp
+        # 32-lane segments of at most 64 rows: one bulk copy per segment, 4 per warp
         segs = lanes == 32 and rows <= 64
         assert L["kernel"] == (loom.LOOM_KERNEL_ROWSUM_SEGMENTS if segs else loom.LOOM_KERNEL_ROWSUM_STAGED)
         if segs:   # a ring of 8 KiB and four barriers: four segments in flight
-            assert L["units_per_cta"] == 8 and L["smem_bytes"] == 8192 + 4 * 8
+            assert L["units_per_cta"] == 4 and L["smem_bytes"] == 8192 + 4 * 8
         d = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [s, rows, lanes, 0])
         assert d["kernel"] == loom.LOOM_KERNEL_ROWSUM_DIRECT and d["smem_bytes"] == 0
     # one stage of 4 KiB plus one barrier per warp and depth
@@ -308,17 +308,19 @@ def test_unpack_validation(loom):
 def test_packed_dot_launch(loom):
     # 256 lanes of one instance per CTA; grid.y = instances.  Staged (TMA ring,
     # 256 consumers + a producer warp) when lanes % 8 == 0 and streams <= 64.
-    L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [128, 128, 2048, 64])
+    # staged: two CTAs per SM over tiles of 256 lanes of one instance (1024 tiles: 4 per CTA, at most)
+    L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [128, 128, 2048, 64, 1, 0, 0, SMS])
     assert L["kernel"] == loom.LOOM_KERNEL_PACKED_STAGED
-    assert L["grid"] == (4, 128, 1) and L["block"] == (288, 1, 1) and L["units_per_cta"] == 512
-    # default ring: 2 stages of 12 records x (2 KiB of words + 1 KiB of scales + 1 KiB of activations)
-    assert L["smem_bytes"] == 128 + 2 * 12 * (2048 + 1024 + 64 * 16) + 16 * 2
+    assert L["grid"] == (2 * SMS, 1, 1) and L["block"] == (288, 1, 1) and L["units_per_cta"] == 4
+    # default ring: 3 stages of 12 records x (1 KiB of words + 512 B of scales + 1 KiB of activations)
+    assert L["smem_bytes"] == 128 + 3 * 12 * (1024 + 512 + 64 * 16) + 16 * 3
     for P, R, Ln, S in ((1, 128, 2048, 64), (3, 5, 1000, 7), (2, 0, 8, 1), (65535, 1, 1, 1)):
         for aligned in (0, 1):
-            L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [P, R, Ln, S, aligned])
+            L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [P, R, Ln, S, aligned, 0, 0, SMS])
             staged = aligned == 1 and Ln % 8 == 0 and S <= 64
             assert L["kernel"] == (loom.LOOM_KERNEL_PACKED_STAGED if staged else loom.LOOM_KERNEL_PACKED_DIRECT)
-            assert L["grid"] == (oracle.workgroups(Ln, 512 if staged else 256), P, 1)
+            tiles = P * oracle.workgroups(Ln, 256)
+            assert L["grid"] == ((min(tiles, 2 * SMS), 1, 1) if staged else (oracle.workgroups(Ln, 256), P, 1))
             assert L["block"][0] == (288 if staged else 256)
     L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [1, 128, 2048, 128])   # too many streams to stage
     assert L["kernel"] == loom.LOOM_KERNEL_PACKED_DIRECT and L["smem_bytes"] == 0
@@ -326,7 +328,7 @@ def test_packed_dot_launch(loom):
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, bad)
         assert e.value.status == loom.LOOM_ERR_SHAPE
-    for bad in ([1, 8, 8, 1, 1, 9], [1, 8, 8, 1, 1, 0, 33], [1, 8, 8, 64, 1, 8, 16]):   # depth, rps, smem
+    for bad in ([1, 8, 8, 1, 1, 9], [1, 8, 8, 1, 1, 0, 33], [1, 8, 8, 64, 1, 8, 32]):   # depth, rps, smem
         with pytest.raises(loom.LoomError) as e:
             loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, bad)
         assert e.value.status == loom.LOOM_ERR_ARG
