@@ -111,17 +111,18 @@ struct Ring {
 // ---------------------------------------------------------------------------
 // batch <= 2: lanes across k.  CTA c owns rows [c RPC, (c + 1) RPC) for the
 // whole of k.  Its rows are cut into pieces of at most DOT_K_PIECE_WORDS words
-// (8 KiB) of one row, in row order, and warp w of the CTA takes an equal
-// contiguous share of the pieces: every warp of every CTA moves the same
-// number of bytes, whatever k and the number of rows.  A warp streams its
+// (8 KiB) of one row, numbered chunk by chunk (the first 8 KiB of every row,
+// then the next), and warp w of the CTA takes an equal contiguous share of
+// the pieces: every warp of every CTA moves the same number of bytes,
+// whatever k and the number of rows, and a warp's consecutive pieces share
+// their activation words (held in registers for one vector).  A warp streams its
 // pieces through its own ring of `depth` bulk-copied stages.  Lane l takes
 // words 4l..4l+3 of every 128-word slot of a piece, with the matching
 // activation words.  The activations (batch x k bytes, shared by every row)
 // are copied once into the CTA's shared memory when they fit (p.x_in_smem);
 // else they are read through L1, which measured 2 us slower on 8192 x 16384.
-// A warp's share of a row ends in one warp-wide sum, added into the row's
-// int32 total in shared memory; a row that two warps share gets two integer
-// additions, whose order cannot change the sum.
+// Each piece ends in one warp-wide sum per vector, added into the row's int32
+// total in shared memory; integer additions in any order give the same sum.
 // ---------------------------------------------------------------------------
 template <int NB>
 __global__ void __launch_bounds__(256) dot_rows_k_kernel(const DotParams p)
@@ -170,9 +171,11 @@ __global__ void __launch_bounds__(256) dot_rows_k_kernel(const DotParams p)
     }
     __syncthreads();
 
-    // the first piece of this warp: row rs of the CTA, piece ps of the row
-    const int32_t rs = P ? t0 / P : 0, ps = t0 - rs * P;
-    int32_t pt = t0, pr = rs, pc = ps;   // the producer's next piece
+    // Pieces are numbered chunk-major -- piece t is chunk t / nr of row t % nr --
+    // so a warp's consecutive pieces share their activation words.  The first
+    // piece of this warp: chunk cs0 of row rs.
+    const int32_t cs0 = t0 / nr, rs = t0 - cs0 * nr;
+    int32_t pt = t0, pr = rs, pc = cs0;   // the producer's next piece
     auto produce = [&]() {
         if (pt >= t1)
             return;
@@ -183,9 +186,9 @@ __global__ void __launch_bounds__(256) dot_rows_k_kernel(const DotParams p)
             dev::bulk_g2s(ring.pstage(), p.w + (int64_t)(r0 + pr) * kw + off, bytes, ring.pbar(), policy);
         }
         ++pt;
-        if (++pc == P) {
-            pc = 0;
-            ++pr;
+        if (++pr == nr) {
+            pr = 0;
+            ++pc;
         }
         ring.pnext();
     };
@@ -202,7 +205,11 @@ __global__ void __launch_bounds__(256) dot_rows_k_kernel(const DotParams p)
 #pragma unroll
     for (int b = 0; b < NB; ++b)
         acc[b] = 0;
-    int32_t cr = rs, cc = ps;   // the consumer's piece
+    int32_t cr = rs, cc = cs0;   // the consumer's piece
+    // NB == 1: the activation words of the current chunk held in registers
+    // (16 per lane), loaded again only when the chunk changes
+    int4 xr[NB == 1 ? SLOTS : 1];
+    int32_t xr_chunk = -1;
     bool failed = false;
     // the activations must have landed (a stalled test run issued no copy: its wait runs out)
     if (p.x_in_smem && t0 < t1 && xbytes && !__all_sync(FULL_MASK, dev::mbar_wait_bounded(xbar, 0, p.wait_ns)))
@@ -221,7 +228,17 @@ __global__ void __launch_bounds__(256) dot_rows_k_kernel(const DotParams p)
             xl[b] = x4[b] + (off >> 2) + lane;
         // activation words: from shared memory, or through L1
         auto xload = [&](const int4 *a) { return p.x_in_smem ? *a : __ldg(a); };
-        if (m == DOT_K_PIECE_WORDS) {
+        if (NB == 1 && m == DOT_K_PIECE_WORDS) {
+            if (cc != xr_chunk) {
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s)
+                    xr[s] = xload(xl[0] + 32 * s);
+                xr_chunk = cc;
+            }
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
+                dp4a4(acc[0], s4[32 * s], xr[s]);
+        } else if (m == DOT_K_PIECE_WORDS) {
             // a whole piece: no bounds tests, so the loads of a group of slots issue together
 #pragma unroll
             for (int g = 0; g < SLOTS; g += DOT_K_SLOT_GROUP) {
@@ -252,19 +269,17 @@ __global__ void __launch_bounds__(256) dot_rows_k_kernel(const DotParams p)
         }
         ring.cnext();
         produce();
-        // this warp's share of row cr ends here: add it to the row's total
-        if (cc + 1 == P || t + 1 == t1) {
+        // this warp's share of row cr ends with the piece: add it to the row's total
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const int32_t sum = dev::warp_sum_i32(acc[b]);
-                if (lane == 0)
-                    atomicAdd(rsum + cr * NB + b, sum);
-                acc[b] = 0;
-            }
+        for (int b = 0; b < NB; ++b) {
+            const int32_t sum = dev::warp_sum_i32(acc[b]);
+            if (lane == 0)
+                atomicAdd(rsum + cr * NB + b, sum);
+            acc[b] = 0;
         }
-        if (++cc == P) {
-            cc = 0;
-            ++cr;
+        if (++cr == nr) {
+            cr = 0;
+            ++cc;
         }
     }
     if (failed) {
