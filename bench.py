@@ -746,16 +746,21 @@ def engine_study(torch, loom, stream, work, alg, reps: int = 21):
 
 def read_ahead_study(torch, loom, stream, work, alg):
     """The pages' own comparison: the serial control (read-ahead depth 1) against
-    the default depth, same kernels and workloads, alternated ABAB; single
-    launches after a 512 MB read, CUDA events.  Not part of the step."""
+    a deeper ring, same kernels and workloads, alternated ABAB; single launches
+    after a 512 MB read, CUDA events.  Not part of the step.  The row sums'
+    deeper arm is their default depth; the GEMV's default is already depth 1
+    (its read-ahead comes from sixteen one-stage rings per SM), so its deeper arm
+    is two stages per warp with half the warps: the same ring bytes per CTA."""
     flush = torch.ones(512 << 20, dtype=torch.uint8, device="cuda")
     sink = torch.zeros((), dtype=torch.int64, device="cuda")
     serial = loom.make_tuning(depth=1)
+    deeper = {"segments": (None, "default (4)"), "wide": (None, "default (2)"),
+              "gemv": (loom.make_tuning(depth=2, warps_per_cta=4), "2 (4 warps per CTA)")}
     out = {}
     for name in ("segments", "wide", "gemv"):
-        times = {"depth1": [], "default": []}
+        times = {"depth1": [], "deeper": []}
         for rep in range(6):
-            for label, tu in (("depth1", serial), ("default", None)):
+            for label, tu in (("depth1", serial), ("deeper", deeper[name][0])):
                 saved = work.tuning
                 work.tuning = tu
                 a = torch.cuda.Event(enable_timing=True)
@@ -772,6 +777,7 @@ def read_ahead_study(torch, loom, stream, work, alg):
                     times[label].append(a.elapsed_time(b))
         out[name] = {k: {"avg_ms": sum(v) / len(v), "GB/s": alg[name] / (sum(v) / len(v) * 1e-3) / 1e9}
                      for k, v in times.items()}
+        out[name]["deeper"]["depth"] = deeper[name][1]
     del flush
     return out
 

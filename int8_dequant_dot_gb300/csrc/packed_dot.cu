@@ -17,9 +17,9 @@
 //  * Many independent instances per launch (the pages benchmark one instance
 //    per dispatch, many dispatches per measurement).  The staged path cuts
 //    them into tiles of 256 lanes of one instance and runs a persistent grid
-//    of one CTA per SM over the tile list (tile c, c + G, ...): 1024 tiles
-//    of the 128 x 2048-lane workload give every SM 6 or 7, where CTAs of 512
-//    lanes ran in 1.7 waves.
+//    of two CTAs per SM (one when two rings do not fit) over the tile list
+//    (tile c, c + G, ...): 1024 tiles of the 128 x 2048-lane workload give
+//    every CTA 3 or 4, where CTAs of 512 lanes ran in 1.7 waves.
 //  * One producer thread streams every stage of every tile of its CTA
 //    through one ring of `depth` stages -- `rps` records of the tile's words
 //    (1 KiB per record), scales (512 B) and the instance's activation row
