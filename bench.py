@@ -523,6 +523,9 @@ def run_ours(args, rank, world, dist):
     extras = measure_extras(args, torch, loom, stream, peak, peak_kind)
     extras["read_ahead"] = read_ahead_study(torch, loom, stream, work, alg)
     extras["stream_floor"] = stream_floor(torch, loom, stream, work, alg, extras)
+    work2 = DeviceWorkload(inp, torch, loom, stream, depth=args.depth)
+    extras["stream_floor"]["trains"] = floor_trains(torch, loom, stream, work, work2, alg)
+    del work2
     extras["batched_engines"] = engine_study(torch, loom, stream, work, alg)
 
     line = {
@@ -718,6 +721,58 @@ def stream_floor(torch, loom, stream, work, alg, extras, reps: int = 21):
     del flush, src
     return {"note": "single launches after a 512 MB read, medians of %d; floor = best schedule of a read-only "
                     "launch over the same byte count (loom_stream_floor)" % reps, "workloads": out}
+
+
+def floor_trains(torch, loom, stream, work, work2, alg, reps: int = 7, train: int = 20):
+    """The streaming floor measured on trains of launches rather than single
+    launches: `train` launches back to back between two events, alternating
+    between two copies of the inputs (so no launch finds its bytes in L2), the
+    mean per launch; the median over `reps` trains.  The same for the read-only
+    probe over the same byte count, alternating between two source buffers.  The
+    event timer ticks in ~1 us steps, so the trains resolve what single launches
+    cannot; consecutive launches may overlap their ramp and tail (each kernel may
+    be scheduled while the previous drains), as in the step."""
+    nmax = max(alg.values()) // 16 * 16 + 16
+    srcs = [torch.empty(nmax, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    word = torch.zeros(1, dtype=torch.int64, device="cuda")
+    works = (work, work2)
+
+    def run_train(call):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(200_000)
+            a.record(stream)
+            for i in range(train):
+                call(i & 1)
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) / train
+
+    out = {}
+    for n, nbytes in alg.items():
+        nb = nbytes // 16 * 16
+        floor_t = {sc: [] for sc in FLOOR_SCHEDULES}
+        kern_t = []
+        for rep in range(reps + 1):
+            for sc in FLOOR_SCHEDULES:
+                t = run_train(lambda i: loom.loom_stream_floor(srcs[i], nb, sc[0], sc[1], sc[2], word, stream=stream))
+                if rep:
+                    floor_t[sc].append(t)
+            t = run_train(lambda i: works[i].launch(n))
+            if rep:
+                kern_t.append(t)
+        meds = {sc: statistics.median(v) for sc, v in floor_t.items()}
+        best = min(meds, key=meds.get)
+        k_ms = statistics.median(kern_t)
+        out[n] = {"floor_us": meds[best] * 1e3,
+                  "floor_schedule": {"kind": FLOOR_KINDS[best[0]], "depth": best[1], "ctas_per_sm": best[2]},
+                  "floor_GB/s": nbytes / (meds[best] * 1e-3) / 1e9, "kernel_us": k_ms * 1e3,
+                  "kernel_GB/s": nbytes / (k_ms * 1e-3) / 1e9, "kernel_over_floor": k_ms / meds[best]}
+    del srcs
+    return {"note": "trains of %d launches between two events, alternating two copies of the inputs; mean per "
+                    "launch, median of %d trains; floor = best schedule of the read-only probe" % (train, reps),
+            "workloads": out}
 
 
 def engine_study(torch, loom, stream, work, alg, reps: int = 21):

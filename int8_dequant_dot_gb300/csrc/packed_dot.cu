@@ -32,7 +32,11 @@
 //    left every CTA waiting on one load per record: measured 1.6x slower.)
 //  * Consumers read their word and scale from shared memory (consecutive
 //    lanes, consecutive addresses) and their stream's float4 (32 consecutive
-//    streams per warp: conflict-free), then run the four fused steps.
+//    streams per warp: conflict-free), then run the four fused steps.  The
+//    kernel is bound by instruction issue, so the records go four at a time
+//    with fixed shared-memory offsets, the bytes become f32 by a byte permute
+//    and a packed subtraction, and the scalings are packed multiplies (same
+//    bits as the scalar conversions and multiplies).
 //  * Direct path (inputs a TMA copy cannot take: lanes not a multiple of 8,
 //    more than 64 streams, unaligned pointers): plain loads, same order and
 //    arithmetic, identical bits.
@@ -117,6 +121,51 @@ __device__ __forceinline__ float record_step(float sum, uint32_t word, uint16_t 
     return sum;
 }
 
+// The same record step with fewer instructions, the same bits.  Each byte b
+// becomes the f32 2^23 + (b + 128) by a byte permute (b + 128 is the byte
+// with its sign bit flipped; the exponent byte 0x4B makes the word 2^23 plus
+// that integer), and one packed subtraction of 2^23 + 128 per pair leaves b
+// exactly.  The four scalings are two packed multiplies; each half of a packed
+// operation rounds as the scalar instruction does.
+__device__ __forceinline__ float record_step_packed(float sum, uint32_t word, uint16_t scale_bits, const float4 &a)
+{
+    const float scale = __half2float(__ushort_as_half(scale_bits));
+    const uint32_t u = word ^ 0x80808080u;
+    uint32_t e0, e1, e2, e3;
+    asm("prmt.b32 %0, %1, %2, 0x7540;" : "=r"(e0) : "r"(u), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7541;" : "=r"(e1) : "r"(u), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7542;" : "=r"(e2) : "r"(u), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7543;" : "=r"(e3) : "r"(u), "r"(0x4B000000u));
+    const uint64_t bias = dev::pack2(8388736.0f, 8388736.0f);   // 2^23 + 128
+    const uint64_t b01 = dev::sub2(dev::pack2(__uint_as_float(e0), __uint_as_float(e1)), bias);
+    const uint64_t b23 = dev::sub2(dev::pack2(__uint_as_float(e2), __uint_as_float(e3)), bias);
+    const uint64_t ss = dev::pack2(scale, scale);
+    uint64_t m01, m23;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(m01) : "l"(b01), "l"(ss));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(m23) : "l"(b23), "l"(ss));
+    float m0, m1, m2, m3;
+    dev::unpack2(m01, m0, m1);
+    dev::unpack2(m23, m2, m3);
+    sum = __fmaf_rn(m0, a.x, sum);
+    sum = __fmaf_rn(m1, a.y, sum);
+    sum = __fmaf_rn(m2, a.z, sum);
+    sum = __fmaf_rn(m3, a.w, sum);
+    return sum;
+}
+
+// One record of the staged consumer: the lane's word and scale and its
+// stream's activations from shared memory, then the record step.
+__device__ __forceinline__ float staged_record(float sum, uint32_t fw, uint32_t sw, uint32_t aw)
+{
+    uint32_t w;
+    uint16_t h;
+    float4 v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(fw));
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(sw));
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(aw));
+    return record_step_packed(sum, w, h, v);
+}
+
 __device__ __forceinline__ int32_t instance_count(const PackedDeviceParams &p, int32_t inst)
 {
     const int32_t raw = p.counts ? __ldg(p.counts + inst) : p.count_scalar;
@@ -198,6 +247,7 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel
 
     // ---- consumers: thread t owns lane t of each tile
     const int t = threadIdx.x;
+    const uint32_t astep = 16u * (uint32_t)p.streams;   // activations of one record
     int s = 0;
     uint32_t fph = 0;   // parity of the copies into stage s
     bool ok = true;
@@ -214,19 +264,27 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel
                 ok = false;
                 break;
             }
-            const uint32_t f = stage(s), sc = f + st.fields_bytes, a = sc + st.scales_bytes;
+            // this lane's word and scale of record k: fw + k * 1 KiB, sw + k * 512 B;
+            // its stream's activations: aw + k * astep
+            uint32_t fw = stage(s) + 4u * (uint32_t)t;
+            uint32_t sw = stage(s) + st.fields_bytes + 2u * (uint32_t)t;
+            uint32_t aw = stage(s) + st.fields_bytes + st.scales_bytes + 16u * (uint32_t)sl;
             const int n_here = min(RPS, count - r0);
-            for (int k = 0; k < n_here; ++k) {
-                uint32_t w;
-                uint16_t h;
-                float4 v;
-                const uint32_t row = (uint32_t)(k * PD_TILE + t);
-                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(f + row * 4u));
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(sc + row * 2u));
-                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                             : "r"(a + (uint32_t)(k * p.streams + sl) * 16u));
-                sum = record_step(sum, w, h, v);
+            int k = 0;
+            for (; k + 4 <= n_here; k += 4) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    sum = staged_record(sum, fw + (uint32_t)i * PD_TILE * 4u, sw + (uint32_t)i * PD_TILE * 2u,
+                                        aw + (uint32_t)i * astep);
+                fw += 4u * PD_TILE * 4u;
+                sw += 4u * PD_TILE * 2u;
+                aw += 4u * astep;
+            }
+            for (; k < n_here; ++k) {
+                sum = staged_record(sum, fw, sw, aw);
+                fw += PD_TILE * 4u;
+                sw += PD_TILE * 2u;
+                aw += astep;
             }
             __syncwarp();
             if (lane == 0)
