@@ -923,6 +923,10 @@ def run_e2e(args, inp, total, torch, loom, stream, work):
                    "each lane of the step uploads, runs and reads back its own workloads"}
 
 
+#: algorithmic bytes of the step's workloads (the seeded inputs fix them), for --profile floor_<workload>
+FLOOR_PROFILE_BYTES = {"gemv": 134_299_652, "segments": 265_410_432, "batched": 135_036_992, "wide": 535_147_296}
+
+
 def run_profile(args):
     """One kernel's workload, `--launches` times, for an ncu capture (not timed)."""
     import torch
@@ -930,6 +934,19 @@ def run_profile(args):
     import synth
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
+    if args.profile.startswith("floor_"):
+        # the read-only probe over a workload's algorithmic byte count, in the
+        # schedule that measured best for the step's workloads (bulk-copy ring,
+        # depth 2, 12 CTAs per SM)
+        nb = FLOOR_PROFILE_BYTES[args.profile[len("floor_"):]] // 16 * 16
+        src = torch.empty(nb + 16, dtype=torch.uint8, device="cuda")
+        word = torch.zeros(1, dtype=torch.int64, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(args.launches):
+                loom.loom_stream_floor(src, nb, 2, 2, 12, word, stream=stream)
+        stream.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": args.launches, "bytes": nb}))
+        return
     if args.profile == "packed":
         d = synth.packed_dot_case()
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
@@ -1012,8 +1029,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--depth", type=int, default=0, help="read-ahead depth (0 = library default)")
-    ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows", "routed"),
-                    default=None)
+    ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows", "routed")
+                    + tuple("floor_" + n for n in ORDER), default=None)
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--lanes", type=int, choices=(1, 2), default=2,
                     help="2: the step's two concurrent stream lanes; 1: every kernel on one stream")

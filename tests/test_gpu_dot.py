@@ -98,6 +98,48 @@ def test_dot_extremes(env):
     check(d, y, acc, "extremes")
 
 
+@pytest.mark.parametrize("k,b", [(131068, 16), (131068, 1), (131056, 16), (131056, 2), (131056, 3)])
+def test_dot_at_the_largest_k(env, k, b):
+    # |acc| <= 128 * 128 * k stays below 2^31 up to k = 131068, the largest k the
+    # call accepts: -128 x -128 over all of k sums to 2,147,418,112 there (plain
+    # loads: its rows are not 16-byte aligned).  131056, the largest multiple of 16,
+    # also goes through the staged dp4a kernels and the tensor-core kernels (whole
+    # rows, split bands, band clusters, whole bands) with 1024 units of k.
+    torch, loom = env
+    n = 40
+    d = small(n, k, b, seed=k + b)
+    w, x = d["w"].copy(), d["x"].copy()
+    w[0], w[1] = -128, 127
+    w[2, 0::2], w[2, 1::2] = -128, 127
+    x[0] = -128
+    if b > 1:
+        x[1] = 127
+    d = dict(w=w, x=x, scale_w=d["scale_w"], scale_x=d["scale_x"])
+    runs = [("auto", None), ("direct", loom.make_tuning(path=loom.LOOM_PATH_DIRECT))]
+    if k % 16 != 0:
+        # rows of 131068 bytes are not 16-byte aligned: the staged kernels cannot take them
+        with pytest.raises(loom.LoomError) as e:
+            run_dot(loom, torch, d, tuning=loom.make_tuning(path=loom.LOOM_PATH_STAGED))
+        assert e.value.status == loom.LOOM_ERR_ALIGN
+    else:
+        runs.append(("staged", loom.make_tuning(path=loom.LOOM_PATH_STAGED)))
+    if k % 16 == 0 and b >= 3:
+        runs += [(f"tensor schedule {sc}", loom.make_tuning(path=loom.LOOM_PATH_TENSOR, tc_schedule=sc))
+                 for sc in (4, 2, 3, 1)]
+    ref = None
+    for what, tu in runs:
+        y, acc = run_dot(loom, torch, d, tuning=tu)
+        assert acc[0, 0] == 16384 * k and acc[1, 0] == -127 * 128 * k, what
+        assert acc[2, 0] == -128 * (-128 + 127) * (k // 2), what
+        if b > 1:
+            assert acc[0, 1] == -128 * 127 * k and acc[1, 1] == 127 * 127 * k, what
+        if ref is None:
+            check(d, y, acc, f"k={k} b={b} {what}")
+            ref = (y, acc)
+        else:
+            assert np.array_equal(acc, ref[1]) and same_bits(y, ref[0]), what
+
+
 def test_dot_path_and_depth_invariance(env):
     torch, loom = env
     for b in (1, 16):
