@@ -938,7 +938,7 @@ def run_profile(args):
         # the read-only probe over a workload's algorithmic byte count, in the
         # schedule that measured best for the step's workloads (bulk-copy ring,
         # depth 2, 12 CTAs per SM)
-        nb = FLOOR_PROFILE_BYTES[args.profile[len("floor_"):]] // 16 * 16
+        nb = FLOOR_PROFILE_BYTES[args.profile[len("floor_"):]] * args.scale // 16 * 16
         src = torch.empty(nb + 16, dtype=torch.uint8, device="cuda")
         word = torch.zeros(1, dtype=torch.int64, device="cuda")
         with torch.cuda.stream(stream):
@@ -983,12 +983,13 @@ def run_profile(args):
         stream.synchronize()
         print(json.dumps({"profile": args.profile, "launches": args.launches}))
         return
+    sc = args.scale
     if args.profile in ("segments", "wide"):
-        inp = {"segments": synth.batched_segments() if args.profile == "segments" else None,
+        inp = {"segments": synth.batched_segments(num_segments=65536 * sc) if args.profile == "segments" else None,
                "wide": synth.wide_rows() if args.profile == "wide" else None}
     else:
-        inp = {"gemv": synth.dequant_gemv() if args.profile == "gemv" else None,
-               "batched": synth.dequant_batched() if args.profile == "batched" else None}
+        inp = {"gemv": synth.dequant_gemv(n_rows=8192 * sc) if args.profile == "gemv" else None,
+               "batched": synth.dequant_batched(n_rows=8192 * sc) if args.profile == "batched" else None}
     work = _SingleWorkload(args.profile, inp, torch, loom, stream, args.depth)
     with torch.cuda.stream(stream):
         for _ in range(args.launches):
@@ -1005,14 +1006,14 @@ class _SingleWorkload:
         self.tuning = loom.make_tuning(depth=depth) if depth else None
         if name == "segments":
             s = inp["segments"]
-            self.args = (t(s["values"]), 65536, 2016, 63, 32, t(s["counts"]), t(s["initial"]), 8)
+            self.args = (t(s["values"]), s["num_segments"], 2016, 63, 32, t(s["counts"]), t(s["initial"]), 8)
         elif name == "wide":
             s = inp["wide"]
             self.args = (t(s["values"]), 16384, 16384, 16384, 1, t(s["counts"]), None, 8)
         else:
             s = inp[name]
             b = s["x"].shape[0]
-            self.args = (t(s["w"].view("<i4")), t(s["scale_w"]), 8192, 16384, t(s["x"].view("<i4")),
+            self.args = (t(s["w"].view("<i4")), t(s["scale_w"]), s["n_rows"], 16384, t(s["x"].view("<i4")),
                          t(s["scale_x"]), b)
 
     def launch(self):
@@ -1032,6 +1033,9 @@ def main():
     ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows", "routed")
                     + tuple("floor_" + n for n in ORDER), default=None)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--scale", type=int, default=1,
+                    help="with --profile segments/gemv/batched/floor_*: that many times the rows (segments) "
+                         "of the workload, for captures of the same kernel over a longer launch")
     ap.add_argument("--lanes", type=int, choices=(1, 2), default=2,
                     help="2: the step's two concurrent stream lanes; 1: every kernel on one stream")
     args = ap.parse_args()

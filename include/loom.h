@@ -115,17 +115,20 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_TENSOR_SPLIT 8 /* the same kernel over equal shares of all units, then
                                           a finishing kernel for the bands split between CTAs
                                           (two launches per pass) */
-#define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: one CTA per SM over tiles of 256 lanes
-                                        (units_per_cta = tiles), one 3-D TMA read-ahead ring */
+#define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: two persistent CTAs per SM (one when two
+                                        rings do not fit) over tiles of 256 lanes (units_per_cta
+                                        = tiles), one 3-D TMA read-ahead ring per CTA */
 #define LOOM_KERNEL_PACKED_DIRECT 10 /* packed dot: plain loads */
 #define LOOM_KERNEL_LANESUM_STAGED 11 /* per-lane sums: bulk-copy read-ahead ring per warp */
 #define LOOM_KERNEL_LANESUM_DIRECT 12 /* per-lane sums: plain loads */
 #define LOOM_KERNEL_ROUTED_STAGED 13  /* routed combine: bulk-copy ring of payload pieces per warp */
 #define LOOM_KERNEL_ROUTED_DIRECT 14  /* routed combine: plain loads */
 #define LOOM_KERNEL_STAGE_ROWS 15     /* upload of ragged rows: one CTA per 8 KiB of a segment */
-#define LOOM_KERNEL_ROWSUM_SEGMENTS 17 /* 32-lane segments of at most 64 rows: one bulk copy and
-                                          one wait per segment, a ring of `depth` 8 KiB stages
-                                          per warp; the same bits as LOOM_KERNEL_ROWSUM_STAGED */
+#define LOOM_KERNEL_ROWSUM_SEGMENTS 17 /* 32-lane segments that fit the ring (128 x rows <=
+                                          chunk_bytes, default 8 KiB): one bulk copy and one wait
+                                          per segment, whole segments back to back in a byte ring
+                                          per warp, up to `depth` in flight; the same bits as
+                                          LOOM_KERNEL_ROWSUM_STAGED */
 #define LOOM_KERNEL_DOT_TENSOR_ROWS 16 /* tcgen05 MMA on exact f16 copies, batch 3..16 per pass; one
                                           CTA per SM owning whole rows (units_per_cta = rows),
                                           two k ranges per MMA; one launch, no workspace */
