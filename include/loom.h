@@ -274,9 +274,9 @@ loom_status loom_i8_dequant_dot_noalloc(const int32_t *d_w_packed, const float *
  * [problems] (NULL: `count` for every instance); d_initial f32
  * [problems][lanes] (NULL: 0); d_out f32 [problems][lanes].
  * Schedule: with lanes a multiple of 8, at most 64 streams and 16-byte
- * aligned inputs, 512 lanes of one instance per CTA (two per thread) fed by
- * a read-ahead ring of 3-D TMA copies; else 256 lanes per CTA with plain
- * loads (same bits).
+ * aligned inputs, persistent CTAs (two per SM) walk tiles of 256 lanes of one
+ * instance, one lane per thread, fed by one read-ahead ring of 3-D TMA copies
+ * per CTA; else 256 lanes per CTA with plain loads (same bits).
  * Errors: NULL required pointer -> LOOM_ERR_NULL; pointers not 4-byte (fields,
  * rhs, initial, out) or 2-byte (scales) aligned -> LOOM_ERR_ALIGN; negative
  * sizes, streams < 1, or more than 65535 instances -> LOOM_ERR_SHAPE; host

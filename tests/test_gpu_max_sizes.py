@@ -82,3 +82,33 @@ def test_routed_plain_loads_row_of_2_31_minus_1_floats(big):
     torch.cuda.synchronize()
     assert int(torch.count_nonzero(out).item()) == 0
     del out
+
+
+def test_packed_dot_instance_of_2_31_words():
+    # One instance of 2^20 records x 2048 lanes: 2^31 words, so element offsets pass
+    # INT32_MAX (8 GiB of words, 4 GiB of scales, 1 GiB of activations).  Every byte is
+    # 1, every scale 1.0 and every activation of record r is 0.25 ((r mod 7) - 3): each
+    # record adds (r mod 7) - 3 to every lane in four exact quarter steps, so a lane
+    # ends at initial + S(count) exactly.  Full and ragged counts; the TMA-staged and
+    # the plain-load paths.
+    torch = require_gpu()
+    loom = loom_module()
+    R, L, ST = 2**20, 2048, 64
+    fields = torch.full((1, R, L), 0x01010101, dtype=torch.int32, device="cuda")
+    scales = torch.full((1, R, L), 0x3C00, dtype=torch.int16, device="cuda")
+    r = torch.arange(R, device="cuda")
+    rhs = ((r % 7) - 3).to(torch.float32).mul_(0.25).view(1, R, 1, 1).expand(1, R, ST, 4).contiguous()
+    del r
+    initial = torch.arange(L, dtype=torch.float32, device="cuda").view(1, L) * 0.5
+    for count in (R, R - 5):
+        want = initial + float(S(count))
+        for what, tu in (("staged", loom.make_tuning(path=loom.LOOM_PATH_STAGED)),
+                         ("direct", loom.make_tuning(path=loom.LOOM_PATH_DIRECT))):
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            out = torch.full((1, L), float("nan"), dtype=torch.float32, device="cuda")
+            loom.loom_packed_dot_ex(fields, scales, rhs, None, count, initial, out=out, error=err, tuning=tu)
+            torch.cuda.synchronize()
+            assert torch.equal(out, want), (what, count)
+            assert int(err.item()) == 0, what
+    del fields, scales, rhs
+    torch.cuda.empty_cache()
