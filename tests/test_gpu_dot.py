@@ -229,9 +229,10 @@ def test_tensor_core_schedule_invariance(env, n, k, b):
 
 
 @pytest.mark.parametrize("n,k,b", [(9729, 2048, 16), (9729, 2048, 5), (10000, 4112, 16), (4864, 2048, 3),
-                                   (1, 16384, 16), (153, 1152, 16)])
+                                   (1, 16384, 16), (153, 1152, 16), (50000, 2064, 16)])
 def test_tensor_core_whole_rows(env, n, k, b):
     # CTAs owning whole rows: two blocks per CTA (9729 rows: 65 per CTA, blocks of 33),
+    # six blocks per CTA (50000 rows: 329 per CTA, blocks of 55, with a k tail),
     # a short last CTA, k tails and k quarters that end past k (zero-filled units), one
     # row, one row per CTA; the bits of the dp4a kernels and the oracle's integers.
     torch, loom = env
