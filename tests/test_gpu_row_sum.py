@@ -167,6 +167,36 @@ def test_batched_depth_and_path_invariance(env, config2):
         assert np.array_equal(a.view(np.int32), b.view(np.int32)), "run to run"
 
 
+@pytest.mark.parametrize("rows,chunk", [(64, 8192), (100, 16384), (127, 16384), (20, 2560)])
+def test_segment_ring_sizes(env, rows, chunk):
+    # Segments that fill the one-copy-per-segment ring exactly (64 x 32 lanes in 8 KiB),
+    # larger segments under a larger ring (100 and 127 rows in 16 KiB: one segment in
+    # flight beside part of the next), and a ring that is not a power of two.  Same bits
+    # as the chunked kernel and the direct path, and the oracle's sums.
+    torch, loom = env
+    S = 3001
+    d = _batched_case(S, rows=rows, seed=rows * 7 + chunk)
+    vals, counts, init = to_dev(d["values"], torch), to_dev(d["counts"], torch), to_dev(d["initial"], torch)
+    stride = rows * 32
+    want = oracle.row_sum_batched(d["values"], stride, rows, 32, d["counts"], d["initial"], 8, threads=8)
+    L = loom.loom_launch_config(loom.LOOM_OP_ROW_SUM_BATCHED, [S, rows, 32, 1, 0, 0, 0, chunk])
+    assert L["kernel"] == loom.LOOM_KERNEL_ROWSUM_SEGMENTS
+    ref = None
+    for depth in (1, 2, 4):
+        t = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_STAGED, chunk_bytes=chunk)
+        got = run_batched(loom, torch, vals, S, stride, rows, 32, counts, init, 8, tuning=t)
+        compare(got, want, f"rows {rows} ring {chunk} depth {depth}", rel=ULP_REL)
+        if ref is None:
+            ref = got
+        for a, b in zip(got, ref):
+            assert np.array_equal(a.view(np.int32), b.view(np.int32)), depth
+    for t in (loom.make_tuning(path=loom.LOOM_PATH_STAGED, chunk_bytes=2048),
+              loom.make_tuning(path=loom.LOOM_PATH_DIRECT)):
+        got = run_batched(loom, torch, vals, S, stride, rows, 32, counts, init, 8, tuning=t)
+        for a, b in zip(got, ref):
+            assert np.array_equal(a.view(np.int32), b.view(np.int32)), "chunked / direct"
+
+
 def test_unaligned_input_takes_direct_path_with_same_bits(env):
     torch, loom = env
     S = 300
