@@ -670,8 +670,8 @@ loom_status packed_geometry(int64_t problems, int64_t records, int64_t lanes, in
         if (st != LOOM_OK)
             return st;
     }
-    // two CTAs per SM when their rings fit (each SM then keeps 16 consumer warps busy)
-    const int64_t per_sm = smem <= 113 * 1024 ? 2 : 1;
+    // up to three CTAs per SM, as many as their rings fit (each CTA: 8 consumer warps)
+    const int64_t per_sm = smem <= 74 * 1024 ? 3 : smem <= 113 * 1024 ? 2 : 1;
     const int64_t tiles = packed_dot_tiles(problems, lanes);
     const int64_t grid = tiles < per_sm * sms ? tiles : per_sm * sms;
     // units per CTA: tiles (of 256 lanes of one instance), at most

@@ -17,9 +17,9 @@
 //  * Many independent instances per launch (the pages benchmark one instance
 //    per dispatch, many dispatches per measurement).  The staged path cuts
 //    them into tiles of 256 lanes of one instance and runs a persistent grid
-//    of two CTAs per SM (one when two rings do not fit) over the tile list
-//    (tile c, c + G, ...): 1024 tiles of the 128 x 2048-lane workload give
-//    every CTA 3 or 4, where CTAs of 512 lanes ran in 1.7 waves.
+//    of up to three CTAs per SM (as many as their rings fit) over the tile
+//    list (tile c, c + G, ...): 1024 tiles of the 128 x 2048-lane workload
+//    give every CTA 2 or 3, where CTAs of 512 lanes ran in 1.7 waves.
 //  * One producer thread streams every stage of every tile of its CTA
 //    through one ring of `depth` stages -- `rps` records of the tile's words
 //    (1 KiB per record), scales (512 B) and the instance's activation row
@@ -175,13 +175,13 @@ __device__ __forceinline__ int32_t instance_count(const PackedDeviceParams &p, i
     return c;
 }
 
-// Staged path: a persistent grid of one or two CTAs per SM.  The work is a
+// Staged path: a persistent grid of up to three CTAs per SM.  The work is a
 // list of tiles -- 256 lanes of one instance, instance-major -- and CTA c
 // takes tiles c, c + G, c + 2G, ... (1024 tiles of the 128 x 2048-lane
 // workload: 6 or 7 per SM).  The producer streams every stage of every tile of the CTA through one
 // ring, so the copies of a CTA's next tile are in flight while its consumers
 // finish the current one; consumer thread t owns lane t of the tile.
-__global__ void __launch_bounds__(PD_THREADS_STAGED, 2) packed_dot_staged_kernel(
+__global__ void __launch_bounds__(PD_THREADS_STAGED, 3) packed_dot_staged_kernel(
     const __grid_constant__ CUtensorMap tm_fields, const __grid_constant__ CUtensorMap tm_scales,
     const __grid_constant__ CUtensorMap tm_rhs, const PackedDeviceParams p)
 {
