@@ -632,7 +632,14 @@ def measure_extras(args, torch, loom, stream, peak, peak_kind):
     L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [d["problems"], d["records"], d["lanes"], d["streams"]])
     out["packed_dot"] = _extra_line(PACKED_WORKLOAD, packed_alg_bytes(d), times, peak, peak_kind,
                                     traffic.get("packed"), L)
-    del f, sc, rhs, counts, init, y, d
+    # trains over two copies of the inputs, beside the read-only probe's trains
+    copies = [(f, sc, rhs), (f.clone(), sc.clone(), rhs.clone())]
+    srcs, word = floor_srcs(torch, packed_alg_bytes(d))
+    tr = train_vs_floor(torch, loom, stream,
+                        lambda i: loom.loom_packed_dot(*copies[i], counts, 0, init, out=y, stream=stream),
+                        packed_alg_bytes(d), srcs, word)
+    out["packed_dot"]["trains"] = tr | {"note": TRAIN_NOTE}
+    del f, sc, rhs, counts, init, y, d, copies, srcs
 
     d = synth.routed_case()
     ids, wts, pay = t(d["ids"]), t(d["weights"]), t(d["payload"])
@@ -723,6 +730,57 @@ def stream_floor(torch, loom, stream, work, alg, extras, reps: int = 21):
                     "launch over the same byte count (loom_stream_floor)" % reps, "workloads": out}
 
 
+def _run_train(torch, stream, call, train: int):
+    """`train` launches back to back between two events, call(i) alternating i = 0, 1
+    between two copies of the inputs; the mean per launch in ms."""
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000)
+        a.record(stream)
+        for i in range(train):
+            call(i & 1)
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / train
+
+
+def train_vs_floor(torch, loom, stream, call, nbytes: int, srcs, word, reps: int = 7, train: int = 20):
+    """A kernel's trains (call(i) alternating two input copies) beside the read-only
+    probe's trains over the same byte count (every FLOOR_SCHEDULES entry, alternating
+    two source buffers); medians over `reps` trains, the probe's best schedule."""
+    nb = nbytes // 16 * 16
+    floor_t = {sc: [] for sc in FLOOR_SCHEDULES}
+    kern_t = []
+    for rep in range(reps + 1):
+        for sc in FLOOR_SCHEDULES:
+            t = _run_train(torch, stream,
+                           lambda i: loom.loom_stream_floor(srcs[i], nb, sc[0], sc[1], sc[2], word, stream=stream), train)
+            if rep:
+                floor_t[sc].append(t)
+        t = _run_train(torch, stream, call, train)
+        if rep:
+            kern_t.append(t)
+    meds = {sc: statistics.median(v) for sc, v in floor_t.items()}
+    best = min(meds, key=meds.get)
+    k_ms = statistics.median(kern_t)
+    return {"floor_us": meds[best] * 1e3,
+            "floor_schedule": {"kind": FLOOR_KINDS[best[0]], "depth": best[1], "ctas_per_sm": best[2]},
+            "floor_GB/s": nbytes / (meds[best] * 1e-3) / 1e9, "kernel_us": k_ms * 1e3,
+            "kernel_GB/s": nbytes / (k_ms * 1e-3) / 1e9, "kernel_over_floor": k_ms / meds[best]}
+
+
+def floor_srcs(torch, nbytes: int):
+    """Two source buffers for the read-only probe's trains, and its sink word."""
+    n = nbytes // 16 * 16 + 16
+    return ([torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(2)],
+            torch.zeros(1, dtype=torch.int64, device="cuda"))
+
+
+TRAIN_NOTE = ("trains of 20 launches between two events, alternating two copies of the inputs; mean per "
+              "launch, median of 7 trains; floor = best schedule of the read-only probe")
+
+
 def floor_trains(torch, loom, stream, work, work2, alg, reps: int = 7, train: int = 20):
     """The streaming floor measured on trains of launches rather than single
     launches: `train` launches back to back between two events, alternating
@@ -732,47 +790,12 @@ def floor_trains(torch, loom, stream, work, work2, alg, reps: int = 7, train: in
     event timer ticks in ~1 us steps, so the trains resolve what single launches
     cannot; consecutive launches may overlap their ramp and tail (each kernel may
     be scheduled while the previous drains), as in the step."""
-    nmax = max(alg.values()) // 16 * 16 + 16
-    srcs = [torch.empty(nmax, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    word = torch.zeros(1, dtype=torch.int64, device="cuda")
+    srcs, word = floor_srcs(torch, max(alg.values()))
     works = (work, work2)
-
-    def run_train(call):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(200_000)
-            a.record(stream)
-            for i in range(train):
-                call(i & 1)
-            b.record(stream)
-        stream.synchronize()
-        return a.elapsed_time(b) / train
-
-    out = {}
-    for n, nbytes in alg.items():
-        nb = nbytes // 16 * 16
-        floor_t = {sc: [] for sc in FLOOR_SCHEDULES}
-        kern_t = []
-        for rep in range(reps + 1):
-            for sc in FLOOR_SCHEDULES:
-                t = run_train(lambda i: loom.loom_stream_floor(srcs[i], nb, sc[0], sc[1], sc[2], word, stream=stream))
-                if rep:
-                    floor_t[sc].append(t)
-            t = run_train(lambda i: works[i].launch(n))
-            if rep:
-                kern_t.append(t)
-        meds = {sc: statistics.median(v) for sc, v in floor_t.items()}
-        best = min(meds, key=meds.get)
-        k_ms = statistics.median(kern_t)
-        out[n] = {"floor_us": meds[best] * 1e3,
-                  "floor_schedule": {"kind": FLOOR_KINDS[best[0]], "depth": best[1], "ctas_per_sm": best[2]},
-                  "floor_GB/s": nbytes / (meds[best] * 1e-3) / 1e9, "kernel_us": k_ms * 1e3,
-                  "kernel_GB/s": nbytes / (k_ms * 1e-3) / 1e9, "kernel_over_floor": k_ms / meds[best]}
+    out = {n: train_vs_floor(torch, loom, stream, lambda i, n=n: works[i].launch(n), nbytes, srcs, word, reps, train)
+           for n, nbytes in alg.items()}
     del srcs
-    return {"note": "trains of %d launches between two events, alternating two copies of the inputs; mean per "
-                    "launch, median of %d trains; floor = best schedule of the read-only probe" % (train, reps),
-            "workloads": out}
+    return {"note": TRAIN_NOTE, "workloads": out}
 
 
 def engine_study(torch, loom, stream, work, alg, reps: int = 21):
