@@ -115,10 +115,10 @@ typedef struct loom_launch {
 #define LOOM_KERNEL_DOT_TENSOR_SPLIT 8 /* the same kernel over equal shares of all units, then
                                           a finishing kernel for the bands split between CTAs
                                           (two launches per pass) */
-#define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: up to three persistent CTAs per SM (as
-                                        many as their rings fit) over tiles of 256 lanes
-                                        (units_per_cta = tiles), one 3-D TMA read-ahead ring
-                                        per CTA */
+#define LOOM_KERNEL_PACKED_STAGED 9  /* packed dot: up to seven CTAs per SM (as many as
+                                        their rings fit) over tiles of 256 lanes, two lanes per
+                                        consumer thread (units_per_cta = tiles), one 3-D TMA
+                                        read-ahead ring per CTA */
 #define LOOM_KERNEL_PACKED_DIRECT 10 /* packed dot: plain loads */
 #define LOOM_KERNEL_LANESUM_STAGED 11 /* per-lane sums: bulk-copy read-ahead ring per warp */
 #define LOOM_KERNEL_LANESUM_DIRECT 12 /* per-lane sums: plain loads */
@@ -275,8 +275,8 @@ loom_status loom_i8_dequant_dot_noalloc(const int32_t *d_w_packed, const float *
  * [problems] (NULL: `count` for every instance); d_initial f32
  * [problems][lanes] (NULL: 0); d_out f32 [problems][lanes].
  * Schedule: with lanes a multiple of 8, at most 64 streams and 16-byte
- * aligned inputs, persistent CTAs (up to three per SM) walk tiles of 256 lanes of one
- * instance, one lane per thread, fed by one read-ahead ring of 3-D TMA copies
+ * aligned inputs, CTAs (up to seven per SM) walk tiles of 256 lanes of one
+ * instance, two lanes per thread, fed by one read-ahead ring of 3-D TMA copies
  * per CTA; else 256 lanes per CTA with plain loads (same bits).
  * Errors: NULL required pointer -> LOOM_ERR_NULL; pointers not 4-byte (fields,
  * rhs, initial, out) or 2-byte (scales) aligned -> LOOM_ERR_ALIGN; negative

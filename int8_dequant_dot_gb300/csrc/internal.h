@@ -202,7 +202,7 @@ cudaError_t launch_routed(const RoutedParams &p, bool staged, const loom_launch 
 
 // ---- the pages' packed-dot example (packed_dot.cu) ---------------------------
 constexpr int PD_DEFAULT_DEPTH = 3;        // stages of the read-ahead ring ...
-constexpr int PD_DEFAULT_RPS = 8;          // ... of 8 records (20 KiB): three CTAs per SM (measured best)
+constexpr int PD_DEFAULT_RPS = 4;          // ... of 4 records (10 KiB): seven CTAs per SM (measured best)
 constexpr int PD_MAX_RPS = 32;
 constexpr int PD_MAX_STAGED_STREAMS = 64;  // one TMA box row holds every stream of a record
 constexpr int PD_LANES_PER_CTA = 256;      // direct path; staged path: lanes per tile

@@ -670,8 +670,10 @@ loom_status packed_geometry(int64_t problems, int64_t records, int64_t lanes, in
         if (st != LOOM_OK)
             return st;
     }
-    // up to three CTAs per SM, as many as their rings fit (each CTA: 8 consumer warps)
-    const int64_t per_sm = smem <= 74 * 1024 ? 3 : smem <= 113 * 1024 ? 2 : 1;
+    // as many CTAs per SM as their rings fit, at most seven (the registers of
+    // seven CTAs of four consumer warps and a producer)
+    int64_t per_sm = (227 * 1024) / ((int64_t)smem + 1024);
+    per_sm = per_sm > 7 ? 7 : (per_sm < 1 ? 1 : per_sm);
     const int64_t tiles = packed_dot_tiles(problems, lanes);
     const int64_t grid = tiles < per_sm * sms ? tiles : per_sm * sms;
     // units per CTA: tiles (of 256 lanes of one instance), at most

@@ -16,10 +16,10 @@
 // GB300 design
 //  * Many independent instances per launch (the pages benchmark one instance
 //    per dispatch, many dispatches per measurement).  The staged path cuts
-//    them into tiles of 256 lanes of one instance and runs a persistent grid
-//    of up to three CTAs per SM (as many as their rings fit) over the tile
-//    list (tile c, c + G, ...): 1024 tiles of the 128 x 2048-lane workload
-//    give every CTA 2 or 3, where CTAs of 512 lanes ran in 1.7 waves.
+//    them into tiles of 256 lanes of one instance and runs a grid of up to
+//    seven CTAs per SM (as many as their rings and registers allow) over the
+//    tile list (tile c, c + G, ...; 1024 tiles of the 128 x 2048-lane workload
+//    take one each), where CTAs of 512 lanes ran in 1.7 waves.
 //  * One producer thread streams every stage of every tile of its CTA
 //    through one ring of `depth` stages -- `rps` records of the tile's words
 //    (1 KiB per record), scales (512 B) and the instance's activation row
@@ -30,13 +30,18 @@
 //    the pages' pipeline(depth); depth 1 is the serial control and the depth
 //    never changes a result.  (Reading the activations through L1 instead
 //    left every CTA waiting on one load per record: measured 1.6x slower.)
-//  * Consumers read their word and scale from shared memory (consecutive
-//    lanes, consecutive addresses) and their stream's float4 (32 consecutive
-//    streams per warp: conflict-free), then run the four fused steps.  The
-//    kernel is bound by instruction issue, so the records go four at a time
-//    with fixed shared-memory offsets, the bytes become f32 by a byte permute
-//    and a packed subtraction, and the scalings are packed multiplies (same
-//    bits as the scalar conversions and multiplies).
+//  * Consumer thread t owns lanes t and t + 128 of a tile: two independent
+//    recurrences advanced together by packed f32x2 instructions (each half
+//    rounds as the scalar instruction does: the same bits).  When 128 is a
+//    multiple of the stream count the two lanes read the same activations, so
+//    one float4 serves both.  Per record a thread reads two words and two
+//    scales from shared memory (consecutive lanes, consecutive addresses) and
+//    its stream's float4 (conflict-free); the bytes become f32 by a byte
+//    permute and a packed subtraction, the scalings are packed multiplies and
+//    the four ordered fused steps are packed fused multiply-adds.  The kernel
+//    is bound by instruction issue: two lanes per thread measured 33.1 us
+//    against 37.5 us with one (trains of launches; four-record stages, seven
+//    CTAs of four consumer warps per SM).
 //  * Direct path (inputs a TMA copy cannot take: lanes not a multiple of 8,
 //    more than 64 streams, unaligned pointers): plain loads, same order and
 //    arithmetic, identical bits.
@@ -53,9 +58,10 @@ namespace loom {
 namespace {
 
 constexpr int PD_LANES = 256;                 // lanes per direct CTA
-constexpr int PD_TILE = 256;                  // staged path: lanes per tile, one per consumer thread
-constexpr int PD_CONSUMER_WARPS = PD_TILE / 32;
-constexpr int PD_THREADS_STAGED = PD_TILE + 32;   // + the producer warp
+constexpr int PD_TILE = 256;                  // staged path: lanes per tile, two per consumer thread
+constexpr int PD_PAIR = PD_TILE / 2;          // thread t owns lanes t and t + PD_PAIR
+constexpr int PD_CONSUMER_WARPS = PD_PAIR / 32;
+constexpr int PD_THREADS_STAGED = PD_PAIR + 32;   // + the producer warp
 
 struct PackedDeviceParams {
     const int32_t *fields;
@@ -121,49 +127,89 @@ __device__ __forceinline__ float record_step(float sum, uint32_t word, uint16_t 
     return sum;
 }
 
-// The same record step with fewer instructions, the same bits.  Each byte b
-// becomes the f32 2^23 + (b + 128) by a byte permute (b + 128 is the byte
-// with its sign bit flipped; the exponent byte 0x4B makes the word 2^23 plus
-// that integer), and one packed subtraction of 2^23 + 128 per pair leaves b
-// exactly.  The four scalings are two packed multiplies; each half of a packed
-// operation rounds as the scalar instruction does.
-__device__ __forceinline__ float record_step_packed(float sum, uint32_t word, uint16_t scale_bits, const float4 &a)
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
 {
-    const float scale = __half2float(__ushort_as_half(scale_bits));
-    const uint32_t u = word ^ 0x80808080u;
-    uint32_t e0, e1, e2, e3;
-    asm("prmt.b32 %0, %1, %2, 0x7540;" : "=r"(e0) : "r"(u), "r"(0x4B000000u));
-    asm("prmt.b32 %0, %1, %2, 0x7541;" : "=r"(e1) : "r"(u), "r"(0x4B000000u));
-    asm("prmt.b32 %0, %1, %2, 0x7542;" : "=r"(e2) : "r"(u), "r"(0x4B000000u));
-    asm("prmt.b32 %0, %1, %2, 0x7543;" : "=r"(e3) : "r"(u), "r"(0x4B000000u));
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// One record of two lanes (words w0, w1, f16 scales h0, h1; activations a0 of
+// the first lane, a1 of the second), their sums packed in `sum`: the record
+// step of both lanes at once, with the same roundings as record_step.
+__device__ __forceinline__ uint64_t pair_products(uint32_t w0, uint32_t w1, uint16_t h0, uint16_t h1, uint64_t (&m)[4])
+{
+    const uint64_t ss = dev::pack2(__half2float(__ushort_as_half(h0)), __half2float(__ushort_as_half(h1)));
+    const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
+    uint32_t x0, x1, y0, y1, z0, z1, v0, v1;   // byte j of each word as 2^23 + (b + 128)
+    asm("prmt.b32 %0, %1, %2, 0x7540;" : "=r"(x0) : "r"(u0), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7540;" : "=r"(x1) : "r"(u1), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7541;" : "=r"(y0) : "r"(u0), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7541;" : "=r"(y1) : "r"(u1), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7542;" : "=r"(z0) : "r"(u0), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7542;" : "=r"(z1) : "r"(u1), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7543;" : "=r"(v0) : "r"(u0), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7543;" : "=r"(v1) : "r"(u1), "r"(0x4B000000u));
     const uint64_t bias = dev::pack2(8388736.0f, 8388736.0f);   // 2^23 + 128
-    const uint64_t b01 = dev::sub2(dev::pack2(__uint_as_float(e0), __uint_as_float(e1)), bias);
-    const uint64_t b23 = dev::sub2(dev::pack2(__uint_as_float(e2), __uint_as_float(e3)), bias);
-    const uint64_t ss = dev::pack2(scale, scale);
-    uint64_t m01, m23;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(m01) : "l"(b01), "l"(ss));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(m23) : "l"(b23), "l"(ss));
-    float m0, m1, m2, m3;
-    dev::unpack2(m01, m0, m1);
-    dev::unpack2(m23, m2, m3);
-    sum = __fmaf_rn(m0, a.x, sum);
-    sum = __fmaf_rn(m1, a.y, sum);
-    sum = __fmaf_rn(m2, a.z, sum);
-    sum = __fmaf_rn(m3, a.w, sum);
+    m[0] = mul2(dev::sub2(dev::pack2(__uint_as_float(x0), __uint_as_float(x1)), bias), ss);
+    m[1] = mul2(dev::sub2(dev::pack2(__uint_as_float(y0), __uint_as_float(y1)), bias), ss);
+    m[2] = mul2(dev::sub2(dev::pack2(__uint_as_float(z0), __uint_as_float(z1)), bias), ss);
+    m[3] = mul2(dev::sub2(dev::pack2(__uint_as_float(v0), __uint_as_float(v1)), bias), ss);
+    return ss;
+}
+
+// Both lanes against the same activations.
+__device__ __forceinline__ uint64_t pair_record(uint64_t sum, uint32_t w0, uint32_t w1, uint16_t h0, uint16_t h1,
+                                                const float4 &a)
+{
+    uint64_t m[4];
+    pair_products(w0, w1, h0, h1, m);
+    sum = fma2(m[0], dev::pack2(a.x, a.x), sum);
+    sum = fma2(m[1], dev::pack2(a.y, a.y), sum);
+    sum = fma2(m[2], dev::pack2(a.z, a.z), sum);
+    sum = fma2(m[3], dev::pack2(a.w, a.w), sum);
     return sum;
 }
 
-// One record of the staged consumer: the lane's word and scale and its
-// stream's activations from shared memory, then the record step.
-__device__ __forceinline__ float staged_record(float sum, uint32_t fw, uint32_t sw, uint32_t aw)
+// Each lane against its own activations.
+__device__ __forceinline__ uint64_t pair_record(uint64_t sum, uint32_t w0, uint32_t w1, uint16_t h0, uint16_t h1,
+                                                const float4 &a0, const float4 &a1)
 {
-    uint32_t w;
-    uint16_t h;
+    uint64_t m[4];
+    pair_products(w0, w1, h0, h1, m);
+    sum = fma2(m[0], dev::pack2(a0.x, a1.x), sum);
+    sum = fma2(m[1], dev::pack2(a0.y, a1.y), sum);
+    sum = fma2(m[2], dev::pack2(a0.z, a1.z), sum);
+    sum = fma2(m[3], dev::pack2(a0.w, a1.w), sum);
+    return sum;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t a)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t a)
+{
     float4 v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(fw));
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(sw));
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(aw));
-    return record_step_packed(sum, w, h, v);
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
 }
 
 __device__ __forceinline__ int32_t instance_count(const PackedDeviceParams &p, int32_t inst)
@@ -175,13 +221,14 @@ __device__ __forceinline__ int32_t instance_count(const PackedDeviceParams &p, i
     return c;
 }
 
-// Staged path: a persistent grid of up to three CTAs per SM.  The work is a
+// Staged path: a grid of up to seven CTAs per SM.  The work is a
 // list of tiles -- 256 lanes of one instance, instance-major -- and CTA c
 // takes tiles c, c + G, c + 2G, ... (1024 tiles of the 128 x 2048-lane
 // workload: 6 or 7 per SM).  The producer streams every stage of every tile of the CTA through one
 // ring, so the copies of a CTA's next tile are in flight while its consumers
 // finish the current one; consumer thread t owns lane t of the tile.
-__global__ void __launch_bounds__(PD_THREADS_STAGED, 3) packed_dot_staged_kernel(
+template <bool SAME>
+__global__ void __launch_bounds__(PD_THREADS_STAGED, 7) packed_dot_staged_kernel(
     const __grid_constant__ CUtensorMap tm_fields, const __grid_constant__ CUtensorMap tm_scales,
     const __grid_constant__ CUtensorMap tm_rhs, const PackedDeviceParams p)
 {
@@ -245,7 +292,7 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 3) packed_dot_staged_kernel
         return;
     }
 
-    // ---- consumers: thread t owns lane t of each tile
+    // ---- consumers: thread t owns lanes t and t + PD_PAIR of each tile
     const int t = threadIdx.x;
     const uint32_t astep = 16u * (uint32_t)p.streams;   // activations of one record
     int s = 0;
@@ -253,35 +300,37 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 3) packed_dot_staged_kernel
     bool ok = true;
     for (int32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int32_t inst = tile / lblocks;
-        const int32_t l = (tile - inst * lblocks) * PD_TILE + t;
-        const bool live = l < p.lanes;
-        const int32_t sl = l % p.streams;
+        const int32_t la = (tile - inst * lblocks) * PD_TILE + t, lb = la + PD_PAIR;
+        const bool livea = la < p.lanes, liveb = lb < p.lanes;
+        // the lanes' activation streams: offsets within a stage's activations
+        const uint32_t xa = 16u * (uint32_t)(la % p.streams), xb = SAME ? xa : 16u * (uint32_t)(lb % p.streams);
         const int32_t count = instance_count(p, inst);
-        float sum = (live && p.initial) ? __ldg(p.initial + (int64_t)inst * p.lanes + l) : 0.f;
+        const float *init = p.initial ? p.initial + (int64_t)inst * p.lanes : nullptr;
+        uint64_t sum = dev::pack2(livea && init ? __ldg(init + la) : 0.f, liveb && init ? __ldg(init + lb) : 0.f);
         for (int32_t r0 = 0; r0 < count && ok; r0 += RPS) {
             const bool landed = dev::mbar_wait_bounded(full(s), fph, p.wait_ns);
             if (!__all_sync(dev::FULL_MASK, landed)) {
                 ok = false;
                 break;
             }
-            // this lane's word and scale of record k: fw + k * 1 KiB, sw + k * 512 B;
-            // its stream's activations: aw + k * astep
+            // this thread's words and scales of record k: fw + k * 1 KiB (+ 512 B for
+            // the second lane), sw + k * 512 B (+ 256 B); activations aw + k * astep
             uint32_t fw = stage(s) + 4u * (uint32_t)t;
             uint32_t sw = stage(s) + st.fields_bytes + 2u * (uint32_t)t;
-            uint32_t aw = stage(s) + st.fields_bytes + st.scales_bytes + 16u * (uint32_t)sl;
+            const uint32_t a0 = stage(s) + st.fields_bytes + st.scales_bytes;
+            uint32_t aw = a0 + xa, bw = a0 + xb;
             const int n_here = min(RPS, count - r0);
-            int k = 0;
-            for (; k + 4 <= n_here; k += 4) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    sum = staged_record(sum, fw + (uint32_t)i * PD_TILE * 4u, sw + (uint32_t)i * PD_TILE * 2u,
-                                        aw + (uint32_t)i * astep);
-                fw += 4u * PD_TILE * 4u;
-                sw += 4u * PD_TILE * 2u;
-                aw += 4u * astep;
-            }
-            for (; k < n_here; ++k) {
-                sum = staged_record(sum, fw, sw, aw);
+#pragma unroll 4
+            for (int k = 0; k < n_here; ++k) {
+                const uint32_t w0 = lds32(fw), w1 = lds32(fw + 4u * PD_PAIR);
+                const uint16_t h0 = lds16(sw), h1 = lds16(sw + 2u * PD_PAIR);
+                const float4 va = lds128f(aw);
+                if (SAME) {
+                    sum = pair_record(sum, w0, w1, h0, h1, va);
+                } else {
+                    sum = pair_record(sum, w0, w1, h0, h1, va, lds128f(bw));
+                    bw += astep;
+                }
                 fw += PD_TILE * 4u;
                 sw += PD_TILE * 2u;
                 aw += astep;
@@ -296,8 +345,12 @@ __global__ void __launch_bounds__(PD_THREADS_STAGED, 3) packed_dot_staged_kernel
         }
         if (!ok)
             dev::flag_error(p.error, LOOM_DEVERR_TIMEOUT);
-        if (live)
-            p.out[(int64_t)inst * p.lanes + l] = ok ? sum : __int_as_float(0x7fc00000);
+        float ya, yb;
+        dev::unpack2(sum, ya, yb);
+        if (livea)
+            p.out[(int64_t)inst * p.lanes + la] = ok ? ya : __int_as_float(0x7fc00000);
+        if (liveb)
+            p.out[(int64_t)inst * p.lanes + lb] = ok ? yb : __int_as_float(0x7fc00000);
     }
 }
 
@@ -410,7 +463,9 @@ cudaError_t launch_packed_dot(const PackedParams &q, bool staged, const loom_lau
         !encode_3d(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q.rhs, (uint64_t)q.streams * 4, (uint64_t)q.records,
                    (uint64_t)q.problems, (uint32_t)q.streams * 4, (uint32_t)q.rps))
         return cudaErrorInvalidValue;
-    return launch_with(packed_dot_staged_kernel, L, stream, tf, ts, tr, p);
+    // both lanes of a consumer thread read the same activations when PD_PAIR is a multiple of the streams
+    return PD_PAIR % q.streams == 0 ? launch_with(packed_dot_staged_kernel<true>, L, stream, tf, ts, tr, p)
+                                    : launch_with(packed_dot_staged_kernel<false>, L, stream, tf, ts, tr, p);
 }
 
 }  // namespace loom

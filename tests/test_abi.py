@@ -306,14 +306,18 @@ def test_unpack_validation(loom):
 
 
 def test_packed_dot_launch(loom):
-    # 256 lanes of one instance per CTA; grid.y = instances.  Staged (TMA ring,
-    # 256 consumers + a producer warp) when lanes % 8 == 0 and streams <= 64.
-    # staged: three CTAs per SM over tiles of 256 lanes of one instance (1024 tiles: 3 per CTA, at most)
+    # Staged (TMA ring, 128 consumer threads of two lanes each + a producer warp) when
+    # lanes % 8 == 0 and streams <= 64: CTAs over tiles of 256 lanes of one instance, as
+    # many per SM as their rings fit (at most seven); else 256 lanes per CTA, grid.y =
+    # instances.
+    def per_sm(smem):
+        return max(1, min(7, (227 * 1024) // (smem + 1024)))
+
     L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [128, 128, 2048, 64, 1, 0, 0, SMS])
     assert L["kernel"] == loom.LOOM_KERNEL_PACKED_STAGED
-    assert L["grid"] == (3 * SMS, 1, 1) and L["block"] == (288, 1, 1) and L["units_per_cta"] == 3
-    # default ring: 3 stages of 8 records x (1 KiB of words + 512 B of scales + 1 KiB of activations)
-    assert L["smem_bytes"] == 128 + 3 * 8 * (1024 + 512 + 64 * 16) + 16 * 3
+    # default ring: 3 stages of 4 records x (1 KiB of words + 512 B of scales + 1 KiB of activations)
+    assert L["smem_bytes"] == 128 + 3 * 4 * (1024 + 512 + 64 * 16) + 16 * 3 and per_sm(L["smem_bytes"]) == 7
+    assert L["grid"] == (1024, 1, 1) and L["block"] == (160, 1, 1) and L["units_per_cta"] == 1   # 1024 tiles < 7 SMs' worth
     # rings of 12 records (92 KB) fit twice per SM, of 24 records once
     L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [128, 128, 2048, 64, 1, 3, 12, SMS])
     assert L["grid"] == (2 * SMS, 1, 1) and L["units_per_cta"] == 4
@@ -325,8 +329,9 @@ def test_packed_dot_launch(loom):
             staged = aligned == 1 and Ln % 8 == 0 and S <= 64
             assert L["kernel"] == (loom.LOOM_KERNEL_PACKED_STAGED if staged else loom.LOOM_KERNEL_PACKED_DIRECT)
             tiles = P * oracle.workgroups(Ln, 256)
-            assert L["grid"] == ((min(tiles, 3 * SMS), 1, 1) if staged else (oracle.workgroups(Ln, 256), P, 1))
-            assert L["block"][0] == (288 if staged else 256)
+            want = (min(tiles, per_sm(L["smem_bytes"]) * SMS), 1, 1) if staged else (oracle.workgroups(Ln, 256), P, 1)
+            assert L["grid"] == want
+            assert L["block"][0] == (160 if staged else 256)
     L = loom.loom_launch_config(loom.LOOM_OP_PACKED_DOT, [1, 128, 2048, 128])   # too many streams to stage
     assert L["kernel"] == loom.LOOM_KERNEL_PACKED_DIRECT and L["smem_bytes"] == 0
     for bad in ([-1, 1, 8, 1], [1, -1, 8, 1], [1, 1, -8, 1], [1, 1, 8, 0], [65536, 1, 8, 1]):
