@@ -126,13 +126,41 @@ KERNEL_SOURCES = {
 SHARED_SOURCES = ("common.cuh", "internal.h", "loom_api.cu")
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string and character
+    literals kept whole), so that editing a comment leaves the hash unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def source_hash(workload: str) -> str:
+    """Hash of the code (comments and blank lines left out) that a workload's
+    kernels are built from."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int8_dequant_dot_gb300", "csrc")
     for f in sorted(KERNEL_SOURCES[workload] + SHARED_SOURCES):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

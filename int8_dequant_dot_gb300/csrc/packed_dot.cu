@@ -38,10 +38,12 @@
 //    scales from shared memory (consecutive lanes, consecutive addresses) and
 //    its stream's float4 (conflict-free); the bytes become f32 by a byte
 //    permute and a packed subtraction, the scalings are packed multiplies and
-//    the four ordered fused steps are packed fused multiply-adds.  The kernel
-//    is bound by instruction issue: two lanes per thread measured 33.1 us
-//    against 37.5 us with one (trains of launches; four-record stages, seven
-//    CTAs of four consumer warps per SM).
+//    the four ordered fused steps are packed fused multiply-adds.  With one
+//    lane per thread the kernel was bound by instruction issue (36.8 us per
+//    launch in trains of launches); two lanes per thread issue 12% fewer
+//    instructions and, with four-record stages and seven CTAs of four
+//    consumer warps per SM, run at the time of a launch that only reads the
+//    same bytes (32.5-32.9 us).
 //  * Direct path (inputs a TMA copy cannot take: lanes not a multiple of 8,
 //    more than 64 streams, unaligned pointers): plain loads, same order and
 //    arithmetic, identical bits.
@@ -49,7 +51,6 @@
 //    the affected outputs are NaN.
 #include <cuda.h>
 #include <cuda_fp16.h>
-
 
 #include "common.cuh"
 #include "internal.h"

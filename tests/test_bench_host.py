@@ -52,3 +52,14 @@ def test_whole_job_value():
     # N ranks each moving B bytes per step of T ms: N * B / T
     assert bench.whole_job_gbs(1, 1_000_000_000, 1.0) == 1000.0
     assert bench.whole_job_gbs(4, 1_000_000_000, 2.0) == 2000.0
+
+
+def test_source_hash_ignores_comments_only():
+    src = ('int a = 1; // note\n/* block\n   comment */\nconst char *s = "a // b /* c */";\n'
+           "char q = '\"';\n\n  x = 2; /* y */ z = 3;\n")
+    code = bench.strip_comments(src)
+    assert "note" not in code and "block" not in code and "y */" not in code
+    assert '"a // b /* c */"' in code and "'\"'" in code
+    assert bench.strip_comments(src.replace("note", "other words")) == code
+    assert bench.strip_comments(src.replace("x = 2", "x = 4")) != code
+    assert all(len(bench.source_hash(w)) == 16 for w in bench.KERNEL_SOURCES)
