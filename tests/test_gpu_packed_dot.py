@@ -97,6 +97,22 @@ def test_ragged_shapes(env, P, R, L, S, counts):
         assert same_bits(run(loom, torch, d, device_counts=False), want(d))
 
 
+@pytest.mark.parametrize("streams,tuning_kw", [(64, None), (48, None), (64, {"depth": 3, "units_per_warp": 24})])
+def test_ctas_run_on_across_tiles(env, streams, tuning_kw):
+    # 1344 tiles of 256 lanes, more than the grid holds CTAs (at most seven per SM with the
+    # default stages, one with 24-record stages): each CTA's ring runs on from one tile into
+    # the next, across instances of different lengths; 48 streams do not divide 128, so the
+    # two lanes of a thread read different activations
+    torch, loom = env
+    P = 168
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert P * 2048 // 256 > 7 * sms
+    d = synth.packed_dot_case(problems=P, records=24, lanes=2048, streams=streams,
+                              counts=[(7 * i) % 25 for i in range(P)], seed=707 + streams)
+    t = loom.make_tuning(**tuning_kw) if tuning_kw else None
+    assert same_bits(run(loom, torch, d, tuning=t), want(d))
+
+
 def test_unaligned_inputs_take_plain_loads(env):
     torch, loom = env
     d = synth.packed_dot_case(problems=2, records=16, lanes=256, streams=64, counts=[16, 11], seed=404)
