@@ -18,7 +18,7 @@ The metric is HBM GB/s over algorithmic bytes (only the bytes the method
 must move: active rows, metadata, outputs).  Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --profile {gemv,segments,batched,wide} [--launches N]
+  python bench.py --profile {gemv,segments,batched,batched_dp4a,wide,...} [--launches N]
       (no timing: runs one kernel's workload for an ncu capture)
 """
 from __future__ import annotations
@@ -1040,7 +1040,8 @@ def run_profile(args):
                "wide": synth.wide_rows() if args.profile == "wide" else None}
     else:
         inp = {"gemv": synth.dequant_gemv(n_rows=8192 * sc) if args.profile == "gemv" else None,
-               "batched": synth.dequant_batched(n_rows=8192 * sc) if args.profile == "batched" else None}
+               "batched": (synth.dequant_batched(n_rows=8192 * sc)
+                           if args.profile in ("batched", "batched_dp4a") else None)}
     work = _SingleWorkload(args.profile, inp, torch, loom, stream, args.depth)
     with torch.cuda.stream(stream):
         for _ in range(args.launches):
@@ -1055,6 +1056,10 @@ class _SingleWorkload:
         dev = torch.device("cuda")
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
         self.tuning = loom.make_tuning(depth=depth) if depth else None
+        if name == "batched_dp4a":   # the batched workload on the dp4a engine (the engine comparison)
+            name = "batched"
+            self.tuning = loom.make_tuning(depth=depth, path=loom.LOOM_PATH_STAGED)
+        self.name = name
         if name == "segments":
             s = inp["segments"]
             self.args = (t(s["values"]), s["num_segments"], 2016, 63, 32, t(s["counts"]), t(s["initial"]), 8)
@@ -1081,7 +1086,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--depth", type=int, default=0, help="read-ahead depth (0 = library default)")
-    ap.add_argument("--profile", choices=ORDER + ("packed", "sum_rows", "sum_vector_rows", "guarded_rows", "routed")
+    ap.add_argument("--profile", choices=ORDER + ("batched_dp4a", "packed", "sum_rows", "sum_vector_rows",
+                                                  "guarded_rows", "routed")
                     + tuple("floor_" + n for n in ORDER), default=None)
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--scale", type=int, default=1,
