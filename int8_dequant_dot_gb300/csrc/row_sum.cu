@@ -439,10 +439,10 @@ __global__ void __launch_bounds__(256, 3) row_sum_seg_kernel(const RowSumParams 
         const int nf = kF > g ? (kF - g + 3) >> 2 : 0;   // this lane's full-tile rows
         const int na = kc > g ? (kc - g + 3) >> 2 : 0;   // ... and all its active rows
         int i = 0;
-#pragma unroll 2
+#pragma unroll 4
         for (; i < nf; ++i)
             acc.full4(s4[32 * i]);
-#pragma unroll 2
+#pragma unroll 4
         for (; i < na; ++i)
             acc.tail4(s4[32 * i]);
         __syncwarp();
