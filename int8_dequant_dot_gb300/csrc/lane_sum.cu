@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(256) lane_sum_staged_kernel(const LaneSumParam
             const int32_t rows_here = min(p.chunk_rows, kc - j * p.chunk_rows);
             const float *chunk = ring + (size_t)cs * CH;
             if (lane < p.lanes) {
+#pragma unroll 8
                 for (int32_t r = 0; r < rows_here; ++r) {
                     float v[4];
                     load_row<WIDTH, GUARDED>(v, chunk + (size_t)r * row_elems, lane);
