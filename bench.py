@@ -554,6 +554,7 @@ def run_ours(args, rank, world, dist):
     work2 = DeviceWorkload(inp, torch, loom, stream, depth=args.depth)
     extras["stream_floor"]["trains"] = floor_trains(torch, loom, stream, work, work2, alg)
     del work2
+    extras["stream_floor"]["step"] = step_floor(torch, loom, stream, total, ms_per_step)
     extras["batched_engines"] = engine_study(torch, loom, stream, work, alg)
 
     line = {
@@ -824,6 +825,30 @@ def floor_trains(torch, loom, stream, work, work2, alg, reps: int = 7, train: in
            for n, nbytes in alg.items()}
     del srcs
     return {"note": TRAIN_NOTE, "workloads": out}
+
+
+def step_floor(torch, loom, stream, total: int, ms_per_step: float, reps: int = 7, train: int = 20):
+    """The read-only probe over the whole step's algorithmic bytes in one launch,
+    timed in trains (best of FLOOR_SCHEDULES, median of `reps` trains, alternating
+    two source buffers), beside the step's own time per step (K back-to-back steps):
+    how far the four kernels together are from reading their bytes once."""
+    srcs, word = floor_srcs(torch, total)
+    nb = total // 16 * 16
+    times = {sc: [] for sc in FLOOR_SCHEDULES}
+    for rep in range(reps + 1):
+        for sc in FLOOR_SCHEDULES:
+            t = _run_train(torch, stream,
+                           lambda i: loom.loom_stream_floor(srcs[i], nb, sc[0], sc[1], sc[2], word, stream=stream), train)
+            if rep:
+                times[sc].append(t)
+    del srcs
+    meds = {sc: statistics.median(v) for sc, v in times.items()}
+    best = min(meds, key=meds.get)
+    return {"bytes": total, "floor_us": meds[best] * 1e3,
+            "floor_schedule": {"kind": FLOOR_KINDS[best[0]], "depth": best[1], "ctas_per_sm": best[2]},
+            "floor_GB/s": total / (meds[best] * 1e-3) / 1e9, "step_us": ms_per_step * 1e3,
+            "step_over_floor": ms_per_step / meds[best],
+            "note": "one read-only launch over the step's bytes, trains of 20; the step: K back-to-back steps"}
 
 
 def engine_study(torch, loom, stream, work, alg, reps: int = 21):
